@@ -1,0 +1,543 @@
+"""Throughput of the compressed-KV attention layer on one GB300 (or N replicas).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+
+A step is one pass of the whole per-layer path over one batch:
+  decode workloads  — for every layer: append the new token (raw window +
+                      compressor), indexer top-k on ratio-4 layers, sparse
+                      attention; one new token per sequence;
+  prefill workload  — one 4096-token chunk: append, per-query top-k, chunk
+                      attention with the raw-window commit.
+Default workload: the 43-layer Flash schedule decoding 8 sequences at context
+131,072 (ratio-4 and ratio-128 layers, both lanes, every step of the path).
+`value` is whole-job tokens/s with every input resident in HBM; `e2e` adds the
+per-step host->device copy of the step's inputs (pinned) and the device->host
+read of the last layer's output. The reference arm (--impl reference) times
+the CPU oracle on a bounded sample of the same workload.
+"""
+import argparse
+import json
+import os
+
+os.environ.setdefault("OPENBLAS_NUM_THREADS", "1")   # the oracle legs run single-threaded
+os.environ.setdefault("OMP_NUM_THREADS", "1")
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = ("c4a/c128a decode tok/s & HBM GB/s frac; 4096-chunk prefill tok/s (1×GB300)")
+WORKLOADS = {"flash43": synth.FLASH_STACK, "c4a_decode": synth.C4A_DECODE,
+             "c128a_decode": synth.C128A_DECODE, "prefill": synth.C4A_PREFILL,
+             "tiny": synth.TINY}
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), float(d["bf16_tflops_sustained"]), "measured"
+    except Exception:
+        return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+# ----------------------------------------------------------------- GPU runner
+
+class Runner:
+    """Builds every layer's cache and inputs on the device and runs steps."""
+
+    def __init__(self, wl: synth.Workload, device, rank: int = 0):
+        from compressed_kv_sparse_gb300 import lib
+        self.lib, self.wl, self.dev = lib, wl, device
+        self.decode = wl.mode == "decode"
+        self.T = 1 if self.decode else wl.chunk
+        self.p0 = wl.context
+        seed_wl = wl if rank == 0 else synth.Workload(wl.name, wl.seed + 1000 * rank, wl.batch,
+                                                      wl.layers, wl.context, wl.mode, wl.chunk,
+                                                      wl.hidden)
+        self.layers = []
+        B = wl.batch
+        end = self.p0 + self.T
+        for il, s in enumerate(wl.layers):
+            cap = end // s.ratio + 1 if s.ratio else 0
+            c = lib.LayerCache(ratio=s.ratio, head_dim=s.head_dim, n_rot=s.n_rot, batch=B,
+                               comp_cap=cap, dtype=s.dtype, base=s.rope_base,
+                               rope_max_pos=end + 1, index_dim=s.index_dim,
+                               index_rot=s.index_rot, cap_raw=s.cap_raw, device=device)
+            hist = synth.cache_history(seed_wl, il, self.p0, comp_cap=cap, device=device)
+            c.load_state(hist, self.p0)
+            del hist
+            inp = synth.step_inputs(seed_wl, il, self.p0, self.T, device=device)
+            inp = {k: v.contiguous() for k, v in inp.items()}
+            L = {"s": s, "cache": c, "inp": inp}
+            k = s.top_k
+            if s.ratio == 4:
+                L["topk"] = torch.empty((B, self.T, k) if not self.decode else (B, k),
+                                        dtype=torch.int32, device=device)
+                L["ws_idx"] = lib.workspace(c.workspace_bytes(lib.CALL_INDEX_TOPK, self.T,
+                                                              s.index_heads, k), device)
+            call = lib.CALL_ATTN_DECODE if self.decode else lib.CALL_ATTN_PREFILL
+            L["ws_attn"] = lib.workspace(c.workspace_bytes(call, self.T, s.n_heads, k), device)
+            if self.decode:
+                L["q"] = inp["q"][:, 0].contiguous()
+                L["out"] = torch.empty((B, s.n_heads, s.head_dim), dtype=c.torch_dtype,
+                                       device=device)
+            else:
+                L["q"] = inp["q"]
+                L["out"] = torch.empty((B, self.T, s.n_heads, s.head_dim), dtype=c.torch_dtype,
+                                       device=device)
+                L["chunk"] = torch.empty((B, self.T, s.head_dim), dtype=c.torch_dtype,
+                                         device=device)
+            self.layers.append(L)
+        torch.cuda.synchronize(device)
+
+    # one layer; `ev` = optional list of (name, start_event, end_event) to record
+    def layer_step(self, L, ev=None):
+        lib, s, c, inp = self.lib, L["s"], L["cache"], L["inp"]
+        c.n_tokens = self.p0
+        k, scale = s.top_k, lib.default_scale(s.head_dim)
+
+        def timed(name, fn):
+            if ev is None:
+                fn()
+                return
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            fn()
+            e1.record()
+            ev.append((name, e0, e1))
+
+        if self.decode:
+            timed("append", lambda: lib.ds4a_compress_append(c, self.p0, 1, inp))
+            if s.ratio == 4:
+                timed("index_topk", lambda: lib.ds4a_index_topk(
+                    c, self.p0, 1, inp["q_idx"], inp["w"], s.index_heads, k, L["topk"],
+                    L["ws_idx"]))
+            timed(f"attn_r{s.ratio}", lambda: lib.ds4a_sparse_attn_decode(
+                c, self.p0, L["q"], s.n_heads, L.get("topk"), k, scale, L["out"], L["ws_attn"]))
+        else:
+            timed("append", lambda: lib.ds4a_compress_append(c, self.p0, self.T, inp,
+                                                             raw_chunk_out=L["chunk"]))
+            if s.ratio == 4:
+                timed("index_topk", lambda: lib.ds4a_index_topk(
+                    c, self.p0, self.T, inp["q_idx"], inp["w"], s.index_heads, k, L["topk"],
+                    L["ws_idx"]))
+            timed(f"attn_r{s.ratio}", lambda: lib.ds4a_sparse_attn_prefill_chunk(
+                c, self.p0, self.T, L["q"], s.n_heads, L["chunk"], L.get("topk"), k, scale,
+                L["out"], L["ws_attn"]))
+
+    def step(self, ev=None):
+        for L in self.layers:
+            self.layer_step(L, ev)
+
+    def tokens_per_step(self):
+        return self.wl.batch * self.T
+
+    # algorithmic bytes / FLOPs per call kind (measurement)
+    def algorithmic(self):
+        B, T = self.wl.batch, self.T
+        out = {}
+        for L in self.layers:
+            s = L["s"]
+            eb = 2 if s.dtype == "bf16" else 4
+            p_last = self.p0 + T - 1
+            if s.ratio == 4:
+                vis = (p_last + 1) // 4
+                if self.decode:
+                    by = B * (vis * s.index_dim * eb + s.index_heads * (s.index_dim + 1) * eb +
+                              s.top_k * 4)
+                    fl = 2.0 * B * vis * s.index_heads * s.index_dim
+                else:
+                    pairs = sum((self.p0 + t + 1) // 4 for t in range(T))
+                    by = B * (vis * s.index_dim * eb + T * s.index_heads * (s.index_dim + 1) * eb
+                              + T * s.top_k * 4)
+                    fl = 2.0 * B * pairs * s.index_heads * s.index_dim
+                a = out.setdefault("index_topk", [0, 0.0, 0])
+                a[0] += by
+                a[1] += fl
+                a[2] += 1
+            # append: raw row in/out, lane candidates + scores in, state slots out
+            lanes = [s.head_dim] if s.ratio else []
+            if s.ratio == 4:
+                lanes.append(s.index_dim)
+            by = B * T * (2 * s.head_dim * eb + sum(2 * w * eb + 2 * w * 4 for w in lanes))
+            a = out.setdefault("append", [0, 0.0, 0])
+            a[0] += by
+            a[2] += 1
+            nw = min(p_last + 1, s.cap_raw)
+            ncomp = s.top_k if s.ratio == 4 else (p_last + 1) // 128 if s.ratio == 128 else 0
+            rows = nw + ncomp
+            qo = 2 * s.n_heads * s.head_dim * eb
+            if self.decode:
+                by = B * (rows * s.head_dim * eb + qo + (s.top_k * 4 if s.ratio == 4 else 0))
+            else:
+                by = B * (T * rows * s.head_dim * eb + T * qo)
+            fl = 4.0 * B * T * rows * s.n_heads * s.head_dim
+            a = out.setdefault(f"attn_r{s.ratio}", [0, 0.0, 0])
+            a[0] += by
+            a[1] += fl
+            a[2] += 1
+        return out
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index, self.proc = index, None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                out = ""
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+        else:
+            self.lines = []
+
+    def summary(self):
+        sm, mx, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            try:
+                sm.append(float(f[0]))
+                mx = max(mx, float(f[1]))
+            except (ValueError, IndexError):
+                continue
+            for n, v in zip(names, f[3:7]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def flush_l2(buf):
+    buf.add_(1)
+
+
+def run_gpu(args, wl, rank, world, device):
+    hbm, bf16, bf16s, peak_kind = peaks()
+    lib_mod = __import__("compressed_kv_sparse_gb300.lib", fromlist=["lib"])
+    R = Runner(wl, device, rank)
+    step_bytes = sum(v[0] for v in R.algorithmic().values())
+    flush = None
+    if step_bytes < 512e6:      # working set below ~4x L2: flush between steps
+        flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=device)
+
+    def step():
+        R.step()
+        if flush is not None:
+            flush_l2(flush)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(device)
+
+    # graph of one step (launch overhead off the timed path)
+    use_graph = not args.no_graph
+    if use_graph:
+        n0 = lib_mod.ds4a_launch_count()
+        g = torch.cuda.CUDAGraph()
+        s = torch.cuda.Stream(device)
+        s.wait_stream(torch.cuda.current_stream(device))
+        with torch.cuda.stream(s):
+            R.step()           # one eager pass on the capture stream
+        torch.cuda.current_stream(device).wait_stream(s)
+        torch.cuda.synchronize(device)
+        n0 = lib_mod.ds4a_launch_count()
+        with torch.cuda.graph(g):
+            R.step()
+        launches_per_step = lib_mod.ds4a_launch_count() - n0
+        run = lambda: (g.replay(), flush is not None and flush_l2(flush))
+        for _ in range(2):
+            run()
+    else:
+        n0 = lib_mod.ds4a_launch_count()
+        R.step()
+        launches_per_step = lib_mod.ds4a_launch_count() - n0
+        run = step
+    torch.cuda.synchronize(device)
+
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(device)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(device.index if device.index is not None else 0) as clk:
+        e0.record()
+        for _ in range(args.steps):
+            run()
+        e1.record()
+        torch.cuda.synchronize(device)
+    if world > 1:
+        torch.distributed.barrier()
+    ms = e0.elapsed_time(e1) / args.steps
+    flush_ms = 0.0
+    if flush is not None:        # subtract the L2 flush from the step time
+        f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        f0.record()
+        for _ in range(args.steps):
+            flush_l2(flush)
+        f1.record()
+        torch.cuda.synchronize(device)
+        flush_ms = f0.elapsed_time(f1) / args.steps
+    ms_step = max(ms - flush_ms, 1e-6)
+    if world > 1:
+        t = torch.tensor([ms_step], device=device)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms_step = float(t.item())
+    value = world * R.tokens_per_step() / (ms_step / 1e3)
+
+    # per-call device time (eager pass with events around each call, same stream)
+    ev = []
+    torch.cuda.synchronize(device)
+    for _ in range(max(1, min(args.steps, 5))):
+        R.step(ev)
+        if flush is not None:
+            flush_l2(flush)
+    torch.cuda.synchronize(device)
+    per_call = {}
+    for name, a, b in ev:
+        per_call.setdefault(name, []).append(a.elapsed_time(b))
+    alg = R.algorithmic()
+    calls = {}
+    for name, ts in per_call.items():
+        n_per_step = alg[name][2]
+        t_launch = sum(ts) / len(ts) / 1e3          # seconds per call
+        by = alg[name][0] / n_per_step
+        fl = alg[name][1] / n_per_step
+        calls[name] = {"ms_per_call": t_launch * 1e3, "calls_per_step": n_per_step,
+                       "GB/s": by / t_launch / 1e9, "TFLOP/s": fl / t_launch / 1e12,
+                       "bytes": by, "flop": fl}
+    dom = max(calls, key=lambda n: calls[n]["ms_per_call"] * calls[n]["calls_per_step"])
+    dc = calls[dom]
+    tensor_bound = not R.decode
+    if tensor_bound:
+        roof = {"bound": "tensor", "achieved": dc["TFLOP/s"], "peak": bf16s, "unit": "TFLOP/s",
+                "frac": dc["TFLOP/s"] / bf16s, "traffic": None,
+                "kernel": dom, "peak_kind": f"{peak_kind} bf16 sustained"}
+    else:
+        roof = {"bound": "hbm", "achieved": dc["GB/s"], "peak": hbm, "unit": "GB/s",
+                "frac": dc["GB/s"] / hbm, "traffic": None, "kernel": dom,
+                "peak_kind": f"{peak_kind} hbm copy"}
+
+    # end to end: pinned host inputs -> device, step, last output -> host
+    host_in = []
+    for L in R.layers:
+        for name, t in L["inp"].items():
+            if name.startswith(("ape", "gamma")):
+                continue                       # weights stay resident
+            h = torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+            h.copy_(t)
+            host_in.append((h, t))
+    last = R.layers[-1]["out"]
+    host_out = torch.empty(last.shape, dtype=last.dtype, pin_memory=True)
+    h2d = sum(h.numel() * h.element_size() for h, _ in host_in)
+    d2h = host_out.numel() * host_out.element_size()
+
+    def e2e_step():
+        for h, t in host_in:
+            t.copy_(h, non_blocking=True)
+        if R.decode:
+            for L in R.layers:
+                L["q"].copy_(L["inp"]["q"][:, 0])
+        run()
+        host_out.copy_(last, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize(device)
+    if world > 1:
+        torch.distributed.barrier()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        e2e_step()
+        torch.cuda.synchronize(device)
+    e2e_s = (time.perf_counter() - t0) / args.steps - flush_ms / 1e3
+    if world > 1:
+        t = torch.tensor([e2e_s], device=device)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_s = float(t.item())
+    e2e = {"value": world * R.tokens_per_step() / e2e_s, "unit": "tok/s",
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+    res = {"metric": METRIC, "value": value, "unit": "tok/s", "n_gpus": world,
+           "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+           "dtype": wl.dtype, "data": "synthetic",
+           "config": {"workload": wl.name, "mode": wl.mode, "batch_per_gpu": wl.batch,
+                      "context": wl.context, "tokens_per_step_per_gpu": R.tokens_per_step(),
+                      "layers": len(wl.layers),
+                      "ratios": {str(r): sum(1 for s in wl.layers if s.ratio == r)
+                                 for r in (0, 4, 128)},
+                      "l2": "flushed between steps" if flush is not None
+                      else "inputs larger than L2 (algorithmic %.2f GB per step)" % (step_bytes / 1e9),
+                      "cuda_graph": use_graph, "parallelism": f"replicas x{world}",
+                      "algorithmic_GB_per_step": step_bytes / 1e9,
+                      "step_GB/s": step_bytes / (ms_step / 1e3) / 1e9},
+           "roofline": roof, "calls": calls,
+           "gpu_launches": int(launches_per_step) * args.steps,
+           "clocks": clk.summary(), "e2e": e2e}
+    return res, R
+
+
+# ----------------------------------------------------------------- CPU oracle
+# The CPU baseline and the reference arm time the oracle (test infrastructure)
+# as it stands, single-threaded numpy, on a bounded sample of the workload.
+
+def _oracle_layer_case(wl: synth.Workload, il: int):
+    """Oracle cache + step inputs of layer il for the first sequence only."""
+    from oracle.layer import OracleCache
+    s = wl.layers[il]
+    one = synth.Workload(wl.name, wl.seed, 1, wl.layers, wl.context, wl.mode, wl.chunk, wl.hidden)
+    T = 1 if wl.mode == "decode" else wl.chunk
+    cap = (wl.context + T) // s.ratio + 1 if s.ratio else 0
+    hist = synth.cache_history(one, il, wl.context, comp_cap=cap)
+    inp = synth.step_inputs(one, il, wl.context, T)
+    np_ = lambda t: t.float().numpy()
+    oc = OracleCache(ratio=s.ratio, head_dim=s.head_dim, n_rot=s.n_rot, cap_raw=s.cap_raw,
+                     base=s.rope_base, dtype=s.dtype, n_tokens=wl.context,
+                     index_dim=s.index_dim, index_rot=s.index_rot,
+                     **{k: np_(v) for k, v in hist.items()})
+    return oc, {k: np_(v) for k, v in inp.items()}
+
+
+def oracle_sample(wl: synth.Workload):
+    """Time one bounded oracle pass; return (seconds spent, seconds the oracle
+    would take for one whole step of the workload, description)."""
+    from oracle import layer as olayer
+    if wl.mode == "decode":
+        kinds = {}
+        for il, s in enumerate(wl.layers):
+            kinds.setdefault(s.ratio, []).append(il)
+        spent, per_seq = 0.0, 0.0
+        for ratio, ils in kinds.items():
+            oc, inp = _oracle_layer_case(wl, ils[0])
+            t0 = time.perf_counter()
+            olayer.decode_step(oc, wl.context, inp, wl.layers[ils[0]].top_k)
+            dt = time.perf_counter() - t0
+            spent += dt
+            per_seq += dt * len(ils)
+        desc = (f"sequence 0 only, one layer of each ratio {sorted(kinds)} "
+                f"(append + top-k + attention), scaled by layers per ratio and by {wl.batch} sequences")
+        return spent, per_seq * wl.batch, desc
+    s = wl.layers[0]
+    oc, inp = _oracle_layer_case(wl, 0)
+    ring = oc.raw_kv.copy()
+    t0 = time.perf_counter()
+    rows = olayer.compress_append(oc, wl.context, inp, chunk=True)
+    t_app = time.perf_counter() - t0
+    nq = 2
+    qs = [(0, 0), (0, wl.chunk - 1)]
+    t0 = time.perf_counter()
+    tk = olayer.index_topk(oc, wl.context, inp["q_idx"], inp["w"], s.top_k, queries=qs)
+    olayer.attention(oc, wl.context, inp["q"], tk, None, ring=ring, chunk_rows=rows, queries=qs)
+    t_q = (time.perf_counter() - t0) / nq
+    desc = (f"whole-chunk compressor append + {nq} of {wl.chunk} queries (indexer scan, top-k, "
+            "attention), queries scaled to the chunk")
+    return t_app + nq * t_q, (t_app + wl.chunk * t_q) * wl.batch, desc
+
+
+def _threads():
+    return int(os.environ.get("OPENBLAS_NUM_THREADS", "1"))
+
+
+def cpu_baseline(wl: synth.Workload, budget_s: float = 10.0):
+    spent_all, est = 0.0, []
+    while spent_all < budget_s:
+        spent, step_s, desc = oracle_sample(wl)
+        spent_all += spent
+        est.append(step_s)
+    step_s = statistics.median(est)
+    tokens = wl.batch * (1 if wl.mode == "decode" else wl.chunk)
+    return {"value": tokens / step_s, "unit": "tok/s", "cores": _threads(), "kind": "oracle",
+            "sample": f"{desc}; {len(est)} repeats, {spent_all:.1f} s of CPU work"}
+
+
+def reference_arm(wl: synth.Workload, steps: int, warmup: int, world: int):
+    tokens = wl.batch * (1 if wl.mode == "decode" else wl.chunk)
+    for _ in range(warmup):
+        oracle_sample(wl)
+    vals, spent_all, desc = [], 0.0, ""
+    for _ in range(steps):
+        spent, step_s, desc = oracle_sample(wl)
+        spent_all += spent
+        vals.append(step_s)
+    step_s = statistics.median(vals)
+    v = tokens / step_s
+    return {"metric": METRIC, "value": v, "unit": "tok/s", "n_gpus": world, "steps": steps,
+            "warmup": warmup, "ms_per_step": step_s * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic",
+            "impl": "reference",
+            "config": {"workload": wl.name, "mode": wl.mode, "batch_per_gpu": wl.batch,
+                       "context": wl.context},
+            "cpu_baseline": {"value": v, "unit": "tok/s", "cores": _threads(), "kind": "oracle",
+                             "sample": desc},
+            "e2e": {"value": v, "unit": "tok/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="flash43", choices=sorted(WORKLOADS))
+    ap.add_argument("--impl", default="gpu", choices=["gpu", "reference"])
+    ap.add_argument("--no-graph", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    wl = WORKLOADS[args.workload]
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        print(json.dumps(reference_arm(wl, args.steps, args.warmup, world)))
+        return
+
+    if world > 1:
+        torch.distributed.init_process_group("nccl")
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    res, _ = run_gpu(args, wl, rank, world, device)
+    if rank == 0:
+        if not args.no_cpu_baseline:
+            res["cpu_baseline"] = cpu_baseline(wl)
+        print(json.dumps(res))
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,316 @@
+// Raw-window insert and KV compressor ("【#3】ds4.c を読み解く" §4 compressor
+// steps, §5 ratio-4 frontier, §8 tail RoPE; vLLM DeepSeek V4 page: c4a pools
+// 8 tokens at stride 4, c128a 128 tokens at stride 128).
+//
+// One fused, elementwise pass per call. A thread owns one (or two) adjacent
+// channel pairs of a row, so the rotation pair, the per-channel pooling over
+// the window slots and the state writes of a channel all stay in one thread;
+// only the RMS of the pooled row needs a block reduction.
+//
+// Decode (T = 1): one launch, grid (B, 1 + lanes). Block y = 0 rotates the raw
+// row into the ring; block y = 1 + l stores the token into lane l's state and,
+// at a ratio boundary, pools, normalises, rotates and appends the compressed
+// row, then (ratio 4) moves slots 4..7 to 0..3.
+// Chunk (T > 1): every compressed row completed inside the chunk is built in
+// parallel, one block per row, reading window tokens from the chunk inputs or,
+// for tokens before pos0, from the state as it was before the chunk; a second
+// launch then writes the state as the token-by-token process would leave it.
+#include "common.cuh"
+
+namespace ds4a {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr float kRmsEps = 1e-6f;
+constexpr int kMaxPairsPerThread = 2;  // width <= 1024
+
+struct SlotVal {
+  float kv, score;
+};
+
+// Pool window slots per channel, RMS-normalise, rotate at `pos` and store row
+// i of the lane. get(s, c) returns slot s of channel c (score without APE,
+// -inf when empty). Called by every thread of the block (uniform).
+template <typename T, typename Get>
+__device__ void pool_norm_rope_store(const LaneArgs &L, uint32_t W, uint32_t b, uint32_t i,
+                                     uint32_t comp_cap, uint32_t pos, Get get, float *red) {
+  const T *ape = static_cast<const T *>(L.ape);
+  const T *gamma = static_cast<const T *>(L.gamma);
+  T *comp = static_cast<T *>(L.comp);
+  const uint32_t width = L.width, npair = width / 2, n_nope = width - L.n_rot;
+  float y[kMaxPairsPerThread][2];
+  float ss = 0.f;
+#pragma unroll
+  for (int k = 0; k < kMaxPairsPerThread; ++k) {
+    const uint32_t j = threadIdx.x + k * blockDim.x;
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      float out = 0.f;
+      if (j < npair) {
+        const uint32_t c = 2 * j + e;
+        float m = -INFINITY;
+        for (uint32_t s = 0; s < W; ++s) {
+          const float sig = get(s, c).score + ld_f32(ape, (size_t)s * width + c);
+          m = fmaxf(m, sig);
+        }
+        if (m != -INFINITY) {
+          float den = 0.f, num = 0.f;
+          for (uint32_t s = 0; s < W; ++s) {
+            const SlotVal v = get(s, c);
+            const float w = expf(v.score + ld_f32(ape, (size_t)s * width + c) - m);
+            if (w > 0.f) {
+              den += w;
+              num += w * v.kv;
+            }
+          }
+          out = den > 0.f ? num / den : 0.f;
+        }
+      }
+      y[k][e] = out;
+      ss += out * out;
+    }
+  }
+  ss = block_sum(ss, red);
+  const float inv = 1.0f / sqrtf(ss / (float)width + kRmsEps);
+  T *row = comp + ((size_t)b * comp_cap + i) * width;
+#pragma unroll
+  for (int k = 0; k < kMaxPairsPerThread; ++k) {
+    const uint32_t j = threadIdx.x + k * blockDim.x;
+    if (j >= npair) continue;
+    const uint32_t c = 2 * j;
+    float a = ld_f32(gamma, c) * (y[k][0] * inv);
+    float bb = ld_f32(gamma, c + 1) * (y[k][1] * inv);
+    if (c >= n_nope) {
+      const uint32_t fi = (c - n_nope) / 2;
+      const float co = L.cos[(size_t)pos * (L.n_rot / 2) + fi];
+      const float si = L.sin[(size_t)pos * (L.n_rot / 2) + fi];
+      const float ra = a * co - bb * si;
+      const float rb = a * si + bb * co;
+      a = ra;
+      bb = rb;
+    }
+    st_elem(row, c, a);
+    st_elem(row, c + 1, bb);
+  }
+}
+
+// Rotate one raw row (tail pairs) from src into dst.
+template <typename T>
+__device__ void raw_row(const T *src, T *dst, uint32_t D, uint32_t n_rot, uint32_t pos,
+                        const float *cos, const float *sin) {
+  const uint32_t n_nope = D - n_rot;
+  for (uint32_t j = threadIdx.x; j < D / 2; j += blockDim.x) {
+    const uint32_t c = 2 * j;
+    float a = ld_f32(src, c), bb = ld_f32(src, c + 1);
+    if (c >= n_nope) {
+      const uint32_t fi = (c - n_nope) / 2;
+      const float co = cos[(size_t)pos * (n_rot / 2) + fi];
+      const float si = sin[(size_t)pos * (n_rot / 2) + fi];
+      const float ra = a * co - bb * si;
+      const float rb = a * si + bb * co;
+      a = ra;
+      bb = rb;
+    }
+    st_elem(dst, c, a);
+    st_elem(dst, c + 1, bb);
+  }
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kThreads) append_step_kernel(AppendArgs a) {
+  __shared__ float red[32];
+  const uint32_t b = blockIdx.x, p = a.pos0;
+  if (blockIdx.y == 0) {
+    const T *src = static_cast<const T *>(a.raw_in) + (size_t)b * a.head_dim;
+    T *dst = static_cast<T *>(a.raw_dst) +
+             ((size_t)b * a.cap_raw + p % a.cap_raw) * a.head_dim;
+    raw_row(src, dst, a.head_dim, a.n_rot, p, a.cos, a.sin);
+    return;
+  }
+  const LaneArgs &L = a.lane[blockIdx.y - 1];
+  const uint32_t r = a.ratio, W = a.window, width = L.width;
+  const uint32_t slot = r == 4 ? 4 + p % 4 : p % r;
+  const T *cand = static_cast<const T *>(L.cand) + (size_t)b * width;
+  const T *score = static_cast<const T *>(L.score) + (size_t)b * width;
+  float *skv = L.state_kv + (size_t)b * W * width;
+  float *ssc = L.state_score + (size_t)b * W * width;
+  for (uint32_t c = threadIdx.x; c < width; c += blockDim.x) {
+    skv[(size_t)slot * width + c] = ld_f32(cand, c);
+    ssc[(size_t)slot * width + c] = ld_f32(score, c);
+  }
+  if ((p + 1) % r != 0) return;  // uniform over the block
+  const uint32_t i = (p + 1) / r - 1;
+  auto get = [&](uint32_t s, uint32_t c) {
+    return SlotVal{skv[(size_t)s * width + c], ssc[(size_t)s * width + c]};
+  };
+  // The store above gives thread t channel t; the pool gives it channels 2t
+  // and 2t + 1, written by other threads: make the stores visible first.
+  __syncthreads();
+  pool_norm_rope_store<T>(L, W, b, i, a.comp_cap, i * r, get, red);
+  if (r == 4) {
+    __syncthreads();  // every pool read of slots 0..3 is done
+    for (uint32_t c = threadIdx.x; c < width; c += blockDim.x) {
+#pragma unroll
+      for (int s = 0; s < 4; ++s) {
+        skv[(size_t)s * width + c] = skv[(size_t)(4 + s) * width + c];
+        ssc[(size_t)s * width + c] = ssc[(size_t)(4 + s) * width + c];
+      }
+    }
+  }
+}
+
+// Window slot s of compressed row i, for a chunk that starts at pos0: the
+// token is i*r + s - (W - r); tokens before 0 are empty, tokens of the chunk
+// come from the inputs, earlier ones from the state as it was before the chunk.
+template <typename T>
+struct ChunkSlot {
+  const LaneArgs *L;
+  uint32_t r, W, b, i, pos0, T_len;
+  __device__ SlotVal operator()(uint32_t s, uint32_t c) const {
+    const int64_t tok = (int64_t)i * r + s - (int64_t)(W - r);
+    const uint32_t width = L->width;
+    if (tok < 0) return SlotVal{0.f, -INFINITY};
+    if (tok >= (int64_t)pos0) {
+      const size_t off = ((size_t)b * T_len + (size_t)(tok - pos0)) * width + c;
+      return SlotVal{ld_f32(static_cast<const T *>(L->cand), off),
+                     ld_f32(static_cast<const T *>(L->score), off)};
+    }
+    uint32_t slot;
+    if (r == 4)
+      slot = tok >= (int64_t)(pos0 / 4) * 4 ? 4 + (uint32_t)(tok % 4) : (uint32_t)(tok % 4);
+    else
+      slot = (uint32_t)(tok % r);
+    const size_t off = ((size_t)b * W + slot) * width + c;
+    return SlotVal{L->state_kv[off], L->state_score[off]};
+  }
+};
+
+template <typename T>
+__global__ void __launch_bounds__(kThreads)
+    append_rows_kernel(AppendArgs a, uint32_t n_raw, uint32_t n_emit) {
+  __shared__ float red[32];
+  const uint32_t b = blockIdx.y;
+  uint32_t x = blockIdx.x;
+  if (x < n_raw) {
+    const uint32_t t = (a.direct ? a.T - n_raw : 0) + x;
+    const uint32_t p = a.pos0 + t;
+    const T *src = static_cast<const T *>(a.raw_in) + ((size_t)b * a.T + t) * a.head_dim;
+    T *dst = static_cast<T *>(a.raw_dst) +
+             (a.direct ? ((size_t)b * a.cap_raw + p % a.cap_raw) * a.head_dim
+                       : ((size_t)b * a.T + t) * a.head_dim);
+    raw_row(src, dst, a.head_dim, a.n_rot, p, a.cos, a.sin);
+    return;
+  }
+  x -= n_raw;
+  const uint32_t l = x / n_emit, e = x % n_emit;
+  const LaneArgs &L = a.lane[l];
+  const uint32_t r = a.ratio, i = a.pos0 / r + e;
+  ChunkSlot<T> get{&L, r, a.window, b, i, a.pos0, a.T};
+  pool_norm_rope_store<T>(L, a.window, b, i, a.comp_cap, i * r, get, red);
+}
+
+// State after the chunk, as the token-by-token process leaves it.
+template <typename T>
+__global__ void __launch_bounds__(kThreads) append_state_kernel(AppendArgs a) {
+  const uint32_t b = blockIdx.x;
+  const LaneArgs &L = a.lane[blockIdx.y];
+  const uint32_t r = a.ratio, W = a.window, width = L.width;
+  const uint32_t pos0 = a.pos0, n = a.pos0 + a.T;
+  float *skv = L.state_kv + (size_t)b * W * width;
+  float *ssc = L.state_score + (size_t)b * W * width;
+  const T *cand = static_cast<const T *>(L.cand) + (size_t)b * a.T * width;
+  const T *score = static_cast<const T *>(L.score) + (size_t)b * a.T * width;
+  for (uint32_t c = threadIdx.x; c < width; c += blockDim.x) {
+    if (r == 4) {
+      float nkv[8], nsc[8];
+      bool wr[8];
+#pragma unroll
+      for (int s = 0; s < 8; ++s) wr[s] = false;
+      // slots 4+j: the last chunk token with p % 4 == j
+#pragma unroll
+      for (uint32_t j = 0; j < 4; ++j) {
+        const int64_t tl = (int64_t)n - 1 - (int64_t)((n - 1 + 4 - j) % 4);
+        if (tl >= (int64_t)pos0) {
+          nkv[4 + j] = ld_f32(cand, (size_t)(tl - pos0) * width + c);
+          nsc[4 + j] = ld_f32(score, (size_t)(tl - pos0) * width + c);
+          wr[4 + j] = true;
+        }
+      }
+      // slots 0..3: the group moved there by the last boundary inside the chunk
+      const int64_t pb = (int64_t)(n / 4) * 4 - 1;
+      if (pb >= (int64_t)pos0) {
+#pragma unroll
+        for (uint32_t j = 0; j < 4; ++j) {
+          const int64_t tok = pb - 3 + j;
+          if (tok >= (int64_t)pos0) {
+            nkv[j] = ld_f32(cand, (size_t)(tok - pos0) * width + c);
+            nsc[j] = ld_f32(score, (size_t)(tok - pos0) * width + c);
+          } else {
+            nkv[j] = skv[(size_t)(4 + j) * width + c];
+            nsc[j] = ssc[(size_t)(4 + j) * width + c];
+          }
+          wr[j] = true;
+        }
+      }
+#pragma unroll
+      for (int s = 0; s < 8; ++s)
+        if (wr[s]) {
+          skv[(size_t)s * width + c] = nkv[s];
+          ssc[(size_t)s * width + c] = nsc[s];
+        }
+    } else {
+      for (uint32_t s = 0; s < W; ++s) {
+        const int64_t tl = (int64_t)n - 1 - (int64_t)((n - 1 + W - s % W) % W);
+        if (tl >= (int64_t)pos0) {
+          skv[(size_t)s * width + c] = ld_f32(cand, (size_t)(tl - pos0) * width + c);
+          ssc[(size_t)s * width + c] = ld_f32(score, (size_t)(tl - pos0) * width + c);
+        }
+      }
+    }
+  }
+}
+
+__global__ void state_reset_kernel(float *kv, float *score, size_t n) {
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n;
+       i += (size_t)gridDim.x * blockDim.x) {
+    kv[i] = 0.f;
+    score[i] = -INFINITY;
+  }
+}
+
+template <typename T>
+cudaError_t launch_append_t(const AppendArgs &a, cudaStream_t s) {
+  if (a.T == 1 && a.direct) {
+    append_step_kernel<T><<<dim3(a.batch, 1 + a.n_lanes), kThreads, 0, s>>>(a);
+    note_launches(1);
+    return cudaGetLastError();
+  }
+  const uint32_t n_raw = a.direct ? (a.T < a.cap_raw ? a.T : a.cap_raw) : a.T;
+  const uint32_t n_emit = a.ratio ? (a.pos0 + a.T) / a.ratio - a.pos0 / a.ratio : 0;
+  const uint32_t nblk = n_raw + n_emit * a.n_lanes;
+  if (nblk) {
+    append_rows_kernel<T><<<dim3(nblk, a.batch), kThreads, 0, s>>>(a, n_raw, n_emit ? n_emit : 1);
+    note_launches(1);
+  }
+  if (a.n_lanes) {
+    append_state_kernel<T><<<dim3(a.batch, a.n_lanes), kThreads, 0, s>>>(a);
+    note_launches(1);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_append(const AppendArgs &a, cudaStream_t s) {
+  return a.dtype == DS4A_BF16 ? launch_append_t<__nv_bfloat16>(a, s) : launch_append_t<float>(a, s);
+}
+
+cudaError_t launch_state_reset(float *kv, float *score, size_t n, cudaStream_t s) {
+  if (!n) return cudaSuccess;
+  const int blocks = (int)((n + 255) / 256 < 1184 ? (n + 255) / 256 : 1184);
+  state_reset_kernel<<<blocks, 256, 0, s>>>(kv, score, n);
+  note_launches(1);
+  return cudaGetLastError();
+}
+
+}  // namespace ds4a

@@ -1,0 +1,48 @@
+// Device helpers shared by the ds4a kernels (element access, reductions).
+#pragma once
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "internal.h"
+
+namespace ds4a {
+
+__device__ __forceinline__ float ld_f32(const float *p, size_t i) { return p[i]; }
+__device__ __forceinline__ float ld_f32(const __nv_bfloat16 *p, size_t i) {
+  return __bfloat162float(p[i]);
+}
+__device__ __forceinline__ void st_elem(float *p, size_t i, float v) { p[i] = v; }
+__device__ __forceinline__ void st_elem(__nv_bfloat16 *p, size_t i, float v) {
+  p[i] = __float2bfloat16_rn(v);
+}
+// Round an fp32 value to the storage type and back (exact for fp32).
+__device__ __forceinline__ float round_to(float v, const float *) { return v; }
+__device__ __forceinline__ float round_to(float v, const __nv_bfloat16 *) {
+  return __bfloat162float(__float2bfloat16_rn(v));
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+// Block-wide sum; every thread gets the result. `red` holds >= 32 floats.
+__device__ __forceinline__ float block_sum(float v, float *red) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  const int nw = (blockDim.x + 31) >> 5;
+  v = warp_sum(v);
+  __syncthreads();
+  if (lane == 0) red[wid] = v;
+  __syncthreads();
+  float t = lane < nw ? red[lane] : 0.f;
+  return warp_sum(t);
+}
+
+}  // namespace ds4a

@@ -1,0 +1,85 @@
+// Internal launcher interface between the C ABI layer (api.cu) and the kernel
+// translation units. Arguments have been validated by the caller.
+#pragma once
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "ds4a.h"
+
+namespace ds4a {
+
+// Counts kernel launches (ds4a_launch_count); call once per launch.
+void note_launches(uint32_t n);
+
+// Records a CUDA error for ds4a_last_error and passes it through.
+cudaError_t note_error(cudaError_t e);
+
+// Raise a kernel's dynamic shared memory limit to `bytes` (no-op below 48 KiB
+// or when already raised that far).
+template <typename F>
+cudaError_t ensure_smem(F *func, size_t bytes, int *done) {
+  if (bytes <= 48 * 1024 || (size_t)*done >= bytes) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  if (e == cudaSuccess) *done = (int)bytes;
+  return e;
+}
+
+// One compressor lane (attention or indexer) of a layer.
+struct LaneArgs {
+  uint32_t width, n_rot;
+  void *comp;             // [B][comp_cap][width]
+  float *state_kv, *state_score;  // [B][W][width]
+  const float *cos, *sin; // [max_pos][n_rot/2]
+  const void *cand, *score;       // [B][T][width]
+  const void *ape, *gamma;        // [W][width], [width]
+};
+
+struct AppendArgs {
+  uint32_t ratio, window, batch, cap_raw, comp_cap, head_dim, n_rot, pos0, T;
+  int dtype;
+  const void *raw_in;     // [B][T][D]
+  void *raw_dst;          // ring [B][cap][D] (direct) or chunk [B][T][D]
+  bool direct;            // raw rows go to the ring
+  const float *cos, *sin; // attention-lane / raw-row table
+  int n_lanes;
+  LaneArgs lane[2];
+};
+cudaError_t launch_append(const AppendArgs &a, cudaStream_t s);
+
+struct IndexArgs {
+  uint32_t batch, T, pos0, n_heads, dim, rot, top_k, comp_cap, n_comp;
+  int dtype;
+  const void *q_idx, *w, *keys;   // [B][T][Hi][Di], [B][T][Hi], [B][comp_cap][Di]
+  const float *cos, *sin;
+  int32_t *topk;
+  void *ws;
+  size_t ws_bytes;
+};
+size_t index_ws_bytes(uint32_t batch, uint32_t T, uint32_t n_heads, uint32_t dim,
+                      uint32_t comp_cap);
+cudaError_t launch_index_topk(const IndexArgs &a, cudaStream_t s);
+
+struct AttnArgs {
+  uint32_t ratio, batch, T, pos0, n_heads, head_dim, n_rot, cap_raw, comp_cap, n_comp, top_k;
+  int dtype;
+  float scale;
+  const void *q;          // [B][T][H][D]
+  const void *ring;       // [B][cap][D]
+  const void *chunk;      // [B][T][D] or NULL
+  const void *comp;       // [B][comp_cap][D]
+  const int32_t *topk;    // [B][T][k] or NULL
+  const float *cos, *sin;
+  void *out;              // [B][T][H][D]
+  void *ws;
+  size_t ws_bytes;
+};
+size_t attn_ws_bytes(uint32_t ratio, uint32_t batch, uint32_t T, uint32_t n_heads,
+                     uint32_t head_dim, uint32_t cap_raw, uint32_t comp_cap, uint32_t top_k);
+cudaError_t launch_attention(const AttnArgs &a, cudaStream_t s);
+cudaError_t launch_ring_commit(int dtype, uint32_t batch, uint32_t T, uint32_t pos0,
+                               uint32_t cap_raw, uint32_t head_dim, const void *chunk,
+                               void *ring, cudaStream_t s);
+cudaError_t launch_state_reset(float *kv, float *score, size_t n, cudaStream_t s);
+
+}  // namespace ds4a

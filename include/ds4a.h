@@ -1,0 +1,260 @@
+/*
+ * ds4a — compressed-KV sparse attention layer for NVIDIA GB300 (sm_103a).
+ *
+ * C ABI of libds4a.so. One call per step of the per-layer path an inference
+ * engine runs for every token of a DeepSeek-V4-style model:
+ *
+ *   ds4a_compress_append          raw-window insert + KV compressor
+ *   ds4a_index_topk               ratio-4 indexer scores + exact top-k
+ *   ds4a_sparse_attn_decode       attention of one new token per sequence
+ *   ds4a_sparse_attn_prefill_chunk attention of a chunk of T tokens
+ *
+ * Sources ("page §n" below): "【#3】ds4.c を読み解く" (qiita, DwarfStar series
+ * part 3) and "vLLM DeepSeek V4 サポート: 効率的な長文コンテキスト注意機構"
+ * (section "DeepSeek V4 アテンションアーキテクチャ").
+ *
+ * Conventions for every call:
+ *  - All tensor pointers are caller-owned DEVICE memory unless stated
+ *    otherwise; the library never allocates, frees or synchronises. Calls are
+ *    asynchronous on the given stream (0 = legacy default stream).
+ *  - Arguments are checked on the host before any launch; a failed check
+ *    returns a negative status and launches nothing. A launch error returns
+ *    DS4A_ERR_CUDA (the CUDA error is left for the caller to read).
+ *  - All sequences of a batch are at the same position. ds4a_layer_cache.n_tokens
+ *    is the host-side count of tokens appended so far; ds4a_compress_append
+ *    requires pos0 == n_tokens and advances it, the other calls require the
+ *    tokens they read to have been appended (DS4A_ERR_POSITION otherwise).
+ *  - Row-major layouts, innermost dimension last. Element type of rows,
+ *    inputs and outputs is ds4a_layer_cache.dtype (fp32 or bf16); the
+ *    compressor state is always fp32.
+ *  - Order within a step: append -> index_topk (ratio 4) -> attention.
+ */
+#ifndef DS4A_H
+#define DS4A_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *ds4a_stream_t; /* same as cudaStream_t */
+
+typedef enum {
+  DS4A_OK = 0,
+  DS4A_ERR_ARG = -1,       /* NULL pointer or unsupported parameter value */
+  DS4A_ERR_SHAPE = -2,     /* inconsistent or unsupported sizes */
+  DS4A_ERR_CAPACITY = -3,  /* comp_cap or a table too small for the request */
+  DS4A_ERR_POSITION = -4,  /* pos0 does not match the cache's token count */
+  DS4A_ERR_DTYPE = -5,     /* unknown dtype */
+  DS4A_ERR_CUDA = -6,      /* a CUDA launch or API call failed */
+  DS4A_ERR_TIMEOUT = -7,   /* a bounded device-side wait gave up */
+  DS4A_ERR_WORKSPACE = -8  /* workspace missing or smaller than required */
+} ds4a_status;
+
+typedef enum { DS4A_F32 = 0, DS4A_BF16 = 1 } ds4a_dtype;
+
+/*
+ * One layer's cache for `batch` sequences (page §2, ds4_layer_cache).
+ *
+ *  ratio        0 (raw window only), 4 (c4a) or 128 (c128a) — page §1.
+ *  head_dim     D, the shared K = V head dimension; even, <= 1024.
+ *  n_rot        rotated tail dims of attention rows and queries (page §8: 64);
+ *               even, <= head_dim.
+ *  index_dim    Di, indexer head dim (ratio 4 only; page §6: 128); even, <= 256.
+ *  index_rot    rotated tail dims of indexer rows and queries (min(64, Di)).
+ *  batch        B.
+ *  cap_raw      raw window rows (page §2: 128); row of position p is at slot
+ *               p % cap_raw. 1 <= cap_raw <= 1024.
+ *  comp_cap     compressed rows held per sequence (ratio != 0).
+ *  dtype        ds4a_dtype of rows, inputs and outputs.
+ *  n_tokens     HOST field: tokens appended so far (same for every sequence).
+ *
+ *  raw_kv            [B][cap_raw][D]      rotated raw rows (K = V)
+ *  attn_comp_kv      [B][comp_cap][D]     compressed attention rows
+ *  attn_state_kv     [B][W][D] fp32       W = 8 (ratio 4) or 128 (ratio 128)
+ *  attn_state_score  [B][W][D] fp32       scores WITHOUT the APE bias; -inf = empty
+ *  index_comp_kv     [B][comp_cap][Di]    compressed indexer rows (ratio 4, else NULL)
+ *  index_state_kv    [B][8][Di] fp32
+ *  index_state_score [B][8][Di] fp32
+ *  rope_cos/rope_sin [rope_max_pos][n_rot/2] fp32: this layer's rotation
+ *                    coefficients (ds4a_rope_table), base = compression base on
+ *                    layers with ratio != 0, normal base otherwise (page §8).
+ *  index_rope_cos/sin [rope_max_pos][index_rot/2] fp32 (same base), ratio 4.
+ *  rope_max_pos      rows of the tables; every position used must be below it.
+ *
+ * State layout: ratio 4 keeps the last complete group of 4 tokens in slots
+ * 0..3 and token p of the current group in slot 4 + p % 4 (page §5's 8-row
+ * frontier); ratio 128 keeps token p in slot p % 128. A fresh cache must have
+ * every state score at -inf (ds4a_cache_reset).
+ */
+typedef struct {
+  uint32_t ratio, head_dim, n_rot, index_dim, index_rot, batch, cap_raw, comp_cap;
+  int32_t dtype;
+  uint32_t n_tokens;
+  void *raw_kv;
+  void *attn_comp_kv;
+  float *attn_state_kv, *attn_state_score;
+  void *index_comp_kv;
+  float *index_state_kv, *index_state_score;
+  const float *rope_cos, *rope_sin;
+  const float *index_rope_cos, *index_rope_sin;
+  uint32_t rope_max_pos;
+} ds4a_layer_cache;
+
+/* Workspace selectors for ds4a_workspace_bytes. */
+enum { DS4A_CALL_APPEND = 0, DS4A_CALL_INDEX_TOPK = 1, DS4A_CALL_ATTN_DECODE = 2,
+       DS4A_CALL_ATTN_PREFILL = 3 };
+
+/*
+ * Empty the compressor state (kv 0, score -inf) and set n_tokens = 0. Rows
+ * are left as they are. Asynchronous on `stream`.
+ */
+ds4a_status ds4a_cache_reset(ds4a_layer_cache *cache, ds4a_stream_t stream);
+
+/*
+ * Append tokens pos0 .. pos0+T-1 of every sequence (page §4 compressor steps
+ * 1-7, §5 frontier, §8 tail RoPE; vLLM c4a / c128a window geometry).
+ *
+ *  raw_kv_in    [B][T][D]   projected raw KV row of each token (before RoPE)
+ *  attn_cand    [B][T][D]   compressor KV candidate (wkv output)   } ratio != 0,
+ *  attn_score   [B][T][D]   compressor score (wgate output)        } else NULL
+ *  ape_attn     [W][D]      APE bias, row = slot within the window (0 = oldest)
+ *  gamma_attn   [D]         RMSNorm gain of compressed attention rows
+ *  idx_cand, idx_score [B][T][Di], ape_idx [8][Di], gamma_idx [Di]: the indexer
+ *               lane (ratio 4, else NULL).
+ *  raw_chunk_out NULL: each token's rotated raw row goes into raw_kv at slot
+ *               p % cap_raw (decode). Non-NULL: [B][T][D] receives the rotated
+ *               raw rows and raw_kv is NOT touched; ds4a_sparse_attn_prefill_chunk
+ *               then attends them and writes the last min(T, cap_raw) of them
+ *               into raw_kv (prefill).
+ *
+ * Per token p: raw row = tail-RoPE(raw_kv_in, p). For each lane, the candidate
+ * and score go into the state slot of p; when (p + 1) % ratio == 0 the window
+ * is pooled per channel with weights exp(score + APE - max) (empty slots weigh
+ * 0, an all-empty channel gives 0), RMS-normalised (eps 1e-6) with the gain,
+ * rotated at position i * ratio and stored as compressed row i = (p+1)/ratio - 1;
+ * ratio 4 then moves slots 4..7 to 0..3. Requires pos0 == n_tokens and
+ * (pos0 + T) / ratio <= comp_cap; sets n_tokens = pos0 + T.
+ */
+ds4a_status ds4a_compress_append(ds4a_layer_cache *cache, uint32_t pos0, uint32_t T,
+                                 const void *raw_kv_in, const void *attn_cand,
+                                 const void *attn_score, const void *ape_attn,
+                                 const void *gamma_attn, const void *idx_cand,
+                                 const void *idx_score, const void *ape_idx,
+                                 const void *gamma_idx, void *raw_chunk_out,
+                                 ds4a_stream_t stream);
+
+/*
+ * Indexer top-k for queries at positions pos0 .. pos0+T-1 (ratio 4 only;
+ * page §6 indexer, §7 visible rows; vLLM DSA).
+ *
+ *  q_idx   [B][T][Hi][Di]  indexer queries before RoPE (dtype)
+ *  w       [B][T][Hi]      per-head weights (dtype)
+ *  n_heads Hi (1..128), top_k k (1..2048)
+ *  topk    [B][T][k] int32 out: for the query at p, the k rows s < floor((p+1)/4)
+ *          with the largest score I = sum_h w_h * ReLU(q'_h . k_s), ties to the
+ *          lower index, in ascending order, padded with -1 when fewer are visible.
+ *  ws      workspace of ds4a_workspace_bytes(DS4A_CALL_INDEX_TOPK, ...) bytes.
+ *
+ * q' = tail rotation of q_idx at p, computed in fp32 (one rounding per
+ * operation) and rounded to dtype. The selection is exact with respect to the
+ * fp32 score defined by: dot_h accumulated in ascending d with separately
+ * rounded products and sums, ReLU to +0, then w_h * relu_h summed in ascending
+ * h from +0. Requires pos0 + T <= n_tokens.
+ */
+ds4a_status ds4a_index_topk(const ds4a_layer_cache *cache, uint32_t pos0, uint32_t T,
+                            const void *q_idx, const void *w, uint32_t n_heads,
+                            uint32_t top_k, int32_t *topk, void *ws, size_t ws_bytes,
+                            ds4a_stream_t stream);
+
+/*
+ * Attention of the token at position pos of every sequence (page §7 mixed
+ * attention; vLLM shared K = V, inverse RoPE, 128-token window).
+ *
+ *  q       [B][H][D]  queries before RoPE (dtype); n_heads = H (1..128)
+ *  topk    [B][top_k] int32 compressed rows to attend (ratio 4): entries < 0 are
+ *          skipped and the list ends at the first entry >= floor((pos+1)/4).
+ *          Ignored (may be NULL) on ratio 0 and 128 layers: ratio 128 attends
+ *          every visible row s < floor((pos+1)/128), ratio 0 none.
+ *  scale   softmax scale (1/sqrt(D) is the usual choice)
+ *  out     [B][H][D] (dtype): softmax over the raw rows of positions
+ *          max(0, pos-cap_raw+1)..pos plus the compressed rows, V = K, with the
+ *          output tail rotated back by -pos.
+ *  ws      ds4a_workspace_bytes(DS4A_CALL_ATTN_DECODE, ...) bytes.
+ * Requires pos + 1 == n_tokens (the token has been appended).
+ */
+ds4a_status ds4a_sparse_attn_decode(const ds4a_layer_cache *cache, uint32_t pos,
+                                    const void *q, uint32_t n_heads, const int32_t *topk,
+                                    uint32_t top_k, float scale, void *out, void *ws,
+                                    size_t ws_bytes, ds4a_stream_t stream);
+
+/*
+ * Attention of a prefill chunk, queries at pos0 .. pos0+T-1, then the raw
+ * window commit (page §3: chunked prefill keeps absolute positions).
+ *
+ *  q         [B][T][H][D] queries before RoPE
+ *  raw_chunk [B][T][D] the rotated raw rows ds4a_compress_append wrote to its
+ *            raw_chunk_out for the same tokens
+ *  topk      [B][T][top_k] (ratio 4) as for decode, per query
+ *  out       [B][T][H][D]
+ * The raw window of query p spans positions max(0, p-cap_raw+1)..p: rows before
+ * pos0 come from raw_kv (still as it was before the chunk), the rest from
+ * raw_chunk. Compressed rows visible to p are s < floor((p+1)/ratio). After the
+ * attention, the last min(T, cap_raw) chunk rows are written to raw_kv.
+ * Requires pos0 + T == n_tokens.
+ */
+ds4a_status ds4a_sparse_attn_prefill_chunk(ds4a_layer_cache *cache, uint32_t pos0, uint32_t T,
+                                           const void *q, uint32_t n_heads,
+                                           const void *raw_chunk, const int32_t *topk,
+                                           uint32_t top_k, float scale, void *out, void *ws,
+                                           size_t ws_bytes, ds4a_stream_t stream);
+
+/* Workspace bytes a call needs for these sizes (0: none). */
+size_t ds4a_workspace_bytes(int call, const ds4a_layer_cache *cache, uint32_t T,
+                            uint32_t n_heads, uint32_t top_k);
+
+/*
+ * Host helper: rotation coefficients for positions 0..n_pos-1 into HOST arrays
+ * cos_out/sin_out [n_pos][n_rot/2]: theta_i = base^(-2i/n_rot), angle p*theta_i,
+ * all in fp64, cos and sin then rounded to fp32 (page §8 tail-only RoPE; the
+ * fp64 angle keeps positions up to 1M exact to fp32 resolution).
+ */
+ds4a_status ds4a_rope_table(double base, uint32_t n_rot, uint32_t n_pos, float *cos_out,
+                            float *sin_out);
+
+/*
+ * KV-cache bytes of one layer holding ctx tokens for `batch` sequences: the raw
+ * window min(128, ctx) rows plus floor(ctx / ratio) compressed rows (c4a rows
+ * also carry the indexer row), elem_bytes per element. Summed over the Pro
+ * schedule (61 layers, D 512, Di 128, bf16) at 1M tokens this is the vLLM
+ * page's 9.62 GiB. The compressor state is not included.
+ */
+uint64_t ds4a_cache_bytes(uint32_t ratio, uint32_t head_dim, uint32_t index_dim, uint64_t ctx,
+                          uint32_t batch, uint32_t elem_bytes);
+
+/* Page §1 schedule: variant 0 = Flash (layers 0-1 ratio 0), 1 = Pro (layers
+ * 0-1 ratio 128); then even layers 4, odd layers 128. */
+uint32_t ds4a_layer_compress_ratio(int variant, uint32_t il);
+
+/* Page §3: largest prefill chunk for a prompt (4096 beyond 4096 tokens, else 0
+ * = the whole prompt at once). */
+uint32_t ds4a_prefill_chunk_cap(uint32_t prompt_len);
+
+const char *ds4a_status_string(ds4a_status status);
+
+/* Diagnostic: kernel launches this library has enqueued in this process so
+ * far (all threads, all streams; a launch captured into a CUDA graph counts
+ * once, at capture). */
+uint64_t ds4a_launch_count(void);
+
+/* Diagnostic: text of the last CUDA error a call of this library returned
+ * DS4A_ERR_CUDA for ("no error" if none). */
+const char *ds4a_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DS4A_H */

@@ -14,19 +14,26 @@ Readings (the pages do not give them):
   angle at p ~ 1.3e5 would be off by ~1e-2 rad);
 * the indexer rotates min(64, Di) tail dims of its rows and queries.
 """
+import math
+
 import numpy as np
+
+_cos = np.vectorize(math.cos, otypes=[np.float64])
+_sin = np.vectorize(math.sin, otypes=[np.float64])
 
 
 def inv_freq(base: float, n_rot: int) -> np.ndarray:
-    i = np.arange(n_rot // 2, dtype=np.float64)
-    return np.power(np.float64(base), -2.0 * i / n_rot)
+    """theta_i = base^(-2i / n_rot), fp64 (C library pow)."""
+    return np.array([math.pow(base, -2.0 * i / n_rot) for i in range(n_rot // 2)])
 
 
 def rope_coeffs(pos, base: float, n_rot: int):
-    """fp32 cos / sin of p * theta_i, shape pos.shape + (n_rot/2,), as float32."""
+    """fp32 cos / sin of p * theta_i, shape pos.shape + (n_rot/2,), as float32.
+    The angle is one fp64 product; cos and sin are the C library's fp64
+    functions (argument reduction included), each rounded once to fp32."""
     pos = np.asarray(pos, dtype=np.float64)
     ang = pos[..., None] * inv_freq(base, n_rot)
-    return np.cos(ang).astype(np.float32), np.sin(ang).astype(np.float32)
+    return _cos(ang).astype(np.float32), _sin(ang).astype(np.float32)
 
 
 def rope_tail(x, pos, base: float, n_rot: int, inverse: bool = False) -> np.ndarray:

@@ -1,0 +1,140 @@
+"""The C ABI without a GPU: the library loads, exports every function the
+header declares, its host helpers agree with the oracle, and argument checks
+reject bad calls before any launch (host-side fault handling)."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+from compressed_kv_sparse_gb300 import lib
+from oracle import rope, schedule
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(__file__)), "include", "ds4a.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    if not os.path.exists(lib.LIB_PATH):
+        import __graft_entry__
+        __graft_entry__.build()
+    return lib.load()
+
+
+def declared():
+    src = open(HEADER).read()
+    return sorted(set(re.findall(r"^[a-z_0-9 \*]*?\b(ds4a_[a-z_0-9]+)\s*\(", src, re.M)))
+
+
+def test_exports_every_declared_symbol(L):
+    names = declared()
+    assert set(names) == set(lib.EXPORTS)
+    for n in names:
+        assert hasattr(L, n), n
+        assert n in lib.EXPORTS, f"binding does not declare {n}"
+
+
+def test_schedule_and_chunk_cap_match_oracle(L):
+    for variant in (0, 1):
+        for il in range(64):
+            assert L.ds4a_layer_compress_ratio(variant, il) == \
+                schedule.layer_compress_ratio(variant, il)
+    for n in (1, 4096, 4097, 28672, 100000):
+        assert L.ds4a_prefill_chunk_cap(n) == schedule.prefill_chunk_cap(n)
+
+
+def test_cache_bytes_match_oracle_and_page(L):
+    ctx = 1 << 20
+    tot = sum(L.ds4a_cache_bytes(schedule.layer_compress_ratio(1, il), 512, 128, ctx, 1, 2)
+              for il in range(61))
+    assert round(tot / 2**30, 2) == 9.62
+    for ratio in (0, 4, 128):
+        for c in (5, 127, 65536, 131072):
+            assert L.ds4a_cache_bytes(ratio, 512, 128, c, 3, 2) == \
+                schedule.kv_cache_bytes(ratio, 512, 128, c, 3, 2)
+
+
+def test_rope_table_bitwise_equal_to_oracle(L):
+    for base, n_rot in ((10000.0, 64), (160000.0, 64), (160000.0, 32)):
+        n_pos = 2000
+        c = np.empty((n_pos, n_rot // 2), np.float32)
+        s = np.empty((n_pos, n_rot // 2), np.float32)
+        assert L.ds4a_rope_table(base, n_rot, n_pos, c.ctypes.data, s.ctypes.data) == 0
+        pos = np.concatenate([np.arange(n_pos)])
+        oc, os_ = rope.rope_coeffs(pos, base, n_rot)
+        assert np.array_equal(c, oc) and np.array_equal(s, os_)
+    # large positions (the 131,072-token workloads)
+    n_pos = 131073
+    c = np.empty((n_pos, 32), np.float32)
+    s = np.empty((n_pos, 32), np.float32)
+    L.ds4a_rope_table(160000.0, 64, n_pos, c.ctypes.data, s.ctypes.data)
+    idx = np.array([65535, 65536, 100003, 131071, 131072])
+    oc, os_ = rope.rope_coeffs(idx, 160000.0, 64)
+    assert np.array_equal(c[idx], oc) and np.array_equal(s[idx], os_)
+
+
+def test_status_strings(L):
+    for st in range(0, -9, -1):
+        assert L.ds4a_status_string(st).decode() == lib.STATUS[st]
+
+
+def _fake_cache(ratio=4, n_tokens=10, dtype=lib.DS4A_BF16):
+    """A struct with non-NULL fake device pointers: only ever read by the host
+    checks below, which return before touching them."""
+    fake = 0x1000
+    return lib.LayerCacheC(ratio=ratio, head_dim=512, n_rot=64, index_dim=128, index_rot=64,
+                           batch=2, cap_raw=128, comp_cap=16, dtype=dtype, n_tokens=n_tokens,
+                           raw_kv=fake, attn_comp_kv=fake, attn_state_kv=fake,
+                           attn_state_score=fake, index_comp_kv=fake, index_state_kv=fake,
+                           index_state_score=fake, rope_cos=fake, rope_sin=fake,
+                           index_rope_cos=fake, index_rope_sin=fake, rope_max_pos=1000)
+
+
+def test_argument_checks_reject_before_launch(L):
+    fake = 0x1000
+    c = _fake_cache()
+    r = ctypes.byref(c)
+    P = [fake] * 9
+    # wrong position: the cache holds 10 tokens
+    assert L.ds4a_compress_append(r, 9, 1, *P, None, None) == -4
+    # capacity: 16 compressed rows hold 64 tokens of ratio 4
+    assert L.ds4a_compress_append(r, 10, 60, *P, None, None) == -3
+    # rope table too short
+    c.comp_cap = 10**6
+    assert L.ds4a_compress_append(r, 10, 991, *P, None, None) == -3
+    c.comp_cap = 16
+    # missing lane inputs
+    assert L.ds4a_compress_append(r, 10, 1, fake, None, fake, fake, fake, fake, fake, fake, fake,
+                                  None, None) == -1
+    assert c.n_tokens == 10        # nothing advanced
+    # bad dtype / ratio / shapes
+    bad = _fake_cache(dtype=7)
+    assert L.ds4a_compress_append(ctypes.byref(bad), 10, 1, *P, None, None) == -5
+    bad = _fake_cache(ratio=8)
+    assert L.ds4a_compress_append(ctypes.byref(bad), 10, 1, *P, None, None) == -1
+    bad = _fake_cache()
+    bad.n_rot = 1000
+    assert L.ds4a_compress_append(ctypes.byref(bad), 10, 1, *P, None, None) == -2
+    # index: reads beyond the appended tokens, workspace too small, bad ratio
+    assert L.ds4a_index_topk(r, 10, 1, fake, fake, 64, 512, fake, fake, 1 << 30, None) == -4
+    assert L.ds4a_index_topk(r, 9, 1, fake, fake, 64, 512, fake, fake, 16, None) == -8
+    assert L.ds4a_index_topk(r, 9, 1, fake, fake, 64, 0, fake, fake, 1 << 30, None) == -2
+    c128 = _fake_cache(ratio=128)
+    assert L.ds4a_index_topk(ctypes.byref(c128), 9, 1, fake, fake, 64, 512, fake, fake,
+                             1 << 30, None) == -1
+    # attention: position, missing top-k on a ratio-4 layer, workspace
+    assert L.ds4a_sparse_attn_decode(r, 8, fake, 64, fake, 512, 0.1, fake, fake, 1 << 30,
+                                     None) == -4
+    assert L.ds4a_sparse_attn_decode(r, 9, fake, 64, None, 512, 0.1, fake, fake, 1 << 30,
+                                     None) == -1
+    need = L.ds4a_workspace_bytes(lib.CALL_ATTN_DECODE, r, 1, 64, 512)
+    assert need > 0
+    assert L.ds4a_sparse_attn_decode(r, 9, fake, 64, fake, 512, 0.1, fake, fake, need - 1,
+                                     None) == -8
+    assert L.ds4a_sparse_attn_prefill_chunk(r, 0, 5, fake, 64, None, fake, 512, 0.1, fake,
+                                            fake, 1 << 30, None) == -1
+    assert L.ds4a_sparse_attn_prefill_chunk(r, 0, 5, fake, 64, fake, fake, 512, 0.1, fake,
+                                            fake, 1 << 30, None) == -4
+    assert L.ds4a_sparse_attn_decode(None, 9, fake, 64, fake, 512, 0.1, fake, fake, 1 << 30,
+                                     None) == -1
