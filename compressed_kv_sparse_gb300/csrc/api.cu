@@ -184,7 +184,7 @@ size_t ds4a_workspace_bytes(int call, const ds4a_layer_cache *c, uint32_t T, uin
   if (!c) return 0;
   switch (call) {
     case DS4A_CALL_INDEX_TOPK:
-      return index_ws_bytes(c->batch, T, n_heads, c->index_dim, c->comp_cap);
+      return index_ws_bytes(c->dtype, c->batch, T, n_heads, c->index_dim, c->comp_cap);
     case DS4A_CALL_ATTN_DECODE:
       return attn_ws_bytes(c->ratio, c->batch, 1, n_heads, c->head_dim, c->cap_raw, c->comp_cap,
                            top_k);
@@ -208,7 +208,7 @@ ds4a_status ds4a_index_topk(const ds4a_layer_cache *c, uint32_t pos0, uint32_t T
   const uint32_t Hp = (n_heads + 7u) & ~7u;
   if (((size_t)c->index_dim * Hp + Hp + 128 * (size_t)(c->index_dim + 1)) * 4 > 227 * 1024)
     return DS4A_ERR_SHAPE;
-  const size_t need = index_ws_bytes(c->batch, T, n_heads, c->index_dim, c->comp_cap);
+  const size_t need = index_ws_bytes(c->dtype, c->batch, T, n_heads, c->index_dim, c->comp_cap);
   if (!ws || ws_bytes < need) return DS4A_ERR_WORKSPACE;
   IndexArgs a;
   a.batch = c->batch;

@@ -1,0 +1,336 @@
+// Indexer scores on the tensor cores (bf16 layers): approximate fp32 scores
+// plus the per-row key norms that bound their error ("【#3】ds4.c を読み解く"
+// §6 indexer; vLLM DeepSeek V4 page, DSA).
+//
+// For every visible compressed index row s of sequence b and every query t of
+// a group of QG queries:  S~(t, s) = sum_h w_h(t) * max(0, q'_h(t) . k_s).
+// The dot products are one tcgen05 MMA per 128-row tile: A = 128 key rows
+// (M = 128, K = Di = 128, TMA-loaded with the 128-byte swizzle), B = the QG x 64
+// rotated query heads (N = 64 QG); the fp32 accumulator sits in TMEM (two
+// buffers so the epilogue of one tile overlaps the MMA of the next). Each
+// epilogue thread owns one TMEM lane = one key row: it reads its QG x 64 head
+// dots, applies ReLU and the head weights, and also sums the squares of its
+// key row straight from the swizzled shared-memory tile (the error bound of
+// the certified top-k uses ||k_s||).
+//
+// Persistent kernel, one CTA per SM, 6 warps: warp 0 issues TMA, warp 1 issues
+// MMAs (one thread each), warps 2..5 run the epilogue. Work items are
+// (sequence, query group, 128-row tile), split into contiguous ranges so the
+// B operand (the query group's heads) is reloaded only when the group changes.
+// Every wait is bounded (tc.cuh); on a timeout the kernel sets *err and winds
+// down, still freeing its TMEM.
+#include <cuda_bf16.h>
+
+#include "common.cuh"
+#include "tc.cuh"
+
+namespace ds4a {
+namespace {
+
+constexpr int kRows = 128;         // key rows per tile (MMA M)
+constexpr int kDim = 128;          // Di (MMA K)
+constexpr int kHeads = 64;         // Hi
+constexpr int kKBlockBytes = kRows * 128;          // one 64-column K block of A
+constexpr int kABytes = 2 * kKBlockBytes;          // 32 KiB per A stage
+constexpr int kThreads = 192;
+
+template <int QG>
+struct Cfg {
+  static constexpr int N = kHeads * QG;
+  static constexpr int kStages = QG == 1 ? 6 : 4;
+  static constexpr int kBBytes = N * kDim * 2;
+  static constexpr int kTmemCols = QG == 1 ? 128 : 512;
+  static constexpr size_t kSmem = 1024 + (size_t)kStages * kABytes + kBBytes + 1024 +
+                                  4 * QG * kHeads * 4;
+};
+
+struct ScoreParams {
+  uint32_t batch, T, pos0, comp_cap, n_comp, n_groups, tiles_per, total_items;
+  const __nv_bfloat16 *w;   // [B][T][Hi]
+  float *scores;            // [B][T][comp_cap]
+  float *norms;             // [B][comp_cap]
+  int *err;
+};
+
+__device__ __forceinline__ uint32_t vis_of(const ScoreParams &P, uint32_t t) {
+  return min((P.pos0 + t + 1) / 4, P.n_comp);
+}
+
+template <int QG>
+__device__ __forceinline__ bool decode_item(const ScoreParams &P, uint32_t item, uint32_t &b,
+                                            uint32_t &g, uint32_t &tile) {
+  tile = item % P.tiles_per;
+  const uint32_t rest = item / P.tiles_per;
+  g = rest % P.n_groups;
+  b = rest / P.n_groups;
+  const uint32_t last = min(P.T, (g + 1) * QG) - 1;
+  return tile * kRows < vis_of(P, last);   // false: every row of the tile is invisible
+}
+
+template <int QG>
+__global__ void __launch_bounds__(kThreads, 1)
+    index_score_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
+                          const __grid_constant__ CUtensorMap tmap_q, ScoreParams P) {
+  using C = Cfg<QG>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+  uint8_t *sA = smem;                                   // [stages][32 KiB]
+  uint8_t *sB = sA + (size_t)C::kStages * kABytes;       // [2 K blocks][N][64] bf16
+  uint64_t *bars = reinterpret_cast<uint64_t *>(sB + C::kBBytes);
+  uint64_t *a_full = bars, *a_empty = bars + C::kStages;
+  uint64_t *acc_full = a_empty + C::kStages, *acc_empty = acc_full + 2;
+  uint64_t *b_full = acc_empty + 2, *b_empty = b_full + 1;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(b_empty + 1);
+  float *sw_all = reinterpret_cast<float *>(sB + C::kBBytes + 1024);   // [4 warps][QG][64]
+
+  const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t per = (P.total_items + gridDim.x - 1) / gridDim.x;
+  const uint32_t it0 = blockIdx.x * per;
+  const uint32_t it1 = min(P.total_items, it0 + per);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(&a_full[s], 1);
+      mbar_init(&a_empty[s], 1 + 4);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&acc_full[s], 1);
+      mbar_init(&acc_empty[s], 4);
+    }
+    mbar_init(b_full, 1);
+    mbar_init(b_empty, 1);
+    fence_mbar_init();
+    prefetch_tmap(&tmap_k);
+    prefetch_tmap(&tmap_q);
+  }
+  if (warp == 1) tmem_alloc(tmem_slot, C::kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------- TMA producer
+      uint32_t stage = 0, phase = 0, b_phase = 0;
+      int32_t cur = -1;
+      int issued[C::kStages];
+      for (int s = 0; s < C::kStages; ++s) issued[s] = -1;
+      for (uint32_t it = it0; it < it1; ++it) {
+        uint32_t b, g, tile;
+        if (!decode_item<QG>(P, it, b, g, tile)) continue;
+        const int32_t bg = (int32_t)(b * P.n_groups + g);
+        if (bg != cur) {
+          if (cur >= 0) {
+            if (!mbar_wait(b_empty, b_phase, P.err)) break;
+            b_phase ^= 1;
+          }
+          mbar_arrive_expect_tx(b_full, C::kBBytes);
+          const int row0 = (int)((b * P.T + g * QG) * kHeads);
+          tma_load_2d(sB, &tmap_q, b_full, 0, row0);
+          tma_load_2d(sB + C::kBBytes / 2, &tmap_q, b_full, 64, row0);
+          cur = bg;
+        }
+        if (!mbar_wait(&a_empty[stage], phase ^ 1, P.err)) break;
+        mbar_arrive_expect_tx(&a_full[stage], kABytes);
+        tma_load_3d(sA + (size_t)stage * kABytes, &tmap_k, &a_full[stage], 0, (int)(tile * kRows),
+                    (int)b);
+        tma_load_3d(sA + (size_t)stage * kABytes + kKBlockBytes, &tmap_k, &a_full[stage], 64,
+                    (int)(tile * kRows), (int)b);
+        issued[stage] = (int)phase;
+        if (++stage == C::kStages) {
+          stage = 0;
+          phase ^= 1;
+        }
+      }
+      // let every load this CTA issued land before the CTA can exit
+      for (int s = 0; s < C::kStages; ++s) {
+        if (issued[s] < 0) continue;
+        const uint64_t t0 = global_ns();
+        while (!mbar_try_wait(&a_full[s], (uint32_t)issued[s]) &&
+               global_ns() - t0 < kWaitLimitNs) {
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------- MMA issuer
+      constexpr uint32_t idesc = idesc_bf16_f32(kRows, C::N);
+      uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0, bf_phase = 0;
+      int32_t cur = -1;
+      const uint32_t a_base = smem_u32(sA), b_base = smem_u32(sB);
+      for (uint32_t it = it0; it < it1; ++it) {
+        uint32_t b, g, tile;
+        if (!decode_item<QG>(P, it, b, g, tile)) continue;
+        const int32_t bg = (int32_t)(b * P.n_groups + g);
+        if (bg != cur) {
+          if (cur >= 0) mma_commit(b_empty);
+          if (!mbar_wait(b_full, bf_phase, P.err)) break;
+          bf_phase ^= 1;
+          cur = bg;
+        }
+        if (!mbar_wait(&acc_empty[acc], acc_phase ^ 1, P.err)) break;
+        if (!mbar_wait(&a_full[stage], phase, P.err)) break;
+        tc_fence_after();
+        const uint32_t d = tmem + acc * C::N;
+        const uint32_t a0 = a_base + stage * kABytes;
+#pragma unroll
+        for (uint32_t kk = 0; kk < kDim / 16; ++kk) {
+          const uint32_t koff = (kk % 4) * 32;   // 16 bf16 = 32 B inside a swizzle row
+          const uint64_t ad = sdesc_sw128(a0 + (kk / 4) * kKBlockBytes + koff);
+          const uint64_t bd = sdesc_sw128(b_base + (kk / 4) * (C::kBBytes / 2) + koff);
+          mma_bf16(d, ad, bd, idesc, kk > 0 ? 1u : 0u);
+        }
+        mma_commit(&a_empty[stage]);
+        mma_commit(&acc_full[acc]);
+        if (++stage == C::kStages) {
+          stage = 0;
+          phase ^= 1;
+        }
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1;
+      }
+    }
+  } else {
+    // ---------------- epilogue: warps 2..5, TMEM lanes 32 * (warp % 4) ..
+    const uint32_t lg = warp & 3;
+    const uint32_t row = lg * 32 + lane;
+    float *sw = sw_all + (warp - 2) * QG * kHeads;   // this warp's copy of the weights
+    uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
+    int32_t cur = -1;
+    bool ok = true;
+    for (uint32_t it = it0; it < it1 && ok; ++it) {
+      uint32_t b, g, tile;
+      if (!decode_item<QG>(P, it, b, g, tile)) continue;
+      const int32_t bg = (int32_t)(b * P.n_groups + g);
+      if (bg != cur) {
+        __syncwarp();
+        for (uint32_t i = lane; i < QG * kHeads; i += 32) {
+          const uint32_t t = g * QG + i / kHeads;
+          sw[i] = t < P.T ? __bfloat162float(P.w[((size_t)b * P.T + t) * kHeads + i % kHeads])
+                          : 0.f;
+        }
+        __syncwarp();
+        cur = bg;
+      }
+      // key-row norm from the swizzled tile: the row's two 128-byte lines hold
+      // its 128 values (chunk order permuted, which a sum of squares ignores)
+      if (!mbar_wait(&a_full[stage], phase, P.err)) {
+        ok = false;
+        break;
+      }
+      float ss = 0.f;
+      {
+        const uint8_t *tileA = sA + (size_t)stage * kABytes;
+#pragma unroll
+        for (int kb = 0; kb < 2; ++kb) {
+          const uint8_t *line = tileA + kb * kKBlockBytes + (row >> 3) * 1024 + (row & 7) * 128;
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const uint4 v = *reinterpret_cast<const uint4 *>(line + ((j + row) & 7) * 16);
+            const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float lo = __uint_as_float(w4[e] << 16);
+              const float hi = __uint_as_float(w4[e] & 0xFFFF0000u);
+              ss = fmaf(lo, lo, ss);
+              ss = fmaf(hi, hi, ss);
+            }
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&a_empty[stage]);
+      if (++stage == C::kStages) {
+        stage = 0;
+        phase ^= 1;
+      }
+      if (!mbar_wait(&acc_full[acc], acc_phase, P.err)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t grow = tile * kRows + row;
+#pragma unroll 1
+      for (int q = 0; q < QG; ++q) {
+        uint32_t r0[32], r1[32];
+        const uint32_t taddr = tmem + ((lg * 32) << 16) + acc * C::N + q * kHeads;
+        tmem_ld32(taddr, r0);
+        tmem_ld32(taddr + 32, r1);
+        tmem_ld_wait();
+        const float *wq = sw + q * kHeads;
+        float s = 0.f;
+#pragma unroll
+        for (int h = 0; h < 32; ++h) s = fmaf(wq[h], fmaxf(__uint_as_float(r0[h]), 0.f), s);
+#pragma unroll
+        for (int h = 0; h < 32; ++h) s = fmaf(wq[32 + h], fmaxf(__uint_as_float(r1[h]), 0.f), s);
+        const uint32_t t = g * QG + q;
+        if (t < P.T && grow < vis_of(P, t))
+          P.scores[((size_t)b * P.T + t) * P.comp_cap + grow] = s;
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acc_empty[acc]);
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1;
+      // the first query group that processes this tile writes its norms
+      const bool first = g == 0 || tile * kRows >= vis_of(P, g * QG - 1);
+      if (first && grow < P.n_comp) P.norms[(size_t)b * P.comp_cap + grow] = sqrtf(ss);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, C::kTmemCols);
+}
+
+template <int QG>
+cudaError_t launch_qg(const IndexTcArgs &a, cudaStream_t s) {
+  using C = Cfg<QG>;
+  CUtensorMap tk, tq;
+  const uint64_t kd[3] = {kDim, a.comp_cap, a.batch};
+  const uint64_t ks[2] = {(uint64_t)kDim * 2, (uint64_t)a.comp_cap * kDim * 2};
+  const uint32_t kb[3] = {64, kRows, 1};
+  cudaError_t e = make_tmap_bf16(&tk, a.keys, 3, kd, ks, kb);
+  if (e != cudaSuccess) return e;
+  const uint64_t qd[2] = {kDim, (uint64_t)a.batch * a.T * kHeads};
+  const uint64_t qs[1] = {(uint64_t)kDim * 2};
+  const uint32_t qb[2] = {64, (uint32_t)C::N};
+  e = make_tmap_bf16(&tq, a.qbf, 2, qd, qs, qb);
+  if (e != cudaSuccess) return e;
+  ScoreParams P;
+  P.batch = a.batch;
+  P.T = a.T;
+  P.pos0 = a.pos0;
+  P.comp_cap = a.comp_cap;
+  P.n_comp = a.n_comp;
+  P.n_groups = (a.T + QG - 1) / QG;
+  const uint32_t vis_max = min((a.pos0 + a.T) / 4, a.n_comp);
+  P.tiles_per = (vis_max + kRows - 1) / kRows;
+  P.total_items = a.batch * P.n_groups * P.tiles_per;
+  P.w = static_cast<const __nv_bfloat16 *>(a.w);
+  P.scores = a.scores;
+  P.norms = a.norms;
+  P.err = a.err;
+  if (P.total_items == 0) return cudaSuccess;
+  static int smem_set = 0;
+  e = ensure_smem(index_score_tc_kernel<QG>, C::kSmem, &smem_set);
+  if (e != cudaSuccess) return e;
+  const uint32_t grid = min(P.total_items, (uint32_t)num_sms());
+  index_score_tc_kernel<QG><<<grid, kThreads, C::kSmem, s>>>(tk, tq, P);
+  note_launches(1);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+bool index_tc_supported(uint32_t n_heads, uint32_t dim) {
+  return n_heads == kHeads && dim == kDim;
+}
+
+cudaError_t launch_index_score_tc(const IndexTcArgs &a, cudaStream_t s) {
+  return a.T >= 4 ? launch_qg<4>(a, s) : launch_qg<1>(a, s);
+}
+
+}  // namespace ds4a

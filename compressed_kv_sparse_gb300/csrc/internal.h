@@ -1,6 +1,7 @@
 // Internal launcher interface between the C ABI layer (api.cu) and the kernel
 // translation units. Arguments have been validated by the caller.
 #pragma once
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -24,6 +25,11 @@ cudaError_t ensure_smem(F *func, size_t bytes, int *done) {
   if (e == cudaSuccess) *done = (int)bytes;
   return e;
 }
+
+// TMA tensor map over bf16 data with 128-byte swizzle (tmap.cu).
+cudaError_t make_tmap_bf16(CUtensorMap *map, const void *base, int rank, const uint64_t *dims,
+                           const uint64_t *strides_bytes, const uint32_t *box);
+int num_sms();
 
 // One compressor lane (attention or indexer) of a layer.
 struct LaneArgs {
@@ -56,8 +62,21 @@ struct IndexArgs {
   void *ws;
   size_t ws_bytes;
 };
-size_t index_ws_bytes(uint32_t batch, uint32_t T, uint32_t n_heads, uint32_t dim,
+size_t index_ws_bytes(int dtype, uint32_t batch, uint32_t T, uint32_t n_heads, uint32_t dim,
                       uint32_t comp_cap);
+
+// Tensor-core scorer of bf16 layers (indexer_tc.cu).
+struct IndexTcArgs {
+  uint32_t batch, T, pos0, comp_cap, n_comp;
+  const void *keys;   // [B][comp_cap][128] bf16
+  const void *qbf;    // [B][T][64][128] bf16, rotated queries
+  const void *w;      // [B][T][64] bf16
+  float *scores;      // [B][T][comp_cap]
+  float *norms;       // [B][comp_cap]
+  int *err;
+};
+bool index_tc_supported(uint32_t n_heads, uint32_t dim);
+cudaError_t launch_index_score_tc(const IndexTcArgs &a, cudaStream_t s);
 cudaError_t launch_index_topk(const IndexArgs &a, cudaStream_t s);
 
 struct AttnArgs {

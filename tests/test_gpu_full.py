@@ -1,0 +1,115 @@
+"""GPU parity at the full workload sizes, in the launch configuration the
+benchmark uses, on outputs the oracle can compute one by one (sampled
+sequences / queries), plus the tensor-core indexer path on ragged and tied
+inputs."""
+import numpy as np
+import pytest
+import torch
+
+import synth
+from helpers import TOL, gpu_cache, np_, oracle_cache, rel_l2
+from oracle import layer as olayer
+from test_gpu_parity import lib_, run_attn, run_index
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def test_index_tc_prefill_ragged():
+    """Flash indexer shape, 37 queries (not a multiple of the 4-query MMA
+    group), visible counts above k, two sequences."""
+    run_index(lib_(), synth.LayerShape(ratio=4), 2, 3001, 37, seed=31)
+
+
+def test_index_tc_grid_ties():
+    """Flash indexer shape on 1/8-grid inputs: many exact ties at the cut."""
+    run_index(lib_(), synth.LayerShape(ratio=4), 2, 4000, 6, seed=32, grid=True)
+
+
+def test_index_tc_prefill_visibility_edges():
+    """Chunk starting below 4 k (some queries see <= k rows, the rest more)."""
+    run_index(lib_(), synth.LayerShape(ratio=4), 1, 2030, 40, seed=33)
+
+
+def test_c4a_decode_full_size_sampled():
+    """32 sequences at 65,536 tokens (16,384 rows each): exact top-k and
+    attention for sampled sequences."""
+    lib = lib_()
+    wl = synth.C4A_DECODE
+    s = wl.layers[0]
+    B, p = wl.batch, wl.context
+    cap = (p + 1) // 4 + 1
+    hist = synth.cache_history(wl, 0, p, comp_cap=cap, device=DEV)
+    inp = {k: v.contiguous() for k, v in synth.step_inputs(wl, 0, p, 1, device=DEV).items()}
+    gc = gpu_cache(s, B, cap, p + 2, hist, p)
+    lib.ds4a_compress_append(gc, p, 1, inp)
+    k = s.top_k
+    topk = torch.empty((B, k), dtype=torch.int32, device=DEV)
+    ws = lib.workspace(gc.workspace_bytes(lib.CALL_INDEX_TOPK, 1, s.index_heads, k))
+    lib.ds4a_index_topk(gc, p, 1, inp["q_idx"], inp["w"], s.index_heads, k, topk, ws)
+    out = torch.empty((B, s.n_heads, s.head_dim), dtype=torch.bfloat16, device=DEV)
+    wa = lib.workspace(gc.workspace_bytes(lib.CALL_ATTN_DECODE, 1, s.n_heads, k))
+    lib.ds4a_sparse_attn_decode(gc, p, inp["q"][:, 0].contiguous(), s.n_heads, topk, k,
+                                1 / np.sqrt(s.head_dim), out, wa)
+    torch.cuda.synchronize()
+    for b in (0, 13, 31):
+        one = {n: t[b:b + 1].cpu() for n, t in hist.items()}
+        oc = oracle_cache(s, one, p)
+        o_ref, tk_ref = olayer.decode_step(oc, p, {n: np_(t[b:b + 1]) if t.dim() > 2 else np_(t)
+                                                   for n, t in inp.items()}, k)
+        assert np.array_equal(topk[b].cpu().numpy(), tk_ref[0]), b
+        assert rel_l2(np_(out[b]), o_ref[0]) <= TOL["bf16"], b
+
+
+def test_c4a_prefill_full_size_sampled():
+    """One 4096-token chunk at 28,672 over a 28,672-token cache: exact top-k
+    and attention for sampled queries (first, boundary, middle, last)."""
+    lib = lib_()
+    wl = synth.C4A_PREFILL
+    s = wl.layers[0]
+    p0, T = wl.context, wl.chunk
+    cap = (p0 + T) // 4 + 1
+    hist = synth.cache_history(wl, 0, p0, comp_cap=cap, device=DEV)
+    inp = {k: v.contiguous() for k, v in synth.step_inputs(wl, 0, p0, T, device=DEV).items()}
+    gc = gpu_cache(s, 1, cap, p0 + T + 1, hist, p0)
+    ring0 = gc.raw_kv.clone()
+    chunk = torch.empty((1, T, s.head_dim), dtype=torch.bfloat16, device=DEV)
+    lib.ds4a_compress_append(gc, p0, T, inp, raw_chunk_out=chunk)
+    k = s.top_k
+    topk = torch.empty((1, T, k), dtype=torch.int32, device=DEV)
+    ws = lib.workspace(gc.workspace_bytes(lib.CALL_INDEX_TOPK, T, s.index_heads, k))
+    lib.ds4a_index_topk(gc, p0, T, inp["q_idx"], inp["w"], s.index_heads, k, topk, ws)
+    out = torch.empty((1, T, s.n_heads, s.head_dim), dtype=torch.bfloat16, device=DEV)
+    wa = lib.workspace(gc.workspace_bytes(lib.CALL_ATTN_PREFILL, T, s.n_heads, k))
+    lib.ds4a_sparse_attn_prefill_chunk(gc, p0, T, inp["q"], s.n_heads, chunk, topk, k,
+                                       1 / np.sqrt(s.head_dim), out, wa)
+    torch.cuda.synchronize()
+    # the oracle on the same chunk: compressor over the whole chunk, then samples
+    oc = oracle_cache(s, {n: t.cpu() for n, t in hist.items()}, p0)
+    ninp = {n: np_(t) for n, t in inp.items()}
+    rows = olayer.compress_append(oc, p0, ninp, chunk=True)
+    assert rel_l2(np_(chunk), rows) <= TOL["bf16"]
+    assert oc.n_comp == 8192 and gc.n_tokens == p0 + T
+    assert rel_l2(np_(gc.attn_comp_kv)[:, 7168:8192], oc.attn_comp_kv[:, 7168:8192]) <= TOL["bf16"]
+    qs = [(0, t) for t in (0, 1, 2, 3, 4, 127, 128, 1000, 2047, 4092, 4094, 4095)]
+    tk_ref = olayer.index_topk(oc, p0, ninp["q_idx"], ninp["w"], k, queries=qs)
+    got_tk = topk.cpu().numpy()
+    for b, t in qs:
+        assert np.array_equal(got_tk[b, t], tk_ref[b, t]), t
+    o_ref = olayer.attention(oc, p0, ninp["q"], tk_ref, None, ring=np_(ring0), chunk_rows=rows,
+                             queries=qs)
+    got = np.stack([np_(out[b, t]) for b, t in qs])
+    ref = np.stack([o_ref[b, t] for b, t in qs])
+    assert rel_l2(got, ref) <= TOL["bf16"]
+
+
+def test_c128a_decode_full_size():
+    """One sequence at 65,536 tokens on a ratio-128 layer: 128 window rows plus
+    all 512 compressed rows."""
+    run_attn(lib_(), synth.LayerShape(ratio=128), 1, 65536, 1, 65536, seed=41)
+
+
+def test_c4a_decode_attn_b32():
+    """Attention with random top-k lists at the 32-sequence decode shape."""
+    run_attn(lib_(), synth.LayerShape(ratio=4), 32, 65536, 1, 65536, seed=42,
+             queries=[(0, 0), (17, 0), (31, 0)])
