@@ -66,6 +66,9 @@ EXPORTS = {
                                                       ctypes.c_float, ctypes.c_void_p,
                                                       ctypes.c_void_p, ctypes.c_size_t,
                                                       ctypes.c_void_p]),
+    "ds4a_index_topk_noalloc": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_uint32, ctypes.c_uint32,
+                                               ctypes.c_void_p, ctypes.c_void_p, ctypes.c_uint32,
+                                               ctypes.c_uint32, ctypes.c_void_p, ctypes.c_void_p]),
     "ds4a_workspace_bytes": (ctypes.c_size_t, [ctypes.c_int, ctypes.c_void_p, ctypes.c_uint32,
                                                ctypes.c_uint32, ctypes.c_uint32]),
     "ds4a_rope_table": (ctypes.c_int, [ctypes.c_double, ctypes.c_uint32, ctypes.c_uint32,
@@ -224,6 +227,18 @@ def ds4a_index_topk(cache: LayerCache, pos0: int, T: int, q_idx: torch.Tensor, w
     _check(load().ds4a_index_topk(cache.ref(), pos0, T, _ptr(q_idx), _ptr(w), n_heads, top_k,
                                   _ptr(topk), _ptr(ws), ws.numel() * ws.element_size(),
                                   _stream(stream)), "ds4a_index_topk")
+
+
+STATIC_SCRATCH_BYTES = 8 << 20
+
+
+def ds4a_index_topk_noalloc(cache: LayerCache, pos0: int, T: int, q_idx: torch.Tensor,
+                            w: torch.Tensor, n_heads: int, top_k: int, topk: torch.Tensor,
+                            stream=None):
+    """ds4a_index_topk with the library's static scratch instead of a workspace."""
+    _check(load().ds4a_index_topk_noalloc(cache.ref(), pos0, T, _ptr(q_idx), _ptr(w), n_heads,
+                                          top_k, _ptr(topk), _stream(stream)),
+           "ds4a_index_topk_noalloc")
 
 
 def ds4a_sparse_attn_decode(cache: LayerCache, pos: int, q: torch.Tensor, n_heads: int,

@@ -211,6 +211,37 @@ ds4a_status ds4a_sparse_attn_prefill_chunk(ds4a_layer_cache *cache, uint32_t pos
                                            uint32_t top_k, float scale, void *out, void *ws,
                                            size_t ws_bytes, ds4a_stream_t stream);
 
+/*
+ * ds4a_index_topk for callers that cannot allocate device memory (the pages
+ * describe no such entry point; it has no counterpart in the method).
+ *
+ * Some callers of this library cannot call cudaMalloc: a host program that
+ * links the C ABI without any device allocator of its own, code running
+ * inside another runtime that owns all device memory through a fixed pool, or
+ * a serving loop that must not take cudaMalloc's implicit device-wide
+ * synchronisation in the middle of a step. This call takes the same
+ * arguments as ds4a_index_topk minus the workspace and uses a scratch area of
+ * DS4A_STATIC_SCRATCH_BYTES that lives inside the library as a static device
+ * array. Every GPU that loads the library holds that array until the process
+ * exits.
+ *
+ *  - The caller still passes (and owns) every input and output.
+ *  - The first call on a device, with that device current, looks up the
+ *    array's device address (cudaGetSymbolAddress); make that first call
+ *    before any stream capture.
+ *  - Requests whose ds4a_workspace_bytes(DS4A_CALL_INDEX_TOPK, ...) exceeds
+ *    DS4A_STATIC_SCRATCH_BYTES return DS4A_ERR_WORKSPACE and launch nothing.
+ *  - The call allocates nothing and frees nothing.
+ *  - All calls share the one array, which keeps the previous call's contents
+ *    (everything the call reads back is written first within the call). Calls
+ *    that overlap on the GPU (different streams without ordering between
+ *    them) race on it: order them.
+ */
+#define DS4A_STATIC_SCRATCH_BYTES (8u << 20)
+ds4a_status ds4a_index_topk_noalloc(const ds4a_layer_cache *cache, uint32_t pos0, uint32_t T,
+                                    const void *q_idx, const void *w, uint32_t n_heads,
+                                    uint32_t top_k, int32_t *topk, ds4a_stream_t stream);
+
 /* Workspace bytes a call needs for these sizes (0: none). */
 size_t ds4a_workspace_bytes(int call, const ds4a_layer_cache *cache, uint32_t T,
                             uint32_t n_heads, uint32_t top_k);
