@@ -186,11 +186,11 @@ size_t ds4a_workspace_bytes(int call, const ds4a_layer_cache *c, uint32_t T, uin
     case DS4A_CALL_INDEX_TOPK:
       return index_ws_bytes(c->dtype, c->batch, T, n_heads, c->index_dim, c->comp_cap);
     case DS4A_CALL_ATTN_DECODE:
-      return attn_ws_bytes(c->ratio, c->batch, 1, n_heads, c->head_dim, c->cap_raw, c->comp_cap,
-                           top_k);
+      return attn_ws_bytes(c->dtype, c->ratio, c->batch, 1, n_heads, c->head_dim, c->n_rot,
+                           c->cap_raw, c->comp_cap, c->ratio == 4 ? top_k : 0);
     case DS4A_CALL_ATTN_PREFILL:
-      return attn_ws_bytes(c->ratio, c->batch, T, n_heads, c->head_dim, c->cap_raw, c->comp_cap,
-                           top_k);
+      return attn_ws_bytes(c->dtype, c->ratio, c->batch, T, n_heads, c->head_dim, c->n_rot,
+                           c->cap_raw, c->comp_cap, c->ratio == 4 ? top_k : 0);
     default:
       return 0;
   }
@@ -240,8 +240,8 @@ static ds4a_status attn_common(const ds4a_layer_cache *c, uint32_t pos0, uint32_
   if (!q || !out) return DS4A_ERR_ARG;
   if (!std::isfinite(scale)) return DS4A_ERR_ARG;
   if (c->ratio == 4 && (!topk || top_k == 0 || top_k > 2048)) return DS4A_ERR_ARG;
-  const size_t need = attn_ws_bytes(c->ratio, c->batch, T, n_heads, c->head_dim, c->cap_raw,
-                                    c->comp_cap, c->ratio == 4 ? top_k : 0);
+  const size_t need = attn_ws_bytes(c->dtype, c->ratio, c->batch, T, n_heads, c->head_dim,
+                                    c->n_rot, c->cap_raw, c->comp_cap, c->ratio == 4 ? top_k : 0);
   if (need && (!ws || ws_bytes < need)) return DS4A_ERR_WORKSPACE;
   AttnArgs a;
   a.ratio = c->ratio;

@@ -93,9 +93,15 @@ struct AttnArgs {
   void *ws;
   size_t ws_bytes;
 };
-size_t attn_ws_bytes(uint32_t ratio, uint32_t batch, uint32_t T, uint32_t n_heads,
-                     uint32_t head_dim, uint32_t cap_raw, uint32_t comp_cap, uint32_t top_k);
+size_t attn_ws_bytes(int dtype, uint32_t ratio, uint32_t batch, uint32_t T, uint32_t n_heads,
+                     uint32_t head_dim, uint32_t n_rot, uint32_t cap_raw, uint32_t comp_cap,
+                     uint32_t top_k);
 cudaError_t launch_attention(const AttnArgs &a, cudaStream_t s);
+
+// Tensor-core attention (attention_tc.cu): bf16, 64 heads x 512 dims, 64-dim tail.
+bool attn_tc_supported(int dtype, uint32_t H, uint32_t D, uint32_t n_rot);
+uint32_t attn_tc_splits(uint32_t T, uint32_t rows_max);
+cudaError_t launch_attention_tc(const AttnArgs &a, uint32_t rows_max, int *err, cudaStream_t s);
 cudaError_t launch_ring_commit(int dtype, uint32_t batch, uint32_t T, uint32_t pos0,
                                uint32_t cap_raw, uint32_t head_dim, const void *chunk,
                                void *ring, cudaStream_t s);

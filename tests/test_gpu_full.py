@@ -113,3 +113,24 @@ def test_c4a_decode_attn_b32():
     """Attention with random top-k lists at the 32-sequence decode shape."""
     run_attn(lib_(), synth.LayerShape(ratio=4), 32, 65536, 1, 65536, seed=42,
              queries=[(0, 0), (17, 0), (31, 0)])
+
+
+@pytest.mark.parametrize("ratio,p0,T", [(4, 300, 50), (128, 1000, 70), (0, 60, 100), (4, 0, 40)])
+def test_attn_tc_prefill(ratio, p0, T):
+    """Tensor-core chunk attention (64 heads x 512): window across the old ring
+    and the chunk, padded / ending top-k lists, ring commit."""
+    run_attn(lib_(), synth.LayerShape(ratio=ratio), 2, p0, T, p0, topk_mode="pad", seed=43)
+
+
+@pytest.mark.parametrize("ratio,p0,T", [(4, 700, 20), (128, 5000, 3)])
+def test_attn_tc_prefill_running_max_raised(ratio, p0, T):
+    """Scale 1.0 spreads the scores over hundreds of units, so later rows
+    exceed the first row's score by far more than 2^8: the running max must be
+    raised and the partial output and sums rescaled."""
+    run_attn(lib_(), synth.LayerShape(ratio=ratio), 2, p0, T, p0, seed=44, scale=1.0)
+
+
+@pytest.mark.parametrize("ratio,p", [(4, 900), (128, 65536), (0, 40)])
+def test_attn_tc_decode_running_max_raised(ratio, p):
+    run_attn(lib_(), synth.LayerShape(ratio=ratio), 3, p, 1, p, topk_mode="pad", seed=45,
+             scale=1.0)

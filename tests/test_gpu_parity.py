@@ -171,7 +171,8 @@ def test_index_flash_shape_decode():
 
 # ------------------------------------------------------------------ attention
 
-def run_attn(lib, shape, B, p0, T, n_hist, topk_mode="random", seed=21, queries=None):
+def run_attn(lib, shape, B, p0, T, n_hist, topk_mode="random", seed=21, queries=None,
+             scale=None):
     wl = synth.Workload("att", seed, B, (shape,), n_hist, "prefill")
     r = shape.ratio
     cap = max(1, (p0 + T) // r) if r else 0
@@ -191,7 +192,7 @@ def run_attn(lib, shape, B, p0, T, n_hist, topk_mode="random", seed=21, queries=
             topk[..., -3:] = vis + 5
     gc = gpu_cache(shape, B, cap, p0 + T + 1, hist, p0 + T)
     out = torch.empty((B, T, shape.n_heads, shape.head_dim), dtype=gc.torch_dtype, device=DEV)
-    scale = 1.0 / np.sqrt(shape.head_dim)
+    scale = 1.0 / np.sqrt(shape.head_dim) if scale is None else scale
     tk_dev = topk.to(DEV) if topk is not None else None
     if T == 1 and chunk is None:
         ws = lib.workspace(gc.workspace_bytes(lib.CALL_ATTN_DECODE, 1, shape.n_heads, k))
