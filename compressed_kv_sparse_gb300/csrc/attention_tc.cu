@@ -54,7 +54,7 @@ struct Smem {
   uint8_t p[kRows * 128];   // 16 KiB
   uint64_t kv_full[8], kv_empty[8];
   uint64_t q_full, q_empty, s_full, p_full, p_empty, o_full, o_empty, sm_bar, ld_bar;
-  float mref[kH], alpha[kH], lsh[kH];
+  float mref[kH], alpha[kH], lsh[kH], linv[kH];
   float tmax[4][kH], lpart[4][kH];
   uint32_t first_row, flagcnt[3], tmem;
 };
@@ -76,13 +76,23 @@ __device__ __forceinline__ QueryGeo query_geo(const TcAttnParams &P, uint32_t it
   g.n_list = 0;
   if (P.ratio == 4) {
     const uint32_t vis = min((g.p + 1) / 4, P.n_comp);
+    // the list ends at its first entry >= vis; 8 independent loads per round
     g.n_list = P.top_k;
-    for (uint32_t base = 0; base < P.top_k; base += 32) {
-      const uint32_t j = base + lane;
-      const int32_t v = j < P.top_k ? g.tk[j] : -1;
-      const uint32_t bal = __ballot_sync(0xffffffffu, v >= 0 && (uint32_t)v >= vis);
-      if (bal) {
-        g.n_list = base + __ffs(bal) - 1;
+    for (uint32_t base = 0; base < P.top_k; base += 256) {
+      int32_t v[8];
+#pragma unroll
+      for (uint32_t i = 0; i < 8; ++i) {
+        const uint32_t j = base + 32 * i + lane;
+        v[i] = j < P.top_k ? g.tk[j] : -1;
+      }
+      uint32_t found = 0xffffffffu;
+#pragma unroll
+      for (uint32_t i = 0; i < 8; ++i) {
+        const uint32_t bal = __ballot_sync(0xffffffffu, v[i] >= 0 && (uint32_t)v[i] >= vis);
+        if (bal && found == 0xffffffffu) found = base + 32 * i + __ffs(bal) - 1;
+      }
+      if (found != 0xffffffffu) {
+        g.n_list = found;
         break;
       }
     }
@@ -148,16 +158,50 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(TcAttnParams P) {
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = S.tmem;
-  const uint32_t tmS = tmem, tmO = tmem + 256;
+  // TMEM columns: S^T 0..63, row sums L 64..127, an all-ones bf16 A operand
+  // 128..159 (L = ones x P^T), O^T 256..511
+  const uint32_t tmS = tmem, tmL = tmem + 64, tmOnes = tmem + 128, tmO = tmem + 256;
+  if (warp < 4) {
+    uint32_t ones[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) ones[i] = 0x3F803F80u;   // two bf16 1.0
+    tmem_st32(tmOnes + ((warp * 32) << 16), ones);
+    tmem_st_wait();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
 
   if (warp >= 4 && warp < 8) {
     // ------------------------------------------------------------ loaders
     const uint32_t lt = threadIdx.x - 128, lw = warp - 4;
     uint32_t n = 0, qn = 0, ld_phase = 0;
+    // issue all eight 64-dim blocks of a tile (one cp.async group each) as
+    // their slots free up; rows of this lane: lw*32 + lane/8 + 4i, chunk lane%8
+    auto issue_tile = [&](const QueryGeo &g, uint32_t tile, uint32_t n) -> bool {
+      const __nv_bfloat16 *src[8];
+#pragma unroll
+      for (uint32_t i = 0; i < 8; ++i)
+        src[i] = row_src(P, g, tile * kRows + lw * 32 + (lane >> 3) + 4 * i);
+      const uint32_t cc = lane & 7;
+      for (uint32_t kb = 0; kb < 8; ++kb) {
+        if (!mbar_wait_warp(&S.kv_empty[kb], (n & 1) ^ 1, P.err)) return false;
+        uint8_t *slot = S.kv + kb * kKBlk;
+#pragma unroll
+        for (uint32_t i = 0; i < 8; ++i) {
+          const uint32_t r = lw * 32 + (lane >> 3) + 4 * i;
+          uint8_t *dst = slot + (r >> 3) * 1024 + (r & 7) * 128 + ((cc ^ (r & 7)) << 4);
+          const __nv_bfloat16 *sp = src[i] ? src[i] + kb * 64 + cc * 8 : P.ring;
+          cp_async16(dst, sp, src[i] ? 16u : 0u);
+        }
+        asm volatile("cp.async.commit_group;" ::: "memory");
+      }
+      return true;
+    };
     for (uint32_t item = blockIdx.x; item < P.n_items; item += gridDim.x) {
       const QueryGeo g = query_geo(P, item, lane);
       if (g.t0 >= g.t1) continue;
-      if (!mbar_wait(&S.q_empty, (qn & 1) ^ 1, P.err)) goto done_loader;
+      if (!mbar_wait_warp(&S.q_empty, (qn & 1) ^ 1, P.err)) goto done_loader;
       {
         // Q: warp lw loads heads 16 lw .. 16 lw + 15, two half rows per head
         const __nv_bfloat16 *q = P.q + (size_t)g.qi * kH * kD;
@@ -171,7 +215,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(TcAttnParams P) {
             cp_async16(dst, q + (size_t)h * kD + ch * 8, 16);
           }
         }
-        cp_async_wait_all();
+        asm volatile("cp.async.commit_group;" ::: "memory");
+        // the first tile's rows start loading before Q is rotated
+        if (!issue_tile(g, g.t0, n)) goto done_loader;
+        asm volatile("cp.async.wait_group 8;" ::: "memory");   // Q landed
         if (!group_sync(&S.ld_bar, ld_phase, P.err)) goto done_loader;
         // rotate the tail (dims 448..511 = block 7) at position p, in place
 #pragma unroll
@@ -193,32 +240,20 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(TcAttnParams P) {
         mbar_arrive(&S.q_full);
       }
       for (uint32_t tile = g.t0; tile < g.t1; ++tile, ++n) {
-        // rows of this lane: lw*32 + lane/8 + 4i (i < 8), chunk lane % 8
-        const __nv_bfloat16 *src[8];
-#pragma unroll
-        for (uint32_t i = 0; i < 8; ++i)
-          src[i] = row_src(P, g, tile * kRows + lw * 32 + (lane >> 3) + 4 * i);
-        const uint32_t cc = lane & 7;
-        for (uint32_t kb = 0; kb < 8; ++kb) {
-          if (!mbar_wait(&S.kv_empty[kb], (n & 1) ^ 1, P.err)) goto done_loader;
-          uint8_t *slot = S.kv + kb * kKBlk;
-#pragma unroll
-          for (uint32_t i = 0; i < 8; ++i) {
-            const uint32_t r = lw * 32 + (lane >> 3) + 4 * i;
-            uint8_t *dst = slot + (r >> 3) * 1024 + (r & 7) * 128 + ((cc ^ (r & 7)) << 4);
-            const __nv_bfloat16 *s = src[i] ? src[i] + kb * 64 + cc * 8 : P.ring;
-            cp_async16(dst, s, src[i] ? 16u : 0u);
-          }
-          asm volatile("cp.async.commit_group;" ::: "memory");
-          if (kb > 0) {
-            asm volatile("cp.async.wait_group 1;" ::: "memory");
-            fence_proxy_async();
-            mbar_arrive(&S.kv_full[kb - 1]);
-          }
-        }
-        cp_async_wait_all();
-        fence_proxy_async();
-        mbar_arrive(&S.kv_full[7]);
+        if (tile != g.t0 && !issue_tile(g, tile, n)) goto done_loader;
+#define DS4A_KV_LANDED(NPEND, KB)                                   \
+  asm volatile("cp.async.wait_group " #NPEND ";" ::: "memory");     \
+  fence_proxy_async();                                              \
+  mbar_arrive(&S.kv_full[KB]);
+        DS4A_KV_LANDED(7, 0)
+        DS4A_KV_LANDED(6, 1)
+        DS4A_KV_LANDED(5, 2)
+        DS4A_KV_LANDED(4, 3)
+        DS4A_KV_LANDED(3, 4)
+        DS4A_KV_LANDED(2, 5)
+        DS4A_KV_LANDED(1, 6)
+        DS4A_KV_LANDED(0, 7)
+#undef DS4A_KV_LANDED
       }
       ++qn;
     }
@@ -265,6 +300,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(TcAttnParams P) {
             mma_commit(&S.kv_empty[2 * m]);
             mma_commit(&S.kv_empty[2 * m + 1]);
           }
+          // per-head row sums of P on the tensor core: every row of L = 1^T P^T
+          constexpr uint32_t idL = idesc_bf16_f32(kRows, kH) | kIdescMajorB_MN;
+#pragma unroll
+          for (uint32_t kk = 0; kk < 8; ++kk)
+            mma_bf16_ta(tmL, tmOnes, sdesc_sw128_mn(p_base + kk * 2048, 8192, 1024), idL,
+                        (first && kk == 0) ? 0u : 1u);
           mma_commit(&S.p_empty);
           if (last) mma_commit(&S.o_full);
         }
@@ -278,27 +319,52 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(TcAttnParams P) {
     const uint32_t r = threadIdx.x;          // tile row / TMEM lane, then dim within a block
     const uint32_t lane_base = (warp * 32) << 16;
     uint32_t n = 0, qn = 0, sm_phase = 0;
+    // P row r from the scores in TMEM with the current running maxima;
+    // returns whether a score exceeds its head's maximum by more than 2^8
+    auto write_p = [&](bool valid) {
+      bool flag = false;
+      uint8_t *prow = S.p + (r >> 3) * 1024 + (r & 7) * 128;
+#pragma unroll
+      for (uint32_t hf = 0; hf < 2; ++hf) {
+        uint32_t a[32];
+        tmem_ld32(tmS + lane_base + 32 * hf, a);
+        tmem_ld_wait();
+#pragma unroll
+        for (uint32_t c4 = 0; c4 < 4; ++c4) {
+          uint32_t w4[4];
+#pragma unroll
+          for (uint32_t e = 0; e < 4; ++e) {
+            const uint32_t hl = 8 * c4 + 2 * e, h = 32 * hf + hl;
+            const float t0 = fmaf(__uint_as_float(a[hl]), P.c2, -S.mref[h]);
+            const float t1 = fmaf(__uint_as_float(a[hl + 1]), P.c2, -S.mref[h + 1]);
+            flag |= valid && (t0 > kRaiseLog2 || t1 > kRaiseLog2);
+            w4[e] = valid ? pack_bf16(ex2_approx(t0), ex2_approx(t1)) : 0u;
+          }
+          *reinterpret_cast<uint4 *>(prow + (((4 * hf + c4) ^ (r & 7)) << 4)) =
+              make_uint4(w4[0], w4[1], w4[2], w4[3]);
+        }
+      }
+      return flag;
+    };
     for (uint32_t item = blockIdx.x; item < P.n_items; item += gridDim.x) {
       const QueryGeo g = query_geo(P, item, lane);
       const bool has_tiles = g.t0 < g.t1;
-      float lsum[kH];
-#pragma unroll
-      for (int h = 0; h < kH; ++h) lsum[h] = 0.f;
       bool any_valid = false;
       for (uint32_t tile = g.t0; tile < g.t1; ++tile, ++n) {
         const bool first = tile == g.t0;
         const uint32_t row = tile * kRows + r;
         bool valid = row < g.n_w;
         if (!valid && row < g.N) valid = P.ratio != 4 || g.tk[row - g.n_w] >= 0;
-        if (!mbar_wait(&S.s_full, n & 1, P.err)) goto done_softmax;
+        if (!mbar_wait_warp(&S.s_full, n & 1, P.err)) goto done_softmax;
         tc_fence_after();
-        // scores are re-read from TMEM per 32-head half instead of being kept
         if (first) {
+          // running maxima start at the scores of the first valid row
           if (r == 0) S.first_row = kNoRow;
           if (!group_sync(&S.sm_bar, sm_phase, P.err)) goto done_softmax;
           if (valid) atomicMin(&S.first_row, r);
           if (!group_sync(&S.sm_bar, sm_phase, P.err)) goto done_softmax;
           const uint32_t fr = S.first_row;
+          // (tcgen05.ld is warp-collective: every lane loads, one lane keeps)
 #pragma unroll 1
           for (uint32_t hf = 0; hf < 2; ++hf) {
             uint32_t a[32];
@@ -307,33 +373,25 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(TcAttnParams P) {
             if (fr == r) {
 #pragma unroll
               for (int h = 0; h < 32; ++h) S.mref[32 * hf + h] = __uint_as_float(a[h]) * P.c2;
-            } else if (fr == kNoRow && r == 0) {
-#pragma unroll
-              for (int h = 0; h < 32; ++h) S.mref[32 * hf + h] = 0.f;
             }
+          }
+          if (fr == kNoRow && r == 0) {
+#pragma unroll
+            for (int h = 0; h < kH; ++h) S.mref[h] = 0.f;
           }
           any_valid = fr != kNoRow;
           if (!group_sync(&S.sm_bar, sm_phase, P.err)) goto done_softmax;
         }
-        // does any score exceed its head's running max by more than 2^8?
-        bool flag = false;
-#pragma unroll 1
-        for (uint32_t hf = 0; hf < 2; ++hf) {
-          uint32_t a[32];
-          tmem_ld32(tmS + lane_base + 32 * hf, a);
-          tmem_ld_wait();
-          if (valid) {
-#pragma unroll
-            for (int h = 0; h < 32; ++h)
-              flag |= fmaf(__uint_as_float(a[h]), P.c2, -S.mref[32 * hf + h]) > kRaiseLog2;
-          }
-        }
+        // P of this tile (the previous PV must be done with the buffer)
+        if (!mbar_wait_warp(&S.p_empty, (n & 1) ^ 1, P.err)) goto done_softmax;
+        const bool flag = write_p(valid);
         const uint32_t fc = n % 3;
         if (r == 0) S.flagcnt[(n + 1) % 3] = 0;
         if (flag) atomicAdd(&S.flagcnt[fc], 1u);
         if (!group_sync(&S.sm_bar, sm_phase, P.err)) goto done_softmax;
         if (S.flagcnt[fc] != 0) {
           // rare path: exact tile max per head, raise the running max, rescale
+          // O and L, rewrite P
 #pragma unroll 1
           for (uint32_t hf = 0; hf < 2; ++hf) {
             uint32_t a[32];
@@ -353,15 +411,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(TcAttnParams P) {
             S.mref[r] = mn;
           }
           if (!group_sync(&S.sm_bar, sm_phase, P.err)) goto done_softmax;
-#pragma unroll
-          for (int h = 0; h < kH; ++h) lsum[h] *= S.alpha[h];
           if (!first) {
-            if (!mbar_wait(&S.p_empty, (n & 1) ^ 1, P.err)) goto done_softmax;
-            tc_fence_after();
 #pragma unroll 1
-            for (uint32_t m = 0; m < 8; ++m) {
+            for (uint32_t m = 0; m < 10; ++m) {   // O^T (8 x 32 columns) then L (2 x 32)
               uint32_t a[32];
-              const uint32_t ta = tmO + lane_base + m * 32;   // block m / 2, heads 32 (m % 2) ..
+              const uint32_t ta = (m < 8 ? tmO + m * 32 : tmL + (m - 8) * 32) + lane_base;
               tmem_ld32(ta, a);
               tmem_ld_wait();
 #pragma unroll
@@ -371,56 +425,39 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(TcAttnParams P) {
             }
             tmem_st_wait();
           }
-        }
-        // probabilities (bf16) into P, row r, 8 chunks of 8 heads
-        if (!mbar_wait(&S.p_empty, (n & 1) ^ 1, P.err)) goto done_softmax;
-        {
-          uint8_t *prow = S.p + (r >> 3) * 1024 + (r & 7) * 128;
-#pragma unroll
-          for (uint32_t hf = 0; hf < 2; ++hf) {
-            uint32_t a[32];
-            tmem_ld32(tmS + lane_base + 32 * hf, a);
-            tmem_ld_wait();
-#pragma unroll
-            for (uint32_t c4 = 0; c4 < 4; ++c4) {
-              const uint32_t c = 4 * hf + c4;
-              uint32_t w4[4];
-#pragma unroll
-              for (uint32_t e = 0; e < 4; ++e) {
-                const uint32_t hl = 8 * c4 + 2 * e, h = 32 * hf + hl;
-                float p0 = 0.f, p1 = 0.f;
-                if (valid) {
-                  p0 = exp2f(fmaf(__uint_as_float(a[hl]), P.c2, -S.mref[h]));
-                  p1 = exp2f(fmaf(__uint_as_float(a[hl + 1]), P.c2, -S.mref[h + 1]));
-                }
-                w4[e] = pack_bf16(p0, p1);
-                lsum[h] += bf16lo(w4[e]);
-                lsum[h + 1] += bf16hi(w4[e]);
-              }
-              *reinterpret_cast<uint4 *>(prow + ((c ^ (r & 7)) << 4)) =
-                  make_uint4(w4[0], w4[1], w4[2], w4[3]);
-            }
-          }
+          write_p(valid);
         }
         fence_proxy_async();
         tc_fence_before();
         mbar_arrive(&S.p_full);
       }
-      // ---- item end: per-head sums, then the output
-#pragma unroll
-      for (int h = 0; h < kH; ++h) {
-        const float v = warp_sum(lsum[h]);
-        if (lane == (uint32_t)(h & 31)) S.lpart[warp][h] = v;
-      }
-      if (!group_sync(&S.sm_bar, sm_phase, P.err)) goto done_softmax;
-      if (r < kH) S.lsh[r] = (S.lpart[0][r] + S.lpart[1][r]) + (S.lpart[2][r] + S.lpart[3][r]);
-      if (!group_sync(&S.sm_bar, sm_phase, P.err)) goto done_softmax;
+      // ---- item end: per-head sums (any lane of L), then the output
       {
         const bool final_out = P.n_splits == 1;
         if (has_tiles) {
-          if (!mbar_wait(&S.o_full, qn & 1, P.err)) goto done_softmax;
+          if (!mbar_wait_warp(&S.o_full, qn & 1, P.err)) goto done_softmax;
           tc_fence_after();
+          if (warp == 0) {   // every row of L holds the sums; warp 0 loads, lane 0 keeps
+#pragma unroll 1
+            for (uint32_t hf = 0; hf < 2; ++hf) {
+              uint32_t a[32];
+              tmem_ld32(tmL + lane_base + 32 * hf, a);
+              tmem_ld_wait();
+              if (lane == 0) {
+#pragma unroll
+                for (int h = 0; h < 32; ++h) {
+                  const float l = __uint_as_float(a[h]);
+                  S.lsh[32 * hf + h] = l;
+                  S.linv[32 * hf + h] = __frcp_rn(l);
+                }
+              }
+            }
+          }
+        } else if (r < kH) {
+          S.lsh[r] = 0.f;
+          S.linv[r] = 0.f;
         }
+        if (!group_sync(&S.sm_bar, sm_phase, P.err)) goto done_softmax;
         float co = 1.f, si = 0.f;
 #pragma unroll 1
         for (uint32_t m = 0; m < 4; ++m) {
@@ -443,13 +480,19 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(TcAttnParams P) {
             }
             if (final_out) {
               __nv_bfloat16 *o = P.out + (size_t)g.qi * kH * kD + (size_t)(32 * hf) * kD + d;
+              if (m == 3 && r >= 64) {   // warp-uniform: the rotated tail dims
 #pragma unroll
-              for (int h = 0; h < 32; ++h) {
-                float v = __uint_as_float(a[h]) / S.lsh[32 * hf + h];
-                const float other = __shfl_xor_sync(0xffffffffu, v, 1);
-                // rotate back by -p: (x0, x1) -> (x0 c + x1 s, -x0 s + x1 c)
-                if (tail) v = (d & 1) ? (v * co - other * si) : (v * co + other * si);
-                o[(size_t)h * kD] = __float2bfloat16_rn(v);
+                for (int h = 0; h < 32; ++h) {
+                  float v = __uint_as_float(a[h]) * S.linv[32 * hf + h];
+                  const float other = __shfl_xor_sync(0xffffffffu, v, 1);
+                  // rotate back by -p: (x0, x1) -> (x0 c + x1 s, -x0 s + x1 c)
+                  v = (d & 1) ? (v * co - other * si) : (v * co + other * si);
+                  o[(size_t)h * kD] = __float2bfloat16_rn(v);
+                }
+              } else {
+#pragma unroll
+                for (int h = 0; h < 32; ++h)
+                  o[(size_t)h * kD] = __float2bfloat16_rn(__uint_as_float(a[h]) * S.linv[32 * hf + h]);
               }
             } else {
               float *po = P.part + ((size_t)g.qi * P.n_splits + g.split) * kH * kD +

@@ -44,13 +44,18 @@ __host__ __device__ inline IndexWs index_ws_split(void *ws, uint32_t nq, uint32_
   return IndexWs{base, base + ((qsz + 63) & ~(size_t)63)};
 }
 
-// Workspace of bf16 layers: err word, A_t [nq], qbf [nq][Hi][Di] bf16,
-// norms [B][comp_cap], scores [nq][comp_cap] (fp32, rewritten in place as the
-// exact selection keys).
+// Workspace of bf16 layers: err word, qbf [nq][Hi][Di] bf16, norms
+// [B][comp_cap], scores [nq][comp_cap] (fp32), per-query histograms of the
+// scores' top 12 key bits [nq][4096], per-sequence max key norm [B], per-query
+// control words [nq][4] (candidate count, finished-block ticket, overflow) and
+// candidate rows [nq][kCandGlobal].
+constexpr uint32_t kHistBins = 4096;
+constexpr uint32_t kCandGlobal = 4096;
 struct TcWs {
   int *err;
-  float *at, *norms, *scores;
+  float *norms, *scores;
   __nv_bfloat16 *qbf;
+  uint32_t *hist, *maxnorm, *ctrl, *cand;
 };
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 inline TcWs tc_ws_split(void *ws, uint32_t nq, uint32_t B, uint32_t Hi, uint32_t Di,
@@ -59,59 +64,54 @@ inline TcWs tc_ws_split(void *ws, uint32_t nq, uint32_t B, uint32_t Hi, uint32_t
   size_t off = 0;
   TcWs w;
   w.err = reinterpret_cast<int *>(base + off);
-  off = align_up(off + 16, 256);
-  w.at = reinterpret_cast<float *>(base + off);
-  off = align_up(off + (size_t)nq * 4, 1024);
+  off = align_up(off + 16, 1024);
   w.qbf = reinterpret_cast<__nv_bfloat16 *>(base + off);
   off = align_up(off + (size_t)nq * Hi * Di * 2, 256);
   w.norms = reinterpret_cast<float *>(base + off);
   off = align_up(off + (size_t)B * comp_cap * 4, 256);
   w.scores = reinterpret_cast<float *>(base + off);
-  off += (size_t)nq * comp_cap * 4;
+  off = align_up(off + (size_t)nq * comp_cap * 4, 256);
+  w.hist = reinterpret_cast<uint32_t *>(base + off);
+  off = align_up(off + (size_t)nq * kHistBins * 4, 256);
+  w.maxnorm = reinterpret_cast<uint32_t *>(base + off);
+  off = align_up(off + (size_t)B * 4, 256);
+  w.ctrl = reinterpret_cast<uint32_t *>(base + off);
+  off = align_up(off + (size_t)nq * 16, 256);
+  w.cand = reinterpret_cast<uint32_t *>(base + off);
+  off += (size_t)nq * kCandGlobal * 4;
   if (total) *total = off;
   return w;
 }
 
-// bf16 layers: q' = rotated query rounded to bf16 (fp32 recipe), and
-// A_t = sum_h |w_h| ||q'_h||. Block 0 also clears the error word.
-__global__ void index_qbf_kernel(IndexArgs a, __nv_bfloat16 *qbf, float *at, int *err) {
-  __shared__ float red[32];
-  const uint32_t qi = blockIdx.x, t = qi % a.T, p = a.pos0 + t;
+// bf16 layers: q' = rotated query rounded to bf16 (fp32 recipe), one thread
+// per pair of dims; the same grid clears the call's counters (error word,
+// max norms, control words and, when the scorer builds them, histograms).
+__global__ void index_qbf_kernel(IndexArgs a, TcWs w, bool clear_hist) {
   const uint32_t Hi = a.n_heads, Di = a.dim, n_nope = Di - a.rot;
-  const __nv_bfloat16 *q = static_cast<const __nv_bfloat16 *>(a.q_idx) + (size_t)qi * Hi * Di;
-  const __nv_bfloat16 *w = static_cast<const __nv_bfloat16 *>(a.w) + (size_t)qi * Hi;
-  __nv_bfloat16 *dst = qbf + (size_t)qi * Hi * Di;
-  if (qi == 0 && threadIdx.x == 0) *err = 0;
-  float part = 0.f;
-  const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
-  for (uint32_t h = warp; h < Hi; h += nw) {
-    float ss = 0.f;
-    for (uint32_t c = 2 * lane; c < Di; c += 64) {
-      float x0 = __bfloat162float(q[(size_t)h * Di + c]);
-      float x1 = __bfloat162float(q[(size_t)h * Di + c + 1]);
-      if (c >= n_nope) {
-        const uint32_t fi = (c - n_nope) / 2;
-        const float co = a.cos[(size_t)p * (a.rot / 2) + fi];
-        const float si = a.sin[(size_t)p * (a.rot / 2) + fi];
-        const float r0 = __fsub_rn(__fmul_rn(x0, co), __fmul_rn(x1, si));
-        const float r1 = __fadd_rn(__fmul_rn(x0, si), __fmul_rn(x1, co));
-        x0 = __bfloat162float(__float2bfloat16_rn(r0));
-        x1 = __bfloat162float(__float2bfloat16_rn(r1));
-      }
-      dst[(size_t)h * Di + c] = __float2bfloat16_rn(x0);
-      dst[(size_t)h * Di + c + 1] = __float2bfloat16_rn(x1);
-      ss = fmaf(x0, x0, fmaf(x1, x1, ss));
-    }
-    ss = warp_sum(ss);
-    part += fabsf(__bfloat162float(w[h])) * sqrtf(ss);
+  const size_t nq = (size_t)a.batch * a.T;
+  const size_t npair = nq * Hi * Di / 2;
+  const size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x;
+  if (i == 0) *w.err = 0;
+  if (i < a.batch) w.maxnorm[i] = 0u;
+  if (i < nq * 4) w.ctrl[i] = 0u;
+  if (clear_hist && i < nq * kHistBins) w.hist[i] = 0u;
+  if (i >= npair) return;
+  const uint32_t c = (uint32_t)(2 * (i % (Di / 2)));
+  const size_t qi = i / ((size_t)Hi * Di / 2);
+  const uint32_t p = a.pos0 + (uint32_t)(qi % a.T);
+  const uint32_t *src = reinterpret_cast<const uint32_t *>(a.q_idx);
+  uint32_t v = src[i];
+  if (c >= n_nope) {
+    const float x0 = __uint_as_float(v << 16), x1 = __uint_as_float(v & 0xFFFF0000u);
+    const uint32_t fi = (c - n_nope) / 2;
+    const float co = a.cos[(size_t)p * (a.rot / 2) + fi];
+    const float si = a.sin[(size_t)p * (a.rot / 2) + fi];
+    const float r0 = __fsub_rn(__fmul_rn(x0, co), __fmul_rn(x1, si));
+    const float r1 = __fadd_rn(__fmul_rn(x0, si), __fmul_rn(x1, co));
+    const __nv_bfloat162 r = __floats2bfloat162_rn(r0, r1);
+    v = *reinterpret_cast<const uint32_t *>(&r);
   }
-  if (lane == 0) red[warp] = part;
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    float tot = 0.f;
-    for (uint32_t i = 0; i < nw; ++i) tot += red[i];
-    at[qi] = tot;
-  }
+  reinterpret_cast<uint32_t *>(w.qbf)[i] = v;
 }
 
 template <typename T>
@@ -242,20 +242,48 @@ __device__ uint32_t radix_kth(KeyF key, uint32_t n, uint32_t k, uint32_t *hist, 
   for (int shift = 24; shift >= 0; shift -= 8) {
     for (uint32_t i = threadIdx.x; i < 256; i += blockDim.x) hist[i] = 0;
     __syncthreads();
-    for (uint32_t s = threadIdx.x; s < n; s += blockDim.x) {
-      const uint32_t kk = key(s);
-      if ((kk & mask) == prefix) atomicAdd(&hist[(kk >> shift) & 255u], 1u);
+    // warp-aggregated: lanes with the same digit add once (keys of similar
+    // magnitude share their top digits, so per-lane atomics would serialise)
+    for (uint32_t base = 0; base < n; base += blockDim.x) {
+      const uint32_t s = base + threadIdx.x;
+      uint32_t bin = 256u;
+      if (s < n) {
+        const uint32_t kk = key(s);
+        if ((kk & mask) == prefix) bin = (kk >> shift) & 255u;
+      }
+      const uint32_t peers = __match_any_sync(0xffffffffu, bin);
+      if (bin < 256u && (threadIdx.x & 31) == (uint32_t)(__ffs(peers) - 1))
+        atomicAdd(&hist[bin], (uint32_t)__popc(peers));
     }
     __syncthreads();
-    if (threadIdx.x == 0) {
-      uint32_t cum = 0;
-      int d = 255;
-      for (; d > 0; --d) {
-        if (cum + hist[d] >= need) break;
-        cum += hist[d];
+    if (threadIdx.x < 32) {
+      // digit holding the need-th largest key: lane l covers digits
+      // 255 - 8l .. 248 - 8l; a scan over lanes runs from the top digit down
+      const uint32_t lane = threadIdx.x;
+      uint32_t c[8], tot = 0;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        c[j] = hist[255 - 8 * lane - j];
+        tot += c[j];
       }
-      sel[0] = (uint32_t)d;
-      sel[1] = cum;
+      uint32_t incl = tot;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= (uint32_t)o) incl += v;
+      }
+      uint32_t cum = incl - tot;
+      if (cum < need && incl >= need) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          if (cum + c[j] >= need) {
+            sel[0] = 255 - 8 * lane - j;
+            sel[1] = cum;
+            break;
+          }
+          cum += c[j];
+        }
+      }
     }
     __syncthreads();
     prefix |= sel[0] << shift;
@@ -267,11 +295,11 @@ __device__ uint32_t radix_kth(KeyF key, uint32_t n, uint32_t k, uint32_t *hist, 
   return prefix;
 }
 
-// Write, in ascending row order, every row with key > kth and the first
-// `need` rows with key == kth (ties to the lower index).
-template <typename KeyF>
+// Write, in ascending order of s, every s with key > kth and the first
+// `need` with key == kth (ties to the lower index); out[pos] = map(s).
+template <typename KeyF, typename MapF>
 __device__ void ordered_emit(KeyF key, uint32_t n, uint32_t kth, uint32_t need, uint32_t k,
-                             int32_t *out, uint32_t *wsum) {
+                             int32_t *out, uint32_t *wsum, MapF map) {
   uint32_t eq_seen = 0, out_pos = 0;
   for (uint32_t base = 0; base < n; base += blockDim.x) {
     const uint32_t s = base + threadIdx.x;
@@ -282,7 +310,7 @@ __device__ void ordered_emit(KeyF key, uint32_t n, uint32_t kth, uint32_t need, 
     const uint32_t eq_rank = eq_seen + block_flag_scan(eq, wsum, &eq_tot);
     const bool take = gt || (eq && eq_rank < need);
     const uint32_t pos = out_pos + block_flag_scan(take, wsum, &sel_tot);
-    if (take && pos < k) out[pos] = (int32_t)s;
+    if (take && pos < k) out[pos] = (int32_t)map(s);
     eq_seen += eq_tot;
     out_pos += sel_tot;
   }
@@ -304,123 +332,364 @@ __global__ void __launch_bounds__(kSelectThreads)
   auto key = [&](uint32_t s) { return score_key(sc[s]); };
   uint32_t need;
   const uint32_t kth = radix_kth(key, vis, k, hist, sel, &need);
-  ordered_emit(key, vis, kth, need, k, out, wsum);
+  ordered_emit(key, vis, kth, need, k, out, wsum, [](uint32_t x) { return x; });
 }
 
 __device__ __forceinline__ float key_to_float(uint32_t k) {
   return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
 }
 
-constexpr uint32_t kBandCap = 4096;
+constexpr uint32_t kCandCap = 4096;    // candidates held in shared memory
+constexpr float kRel = 2.4e-7f;        // slack for the rounding of the bound arithmetic
+constexpr uint32_t kQS = 136;          // padded row stride (bf16) of q' in shared memory
 
-// Certified selection for bf16 layers (see the file comment). `cb` bounds the
-// relative accumulation error; scores are rewritten in place as exact keys.
+// Block-wide exclusive prefix sum of v (every thread gets its prefix and the
+// total). `wsum` holds 33 words.
+__device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t *wsum, uint32_t *total) {
+  const uint32_t lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  uint32_t incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t n = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= (uint32_t)o) incl += n;
+  }
+  if (lane == 31) wsum[wid] = incl;
+  __syncthreads();
+  if (wid == 0) {
+    const uint32_t nw = blockDim.x >> 5;
+    const uint32_t x = lane < nw ? wsum[lane] : 0u;
+    uint32_t in2 = x;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t n = __shfl_up_sync(0xffffffffu, in2, o);
+      if (lane >= (uint32_t)o) in2 += n;
+    }
+    if (lane < nw) wsum[lane] = in2 - x;
+    if (lane == 31) wsum[32] = in2;
+  }
+  __syncthreads();
+  const uint32_t r = wsum[wid] + incl - v;
+  *total = wsum[32];
+  __syncthreads();
+  return r;
+}
+
+inline size_t select_tc_smem(uint32_t comp_cap) {
+  const size_t words = (comp_cap + 31) / 32;
+  return 64 * kQS * 2 + 64 * 4 + 32 * 128 * 4 + 32 * 64 * 4 + 3 * kCandCap * 4 + words * 4;
+}
+
+inline uint32_t select_groups(uint32_t nq) {
+  uint32_t g = 256 / (nq ? nq : 1);
+  return g < 1 ? 1 : (g > 16 ? 16 : g);
+}
+
+// Exact recipe (fp32, fixed order) for key row `kr` against the 64 x 128 query
+// in shared memory; lane 0 returns the score.
+__device__ __forceinline__ float rescore_row(const __nv_bfloat16 *qsm, const float *wsh, float *kb,
+                                             float *rel, const __nv_bfloat16 *kr, uint32_t lane) {
+  __syncwarp();
+  {
+    const uint2 v = *reinterpret_cast<const uint2 *>(kr + 4 * lane);
+    *reinterpret_cast<float4 *>(kb + 4 * lane) =
+        make_float4(__uint_as_float(v.x << 16), __uint_as_float(v.x & 0xFFFF0000u),
+                    __uint_as_float(v.y << 16), __uint_as_float(v.y & 0xFFFF0000u));
+  }
+  __syncwarp();
+#pragma unroll
+  for (uint32_t j = 0; j < 2; ++j) {
+    const uint32_t h = lane + 32 * j;
+    const uint4 *qrow = reinterpret_cast<const uint4 *>(qsm + (size_t)h * kQS);
+    float acc = 0.f;
+#pragma unroll 4
+    for (uint32_t c = 0; c < 16; ++c) {
+      const uint4 q8 = qrow[c];
+      const float4 ka = *reinterpret_cast<const float4 *>(kb + 8 * c);
+      const float4 kc = *reinterpret_cast<const float4 *>(kb + 8 * c + 4);
+      acc = __fadd_rn(acc, __fmul_rn(__uint_as_float(q8.x << 16), ka.x));
+      acc = __fadd_rn(acc, __fmul_rn(__uint_as_float(q8.x & 0xFFFF0000u), ka.y));
+      acc = __fadd_rn(acc, __fmul_rn(__uint_as_float(q8.y << 16), ka.z));
+      acc = __fadd_rn(acc, __fmul_rn(__uint_as_float(q8.y & 0xFFFF0000u), ka.w));
+      acc = __fadd_rn(acc, __fmul_rn(__uint_as_float(q8.z << 16), kc.x));
+      acc = __fadd_rn(acc, __fmul_rn(__uint_as_float(q8.z & 0xFFFF0000u), kc.y));
+      acc = __fadd_rn(acc, __fmul_rn(__uint_as_float(q8.w << 16), kc.z));
+      acc = __fadd_rn(acc, __fmul_rn(__uint_as_float(q8.w & 0xFFFF0000u), kc.w));
+    }
+    rel[h] = acc > 0.f ? acc : 0.f;
+  }
+  __syncwarp();
+  float tot = 0.f;
+  if (lane == 0) {
+#pragma unroll 16
+    for (uint32_t h = 0; h < 64; ++h) tot = __fadd_rn(tot, __fmul_rn(wsh[h], rel[h]));
+  }
+  return tot;
+}
+
+// Certified selection for bf16 layers (64 heads x 128 dims).
+//
+// Every row's exact score lies in [L_s, U_s] = [S~_s - e_s, S~_s + e_s] with
+// e_s = A ||k_s|| (+ rounding slack), A = c * sum_h |w_h| ||q'_h||. The score
+// kernel counted the top 12 key bits of S~ per query; the bin holding the k-th
+// largest gives theta_S with at least k rows S~ >= theta_S, so with
+// E = A max ||k|| and theta = theta_S - E (- slack) at least k rows have
+// L_s >= theta, and every row with U_s < theta is beaten by k rows. The G
+// blocks of a query filter their share of the rows (U_s >= theta) into a
+// candidate list; the last block to finish (atomic ticket, no waiting) runs
+// the certified selection on the candidates: tau~ = k-th largest S~, rows with
+// L_s > tau~ + E are in, rows with U_s < tau~ - E are out, the rest are
+// rescored with the exact recipe and the final selection is exact (ties to
+// the lower index). If the candidates overflow, the same selection runs over
+// every visible row in place.
 __global__ void __launch_bounds__(kSelectThreads)
-    topk_certified_kernel(IndexArgs a, TcWs w, float cb) {
+    topk_select_tc_kernel(IndexArgs a, TcWs w, float cb, uint32_t G, bool local_hist) {
   extern __shared__ float4 dyn4[];
   __shared__ uint32_t hist[256];
   __shared__ uint32_t wsum[33];
   __shared__ uint32_t sel[2];
-  __shared__ uint32_t s_nband, s_maxbits;
-  const uint32_t Hi = a.n_heads, Di = a.dim;
-  float *qT = reinterpret_cast<float *>(dyn4);          // [Di][Hi]
-  float *wsh = qT + (size_t)Di * Hi;                    // [Hi]
-  float *kbuf = wsh + ((Hi + 3) & ~3u);                 // [32 warps][Di]
-  uint32_t *band = reinterpret_cast<uint32_t *>(kbuf + 32 * Di);  // [kBandCap]
+  __shared__ uint32_t s_misc[4];   // bin, last-block flag, band count, tie count
+  __shared__ float s_red[32];
+  __nv_bfloat16 *qsm = reinterpret_cast<__nv_bfloat16 *>(dyn4);   // [64][kQS]
+  float *wsh = reinterpret_cast<float *>(qsm + 64 * kQS);           // [64]
+  float *kbuf = wsh + 64;                                           // [32][128]
+  float *relb = kbuf + 32 * 128;                                    // [32][64]
+  uint32_t *cidx = reinterpret_cast<uint32_t *>(relb + 32 * 64);    // [kCandCap]
+  float *cS = reinterpret_cast<float *>(cidx + kCandCap);           // [kCandCap]
+  float *ce = cS + kCandCap;                                        // [kCandCap]
+  uint32_t *bitmap = reinterpret_cast<uint32_t *>(ce + kCandCap);   // [comp_cap / 32]
 
-  const uint32_t qi = blockIdx.x, b = qi / a.T, t = qi % a.T, p = a.pos0 + t;
+  const uint32_t Hi = 64, Di = 128;
+  const uint32_t qi = blockIdx.x / G, g = blockIdx.x % G;
+  const uint32_t b = qi / a.T, p = a.pos0 + qi % a.T;
   const uint32_t vis = min((p + 1) / 4, a.n_comp), k = a.top_k;
   const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   int32_t *out = a.topk + (size_t)qi * k;
-  if (vis <= k) {
-    for (uint32_t j = threadIdx.x; j < k; j += blockDim.x) out[j] = j < vis ? (int32_t)j : -1;
-    return;
-  }
-  if (*(volatile int *)w.err) {   // the scorer gave up: no valid scores
-    for (uint32_t j = threadIdx.x; j < k; j += blockDim.x) out[j] = -1;
+  if (vis <= k || *(volatile int *)w.err) {
+    const bool bad = vis > k;
+    if (g == 0)
+      for (uint32_t j = threadIdx.x; j < k; j += blockDim.x)
+        out[j] = (!bad && j < vis) ? (int32_t)j : -1;
     return;
   }
   float *sc = w.scores + (size_t)qi * a.comp_cap;
   const float *nr = w.norms + (size_t)b * a.comp_cap;
-  if (threadIdx.x == 0) {
-    s_nband = 0;
-    s_maxbits = 0;
+  const __nv_bfloat16 *qb = w.qbf + (size_t)qi * Hi * Di;
+  const __nv_bfloat16 *wq = static_cast<const __nv_bfloat16 *>(a.w) + (size_t)qi * Hi;
+  uint32_t *ctrl = w.ctrl + (size_t)qi * 4;
+  uint32_t *cand = w.cand + (size_t)qi * kCandGlobal;
+
+  // A = c * sum_h |w_h| ||q'_h|| (two heads per warp); q' rows to shared memory
+  {
+    float part = 0.f;
+#pragma unroll
+    for (uint32_t j = 0; j < 2; ++j) {
+      const uint32_t h = warp + 32 * j;
+      const uint2 v = *reinterpret_cast<const uint2 *>(qb + (size_t)h * Di + 4 * lane);
+      *reinterpret_cast<uint2 *>(qsm + (size_t)h * kQS + 4 * lane) = v;
+      const float x0 = __uint_as_float(v.x << 16), x1 = __uint_as_float(v.x & 0xFFFF0000u);
+      const float x2 = __uint_as_float(v.y << 16), x3 = __uint_as_float(v.y & 0xFFFF0000u);
+      const float ss = warp_sum(x0 * x0 + x1 * x1 + x2 * x2 + x3 * x3);
+      part += fabsf(__bfloat162float(wq[h])) * sqrtf(ss);
+    }
+    if (lane == 0) s_red[warp] = part;
+    if (threadIdx.x < Hi) wsh[threadIdx.x] = __bfloat162float(wq[threadIdx.x]);
+  }
+  // theta_S: lower edge of the histogram bin holding the k-th largest S~
+  {
+    const uint32_t *hq = w.hist + (size_t)qi * kHistBins;
+    if (local_hist) {
+      // one block per query: count the keys' top 12 bits of every visible row
+      uint32_t *lh = reinterpret_cast<uint32_t *>(cS);   // free until the candidates load
+      for (uint32_t i = threadIdx.x; i < kHistBins; i += blockDim.x) lh[i] = 0u;
+      __syncthreads();
+      for (uint32_t base = 0; base < vis; base += blockDim.x) {
+        const uint32_t r = base + threadIdx.x;
+        const uint32_t bin = r < vis ? score_key(sc[r]) >> 20 : kHistBins;
+        const uint32_t peers = __match_any_sync(0xffffffffu, bin);
+        if (bin < kHistBins && lane == (uint32_t)(__ffs(peers) - 1))
+          atomicAdd(&lh[bin], (uint32_t)__popc(peers));
+      }
+      __syncthreads();
+      hq = lh;
+    }
+    uint32_t c4[4], loc = 0;
+#pragma unroll
+    for (uint32_t j = 0; j < 4; ++j) {
+      c4[j] = hq[kHistBins - 1 - (4 * threadIdx.x + j)];
+      loc += c4[j];
+    }
+    uint32_t tot;
+    uint32_t cum = block_excl_scan(loc, wsum, &tot);   // also syncs s_red / wsh / qsm
+    if (cum < k && cum + loc >= k) {
+#pragma unroll
+      for (uint32_t j = 0; j < 4; ++j) {
+        if (cum + c4[j] >= k) {
+          s_misc[0] = kHistBins - 1 - (4 * threadIdx.x + j);
+          break;
+        }
+        cum += c4[j];
+      }
+    }
   }
   __syncthreads();
-  float mx = 0.f;
-  for (uint32_t s = threadIdx.x; s < vis; s += blockDim.x) mx = fmaxf(mx, nr[s]);
-  mx = warp_max(mx);
-  if (lane == 0) atomicMax(&s_maxbits, __float_as_uint(mx));
-  // approximate k-th largest score
+  float At = 0.f;
+  for (uint32_t i = 0; i < 32; ++i) At += s_red[i];
+  const float A = At * (1.0f + 1e-5f) * cb;
+  const float E = A * __uint_as_float(w.maxnorm[b]);
+  const float theta_s = key_to_float(s_misc[0] << 20);
+  const float theta = theta_s - E - fabsf(theta_s) * (2.0f * kRel);
+  auto err_of = [&](float S, float nm) { return A * nm + fabsf(S) * kRel; };
+
+  // ---- this block's share of the rows: candidates with U >= theta
+  {
+    const uint32_t per = ((vis + G * 32 - 1) / (G * 32)) * 32;
+    const uint32_t r0 = g * per, r1 = min(vis, r0 + per);
+    for (uint32_t base = r0 + warp * 32; base < r1; base += blockDim.x) {
+      const uint32_t r = base + lane;
+      const bool ok = r < r1;
+      const float S = ok ? sc[r] : 0.f;
+      const bool c = ok && S + err_of(S, nr[r]) >= theta;
+      const uint32_t bal = __ballot_sync(0xffffffffu, c);
+      if (bal) {
+        uint32_t slot = 0;
+        if (lane == 0) slot = atomicAdd(&ctrl[0], (uint32_t)__popc(bal));
+        slot = __shfl_sync(0xffffffffu, slot, 0) + __popc(bal & ((1u << lane) - 1u));
+        if (c) {
+          if (slot < kCandGlobal)
+            cand[slot] = r;
+          else
+            ctrl[2] = 1u;
+        }
+      }
+    }
+  }
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) s_misc[1] = atomicAdd(&ctrl[1], 1u) == G - 1 ? 1u : 0u;
+  __syncthreads();
+  if (!s_misc[1]) return;
+  __threadfence();
+
+  const __nv_bfloat16 *keys = static_cast<const __nv_bfloat16 *>(a.keys) + (size_t)b * a.comp_cap * Di;
+  float *kb = kbuf + warp * 128, *rel = relb + warp * 64;
+  const uint32_t nc = *(volatile uint32_t *)&ctrl[0];
+  const bool fast = *(volatile uint32_t *)&ctrl[2] == 0u && nc <= kCandCap;
   uint32_t need;
-  const float tau =
-      key_to_float(radix_kth([&](uint32_t s) { return score_key(sc[s]); }, vis, k, hist, sel, &need));
-  const float A = w.at[qi] * cb;
-  const float E = A * __uint_as_float(s_maxbits);
-  const float hi_cut = tau + E + fabsf(tau) * 2.4e-7f;
-  const float lo_cut = tau - E - fabsf(tau) * 2.4e-7f;
-  // classify: certainly in -> +inf, certainly out -> -inf, band rows keep S~
+  if (fast) {
+    // ---- certified selection on the candidates
+    for (uint32_t j = threadIdx.x; j < nc; j += blockDim.x) {
+      const uint32_t r = *(volatile uint32_t *)&cand[j];
+      const float S = sc[r];
+      cidx[j] = r;
+      cS[j] = S;
+      ce[j] = err_of(S, nr[r]);
+    }
+    const uint32_t words = (vis + 31) / 32;
+    for (uint32_t i = threadIdx.x; i < words; i += blockDim.x) bitmap[i] = 0u;
+    __syncthreads();
+    const float tau = key_to_float(
+        radix_kth([&](uint32_t j) { return score_key(cS[j]); }, nc, k, hist, sel, &need));
+    const float hi_cut = tau + E + fabsf(tau) * kRel;
+    const float lo_cut = tau - E - fabsf(tau) * kRel;
+    for (uint32_t j = threadIdx.x; j < nc; j += blockDim.x) {
+      const float S = cS[j], e = ce[j];
+      if (S - e > hi_cut)
+        cS[j] = INFINITY;
+      else if (S + e < lo_cut)
+        cS[j] = -INFINITY;
+    }
+    __syncthreads();
+    for (uint32_t j = warp; j < nc; j += 32) {
+      const float v = cS[j];
+      if (v == INFINITY || v == -INFINITY) continue;
+      const float V = rescore_row(qsm, wsh, kb, rel, keys + (size_t)cidx[j] * Di, lane);
+      if (lane == 0) cS[j] = V;
+    }
+    __syncthreads();
+    auto key = [&](uint32_t j) { return score_key(cS[j]); };
+    const uint32_t kth = radix_kth(key, nc, k, hist, sel, &need);
+    // rows above the k-th key are in; of the rows at it, the `need` lowest
+    // indices (rank among tied rows by index)
+    if (threadIdx.x == 0) s_misc[3] = 0;
+    __syncthreads();
+    for (uint32_t j = threadIdx.x; j < nc; j += blockDim.x) {
+      const uint32_t kk = key(j);
+      if (kk > kth) atomicOr(&bitmap[cidx[j] >> 5], 1u << (cidx[j] & 31));
+      else if (kk == kth) atomicAdd(&s_misc[3], 1u);
+    }
+    __syncthreads();
+    if (s_misc[3] == need) {
+      for (uint32_t j = threadIdx.x; j < nc; j += blockDim.x)
+        if (key(j) == kth) atomicOr(&bitmap[cidx[j] >> 5], 1u << (cidx[j] & 31));
+    } else {
+      // more tied rows than places: keep the lowest indices
+      uint32_t nd2;
+      const uint32_t ith = radix_kth(
+          [&](uint32_t j) { return key(j) == kth ? ~cidx[j] : 0u; }, nc, need, hist, sel, &nd2);
+      for (uint32_t j = threadIdx.x; j < nc; j += blockDim.x)
+        if (key(j) == kth && ~cidx[j] >= ith) atomicOr(&bitmap[cidx[j] >> 5], 1u << (cidx[j] & 31));
+    }
+    __syncthreads();
+    // ascending output from the bitmap
+    const uint32_t per_t = (words + blockDim.x - 1) / blockDim.x;
+    const uint32_t w0 = threadIdx.x * per_t, w1 = min(words, w0 + per_t);
+    uint32_t cnt = 0;
+    for (uint32_t i = w0; i < w1; ++i) cnt += __popc(bitmap[i]);
+    uint32_t tot;
+    uint32_t pos = block_excl_scan(cnt, wsum, &tot);
+    for (uint32_t i = w0; i < w1; ++i) {
+      uint32_t m = bitmap[i];
+      while (m) {
+        const uint32_t bit = __ffs(m) - 1;
+        if (pos < k) out[pos] = (int32_t)(i * 32 + bit);
+        ++pos;
+        m &= m - 1;
+      }
+    }
+    for (uint32_t j = tot + threadIdx.x; j < k; j += blockDim.x) out[j] = -1;
+    return;
+  }
+
+  // ---- fallback: the same certified selection over every visible row
+  const float tau = key_to_float(
+      radix_kth([&](uint32_t s) { return score_key(sc[s]); }, vis, k, hist, sel, &need));
+  const float hi_cut = tau + E + fabsf(tau) * kRel;
+  const float lo_cut = tau - E - fabsf(tau) * kRel;
+  uint32_t *band = cidx;
+  if (threadIdx.x == 0) s_misc[2] = 0;
+  __syncthreads();
   for (uint32_t s = threadIdx.x; s < vis; s += blockDim.x) {
     const float S = sc[s];
-    const float e = A * nr[s] + fabsf(S) * 2.4e-7f;
+    const float e = err_of(S, nr[s]);
     if (S - e > hi_cut) {
       sc[s] = INFINITY;
     } else if (S + e < lo_cut) {
       sc[s] = -INFINITY;
     } else {
-      const uint32_t i = atomicAdd(&s_nband, 1u);
-      if (i < kBandCap) band[i] = s;
+      const uint32_t i = atomicAdd(&s_misc[2], 1u);
+      if (i < kCandCap) band[i] = s;
     }
   }
-  // exact-recipe operands: q'^T, w
-  const __nv_bfloat16 *qb = w.qbf + (size_t)qi * Hi * Di;
-  for (uint32_t i = threadIdx.x; i < Hi * Di; i += blockDim.x) {
-    const uint32_t h = i / Di, d = i % Di;
-    qT[(size_t)d * Hi + h] = __bfloat162float(qb[i]);
-  }
-  const __nv_bfloat16 *wq = static_cast<const __nv_bfloat16 *>(a.w) + (size_t)qi * Hi;
-  for (uint32_t h = threadIdx.x; h < Hi; h += blockDim.x) wsh[h] = __bfloat162float(wq[h]);
   __syncthreads();
-  const __nv_bfloat16 *keys = static_cast<const __nv_bfloat16 *>(a.keys) + (size_t)b * a.comp_cap * Di;
-  float *kb = kbuf + (size_t)warp * Di;
-  auto rescore = [&](uint32_t s) {
-    const __nv_bfloat16 *kr = keys + (size_t)s * Di;
-    for (uint32_t d = lane; d < Di; d += 32) kb[d] = __bfloat162float(kr[d]);
-    __syncwarp();
-    float rel[4];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const uint32_t h = lane + 32 * j;
-      float acc = 0.f;
-      if (h < Hi)
-        for (uint32_t d = 0; d < Di; ++d) acc = __fadd_rn(acc, __fmul_rn(qT[(size_t)d * Hi + h], kb[d]));
-      rel[j] = acc > 0.f ? acc : 0.f;
+  const uint32_t nband = s_misc[2];
+  if (nband <= kCandCap) {
+    for (uint32_t i = warp; i < nband; i += 32) {
+      const uint32_t s = band[i];
+      const float V = rescore_row(qsm, wsh, kb, rel, keys + (size_t)s * Di, lane);
+      if (lane == 0) sc[s] = V;
     }
-    float tot = 0.f;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      for (uint32_t l = 0; l < 32; ++l) {
-        const float r = __shfl_sync(0xffffffffu, rel[j], l);
-        const uint32_t h = 32 * j + l;
-        if (h < Hi) tot = __fadd_rn(tot, __fmul_rn(wsh[h], r));
-      }
-    }
-    __syncwarp();
-    if (lane == 0) sc[s] = tot;
-  };
-  const uint32_t nband = s_nband;
-  if (nband <= kBandCap) {
-    for (uint32_t i = warp; i < nband; i += blockDim.x / 32) rescore(band[i]);
   } else {
-    for (uint32_t s = warp; s < vis; s += blockDim.x / 32) {
+    for (uint32_t s = warp; s < vis; s += 32) {
       const float v = sc[s];
-      if (v != INFINITY && v != -INFINITY) rescore(s);
+      if (v == INFINITY || v == -INFINITY) continue;
+      const float V = rescore_row(qsm, wsh, kb, rel, keys + (size_t)s * Di, lane);
+      if (lane == 0) sc[s] = V;
     }
   }
   __syncthreads();
   auto key = [&](uint32_t s) { return score_key(sc[s]); };
   const uint32_t kth = radix_kth(key, vis, k, hist, sel, &need);
-  ordered_emit(key, vis, kth, need, k, out, wsum);
+  ordered_emit(key, vis, kth, need, k, out, wsum, [](uint32_t x) { return x; });
 }
 
 template <typename T>
@@ -454,7 +723,12 @@ inline double gamma_n(double n) {
 cudaError_t launch_index_tc(const IndexArgs &a, cudaStream_t s) {
   const uint32_t nq = a.batch * a.T;
   TcWs w = tc_ws_split(a.ws, nq, a.batch, a.n_heads, a.dim, a.comp_cap, nullptr);
-  index_qbf_kernel<<<nq, 256, 0, s>>>(a, w.qbf, w.at, w.err);
+  const size_t npair = (size_t)nq * a.n_heads * a.dim / 2;
+  const bool scorer_hist = a.T < 4;   // the 1-query scorer builds the histograms
+  size_t nthreads = npair;
+  if (scorer_hist && (size_t)nq * kHistBins > nthreads) nthreads = (size_t)nq * kHistBins;
+  if ((size_t)nq * 4 > nthreads) nthreads = (size_t)nq * 4;
+  index_qbf_kernel<<<(unsigned)((nthreads + 255) / 256), 256, 0, s>>>(a, w, scorer_hist);
   note_launches(1);
   const uint32_t vis_max = min((a.pos0 + a.T) / 4, a.n_comp);
   if (vis_max > a.top_k) {
@@ -469,6 +743,8 @@ cudaError_t launch_index_tc(const IndexArgs &a, cudaStream_t s) {
     t.w = a.w;
     t.scores = w.scores;
     t.norms = w.norms;
+    t.hist = w.hist;
+    t.maxnorm = w.maxnorm;
     t.err = w.err;
     cudaError_t e = launch_index_score_tc(t, s);
     if (e != cudaSuccess) return e;
@@ -478,12 +754,12 @@ cudaError_t launch_index_tc(const IndexArgs &a, cudaStream_t s) {
   // roundings) plus the fp32 epilogue; widened for the fp32 norms.
   const double cb = (gamma_n(a.dim + a.n_heads + 1) + gamma_n(4.0 * a.dim + a.n_heads + 1)) *
                     (1.0 + std::ldexp(1.0, -8));
-  const size_t smem = ((size_t)a.dim * a.n_heads + ((a.n_heads + 3) & ~3u) + 32 * (size_t)a.dim) * 4 +
-                      kBandCap * 4;
+  const size_t smem = select_tc_smem(a.comp_cap);
   static int smem_set = 0;
-  cudaError_t e = ensure_smem(topk_certified_kernel, smem, &smem_set);
+  cudaError_t e = ensure_smem(topk_select_tc_kernel, smem, &smem_set);
   if (e != cudaSuccess) return e;
-  topk_certified_kernel<<<nq, kSelectThreads, smem, s>>>(a, w, (float)cb);
+  const uint32_t G = scorer_hist ? select_groups(nq) : 1;
+  topk_select_tc_kernel<<<nq * G, kSelectThreads, smem, s>>>(a, w, (float)cb, G, !scorer_hist);
   note_launches(1);
   return cudaGetLastError();
 }

@@ -37,11 +37,12 @@ constexpr int kThreads = 192;
 template <int QG>
 struct Cfg {
   static constexpr int N = kHeads * QG;
-  static constexpr int kStages = QG == 1 ? 6 : 4;
+  static constexpr int kStages = QG == 1 ? 5 : 4;
+  static constexpr int kHistBytes = QG == 1 ? 4096 * 4 : 0;   // per-CTA key histogram
   static constexpr int kBBytes = N * kDim * 2;
   static constexpr int kTmemCols = QG == 1 ? 128 : 512;
   static constexpr size_t kSmem = 1024 + (size_t)kStages * kABytes + kBBytes + 1024 +
-                                  4 * QG * kHeads * 4;
+                                  4 * QG * kHeads * 4 + kHistBytes;
 };
 
 struct ScoreParams {
@@ -49,8 +50,17 @@ struct ScoreParams {
   const __nv_bfloat16 *w;   // [B][T][Hi]
   float *scores;            // [B][T][comp_cap]
   float *norms;             // [B][comp_cap]
+  uint32_t *hist;           // [B*T][4096] counts of the top 12 bits of the score keys
+  uint32_t *maxnorm;        // [B] largest key norm (float bits)
   int *err;
 };
+
+// Order-preserving unsigned key of an fp32 score (+0 and -0 share a key).
+__device__ __forceinline__ uint32_t score_key_tc(float f) {
+  if (f == 0.f) f = 0.f;
+  const uint32_t u = __float_as_uint(f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
 
 __device__ __forceinline__ uint32_t vis_of(const ScoreParams &P, uint32_t t) {
   return min((P.pos0 + t + 1) / 4, P.n_comp);
@@ -83,6 +93,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t *b_full = acc_empty + 2, *b_empty = b_full + 1;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(b_empty + 1);
   float *sw_all = reinterpret_cast<float *>(sB + C::kBBytes + 1024);   // [4 warps][QG][64]
+  uint32_t *shist = reinterpret_cast<uint32_t *>(sw_all + 4 * QG * kHeads);   // [4096] (QG == 1)
+  uint64_t *epi_bar = reinterpret_cast<uint64_t *>(tmem_slot + 2);
 
   const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t per = (P.total_items + gridDim.x - 1) / gridDim.x;
@@ -100,6 +112,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(b_full, 1);
     mbar_init(b_empty, 1);
+    mbar_init(epi_bar, 128);
     fence_mbar_init();
     prefetch_tmap(&tmap_k);
     prefetch_tmap(&tmap_q);
@@ -197,14 +210,35 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lg = warp & 3;
     const uint32_t row = lg * 32 + lane;
     float *sw = sw_all + (warp - 2) * QG * kHeads;   // this warp's copy of the weights
-    uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
+    const uint32_t et = threadIdx.x - 64;             // 0..127
+    uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0, epi_phase = 0;
     int32_t cur = -1;
     bool ok = true;
+    // one query per group when QG == 1: its key histogram is gathered here and
+    // added to the global one when the query changes
+    auto flush_hist = [&](int32_t q) {
+      if (!group_sync(epi_bar, epi_phase, P.err)) return false;
+      for (uint32_t i = et; i < 4096; i += 128) {
+        const uint32_t c = shist[i];
+        if (c) {
+          if (q >= 0) atomicAdd(&P.hist[(size_t)q * 4096 + i], c);
+          shist[i] = 0;
+        }
+      }
+      return group_sync(epi_bar, epi_phase, P.err);
+    };
+    if (QG == 1) {
+      for (uint32_t i = et; i < 4096; i += 128) shist[i] = 0;
+    }
     for (uint32_t it = it0; it < it1 && ok; ++it) {
       uint32_t b, g, tile;
       if (!decode_item<QG>(P, it, b, g, tile)) continue;
       const int32_t bg = (int32_t)(b * P.n_groups + g);
       if (bg != cur) {
+        if (QG == 1 && !flush_hist(cur)) {
+          ok = false;
+          break;
+        }
         __syncwarp();
         for (uint32_t i = lane; i < QG * kHeads; i += 32) {
           const uint32_t t = g * QG + i / kHeads;
@@ -216,7 +250,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // key-row norm from the swizzled tile: the row's two 128-byte lines hold
       // its 128 values (chunk order permuted, which a sum of squares ignores)
-      if (!mbar_wait(&a_full[stage], phase, P.err)) {
+      if (!mbar_wait_warp(&a_full[stage], phase, P.err)) {
         ok = false;
         break;
       }
@@ -246,7 +280,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         stage = 0;
         phase ^= 1;
       }
-      if (!mbar_wait(&acc_full[acc], acc_phase, P.err)) {
+      if (!mbar_wait_warp(&acc_full[acc], acc_phase, P.err)) {
         ok = false;
         break;
       }
@@ -266,8 +300,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int h = 0; h < 32; ++h) s = fmaf(wq[32 + h], fmaxf(__uint_as_float(r1[h]), 0.f), s);
         const uint32_t t = g * QG + q;
-        if (t < P.T && grow < vis_of(P, t))
-          P.scores[((size_t)b * P.T + t) * P.comp_cap + grow] = s;
+        const bool valid = t < P.T && grow < vis_of(P, t);
+        if (valid) P.scores[((size_t)b * P.T + t) * P.comp_cap + grow] = s;
+        if (QG == 1) {
+          // histogram of the keys' top 12 bits (lanes in one bin add once)
+          const uint32_t bin = valid ? score_key_tc(s) >> 20 : 4096u;
+          const uint32_t peers = __match_any_sync(0xffffffffu, bin);
+          if (bin < 4096u && lane == (uint32_t)(__ffs(peers) - 1))
+            atomicAdd(&shist[bin], (uint32_t)__popc(peers));
+        }
       }
       tc_fence_before();
       __syncwarp();
@@ -276,8 +317,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (acc == 0) acc_phase ^= 1;
       // the first query group that processes this tile writes its norms
       const bool first = g == 0 || tile * kRows >= vis_of(P, g * QG - 1);
-      if (first && grow < P.n_comp) P.norms[(size_t)b * P.comp_cap + grow] = sqrtf(ss);
+      if (first) {
+        const float nm = grow < P.n_comp ? sqrtf(ss) : 0.f;
+        if (grow < P.n_comp) P.norms[(size_t)b * P.comp_cap + grow] = nm;
+        const float mx = warp_max(nm);
+        if (lane == 0) atomicMax(&P.maxnorm[b], __float_as_uint(mx));
+      }
     }
+    if (QG == 1 && ok && cur >= 0) flush_hist(cur);
   }
   tc_fence_before();
   __syncthreads();
@@ -312,6 +359,8 @@ cudaError_t launch_qg(const IndexTcArgs &a, cudaStream_t s) {
   P.w = static_cast<const __nv_bfloat16 *>(a.w);
   P.scores = a.scores;
   P.norms = a.norms;
+  P.hist = a.hist;
+  P.maxnorm = a.maxnorm;
   P.err = a.err;
   if (P.total_items == 0) return cudaSuccess;
   static int smem_set = 0;

@@ -73,6 +73,8 @@ struct IndexTcArgs {
   const void *w;      // [B][T][64] bf16
   float *scores;      // [B][T][comp_cap]
   float *norms;       // [B][comp_cap]
+  uint32_t *hist;     // [B*T][4096], zeroed before the call
+  uint32_t *maxnorm;  // [B], zeroed before the call
   int *err;
 };
 bool index_tc_supported(uint32_t n_heads, uint32_t dim);

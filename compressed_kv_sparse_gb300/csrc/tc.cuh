@@ -69,6 +69,13 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, int *e
   }
 }
 
+// The same wait with one outcome for the whole (converged) warp: a lane that
+// gave up makes every lane give up, so warp-collective instructions after it
+// are never reached by part of a warp.
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t *bar, uint32_t parity, int *err) {
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity, err));
+}
+
 // 2D / 3D tiled TMA loads into shared memory, completing on `bar`.
 __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, uint64_t *bar,
                                             int x, int y) {
@@ -116,7 +123,7 @@ __device__ __forceinline__ void fence_proxy_async() {
 // Every member calls it the same number of times; `phase` is per thread.
 __device__ __forceinline__ bool group_sync(uint64_t *bar, uint32_t &phase, int *err) {
   mbar_arrive(bar);
-  const bool ok = mbar_wait(bar, phase, err);
+  const bool ok = mbar_wait_warp(bar, phase, err);
   phase ^= 1;
   return ok;
 }
@@ -152,6 +159,24 @@ __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64
       "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
+}
+
+// D[tmem] (+)= A[tmem] * B[smem]^T (A read from tensor memory), bf16, fp32 accumulate.
+__device__ __forceinline__ void mma_bf16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
+                                            uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// 2^x, hardware approximation (relative error ~2^-22; flushes denormals).
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
 }
 
 // Arrive on `bar` once every tcgen05.mma issued so far by this thread is done.

@@ -26,6 +26,30 @@ def test_index_tc_grid_ties():
     run_index(lib_(), synth.LayerShape(ratio=4), 2, 4000, 6, seed=32, grid=True)
 
 
+def test_index_tc_all_rows_tied_fallback():
+    """Every key row identical: all 16,384 scores tie, the candidate set
+    overflows and the selection falls back to the full pass; the kept rows
+    must be the 512 lowest indices."""
+    lib = lib_()
+    shape = synth.LayerShape(ratio=4)
+    B, p = 2, 65536
+    wl = synth.Workload("ties", 34, B, (shape,), p + 1, "decode")
+    cap = (p + 1) // 4 + 1
+    hist = synth.cache_history(wl, 0, p + 1, comp_cap=cap)
+    hist["index_comp_kv"][:] = hist["index_comp_kv"][:, :1]
+    q_idx = synth.normal((B, 1, 64, 128), 34, "q", dtype="bf16")
+    w = synth.normal((B, 1, 64), 34, "w", dtype="bf16")
+    gc = gpu_cache(shape, B, cap, p + 2, hist, p + 1)
+    topk = torch.empty((B, 1, shape.top_k), dtype=torch.int32, device=DEV)
+    ws = lib.workspace(gc.workspace_bytes(lib.CALL_INDEX_TOPK, 1, 64, shape.top_k))
+    lib.ds4a_index_topk(gc, p, 1, q_idx.to(DEV), w.to(DEV), 64, shape.top_k, topk, ws)
+    torch.cuda.synchronize()
+    oc = oracle_cache(shape, hist, p + 1)
+    ref = olayer.index_topk(oc, p, np_(q_idx), np_(w), shape.top_k)
+    assert np.array_equal(topk.cpu().numpy(), ref)
+    assert np.array_equal(ref[0, 0], np.arange(shape.top_k))
+
+
 def test_index_tc_prefill_visibility_edges():
     """Chunk starting below 4 k (some queries see <= k rows, the rest more)."""
     run_index(lib_(), synth.LayerShape(ratio=4), 1, 2030, 40, seed=33)
