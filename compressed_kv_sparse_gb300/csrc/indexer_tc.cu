@@ -40,7 +40,9 @@ struct Cfg {
   static constexpr int kStages = QG == 1 ? 5 : 4;
   static constexpr int kHistBytes = QG == 1 ? 4096 * 4 : 0;   // per-CTA key histogram
   static constexpr int kBBytes = N * kDim * 2;
-  static constexpr int kTmemCols = QG == 1 ? 128 : 512;
+  // QG == 1: two 64-column score accumulators and two 128-column K K^T tiles
+  // (their diagonals are the key norms); QG == 4: two 256-column accumulators
+  static constexpr int kTmemCols = 512;
   static constexpr size_t kSmem = 1024 + (size_t)kStages * kABytes + kBBytes + 1024 +
                                   4 * QG * kHeads * 4 + kHistBytes;
 };
@@ -104,7 +106,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(&a_full[s], 1);
-      mbar_init(&a_empty[s], 1 + 4);
+      mbar_init(&a_empty[s], QG == 1 ? 1 : 1 + 4);
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&acc_full[s], 1);
@@ -195,6 +197,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint64_t bd = sdesc_sw128(b_base + (kk / 4) * (C::kBBytes / 2) + koff);
           mma_bf16(d, ad, bd, idesc, kk > 0 ? 1u : 0u);
         }
+        if (QG == 1) {
+          // K K^T of the tile: row r's diagonal element is ||k_r||^2
+          constexpr uint32_t idn = idesc_bf16_f32(kRows, kRows);
+#pragma unroll
+          for (uint32_t kk = 0; kk < kDim / 16; ++kk) {
+            const uint64_t ad = sdesc_sw128(a0 + (kk / 4) * kKBlockBytes + (kk % 4) * 32);
+            mma_bf16(tmem + 128 + acc * 128, ad, ad, idn, kk > 0 ? 1u : 0u);
+          }
+        }
         mma_commit(&a_empty[stage]);
         mma_commit(&acc_full[acc]);
         if (++stage == C::kStages) {
@@ -230,6 +241,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (QG == 1) {
       for (uint32_t i = et; i < 4096; i += 128) shist[i] = 0;
     }
+    // running max of the key norms of one sequence, added to the global max
+    // when the sequence changes
+    float run_max = 0.f;
+    int32_t run_b = -1;
+    auto flush_max = [&]() {
+      if (run_b < 0) return;
+      const float mx = warp_max(run_max);
+      if (lane == 0) atomicMax(&P.maxnorm[run_b], __float_as_uint(mx));
+      run_max = 0.f;
+    };
     for (uint32_t it = it0; it < it1 && ok; ++it) {
       uint32_t b, g, tile;
       if (!decode_item<QG>(P, it, b, g, tile)) continue;
@@ -248,34 +269,39 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         cur = bg;
       }
-      // key-row norm from the swizzled tile: the row's two 128-byte lines hold
-      // its 128 values (chunk order permuted, which a sum of squares ignores)
-      if (!mbar_wait_warp(&a_full[stage], phase, P.err)) {
-        ok = false;
-        break;
-      }
+      // the first query group that processes a tile writes its key norms
+      const bool first = g == 0 || tile * kRows >= vis_of(P, g * QG - 1);
       float ss = 0.f;
-      {
-        const uint8_t *tileA = sA + (size_t)stage * kABytes;
+      if (QG != 1) {
+        // QG == 4: ||k_r||^2 from the swizzled tile (the row's two 128-byte
+        // lines hold its 128 values, chunk order permuted, which a sum of
+        // squares ignores); only the writing group computes it
+        if (!mbar_wait_warp(&a_full[stage], phase, P.err)) {
+          ok = false;
+          break;
+        }
+        if (first) {
+          const uint8_t *tileA = sA + (size_t)stage * kABytes;
 #pragma unroll
-        for (int kb = 0; kb < 2; ++kb) {
-          const uint8_t *line = tileA + kb * kKBlockBytes + (row >> 3) * 1024 + (row & 7) * 128;
+          for (int kb = 0; kb < 2; ++kb) {
+            const uint8_t *line = tileA + kb * kKBlockBytes + (row >> 3) * 1024 + (row & 7) * 128;
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const uint4 v = *reinterpret_cast<const uint4 *>(line + ((j + row) & 7) * 16);
-            const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+            for (int j = 0; j < 8; ++j) {
+              const uint4 v = *reinterpret_cast<const uint4 *>(line + ((j + row) & 7) * 16);
+              const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const float lo = __uint_as_float(w4[e] << 16);
-              const float hi = __uint_as_float(w4[e] & 0xFFFF0000u);
-              ss = fmaf(lo, lo, ss);
-              ss = fmaf(hi, hi, ss);
+              for (int e = 0; e < 4; ++e) {
+                const float lo = __uint_as_float(w4[e] << 16);
+                const float hi = __uint_as_float(w4[e] & 0xFFFF0000u);
+                ss = fmaf(lo, lo, ss);
+                ss = fmaf(hi, hi, ss);
+              }
             }
           }
         }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&a_empty[stage]);
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&a_empty[stage]);
       if (++stage == C::kStages) {
         stage = 0;
         phase ^= 1;
@@ -286,6 +312,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_after();
       const uint32_t grow = tile * kRows + row;
+      if (QG == 1) {
+        uint32_t dg[32];
+        tmem_ld32(tmem + ((lg * 32) << 16) + 128 + acc * 128 + lg * 32, dg);
+        tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          if ((uint32_t)j == lane) ss = __uint_as_float(dg[j]);
+      }
 #pragma unroll 1
       for (int q = 0; q < QG; ++q) {
         uint32_t r0[32], r1[32];
@@ -293,12 +327,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld32(taddr, r0);
         tmem_ld32(taddr + 32, r1);
         tmem_ld_wait();
-        const float *wq = sw + q * kHeads;
-        float s = 0.f;
+        // approximate score: any summation order is covered by the error
+        // bound, so eight independent chains and vector loads of the weights
+        const float4 *wq4 = reinterpret_cast<const float4 *>(sw + q * kHeads);
+        float acc8[8];
 #pragma unroll
-        for (int h = 0; h < 32; ++h) s = fmaf(wq[h], fmaxf(__uint_as_float(r0[h]), 0.f), s);
+        for (int j = 0; j < 8; ++j) acc8[j] = 0.f;
 #pragma unroll
-        for (int h = 0; h < 32; ++h) s = fmaf(wq[32 + h], fmaxf(__uint_as_float(r1[h]), 0.f), s);
+        for (int h4 = 0; h4 < 16; ++h4) {
+          const float4 w4 = wq4[h4];
+          const uint32_t *rr = h4 < 8 ? r0 : r1;
+          const int hb = (h4 & 7) * 4;
+          acc8[(2 * h4) & 7] = fmaf(w4.x, fmaxf(__uint_as_float(rr[hb + 0]), 0.f), acc8[(2 * h4) & 7]);
+          acc8[(2 * h4 + 1) & 7] = fmaf(w4.y, fmaxf(__uint_as_float(rr[hb + 1]), 0.f), acc8[(2 * h4 + 1) & 7]);
+          acc8[(2 * h4) & 7] = fmaf(w4.z, fmaxf(__uint_as_float(rr[hb + 2]), 0.f), acc8[(2 * h4) & 7]);
+          acc8[(2 * h4 + 1) & 7] = fmaf(w4.w, fmaxf(__uint_as_float(rr[hb + 3]), 0.f), acc8[(2 * h4 + 1) & 7]);
+        }
+        const float s = ((acc8[0] + acc8[1]) + (acc8[2] + acc8[3])) +
+                        ((acc8[4] + acc8[5]) + (acc8[6] + acc8[7]));
         const uint32_t t = g * QG + q;
         const bool valid = t < P.T && grow < vis_of(P, t);
         if (valid) P.scores[((size_t)b * P.T + t) * P.comp_cap + grow] = s;
@@ -315,15 +361,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive(&acc_empty[acc]);
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1;
-      // the first query group that processes this tile writes its norms
-      const bool first = g == 0 || tile * kRows >= vis_of(P, g * QG - 1);
       if (first) {
-        const float nm = grow < P.n_comp ? sqrtf(ss) : 0.f;
+        // widened by 1e-4 for the rounding of the fp32 sum of squares
+        const float nm = grow < P.n_comp ? sqrtf(ss) * 1.0001f : 0.f;
         if (grow < P.n_comp) P.norms[(size_t)b * P.comp_cap + grow] = nm;
-        const float mx = warp_max(nm);
-        if (lane == 0) atomicMax(&P.maxnorm[b], __float_as_uint(mx));
+        if ((int32_t)b != run_b) {   // warp-uniform: items are the same for all lanes
+          flush_max();
+          run_b = (int32_t)b;
+        }
+        run_max = fmaxf(run_max, nm);
       }
     }
+    if (ok) flush_max();
     if (QG == 1 && ok && cur >= 0) flush_hist(cur);
   }
   tc_fence_before();
