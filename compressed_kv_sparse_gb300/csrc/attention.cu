@@ -329,26 +329,14 @@ cudaError_t launch_attention_t(const AttnArgs &a, cudaStream_t s) {
   return cudaGetLastError();
 }
 
-// bf16 Flash shape: tcgen05 kernel; word 0 of the workspace is its error word,
-// the split partials follow at byte 256.
+// bf16 Flash shape: tcgen05 kernel (decode merges its splits inside a
+// thread-block cluster); word 0 of the workspace is its error word.
 cudaError_t launch_attention_tc_path(const AttnArgs &a, cudaStream_t s) {
   const uint32_t rmax = rows_max(a.ratio, a.cap_raw, a.comp_cap, a.top_k);
   int *err = static_cast<int *>(a.ws);
   cudaError_t e = cudaMemsetAsync(err, 0, sizeof(int), s);
   if (e != cudaSuccess) return e;
-  AttnArgs b = a;
-  b.ws = static_cast<uint8_t *>(a.ws) + 256;
-  e = launch_attention_tc(b, rmax, err, s);
-  if (e != cudaSuccess) return e;
-  const uint32_t ns = attn_tc_splits(a.T, rmax);
-  if (ns > 1) {
-    Plan pl;
-    pl.n_splits = ns;
-    attn_merge_kernel<__nv_bfloat16><<<dim3(a.n_heads, a.batch * a.T), 128, 0, s>>>(
-        a, pl, static_cast<const float *>(b.ws));
-    note_launches(1);
-  }
-  return cudaGetLastError();
+  return launch_attention_tc(a, rmax, err, s);
 }
 
 }  // namespace
@@ -356,10 +344,8 @@ cudaError_t launch_attention_tc_path(const AttnArgs &a, cudaStream_t s) {
 size_t attn_ws_bytes(int dtype, uint32_t ratio, uint32_t batch, uint32_t T, uint32_t n_heads,
                      uint32_t head_dim, uint32_t n_rot, uint32_t cap_raw, uint32_t comp_cap,
                      uint32_t top_k) {
-  if (attn_tc_supported(dtype, n_heads, head_dim, n_rot)) {
-    const uint32_t ns = attn_tc_splits(T, rows_max(ratio, cap_raw, comp_cap, top_k));
-    return 256 + (ns > 1 ? (size_t)batch * T * ns * n_heads * (head_dim + 2) * sizeof(float) : 0);
-  }
+  if (attn_tc_supported(dtype, n_heads, head_dim, n_rot))
+    return attn_tc_ws_bytes(batch, T, rows_max(ratio, cap_raw, comp_cap, top_k));
   const Plan pl = make_plan(ratio, batch, T, n_heads, head_dim, cap_raw, comp_cap, top_k);
   if (pl.n_splits == 1) return 0;
   return (size_t)batch * T * pl.n_splits * n_heads * (head_dim + 2) * sizeof(float);

@@ -2,8 +2,7 @@
 // 64-dim rotated tail): "【#3】ds4.c を読み解く" §7 mixed attention; vLLM
 // DeepSeek V4 page: shared K = V, inverse RoPE on the output, 128-token window.
 //
-// A work item is one query (and, in decode, one 128-row split of its row
-// list). Its rows — the raw window followed by the compressed rows of the
+// A query's rows — the raw window followed by the compressed rows of the
 // top-k list (ratio 4) or of the visible range (ratio 128) — are gathered 128
 // at a time into shared memory, in eight 64-dim blocks laid out with the
 // 128-byte swizzle. Each tile is used twice by the tensor cores, which is
@@ -15,13 +14,25 @@
 // as one 128-byte row of P. The running maximum of each head starts at the
 // scores of the first valid row and is only raised (rescaling O and the sums)
 // when a score exceeds it by 2^8, so the common path needs no reduction across
-// rows; the per-head sums are reduced once per query.
+// rows; the per-head sums come from the tensor core (ones x P^T).
+//
+// Decode: the tiles of a query are spread over a thread-block cluster (rank c
+// takes tiles c, c + C, ...). Each CTA writes its unnormalised O and per-head
+// (max, sum) to the workspace straight from TMEM; after one cluster barrier,
+// rank c pulls heads [64c/C, 64(c+1)/C) of every rank into its freed tile
+// buffer (cp.async from L2), combines them in rank order, normalises, rotates
+// the tail back and writes bf16 rows. (On this part the L2 round trip moves
+// these 128 KiB per CTA faster than distributed shared memory does.) A query
+// that fits one CTA (C = 1) and prefill write the output directly: it is
+// staged in the P buffer 128 dims at a time and stored as 16-byte segments.
 //
 // Warps 0-3: softmax and output epilogue (TMEM lanes = rows, then dims);
 // warps 4-7: gather loaders (cp.async, zero fill for masked rows) and the query
 // rotation; warp 8: MMA issue (one thread) and TMEM allocation. Every wait is
 // bounded (tc.cuh); a timeout sets the error word and the CTA winds down.
 #include <cuda_bf16.h>
+
+#include <atomic>
 
 #include "common.cuh"
 #include "tc.cuh"
@@ -33,61 +44,76 @@ constexpr int kH = 64, kD = 512, kNope = 448, kRows = 128;
 constexpr int kQBlk = kH * 128;        // one 64-dim block of Q: 64 heads x 128 B
 constexpr int kKBlk = kRows * 128;     // one 64-dim block of the row tile
 constexpr int kThreads = 288;
+constexpr uint32_t kMaxCluster = 8;    // portable cluster size
 constexpr uint32_t kNoRow = 0x7fffffffu;
 constexpr float kRaiseLog2 = 8.0f;     // raise the running max beyond 2^8
 
 struct TcAttnParams {
   uint32_t ratio, batch, T, pos0, cap_raw, comp_cap, n_comp, top_k;
-  uint32_t n_splits, tiles_per_split, n_items;
-  float c2;  // softmax scale * log2(e)
+  uint32_t cluster;   // decode: CTAs per query (one cluster); 0: prefill, persistent CTAs
+  uint32_t n_q;       // queries = batch * T
+  float c2;           // softmax scale * log2(e)
   const __nv_bfloat16 *q, *ring, *chunk, *comp;
   const int32_t *topk;
   const float *cos, *sin;
   __nv_bfloat16 *out;
-  float *part;
+  float *part;        // decode, C > 1: [n_q][C][64][512] O, then [n_q][C][64] (max, sum)
   int *err;
 };
 
 struct Smem {
   uint8_t q[8 * kQBlk];     // 64 KiB
-  uint8_t kv[8 * kKBlk];    // 128 KiB
-  uint8_t p[kRows * 128];   // 16 KiB
+  uint8_t kv[8 * kKBlk];    // 128 KiB; decode merge: afterwards the pulled slices (with p)
+  uint8_t p[kRows * 128];   // 16 KiB; direct output: afterwards staging, [64 heads][128] bf16
   uint64_t kv_full[8], kv_empty[8];
   uint64_t q_full, q_empty, s_full, p_full, p_empty, o_full, o_empty, sm_bar, ld_bar;
   float mref[kH], alpha[kH], lsh[kH], linv[kH];
-  float tmax[4][kH], lpart[4][kH];
-  uint32_t first_row, flagcnt[3], tmem;
+  float tmax[4][kH];
+  float mw[kH][kMaxCluster];        // decode merge: weight of each rank, per owned head
+  uint32_t first_row, flagcnt[3], tmem, has_tiles;
 };
+// the merge pulls at most C * ceil(64 / C) rows of 2 KiB (140 KiB at C = 7)
+static_assert(8 * kKBlk + kRows * 128 >= 7 * 10 * kD * 4, "pulled slices fit kv + p");
+static_assert(2 * kH * 128 == kRows * 128, "output staging fills the P buffer");
 
-// Query-level geometry shared by every role.
+// Rows that a query can have at most, without reading its top-k list.
+__device__ __forceinline__ uint32_t rows_bound(const TcAttnParams &P, uint32_t qi) {
+  const uint32_t p = P.pos0 + qi % P.T;
+  uint32_t n = min(p + 1, P.cap_raw);
+  if (P.ratio == 4) n += min(P.top_k, min((p + 1) / 4, P.n_comp));
+  else if (P.ratio == 128) n += min((p + 1) / 128, P.n_comp);
+  return n;
+}
+
+// Query-level geometry shared by every role: tiles t0, t0 + ts, ... < t1.
 struct QueryGeo {
-  uint32_t qi, split, b, p, n_w, n_list, N, t0, t1;
+  uint32_t qi, b, p, n_w, n_list, N, t0, t1, ts;
   const int32_t *tk;
 };
 
-__device__ __forceinline__ QueryGeo query_geo(const TcAttnParams &P, uint32_t item, uint32_t lane) {
+__device__ __forceinline__ QueryGeo query_geo(const TcAttnParams &P, uint32_t qi, uint32_t t0,
+                                              uint32_t ts, uint32_t lane) {
   QueryGeo g;
-  g.qi = item / P.n_splits;
-  g.split = item % P.n_splits;
-  g.b = g.qi / P.T;
-  g.p = P.pos0 + g.qi % P.T;
+  g.qi = qi;
+  g.b = qi / P.T;
+  g.p = P.pos0 + qi % P.T;
   g.n_w = min(g.p + 1, P.cap_raw);
-  g.tk = P.topk ? P.topk + (size_t)g.qi * P.top_k : nullptr;
+  g.tk = P.topk ? P.topk + (size_t)qi * P.top_k : nullptr;
   g.n_list = 0;
   if (P.ratio == 4) {
     const uint32_t vis = min((g.p + 1) / 4, P.n_comp);
-    // the list ends at its first entry >= vis; 8 independent loads per round
+    // the list ends at its first entry >= vis; 16 independent loads per round
     g.n_list = P.top_k;
-    for (uint32_t base = 0; base < P.top_k; base += 256) {
-      int32_t v[8];
+    for (uint32_t base = 0; base < P.top_k; base += 512) {
+      int32_t v[16];
 #pragma unroll
-      for (uint32_t i = 0; i < 8; ++i) {
+      for (uint32_t i = 0; i < 16; ++i) {
         const uint32_t j = base + 32 * i + lane;
         v[i] = j < P.top_k ? g.tk[j] : -1;
       }
       uint32_t found = 0xffffffffu;
 #pragma unroll
-      for (uint32_t i = 0; i < 8; ++i) {
+      for (uint32_t i = 0; i < 16; ++i) {
         const uint32_t bal = __ballot_sync(0xffffffffu, v[i] >= 0 && (uint32_t)v[i] >= vis);
         if (bal && found == 0xffffffffu) found = base + 32 * i + __ffs(bal) - 1;
       }
@@ -100,9 +126,9 @@ __device__ __forceinline__ QueryGeo query_geo(const TcAttnParams &P, uint32_t it
     g.n_list = min((g.p + 1) / 128, P.n_comp);
   }
   g.N = g.n_w + g.n_list;
-  const uint32_t n_tiles = (g.N + kRows - 1) / kRows;
-  g.t0 = g.split * P.tiles_per_split;
-  g.t1 = min(n_tiles, g.t0 + P.tiles_per_split);
+  g.t0 = t0;
+  g.t1 = (g.N + kRows - 1) / kRows;
+  g.ts = ts;
   return g;
 }
 
@@ -130,11 +156,93 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   return *reinterpret_cast<const uint32_t *>(&v);
 }
 
+// Decode merge of rank `rank` of a C-CTA cluster (C > 1; threads 0..255):
+// heads [64 rank / C, 64 (rank + 1) / C) of every rank's partial O land in the
+// row-tile buffer as [j][i][512] fp32 and are combined in rank order with
+// weights 2^(m_j - M) / sum_j 2^(m_j - M) l_j. A rank without rows left
+// m = -inf and zeros; one with only masked rows left m = -inf and O = 0.
+__device__ __forceinline__ void merge_heads(const TcAttnParams &P, Smem &S, uint32_t qi,
+                                            uint32_t rank, uint32_t C) {
+  const uint32_t t = threadIdx.x;
+  const uint32_t h0 = rank * kH / C, h1 = (rank + 1) * kH / C, nh = h1 - h0;
+  const float *part = P.part + (size_t)qi * C * kH * kD;
+  const float *ml = P.part + (size_t)P.n_q * C * kH * kD + (size_t)qi * C * kH * 2;
+  float *recv = reinterpret_cast<float *>(S.kv);
+  const uint32_t n_chunks = C * nh * (kD / 4);
+  for (uint32_t c = t; c < n_chunks; c += 256) {
+    const uint32_t row = c >> 7, ch = c & 127, j = row / nh, i = row - j * nh;
+    cp_async16(recv + row * kD + ch * 4, part + ((size_t)j * kH + h0 + i) * kD + ch * 4, 16);
+  }
+  asm volatile("cp.async.commit_group;" ::: "memory");
+  if (t < nh) {
+    const uint32_t h = h0 + t;
+    float m[kMaxCluster], l[kMaxCluster], M = -INFINITY;
+#pragma unroll
+    for (uint32_t j = 0; j < kMaxCluster; ++j) {
+      m[j] = j < C ? __ldcg(ml + ((size_t)j * kH + h) * 2) : -INFINITY;   // written by peers
+      l[j] = j < C ? __ldcg(ml + ((size_t)j * kH + h) * 2 + 1) : 0.f;
+    }
+#pragma unroll
+    for (uint32_t j = 0; j < kMaxCluster; ++j) M = fmaxf(M, m[j]);
+    float L = 0.f;
+#pragma unroll
+    for (uint32_t j = 0; j < kMaxCluster; ++j) {
+      const float f = m[j] == -INFINITY ? 0.f : exp2f(m[j] - M);
+      S.mw[t][j] = f;
+      L = fmaf(f, l[j], L);
+    }
+    S.linv[t] = L > 0.f ? 1.f / L : 0.f;
+  }
+  cp_async_wait_all();
+  named_bar_sync(1, 256);
+  const uint32_t p = P.pos0 + qi % P.T, c = t & 127, d = 4 * c;
+  float co0 = 1.f, si0 = 0.f, co1 = 1.f, si1 = 0.f;
+  if (d >= (uint32_t)kNope) {
+    const uint32_t fi = (d - kNope) >> 1;
+    co0 = P.cos[(size_t)p * 32 + fi];
+    si0 = P.sin[(size_t)p * 32 + fi];
+    co1 = P.cos[(size_t)p * 32 + fi + 1];
+    si1 = P.sin[(size_t)p * 32 + fi + 1];
+  }
+#pragma unroll 1
+  for (uint32_t i = t >> 7; i < nh; i += 2) {
+    float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+#pragma unroll
+    for (uint32_t j = 0; j < kMaxCluster; ++j) {
+      const float f = S.mw[i][j];
+      if (j < C && f != 0.f) {
+        const float4 v = *reinterpret_cast<const float4 *>(recv + (j * nh + i) * kD + d);
+        a0 = fmaf(f, v.x, a0);
+        a1 = fmaf(f, v.y, a1);
+        a2 = fmaf(f, v.z, a2);
+        a3 = fmaf(f, v.w, a3);
+      }
+    }
+    const float li = S.linv[i];
+    a0 *= li;
+    a1 *= li;
+    a2 *= li;
+    a3 *= li;
+    // rotate back by -p: (x0, x1) -> (x0 c + x1 s, -x0 s + x1 c)
+    const float r0 = a0 * co0 + a1 * si0, r1 = -a0 * si0 + a1 * co0;
+    const float r2 = a2 * co1 + a3 * si1, r3 = -a2 * si1 + a3 * co1;
+    *reinterpret_cast<uint2 *>(P.out + ((size_t)qi * kH + h0 + i) * kD + d) =
+        make_uint2(pack_bf16(r0, r1), pack_bf16(r2, r3));
+  }
+}
+
 __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(TcAttnParams P) {
   extern __shared__ uint8_t smem_raw[];
   Smem &S = *reinterpret_cast<Smem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                       ~(uintptr_t)1023);
   const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // decode: cluster of C CTAs per query, rank c takes tiles c, c + C, ...;
+  // prefill: one whole query at a time per CTA
+  const bool dec = P.cluster != 0;
+  const uint32_t C = dec ? P.cluster : 1u;
+  const uint32_t rank = dec ? cluster_ctarank() : 0u;
+  const uint32_t q_first = dec ? blockIdx.x / C : blockIdx.x;
+  const uint32_t q_step = dec ? P.n_q : gridDim.x;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < 8; ++i) {
@@ -198,13 +306,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(TcAttnParams P) {
       }
       return true;
     };
-    for (uint32_t item = blockIdx.x; item < P.n_items; item += gridDim.x) {
-      const QueryGeo g = query_geo(P, item, lane);
-      if (g.t0 >= g.t1) continue;
+    for (uint32_t qi = q_first; qi < P.n_q; qi += q_step) {
+      if (rank * kRows >= rows_bound(P, qi)) continue;   // no rows for this rank
       if (!mbar_wait_warp(&S.q_empty, (qn & 1) ^ 1, P.err)) goto done_loader;
       {
-        // Q: warp lw loads heads 16 lw .. 16 lw + 15, two half rows per head
-        const __nv_bfloat16 *q = P.q + (size_t)g.qi * kH * kD;
+        // Q first (it needs no list): warp lw loads heads 16 lw .. 16 lw + 15
+        const __nv_bfloat16 *q = P.q + (size_t)qi * kH * kD;
         for (uint32_t hh = 0; hh < 16; ++hh) {
           const uint32_t h = lw * 16 + hh;
 #pragma unroll
@@ -216,44 +323,62 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(TcAttnParams P) {
           }
         }
         asm volatile("cp.async.commit_group;" ::: "memory");
+      }
+      {
+        const QueryGeo g = query_geo(P, qi, rank, C, lane);
+        if (g.t0 >= g.t1) {          // the list is shorter than the bound: nothing to do
+          cp_async_wait_all();
+          continue;
+        }
         // the first tile's rows start loading before Q is rotated
         if (!issue_tile(g, g.t0, n)) goto done_loader;
+        // this thread's 16-byte chunks of the tail: chunk lt (+ 128 i) of block 7
+        // holds pairs 4 lc .. 4 lc + 3 of head id / 8; coefficients load meanwhile
+        float co[16], si[16];
+#pragma unroll
+        for (uint32_t i = 0; i < 4; ++i) {
+          const uint32_t id = lt + 128 * i, h = id >> 3, lc = (id & 7) ^ (h & 7);
+#pragma unroll
+          for (uint32_t e = 0; e < 4; ++e) {
+            co[4 * i + e] = P.cos[(size_t)g.p * 32 + 4 * lc + e];
+            si[4 * i + e] = P.sin[(size_t)g.p * 32 + 4 * lc + e];
+          }
+        }
         asm volatile("cp.async.wait_group 8;" ::: "memory");   // Q landed
         if (!group_sync(&S.ld_bar, ld_phase, P.err)) goto done_loader;
         // rotate the tail (dims 448..511 = block 7) at position p, in place
 #pragma unroll
         for (uint32_t i = 0; i < 4; ++i) {
-          const uint32_t id = lt + 128 * i, h = id >> 3, pc = id & 7, lc = pc ^ (h & 7);
+          const uint32_t id = lt + 128 * i, h = id >> 3, pc = id & 7;
           uint4 *ptr = reinterpret_cast<uint4 *>(S.q + 7 * kQBlk + h * 128 + pc * 16);
           uint4 v = *ptr;
           uint32_t w4[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
           for (uint32_t e = 0; e < 4; ++e) {
-            const uint32_t fi = 4 * lc + e;
-            const float co = P.cos[(size_t)g.p * 32 + fi], si = P.sin[(size_t)g.p * 32 + fi];
+            const float c = co[4 * i + e], sn = si[4 * i + e];
             const float x0 = bf16lo(w4[e]), x1 = bf16hi(w4[e]);
-            w4[e] = pack_bf16(x0 * co - x1 * si, x0 * si + x1 * co);
+            w4[e] = pack_bf16(x0 * c - x1 * sn, x0 * sn + x1 * c);
           }
           *ptr = make_uint4(w4[0], w4[1], w4[2], w4[3]);
         }
         fence_proxy_async();
         mbar_arrive(&S.q_full);
-      }
-      for (uint32_t tile = g.t0; tile < g.t1; ++tile, ++n) {
-        if (tile != g.t0 && !issue_tile(g, tile, n)) goto done_loader;
+        for (uint32_t tile = g.t0; tile < g.t1; tile += g.ts, ++n) {
+          if (tile != g.t0 && !issue_tile(g, tile, n)) goto done_loader;
 #define DS4A_KV_LANDED(NPEND, KB)                                   \
   asm volatile("cp.async.wait_group " #NPEND ";" ::: "memory");     \
   fence_proxy_async();                                              \
   mbar_arrive(&S.kv_full[KB]);
-        DS4A_KV_LANDED(7, 0)
-        DS4A_KV_LANDED(6, 1)
-        DS4A_KV_LANDED(5, 2)
-        DS4A_KV_LANDED(4, 3)
-        DS4A_KV_LANDED(3, 4)
-        DS4A_KV_LANDED(2, 5)
-        DS4A_KV_LANDED(1, 6)
-        DS4A_KV_LANDED(0, 7)
+          DS4A_KV_LANDED(7, 0)
+          DS4A_KV_LANDED(6, 1)
+          DS4A_KV_LANDED(5, 2)
+          DS4A_KV_LANDED(4, 3)
+          DS4A_KV_LANDED(3, 4)
+          DS4A_KV_LANDED(2, 5)
+          DS4A_KV_LANDED(1, 6)
+          DS4A_KV_LANDED(0, 7)
 #undef DS4A_KV_LANDED
+        }
       }
       ++qn;
     }
@@ -266,13 +391,14 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(TcAttnParams P) {
     const uint32_t q_base = smem_u32(S.q), kv_base = smem_u32(S.kv), p_base = smem_u32(S.p);
     uint32_t n = 0, qn = 0;
     bool ok = true;
-    for (uint32_t item = blockIdx.x; item < P.n_items && ok; item += gridDim.x) {
-      const QueryGeo g = query_geo(P, item, lane);
+    for (uint32_t qi = q_first; qi < P.n_q && ok; qi += q_step) {
+      if (rank * kRows >= rows_bound(P, qi)) continue;
+      const QueryGeo g = query_geo(P, qi, rank, C, lane);
       if (g.t0 >= g.t1) continue;
       if (lane == 0) {
         ok = mbar_wait(&S.q_full, qn & 1, P.err);
-        for (uint32_t tile = g.t0; ok && tile < g.t1; ++tile, ++n) {
-          const bool first = tile == g.t0, last = tile + 1 == g.t1;
+        for (uint32_t tile = g.t0; ok && tile < g.t1; tile += g.ts, ++n) {
+          const bool first = tile == g.t0, last = tile + g.ts >= g.t1;
           for (uint32_t kb = 0; kb < 8 && ok; ++kb) {
             ok = mbar_wait(&S.kv_full[kb], n & 1, P.err);
             if (!ok) break;
@@ -346,11 +472,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(TcAttnParams P) {
       }
       return flag;
     };
-    for (uint32_t item = blockIdx.x; item < P.n_items; item += gridDim.x) {
-      const QueryGeo g = query_geo(P, item, lane);
-      const bool has_tiles = g.t0 < g.t1;
+    for (uint32_t qi = q_first; qi < P.n_q; qi += q_step) {
+      const bool maybe = rank * kRows < rows_bound(P, qi);
+      QueryGeo g = {};
+      if (maybe) g = query_geo(P, qi, rank, C, lane);
+      const bool has_tiles = maybe && g.t0 < g.t1;
       bool any_valid = false;
-      for (uint32_t tile = g.t0; tile < g.t1; ++tile, ++n) {
+      for (uint32_t tile = g.t0; has_tiles && tile < g.t1; tile += g.ts, ++n) {
         const bool first = tile == g.t0;
         const uint32_t row = tile * kRows + r;
         bool valid = row < g.n_w;
@@ -431,39 +559,40 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(TcAttnParams P) {
         tc_fence_before();
         mbar_arrive(&S.p_full);
       }
-      // ---- item end: per-head sums (any lane of L), then the output
-      {
-        const bool final_out = P.n_splits == 1;
-        if (has_tiles) {
-          if (!mbar_wait_warp(&S.o_full, qn & 1, P.err)) goto done_softmax;
-          tc_fence_after();
-          if (warp == 0) {   // every row of L holds the sums; warp 0 loads, lane 0 keeps
-#pragma unroll 1
-            for (uint32_t hf = 0; hf < 2; ++hf) {
-              uint32_t a[32];
-              tmem_ld32(tmL + lane_base + 32 * hf, a);
-              tmem_ld_wait();
-              if (lane == 0) {
+      // ---- query end: per-head sums (any lane of L), then the output
+      if (has_tiles) {
+        if (!mbar_wait_warp(&S.o_full, qn & 1, P.err)) goto done_softmax;
+        tc_fence_after();
+        if (warp < 2) {   // every row of L holds the sums: warp w keeps heads 32w + lane
+          uint32_t a[32];
+          tmem_ld32(tmL + lane_base + 32 * warp, a);
+          tmem_ld_wait();
+          float l = 0.f;
 #pragma unroll
-                for (int h = 0; h < 32; ++h) {
-                  const float l = __uint_as_float(a[h]);
-                  S.lsh[32 * hf + h] = l;
-                  S.linv[32 * hf + h] = __frcp_rn(l);
-                }
-              }
-            }
-          }
-        } else if (r < kH) {
-          S.lsh[r] = 0.f;
-          S.linv[r] = 0.f;
+          for (uint32_t i = 0; i < 32; ++i)
+            if (lane == i) l = __uint_as_float(a[i]);
+          S.lsh[32 * warp + lane] = l;
+          S.linv[32 * warp + lane] = l > 0.f ? 1.f / l : 0.f;
         }
-        if (!group_sync(&S.sm_bar, sm_phase, P.err)) goto done_softmax;
-        float co = 1.f, si = 0.f;
+      }
+      if (!group_sync(&S.sm_bar, sm_phase, P.err)) goto done_softmax;
+      if (dec && C > 1) {
+        // (max, sum) of this rank for the cluster merge; O follows from TMEM
+        if (r < kH) {
+          float *ml = P.part + (size_t)P.n_q * C * kH * kD + ((size_t)(qi * C + rank) * kH + r) * 2;
+          ml[0] = (has_tiles && any_valid) ? S.mref[r] : -INFINITY;
+          ml[1] = has_tiles ? S.lsh[r] : 0.f;
+        }
+        if (r == 0) S.has_tiles = has_tiles ? 1u : 0u;
+      } else {
+        // normalise, rotate the tail back by -p, stage [64 heads][128 dims]
+        // bf16 in the P buffer, then write 16-byte row segments
+        uint8_t *stage = S.p;
 #pragma unroll 1
         for (uint32_t m = 0; m < 4; ++m) {
           const uint32_t d = m * 128 + r;
-          const bool tail = final_out && d >= (uint32_t)kNope;
-          if (tail) {
+          float co = 1.f, si = 0.f;
+          if (d >= (uint32_t)kNope) {
             const uint32_t fi = (d - kNope) >> 1;
             co = P.cos[(size_t)g.p * 32 + fi];
             si = P.sin[(size_t)g.p * 32 + fi];
@@ -471,50 +600,40 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(TcAttnParams P) {
 #pragma unroll 1
           for (uint32_t hf = 0; hf < 2; ++hf) {
             uint32_t a[32];
-            if (has_tiles) {
-              tmem_ld32(tmO + lane_base + m * kH + 32 * hf, a);
-              tmem_ld_wait();
-            } else {
+            tmem_ld32(tmO + lane_base + m * kH + 32 * hf, a);
+            tmem_ld_wait();
+            __nv_bfloat16 *srow = reinterpret_cast<__nv_bfloat16 *>(stage) + (32 * hf) * 128 + r;
+            if (m == 3 && r >= 64) {   // warp-uniform: the rotated tail dims
 #pragma unroll
-              for (int h = 0; h < 32; ++h) a[h] = 0u;
-            }
-            if (final_out) {
-              __nv_bfloat16 *o = P.out + (size_t)g.qi * kH * kD + (size_t)(32 * hf) * kD + d;
-              if (m == 3 && r >= 64) {   // warp-uniform: the rotated tail dims
-#pragma unroll
-                for (int h = 0; h < 32; ++h) {
-                  float v = __uint_as_float(a[h]) * S.linv[32 * hf + h];
-                  const float other = __shfl_xor_sync(0xffffffffu, v, 1);
-                  // rotate back by -p: (x0, x1) -> (x0 c + x1 s, -x0 s + x1 c)
-                  v = (d & 1) ? (v * co - other * si) : (v * co + other * si);
-                  o[(size_t)h * kD] = __float2bfloat16_rn(v);
-                }
-              } else {
-#pragma unroll
-                for (int h = 0; h < 32; ++h)
-                  o[(size_t)h * kD] = __float2bfloat16_rn(__uint_as_float(a[h]) * S.linv[32 * hf + h]);
+              for (int h = 0; h < 32; ++h) {
+                float v = __uint_as_float(a[h]) * S.linv[32 * hf + h];
+                const float other = __shfl_xor_sync(0xffffffffu, v, 1);
+                // (x0, x1) -> (x0 c + x1 s, -x0 s + x1 c)
+                v = (d & 1) ? (v * co - other * si) : (v * co + other * si);
+                srow[h * 128] = __float2bfloat16_rn(v);
               }
             } else {
-              float *po = P.part + ((size_t)g.qi * P.n_splits + g.split) * kH * kD +
-                          (size_t)(32 * hf) * kD + d;
 #pragma unroll
-              for (int h = 0; h < 32; ++h) po[(size_t)h * kD] = __uint_as_float(a[h]);
+              for (int h = 0; h < 32; ++h)
+                srow[h * 128] = __float2bfloat16_rn(__uint_as_float(a[h]) * S.linv[32 * hf + h]);
             }
           }
+          if (!group_sync(&S.sm_bar, sm_phase, P.err)) goto done_softmax;
+          __nv_bfloat16 *o = P.out + (size_t)qi * kH * kD + m * 128;
+#pragma unroll
+          for (uint32_t i = 0; i < 8; ++i) {
+            const uint32_t c = r + 128 * i, h = c >> 4, seg = c & 15;
+            *reinterpret_cast<uint4 *>(o + (size_t)h * kD + seg * 8) =
+                *reinterpret_cast<const uint4 *>(stage + h * 256 + seg * 16);
+          }
+          if (!group_sync(&S.sm_bar, sm_phase, P.err)) goto done_softmax;
         }
-        if (!final_out && r < kH) {
-          const size_t nq = (size_t)P.batch * P.T;
-          float *pml = P.part + nq * P.n_splits * kH * kD +
-                       (((size_t)g.qi * P.n_splits + g.split) * kH + r) * 2;
-          pml[0] = any_valid ? S.mref[r] * 0.69314718055994531f : -INFINITY;
-          pml[1] = S.lsh[r];
-        }
-        if (has_tiles) {
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&S.o_empty);
-          ++qn;
-        }
+      }
+      if (has_tiles) {
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&S.o_empty);
+        ++qn;
       }
       // keep the shared sums alive until every thread has read them
       if (!group_sync(&S.sm_bar, sm_phase, P.err)) goto done_softmax;
@@ -524,7 +643,80 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(TcAttnParams P) {
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  if (dec && C > 1 && warp < 8) {
+    // this rank's unnormalised O: warp w reads TMEM lanes 32 (w % 4) .. + 31
+    // (dims) for heads 32 (w / 4) .. + 31; a warp stores 128 contiguous bytes
+    const uint32_t qw = warp & 3, hf = warp >> 2, dl = 32 * qw + lane;
+    float *dst = P.part + ((size_t)q_first * C + rank) * kH * kD + (size_t)(32 * hf) * kD;
+    const bool had = S.has_tiles != 0;
+#pragma unroll 1
+    for (uint32_t m = 0; m < 4; ++m) {
+      uint32_t a[32];
+      if (had) {
+        tmem_ld32(tmO + ((32 * qw) << 16) + m * kH + 32 * hf, a);
+        tmem_ld_wait();
+      } else {
+#pragma unroll
+        for (int h = 0; h < 32; ++h) a[h] = 0u;
+      }
+#pragma unroll
+      for (int h = 0; h < 32; ++h) dst[(size_t)h * kD + m * 128 + dl] = __uint_as_float(a[h]);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
   if (warp == 8) tmem_dealloc(tmem, 512);
+  if (dec && C > 1) {
+    cluster_sync_all();   // every rank's O and (max, sum) are in the workspace
+    if (warp < 8) merge_heads(P, S, q_first, rank, C);
+  }
+}
+
+// Largest number of clusters of each size (1..8) that fit on the device at
+// once, per device; 0 = not yet asked.
+std::atomic<int> g_max_clusters[64][kMaxCluster + 1];
+
+int max_active_clusters(uint32_t C, size_t smem) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
+  int v = g_max_clusters[dev][C].load(std::memory_order_relaxed);
+  if (v > 0) return v;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = C;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  cfg.gridDim = dim3(C * 64);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  if (cudaOccupancyMaxActiveClusters(&v, attn_tc_kernel, &cfg) != cudaSuccess || v <= 0) {
+    (void)cudaGetLastError();
+    v = num_sms() / (int)C;
+  }
+  if (v < 1) v = 1;
+  g_max_clusters[dev][C].store(v, std::memory_order_relaxed);
+  return v;
+}
+
+// Cluster size for a decode batch: fewest rounds of tiles, counting a whole
+// extra round for every wave of clusters beyond the first (a wave also pays
+// the query load and the merge, modelled as two tiles). Ties: fewer CTAs.
+uint32_t pick_cluster(uint32_t n_tiles, uint32_t n_q, size_t smem) {
+  uint32_t best = 1, best_cost = 0xffffffffu;
+  const uint32_t cmax = n_tiles < kMaxCluster ? (n_tiles ? n_tiles : 1u) : kMaxCluster;
+  for (uint32_t C = 1; C <= cmax; ++C) {
+    const uint32_t act = (uint32_t)max_active_clusters(C, smem);
+    const uint32_t waves = (n_q + act - 1) / act, tiles = (n_tiles + C - 1) / C;
+    const uint32_t cost = waves * (tiles + 2);
+    if (cost < best_cost) {
+      best = C;
+      best_cost = cost;
+    }
+  }
+  return best;
 }
 
 }  // namespace
@@ -533,8 +725,13 @@ bool attn_tc_supported(int dtype, uint32_t H, uint32_t D, uint32_t n_rot) {
   return dtype == DS4A_BF16 && H == (uint32_t)kH && D == (uint32_t)kD && n_rot == 64;
 }
 
-uint32_t attn_tc_splits(uint32_t T, uint32_t rows_max) {
-  return T == 1 ? (rows_max + kRows - 1) / kRows : 1;
+// Error word, then (decode) room for the partials of the largest cluster.
+size_t attn_tc_ws_bytes(uint32_t batch, uint32_t T, uint32_t rows_max) {
+  if (T != 1) return 256;
+  const uint32_t n_tiles = (rows_max + kRows - 1) / kRows;
+  const uint32_t cmax = n_tiles < kMaxCluster ? (n_tiles ? n_tiles : 1u) : kMaxCluster;
+  if (cmax < 2) return 256;
+  return 256 + (size_t)batch * cmax * kH * (kD + 2) * sizeof(float);
 }
 
 cudaError_t launch_attention_tc(const AttnArgs &a, uint32_t rows_max, int *err, cudaStream_t s) {
@@ -547,9 +744,7 @@ cudaError_t launch_attention_tc(const AttnArgs &a, uint32_t rows_max, int *err, 
   P.comp_cap = a.comp_cap;
   P.n_comp = a.n_comp;
   P.top_k = a.top_k;
-  P.n_splits = attn_tc_splits(a.T, rows_max);
-  P.tiles_per_split = a.T == 1 ? 1 : (rows_max + kRows - 1) / kRows;
-  P.n_items = a.batch * a.T * P.n_splits;
+  P.n_q = a.batch * a.T;
   P.c2 = a.scale * 1.4426950408889634f;
   P.q = static_cast<const __nv_bfloat16 *>(a.q);
   P.ring = static_cast<const __nv_bfloat16 *>(a.ring);
@@ -559,13 +754,33 @@ cudaError_t launch_attention_tc(const AttnArgs &a, uint32_t rows_max, int *err, 
   P.cos = a.cos;
   P.sin = a.sin;
   P.out = static_cast<__nv_bfloat16 *>(a.out);
-  P.part = static_cast<float *>(a.ws);
+  P.part = reinterpret_cast<float *>(static_cast<uint8_t *>(a.ws) + 256);
   P.err = err;
   const size_t smem = sizeof(Smem) + 1024;
   static int smem_set = 0;
   cudaError_t e = ensure_smem(attn_tc_kernel, smem, &smem_set);
   if (e != cudaSuccess) return e;
-  const uint32_t grid = min(P.n_items, (uint32_t)num_sms());
+  if (a.T == 1) {
+    const uint32_t n_tiles = (rows_max + kRows - 1) / kRows;
+    P.cluster = pick_cluster(n_tiles, P.n_q, smem);
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = P.cluster;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3(P.n_q * P.cluster);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, attn_tc_kernel, P);
+    note_launches(1);
+    return e != cudaSuccess ? e : cudaGetLastError();
+  }
+  P.cluster = 0;
+  const uint32_t grid = min(P.n_q, (uint32_t)num_sms());
   attn_tc_kernel<<<grid, kThreads, smem, s>>>(P);
   note_launches(1);
   return cudaGetLastError();

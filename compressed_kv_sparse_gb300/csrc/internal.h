@@ -102,7 +102,7 @@ cudaError_t launch_attention(const AttnArgs &a, cudaStream_t s);
 
 // Tensor-core attention (attention_tc.cu): bf16, 64 heads x 512 dims, 64-dim tail.
 bool attn_tc_supported(int dtype, uint32_t H, uint32_t D, uint32_t n_rot);
-uint32_t attn_tc_splits(uint32_t T, uint32_t rows_max);
+size_t attn_tc_ws_bytes(uint32_t batch, uint32_t T, uint32_t rows_max);
 cudaError_t launch_attention_tc(const AttnArgs &a, uint32_t rows_max, int *err, cudaStream_t s);
 cudaError_t launch_ring_commit(int dtype, uint32_t batch, uint32_t T, uint32_t pos0,
                                uint32_t cap_raw, uint32_t head_dim, const void *chunk,

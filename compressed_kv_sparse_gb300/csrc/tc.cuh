@@ -53,18 +53,23 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
 }
 
 // Wait for the phase with the given parity to complete. Returns false (and
-// sets *err) after kWaitLimitNs, or at once if *err is already set.
+// sets *err) after kWaitLimitNs, or once *err is set by another thread. The
+// error word lives in global memory, so it is read only after the wait has
+// lasted kErrPollNs: a read costs an L2 round trip, during which this thread
+// would not see the phase complete.
+constexpr uint64_t kErrPollNs = 20000ull;   // 20 us
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, int *err) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_ns();
   for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((i & 63) == 0) {
-      if (*(volatile int *)err) return false;
-      if (global_ns() - t0 > kWaitLimitNs) {
+      const uint64_t dt = global_ns() - t0;
+      if (dt > kWaitLimitNs) {
         atomicExch(err, 1);
         return false;
       }
+      if (dt > kErrPollNs && (i & 1023) == 0 && *(volatile int *)err) return false;
     }
   }
 }
@@ -126,6 +131,48 @@ __device__ __forceinline__ bool group_sync(uint64_t *bar, uint32_t &phase, int *
   const bool ok = mbar_wait_warp(bar, phase, err);
   phase ^= 1;
   return ok;
+}
+
+// Hardware barrier of the first `count` threads (warps 0 .. count/32 - 1).
+__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+// ---- thread-block clusters and distributed shared memory ------------------
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// Every thread of every CTA of the cluster; orders this CTA's earlier
+// shared-memory writes before the peers' reads that follow their wait.
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Address of the same shared-memory location in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t smem_addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_addr), "r"(rank));
+  return r;
+}
+
+__device__ __forceinline__ float ld_cluster_f32(uint32_t addr) {
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ float4 ld_cluster_v4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
 }
 
 // ---- tcgen05 -------------------------------------------------------------
