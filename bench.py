@@ -36,7 +36,75 @@ import synth  # noqa: E402
 METRIC = ("c4a/c128a decode tok/s & HBM GB/s frac; 4096-chunk prefill tok/s (1×GB300)")
 WORKLOADS = {"flash43": synth.FLASH_STACK, "c4a_decode": synth.C4A_DECODE,
              "c128a_decode": synth.C128A_DECODE, "prefill": synth.C4A_PREFILL,
-             "tiny": synth.TINY}
+             "tiny": synth.TINY, "flash_c4a_layer": synth.FLASH_C4A_LAYER}
+# ncu DRAM counters per call, recorded with the hash of the kernel sources they
+# were taken on; a stale record (sources changed since) reports null
+TRAFFIC_PATH = os.path.join(ROOT, "profiles", "traffic.json")
+CALL_KERNELS = {"index_topk": ("index_", "topk_"), "append": ("append_", "state_reset"),
+                "attn": ("attn_", "ring_commit")}
+
+
+def sources_hash() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for d in ("compressed_kv_sparse_gb300/csrc", "include"):
+        base = os.path.join(ROOT, d)
+        for name in sorted(os.listdir(base)):
+            if name.endswith((".cu", ".cuh", ".h")):
+                with open(os.path.join(base, name), "rb") as f:
+                    h.update(name.encode() + b"\0" + f.read())
+    return h.hexdigest()
+
+
+def recorded_traffic(workload: str, call: str):
+    try:
+        with open(TRAFFIC_PATH) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
+        return None
+    if rec.get("sources_sha256") != sources_hash():
+        return None
+    if call.startswith("attn_r"):
+        call = "attn"
+    e = rec.get("entries", {}).get(workload, {}).get(call)
+    return float(e["bytes_per_call"]) if e else None
+
+
+def write_traffic(csv_path: str, workload: str, captured_on: str, calls: int):
+    """Sum DRAM read + write bytes of one call's kernels from an ncu CSV
+    (--metrics dram__bytes_read.sum,dram__bytes_write.sum) into the record."""
+    import csv
+    import re
+    rows = list(csv.reader(open(csv_path)))
+    hi = next(i for i, r in enumerate(rows) if "Kernel Name" in r)
+    h = rows[hi]
+    ki, mi, vi = h.index("Kernel Name"), h.index("Metric Name"), h.index("Metric Value")
+    ui = h.index("Metric Unit") if "Metric Unit" in h else None
+    scale = {"byte": 1, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9}
+    per_call = {}
+    for r in rows[hi + 1:]:
+        if len(r) <= vi or r[mi] not in ("dram__bytes_read.sum", "dram__bytes_write.sum"):
+            continue
+        name = re.sub(r"^.*?<unnamed>::", "", re.sub(r"\(.*", "", r[ki]).replace("void ", ""))
+        v = float(r[vi].replace(",", "")) * scale.get(r[ui] if ui is not None else "byte", 1)
+        for call, prefixes in CALL_KERNELS.items():
+            if name.startswith(prefixes):
+                per_call[call] = per_call.get(call, 0.0) + v
+    try:
+        with open(TRAFFIC_PATH) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
+        rec = {}
+    if rec.get("sources_sha256") != sources_hash():
+        rec = {"sources_sha256": sources_hash(), "entries": {}}
+    ent = rec["entries"].setdefault(WORKLOADS[workload].name, {})
+    for call, v in per_call.items():
+        ent[call] = {"bytes_per_call": v / calls, "captured_on": captured_on,
+                     "kernels": list(CALL_KERNELS[call])}
+    with open(TRAFFIC_PATH, "w") as f:
+        json.dump(rec, f, indent=1, sort_keys=True)
+        f.write("\n")
+    print(json.dumps(ent))
 
 
 def peaks():
@@ -348,11 +416,11 @@ def run_gpu(args, wl, rank, world, device):
     tensor_bound = not R.decode
     if tensor_bound:
         roof = {"bound": "tensor", "achieved": dc["TFLOP/s"], "peak": bf16s, "unit": "TFLOP/s",
-                "frac": dc["TFLOP/s"] / bf16s, "traffic": None,
+                "frac": dc["TFLOP/s"] / bf16s, "traffic": recorded_traffic(wl.name, dom),
                 "kernel": dom, "peak_kind": f"{peak_kind} bf16 sustained"}
     else:
         roof = {"bound": "hbm", "achieved": dc["GB/s"], "peak": hbm, "unit": "GB/s",
-                "frac": dc["GB/s"] / hbm, "traffic": None, "kernel": dom,
+                "frac": dc["GB/s"] / hbm, "traffic": recorded_traffic(wl.name, dom), "kernel": dom,
                 "peak_kind": f"{peak_kind} hbm copy"}
 
     # end to end: pinned host inputs -> device, step, last output -> host
@@ -520,8 +588,17 @@ def main():
     ap.add_argument("--impl", default="gpu", choices=["gpu", "reference"])
     ap.add_argument("--no-graph", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--write-traffic", metavar="NCU_CSV",
+                    help="record per-call DRAM bytes of --workload from an ncu CSV and exit")
+    ap.add_argument("--captured-on", default=None,
+                    help="with --write-traffic: the workload the counters were taken on")
+    ap.add_argument("--calls", type=int, default=1,
+                    help="with --write-traffic: calls of each kind in the CSV")
     args = ap.parse_args()
     wl = WORKLOADS[args.workload]
+    if args.write_traffic:
+        write_traffic(args.write_traffic, args.workload, args.captured_on or wl.name, args.calls)
+        return
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

@@ -39,6 +39,7 @@ ds4a_status check_cache(const ds4a_layer_cache *c) {
     if (c->index_dim == 0 || c->index_dim > 256 || c->index_dim % 4) return DS4A_ERR_SHAPE;
     if (c->index_rot > c->index_dim || c->index_rot % 2) return DS4A_ERR_SHAPE;
     if (!c->index_comp_kv || !c->index_state_kv || !c->index_state_score) return DS4A_ERR_ARG;
+    if (!c->index_norm || !c->index_norm_max) return DS4A_ERR_ARG;
     if (!c->index_rope_cos || !c->index_rope_sin) return DS4A_ERR_ARG;
   }
   return DS4A_OK;
@@ -123,9 +124,23 @@ ds4a_status ds4a_cache_reset(ds4a_layer_cache *c, ds4a_stream_t stream) {
     st = cuda_status(launch_state_reset(c->index_state_kv, c->index_state_score,
                                         (size_t)c->batch * 8 * c->index_dim, s));
     if (st) return st;
+    st = cuda_status(cudaMemsetAsync(c->index_norm_max, 0, sizeof(uint32_t) * c->batch, s));
+    if (st) return st;
   }
   c->n_tokens = 0;
   return DS4A_OK;
+}
+
+ds4a_status ds4a_index_norms(ds4a_layer_cache *c, ds4a_stream_t stream) {
+  ds4a_status st = check_cache(c);
+  if (st) return st;
+  if (c->ratio != 4) return DS4A_ERR_ARG;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  st = cuda_status(cudaMemsetAsync(c->index_norm_max, 0, sizeof(uint32_t) * c->batch, s));
+  if (st) return st;
+  return cuda_status(launch_index_norms(c->dtype, c->index_comp_kv, c->index_dim, c->batch,
+                                        c->comp_cap, comp_rows(c, c->n_tokens), c->index_norm,
+                                        c->index_norm_max, s));
 }
 
 ds4a_status ds4a_compress_append(ds4a_layer_cache *c, uint32_t pos0, uint32_t T,
@@ -166,12 +181,12 @@ ds4a_status ds4a_compress_append(ds4a_layer_cache *c, uint32_t pos0, uint32_t T,
   if (c->ratio) {
     a.lane[0] = LaneArgs{c->head_dim, c->n_rot, c->attn_comp_kv, c->attn_state_kv,
                          c->attn_state_score, c->rope_cos, c->rope_sin, attn_cand, attn_score,
-                         ape_attn, gamma_attn};
+                         ape_attn, gamma_attn, nullptr, nullptr};
   }
   if (c->ratio == 4) {
     a.lane[1] = LaneArgs{c->index_dim, c->index_rot, c->index_comp_kv, c->index_state_kv,
                          c->index_state_score, c->index_rope_cos, c->index_rope_sin, idx_cand,
-                         idx_score, ape_idx, gamma_idx};
+                         idx_score, ape_idx, gamma_idx, c->index_norm, c->index_norm_max};
   }
   st = cuda_status(launch_append(a, reinterpret_cast<cudaStream_t>(stream)));
   if (st) return st;
@@ -224,6 +239,8 @@ ds4a_status ds4a_index_topk(const ds4a_layer_cache *c, uint32_t pos0, uint32_t T
   a.q_idx = q_idx;
   a.w = w;
   a.keys = c->index_comp_kv;
+  a.norms = c->index_norm;
+  a.norm_max = c->index_norm_max;
   a.cos = c->index_rope_cos;
   a.sin = c->index_rope_sin;
   a.topk = topk;

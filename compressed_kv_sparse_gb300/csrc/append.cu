@@ -73,6 +73,7 @@ __device__ void pool_norm_rope_store(const LaneArgs &L, uint32_t W, uint32_t b, 
   ss = block_sum(ss, red);
   const float inv = 1.0f / sqrtf(ss / (float)width + kRmsEps);
   T *row = comp + ((size_t)b * comp_cap + i) * width;
+  float ss_row = 0.f;   // sum of squares of the stored (rounded) row
 #pragma unroll
   for (int k = 0; k < kMaxPairsPerThread; ++k) {
     const uint32_t j = threadIdx.x + k * blockDim.x;
@@ -91,6 +92,39 @@ __device__ void pool_norm_rope_store(const LaneArgs &L, uint32_t W, uint32_t b, 
     }
     st_elem(row, c, a);
     st_elem(row, c + 1, bb);
+    const float sa = round_to(a, row), sb = round_to(bb, row);
+    ss_row = fmaf(sa, sa, fmaf(sb, sb, ss_row));
+  }
+  if (L.norm) {   // uniform: the indexer lane records the row's norm
+    ss_row = block_sum(ss_row, red);
+    if (threadIdx.x == 0) {
+      // widened by 1e-4 for the rounding of the fp32 sum of squares
+      const float nm = sqrtf(ss_row) * 1.0001f;
+      L.norm[(size_t)b * comp_cap + i] = nm;
+      atomicMax(&L.norm_max[b], __float_as_uint(nm));
+    }
+  }
+}
+
+// Euclidean norm of stored indexer rows (rebuild after the caller wrote rows):
+// one warp per row, the same widening as at append time.
+template <typename T>
+__global__ void index_norms_kernel(const T *rows, uint32_t dim, uint32_t comp_cap,
+                                   uint32_t n_rows, float *norm, uint32_t *norm_max) {
+  const uint32_t b = blockIdx.y, lane = threadIdx.x & 31;
+  const uint32_t r = blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
+  if (r >= n_rows) return;
+  const T *row = rows + ((size_t)b * comp_cap + r) * dim;
+  float ss = 0.f;
+  for (uint32_t c = lane; c < dim; c += 32) {
+    const float v = ld_f32(row, c);
+    ss = fmaf(v, v, ss);
+  }
+  ss = warp_sum(ss);
+  if (lane == 0) {
+    const float nm = sqrtf(ss) * 1.0001f;
+    norm[(size_t)b * comp_cap + r] = nm;
+    atomicMax(&norm_max[b], __float_as_uint(nm));
   }
 }
 
@@ -309,6 +343,21 @@ cudaError_t launch_state_reset(float *kv, float *score, size_t n, cudaStream_t s
   if (!n) return cudaSuccess;
   const int blocks = (int)((n + 255) / 256 < 1184 ? (n + 255) / 256 : 1184);
   state_reset_kernel<<<blocks, 256, 0, s>>>(kv, score, n);
+  note_launches(1);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_index_norms(int dtype, const void *rows, uint32_t dim, uint32_t batch,
+                               uint32_t comp_cap, uint32_t n_rows, float *norm,
+                               uint32_t *norm_max, cudaStream_t s) {
+  if (n_rows == 0) return cudaSuccess;
+  const dim3 grid((n_rows + 7) / 8, batch);
+  if (dtype == DS4A_BF16)
+    index_norms_kernel<<<grid, 256, 0, s>>>(static_cast<const __nv_bfloat16 *>(rows), dim,
+                                            comp_cap, n_rows, norm, norm_max);
+  else
+    index_norms_kernel<<<grid, 256, 0, s>>>(static_cast<const float *>(rows), dim, comp_cap,
+                                            n_rows, norm, norm_max);
   note_launches(1);
   return cudaGetLastError();
 }

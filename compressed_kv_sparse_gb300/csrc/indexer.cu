@@ -44,18 +44,18 @@ __host__ __device__ inline IndexWs index_ws_split(void *ws, uint32_t nq, uint32_
   return IndexWs{base, base + ((qsz + 63) & ~(size_t)63)};
 }
 
-// Workspace of bf16 layers: err word, qbf [nq][Hi][Di] bf16, norms
-// [B][comp_cap], scores [nq][comp_cap] (fp32), per-query histograms of the
-// scores' top 12 key bits [nq][4096], per-sequence max key norm [B], per-query
-// control words [nq][4] (candidate count, finished-block ticket, overflow) and
-// candidate rows [nq][kCandGlobal].
+// Workspace of bf16 layers: err word, qbf [nq][Hi][Di] bf16, scores
+// [nq][comp_cap] (fp32), per-query histograms of the scores' top 12 key bits
+// [nq][4096], per-query control words [nq][4] (candidate count, finished-block
+// ticket, overflow) and candidate rows [nq][kCandGlobal]. The row norms of the
+// error bound live in the cache (written when rows are appended).
 constexpr uint32_t kHistBins = 4096;
 constexpr uint32_t kCandGlobal = 4096;
 struct TcWs {
   int *err;
-  float *norms, *scores;
+  float *scores;
   __nv_bfloat16 *qbf;
-  uint32_t *hist, *maxnorm, *ctrl, *cand;
+  uint32_t *hist, *ctrl, *cand;
 };
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 inline TcWs tc_ws_split(void *ws, uint32_t nq, uint32_t B, uint32_t Hi, uint32_t Di,
@@ -67,14 +67,10 @@ inline TcWs tc_ws_split(void *ws, uint32_t nq, uint32_t B, uint32_t Hi, uint32_t
   off = align_up(off + 16, 1024);
   w.qbf = reinterpret_cast<__nv_bfloat16 *>(base + off);
   off = align_up(off + (size_t)nq * Hi * Di * 2, 256);
-  w.norms = reinterpret_cast<float *>(base + off);
-  off = align_up(off + (size_t)B * comp_cap * 4, 256);
   w.scores = reinterpret_cast<float *>(base + off);
   off = align_up(off + (size_t)nq * comp_cap * 4, 256);
   w.hist = reinterpret_cast<uint32_t *>(base + off);
   off = align_up(off + (size_t)nq * kHistBins * 4, 256);
-  w.maxnorm = reinterpret_cast<uint32_t *>(base + off);
-  off = align_up(off + (size_t)B * 4, 256);
   w.ctrl = reinterpret_cast<uint32_t *>(base + off);
   off = align_up(off + (size_t)nq * 16, 256);
   w.cand = reinterpret_cast<uint32_t *>(base + off);
@@ -85,14 +81,13 @@ inline TcWs tc_ws_split(void *ws, uint32_t nq, uint32_t B, uint32_t Hi, uint32_t
 
 // bf16 layers: q' = rotated query rounded to bf16 (fp32 recipe), one thread
 // per pair of dims; the same grid clears the call's counters (error word,
-// max norms, control words and, when the scorer builds them, histograms).
+// control words and, when the scorer builds them, histograms).
 __global__ void index_qbf_kernel(IndexArgs a, TcWs w, bool clear_hist) {
   const uint32_t Hi = a.n_heads, Di = a.dim, n_nope = Di - a.rot;
   const size_t nq = (size_t)a.batch * a.T;
   const size_t npair = nq * Hi * Di / 2;
   const size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x;
   if (i == 0) *w.err = 0;
-  if (i < a.batch) w.maxnorm[i] = 0u;
   if (i < nq * 4) w.ctrl[i] = 0u;
   if (clear_hist && i < nq * kHistBins) w.hist[i] = 0u;
   if (i >= npair) return;
@@ -472,7 +467,7 @@ __global__ void __launch_bounds__(kSelectThreads)
     return;
   }
   float *sc = w.scores + (size_t)qi * a.comp_cap;
-  const float *nr = w.norms + (size_t)b * a.comp_cap;
+  const float *nr = a.norms + (size_t)b * a.comp_cap;
   const __nv_bfloat16 *qb = w.qbf + (size_t)qi * Hi * Di;
   const __nv_bfloat16 *wq = static_cast<const __nv_bfloat16 *>(a.w) + (size_t)qi * Hi;
   uint32_t *ctrl = w.ctrl + (size_t)qi * 4;
@@ -535,7 +530,7 @@ __global__ void __launch_bounds__(kSelectThreads)
   float At = 0.f;
   for (uint32_t i = 0; i < 32; ++i) At += s_red[i];
   const float A = At * (1.0f + 1e-5f) * cb;
-  const float E = A * __uint_as_float(w.maxnorm[b]);
+  const float E = A * __uint_as_float(a.norm_max[b]);
   const float theta_s = key_to_float(s_misc[0] << 20);
   const float theta = theta_s - E - fabsf(theta_s) * (2.0f * kRel);
   auto err_of = [&](float S, float nm) { return A * nm + fabsf(S) * kRel; };
@@ -742,9 +737,7 @@ cudaError_t launch_index_tc(const IndexArgs &a, cudaStream_t s) {
     t.qbf = w.qbf;
     t.w = a.w;
     t.scores = w.scores;
-    t.norms = w.norms;
     t.hist = w.hist;
-    t.maxnorm = w.maxnorm;
     t.err = w.err;
     cudaError_t e = launch_index_score_tc(t, s);
     if (e != cudaSuccess) return e;

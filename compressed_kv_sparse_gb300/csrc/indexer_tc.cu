@@ -1,6 +1,6 @@
 // Indexer scores on the tensor cores (bf16 layers): approximate fp32 scores
-// plus the per-row key norms that bound their error ("【#3】ds4.c を読み解く"
-// §6 indexer; vLLM DeepSeek V4 page, DSA).
+// whose error the certified top-k bounds with the row norms kept in the cache
+// ("【#3】ds4.c を読み解く" §6 indexer; vLLM DeepSeek V4 page, DSA).
 //
 // For every visible compressed index row s of sequence b and every query t of
 // a group of QG queries:  S~(t, s) = sum_h w_h(t) * max(0, q'_h(t) . k_s).
@@ -9,9 +9,9 @@
 // rotated query heads (N = 64 QG); the fp32 accumulator sits in TMEM (two
 // buffers so the epilogue of one tile overlaps the MMA of the next). Each
 // epilogue thread owns one TMEM lane = one key row: it reads its QG x 64 head
-// dots, applies ReLU and the head weights, and also sums the squares of its
-// key row straight from the swizzled shared-memory tile (the error bound of
-// the certified top-k uses ||k_s||).
+// dots and applies ReLU and the head weights; with QG = 1 (decode) it also
+// counts the top 12 bits of each score key into a per-CTA histogram that the
+// selection uses to place its threshold.
 //
 // Persistent kernel, one CTA per SM, 6 warps: warp 0 issues TMA, warp 1 issues
 // MMAs (one thread each), warps 2..5 run the epilogue. Work items are
@@ -40,9 +40,8 @@ struct Cfg {
   static constexpr int kStages = QG == 1 ? 5 : 4;
   static constexpr int kHistBytes = QG == 1 ? 4096 * 4 : 0;   // per-CTA key histogram
   static constexpr int kBBytes = N * kDim * 2;
-  // QG == 1: two 64-column score accumulators and two 128-column K K^T tiles
-  // (their diagonals are the key norms); QG == 4: two 256-column accumulators
-  static constexpr int kTmemCols = 512;
+  // two accumulators of N columns (the allocation is a power of two >= 32)
+  static constexpr int kTmemCols = QG == 1 ? 128 : 512;
   static constexpr size_t kSmem = 1024 + (size_t)kStages * kABytes + kBBytes + 1024 +
                                   4 * QG * kHeads * 4 + kHistBytes;
 };
@@ -51,9 +50,7 @@ struct ScoreParams {
   uint32_t batch, T, pos0, comp_cap, n_comp, n_groups, tiles_per, total_items;
   const __nv_bfloat16 *w;   // [B][T][Hi]
   float *scores;            // [B][T][comp_cap]
-  float *norms;             // [B][comp_cap]
   uint32_t *hist;           // [B*T][4096] counts of the top 12 bits of the score keys
-  uint32_t *maxnorm;        // [B] largest key norm (float bits)
   int *err;
 };
 
@@ -106,7 +103,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(&a_full[s], 1);
-      mbar_init(&a_empty[s], QG == 1 ? 1 : 1 + 4);
+      mbar_init(&a_empty[s], 1);
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&acc_full[s], 1);
@@ -197,15 +194,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint64_t bd = sdesc_sw128(b_base + (kk / 4) * (C::kBBytes / 2) + koff);
           mma_bf16(d, ad, bd, idesc, kk > 0 ? 1u : 0u);
         }
-        if (QG == 1) {
-          // K K^T of the tile: row r's diagonal element is ||k_r||^2
-          constexpr uint32_t idn = idesc_bf16_f32(kRows, kRows);
-#pragma unroll
-          for (uint32_t kk = 0; kk < kDim / 16; ++kk) {
-            const uint64_t ad = sdesc_sw128(a0 + (kk / 4) * kKBlockBytes + (kk % 4) * 32);
-            mma_bf16(tmem + 128 + acc * 128, ad, ad, idn, kk > 0 ? 1u : 0u);
-          }
-        }
         mma_commit(&a_empty[stage]);
         mma_commit(&acc_full[acc]);
         if (++stage == C::kStages) {
@@ -222,7 +210,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t row = lg * 32 + lane;
     float *sw = sw_all + (warp - 2) * QG * kHeads;   // this warp's copy of the weights
     const uint32_t et = threadIdx.x - 64;             // 0..127
-    uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0, epi_phase = 0;
+    uint32_t acc = 0, acc_phase = 0, epi_phase = 0;
     int32_t cur = -1;
     bool ok = true;
     // one query per group when QG == 1: its key histogram is gathered here and
@@ -241,16 +229,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (QG == 1) {
       for (uint32_t i = et; i < 4096; i += 128) shist[i] = 0;
     }
-    // running max of the key norms of one sequence, added to the global max
-    // when the sequence changes
-    float run_max = 0.f;
-    int32_t run_b = -1;
-    auto flush_max = [&]() {
-      if (run_b < 0) return;
-      const float mx = warp_max(run_max);
-      if (lane == 0) atomicMax(&P.maxnorm[run_b], __float_as_uint(mx));
-      run_max = 0.f;
-    };
     for (uint32_t it = it0; it < it1 && ok; ++it) {
       uint32_t b, g, tile;
       if (!decode_item<QG>(P, it, b, g, tile)) continue;
@@ -269,57 +247,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         cur = bg;
       }
-      // the first query group that processes a tile writes its key norms
-      const bool first = g == 0 || tile * kRows >= vis_of(P, g * QG - 1);
-      float ss = 0.f;
-      if (QG != 1) {
-        // QG == 4: ||k_r||^2 from the swizzled tile (the row's two 128-byte
-        // lines hold its 128 values, chunk order permuted, which a sum of
-        // squares ignores); only the writing group computes it
-        if (!mbar_wait_warp(&a_full[stage], phase, P.err)) {
-          ok = false;
-          break;
-        }
-        if (first) {
-          const uint8_t *tileA = sA + (size_t)stage * kABytes;
-#pragma unroll
-          for (int kb = 0; kb < 2; ++kb) {
-            const uint8_t *line = tileA + kb * kKBlockBytes + (row >> 3) * 1024 + (row & 7) * 128;
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              const uint4 v = *reinterpret_cast<const uint4 *>(line + ((j + row) & 7) * 16);
-              const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                const float lo = __uint_as_float(w4[e] << 16);
-                const float hi = __uint_as_float(w4[e] & 0xFFFF0000u);
-                ss = fmaf(lo, lo, ss);
-                ss = fmaf(hi, hi, ss);
-              }
-            }
-          }
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&a_empty[stage]);
-      }
-      if (++stage == C::kStages) {
-        stage = 0;
-        phase ^= 1;
-      }
       if (!mbar_wait_warp(&acc_full[acc], acc_phase, P.err)) {
         ok = false;
         break;
       }
       tc_fence_after();
       const uint32_t grow = tile * kRows + row;
-      if (QG == 1) {
-        uint32_t dg[32];
-        tmem_ld32(tmem + ((lg * 32) << 16) + 128 + acc * 128 + lg * 32, dg);
-        tmem_ld_wait();
-#pragma unroll
-        for (int j = 0; j < 32; ++j)
-          if ((uint32_t)j == lane) ss = __uint_as_float(dg[j]);
-      }
 #pragma unroll 1
       for (int q = 0; q < QG; ++q) {
         uint32_t r0[32], r1[32];
@@ -361,18 +294,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive(&acc_empty[acc]);
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1;
-      if (first) {
-        // widened by 1e-4 for the rounding of the fp32 sum of squares
-        const float nm = grow < P.n_comp ? sqrtf(ss) * 1.0001f : 0.f;
-        if (grow < P.n_comp) P.norms[(size_t)b * P.comp_cap + grow] = nm;
-        if ((int32_t)b != run_b) {   // warp-uniform: items are the same for all lanes
-          flush_max();
-          run_b = (int32_t)b;
-        }
-        run_max = fmaxf(run_max, nm);
-      }
     }
-    if (ok) flush_max();
     if (QG == 1 && ok && cur >= 0) flush_hist(cur);
   }
   tc_fence_before();
@@ -407,9 +329,7 @@ cudaError_t launch_qg(const IndexTcArgs &a, cudaStream_t s) {
   P.total_items = a.batch * P.n_groups * P.tiles_per;
   P.w = static_cast<const __nv_bfloat16 *>(a.w);
   P.scores = a.scores;
-  P.norms = a.norms;
   P.hist = a.hist;
-  P.maxnorm = a.maxnorm;
   P.err = a.err;
   if (P.total_items == 0) return cudaSuccess;
   static int smem_set = 0;

@@ -39,6 +39,8 @@ struct LaneArgs {
   const float *cos, *sin; // [max_pos][n_rot/2]
   const void *cand, *score;       // [B][T][width]
   const void *ape, *gamma;        // [W][width], [width]
+  float *norm;                    // [B][comp_cap] row norms (indexer lane) or NULL
+  uint32_t *norm_max;             // [B] float bits of the largest norm
 };
 
 struct AppendArgs {
@@ -57,6 +59,8 @@ struct IndexArgs {
   uint32_t batch, T, pos0, n_heads, dim, rot, top_k, comp_cap, n_comp;
   int dtype;
   const void *q_idx, *w, *keys;   // [B][T][Hi][Di], [B][T][Hi], [B][comp_cap][Di]
+  const float *norms;             // [B][comp_cap] row norms
+  const uint32_t *norm_max;       // [B] float bits of the largest row norm
   const float *cos, *sin;
   int32_t *topk;
   void *ws;
@@ -72,9 +76,7 @@ struct IndexTcArgs {
   const void *qbf;    // [B][T][64][128] bf16, rotated queries
   const void *w;      // [B][T][64] bf16
   float *scores;      // [B][T][comp_cap]
-  float *norms;       // [B][comp_cap]
   uint32_t *hist;     // [B*T][4096], zeroed before the call
-  uint32_t *maxnorm;  // [B], zeroed before the call
   int *err;
 };
 bool index_tc_supported(uint32_t n_heads, uint32_t dim);
@@ -108,5 +110,8 @@ cudaError_t launch_ring_commit(int dtype, uint32_t batch, uint32_t T, uint32_t p
                                uint32_t cap_raw, uint32_t head_dim, const void *chunk,
                                void *ring, cudaStream_t s);
 cudaError_t launch_state_reset(float *kv, float *score, size_t n, cudaStream_t s);
+cudaError_t launch_index_norms(int dtype, const void *rows, uint32_t dim, uint32_t batch,
+                               uint32_t comp_cap, uint32_t n_rows, float *norm,
+                               uint32_t *norm_max, cudaStream_t s);
 
 }  // namespace ds4a

@@ -41,13 +41,15 @@ class LayerCacheC(ctypes.Structure):
         ("raw_kv", ctypes.c_void_p), ("attn_comp_kv", ctypes.c_void_p),
         ("attn_state_kv", ctypes.c_void_p), ("attn_state_score", ctypes.c_void_p),
         ("index_comp_kv", ctypes.c_void_p), ("index_state_kv", ctypes.c_void_p),
-        ("index_state_score", ctypes.c_void_p), ("rope_cos", ctypes.c_void_p),
+        ("index_state_score", ctypes.c_void_p), ("index_norm", ctypes.c_void_p),
+        ("index_norm_max", ctypes.c_void_p), ("rope_cos", ctypes.c_void_p),
         ("rope_sin", ctypes.c_void_p), ("index_rope_cos", ctypes.c_void_p),
         ("index_rope_sin", ctypes.c_void_p), ("rope_max_pos", ctypes.c_uint32)]
 
 
 EXPORTS = {
     "ds4a_cache_reset": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p]),
+    "ds4a_index_norms": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p]),
     "ds4a_compress_append": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_uint32, ctypes.c_uint32]
                              + [ctypes.c_void_p] * 11),
     "ds4a_index_topk": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_uint32, ctypes.c_uint32,
@@ -152,6 +154,7 @@ class LayerCache:
         self.raw_kv = z(batch, cap_raw, head_dim)
         self.attn_comp_kv = self.attn_state_kv = self.attn_state_score = None
         self.index_comp_kv = self.index_state_kv = self.index_state_score = None
+        self.index_norm = self.index_norm_max = None
         if ratio:
             self.attn_comp_kv = z(batch, comp_cap, head_dim)
             self.attn_state_kv = z(batch, W, head_dim, dt=torch.float32)
@@ -162,6 +165,8 @@ class LayerCache:
             self.index_state_kv = z(batch, 8, index_dim, dt=torch.float32)
             self.index_state_score = torch.full((batch, 8, index_dim), float("-inf"),
                                                 device=device)
+            self.index_norm = z(batch, comp_cap, dt=torch.float32)
+            self.index_norm_max = z(batch, dt=torch.int32)
         self.rope_cos, self.rope_sin = rope_table(base, n_rot, rope_max_pos, device)
         self.index_rope_cos = self.index_rope_sin = None
         if ratio == 4:
@@ -174,7 +179,8 @@ class LayerCache:
             raw_kv=_ptr(self.raw_kv), attn_comp_kv=_ptr(self.attn_comp_kv),
             attn_state_kv=_ptr(self.attn_state_kv), attn_state_score=_ptr(self.attn_state_score),
             index_comp_kv=_ptr(self.index_comp_kv), index_state_kv=_ptr(self.index_state_kv),
-            index_state_score=_ptr(self.index_state_score), rope_cos=_ptr(self.rope_cos),
+            index_state_score=_ptr(self.index_state_score), index_norm=_ptr(self.index_norm),
+            index_norm_max=_ptr(self.index_norm_max), rope_cos=_ptr(self.rope_cos),
             rope_sin=_ptr(self.rope_sin), index_rope_cos=_ptr(self.index_rope_cos),
             index_rope_sin=_ptr(self.index_rope_sin), rope_max_pos=rope_max_pos)
 
@@ -190,7 +196,8 @@ class LayerCache:
         return ctypes.byref(self.c)
 
     def load_state(self, hist: Dict[str, torch.Tensor], n_tokens: int):
-        """Copy a cache snapshot (same layout as the tensors here) in; set n_tokens."""
+        """Copy a cache snapshot (same layout as the tensors here) in, set
+        n_tokens and rebuild the indexer row norms (ds4a_index_norms)."""
         for name, t in hist.items():
             dst = getattr(self, name)
             if name in ("attn_comp_kv", "index_comp_kv") and t.shape[1] < dst.shape[1]:
@@ -198,6 +205,8 @@ class LayerCache:
             else:
                 dst.copy_(t)
         self.n_tokens = n_tokens
+        if self.ratio == 4:
+            ds4a_index_norms(self)
 
     def snapshot(self) -> Dict[str, torch.Tensor]:
         names = ["raw_kv", "attn_comp_kv", "attn_state_kv", "attn_state_score",
@@ -210,6 +219,10 @@ class LayerCache:
 
 def ds4a_cache_reset(cache: LayerCache, stream=None):
     _check(load().ds4a_cache_reset(cache.ref(), _stream(stream)), "ds4a_cache_reset")
+
+
+def ds4a_index_norms(cache: LayerCache, stream=None):
+    _check(load().ds4a_index_norms(cache.ref(), _stream(stream)), "ds4a_index_norms")
 
 
 def ds4a_compress_append(cache: LayerCache, pos0: int, T: int, inp: Dict[str, torch.Tensor],

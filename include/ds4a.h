@@ -78,6 +78,14 @@ typedef enum { DS4A_F32 = 0, DS4A_BF16 = 1 } ds4a_dtype;
  *  index_comp_kv     [B][comp_cap][Di]    compressed indexer rows (ratio 4, else NULL)
  *  index_state_kv    [B][8][Di] fp32
  *  index_state_score [B][8][Di] fp32
+ *  index_norm        [B][comp_cap] fp32 (ratio 4): Euclidean norm of each stored
+ *                    indexer row, widened by 1e-4; the certified top-k bounds
+ *                    the error of its tensor-core scores with it. Written by
+ *                    ds4a_compress_append; after writing rows any other way,
+ *                    call ds4a_index_norms. Not part of the pages' cache.
+ *  index_norm_max    [B] uint32 (ratio 4): float bits of the largest
+ *                    index_norm written to each sequence since the last
+ *                    ds4a_cache_reset.
  *  rope_cos/rope_sin [rope_max_pos][n_rot/2] fp32: this layer's rotation
  *                    coefficients (ds4a_rope_table), base = compression base on
  *                    layers with ratio != 0, normal base otherwise (page §8).
@@ -98,6 +106,8 @@ typedef struct {
   float *attn_state_kv, *attn_state_score;
   void *index_comp_kv;
   float *index_state_kv, *index_state_score;
+  float *index_norm;
+  uint32_t *index_norm_max;
   const float *rope_cos, *rope_sin;
   const float *index_rope_cos, *index_rope_sin;
   uint32_t rope_max_pos;
@@ -108,10 +118,21 @@ enum { DS4A_CALL_APPEND = 0, DS4A_CALL_INDEX_TOPK = 1, DS4A_CALL_ATTN_DECODE = 2
        DS4A_CALL_ATTN_PREFILL = 3 };
 
 /*
- * Empty the compressor state (kv 0, score -inf) and set n_tokens = 0. Rows
- * are left as they are. Asynchronous on `stream`.
+ * Empty the compressor state (kv 0, score -inf), zero index_norm_max and set
+ * n_tokens = 0. Rows are left as they are. Asynchronous on `stream`.
  */
 ds4a_status ds4a_cache_reset(ds4a_layer_cache *cache, ds4a_stream_t stream);
+
+/*
+ * Recompute index_norm for rows 0 .. n_comp - 1 of every sequence (n_comp =
+ * compressed rows of n_tokens tokens) and index_norm_max from them, for a
+ * ratio-4 cache whose indexer rows were written by the caller (a restored or
+ * imported cache). The pages have no counterpart: the norms serve the
+ * certified top-k only. Asynchronous on `stream`.
+ * Errors: DS4A_ERR_ARG (not ratio 4, or a cache field missing),
+ * DS4A_ERR_CUDA.
+ */
+ds4a_status ds4a_index_norms(ds4a_layer_cache *cache, ds4a_stream_t stream);
 
 /*
  * Append tokens pos0 .. pos0+T-1 of every sequence (page §4 compressor steps

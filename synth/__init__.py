@@ -130,7 +130,14 @@ FLASH_STACK = Workload(
     layers=tuple(LayerShape(ratio=flash_ratio(il)) for il in range(43)),
     context=131072, mode="decode")
 
-WORKLOADS = {w.name: w for w in (TINY, C128A_DECODE, C4A_DECODE, C4A_PREFILL, FLASH_STACK)}
+# One c4a layer of the Flash stack alone (same shape, batch and context): a
+# measurement case for counters that cannot be captured on the whole stack.
+FLASH_C4A_LAYER = Workload(
+    name="flash_c4a_layer_b8_ctx131072", seed=4, batch=8,
+    layers=(LayerShape(ratio=4),), context=131072, mode="decode")
+
+WORKLOADS = {w.name: w for w in (TINY, C128A_DECODE, C4A_DECODE, C4A_PREFILL, FLASH_STACK,
+                                 FLASH_C4A_LAYER)}
 
 
 def comp_capacity(shape: LayerShape, n_tokens: int) -> int:

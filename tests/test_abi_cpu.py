@@ -87,8 +87,9 @@ def _fake_cache(ratio=4, n_tokens=10, dtype=lib.DS4A_BF16):
                            batch=2, cap_raw=128, comp_cap=16, dtype=dtype, n_tokens=n_tokens,
                            raw_kv=fake, attn_comp_kv=fake, attn_state_kv=fake,
                            attn_state_score=fake, index_comp_kv=fake, index_state_kv=fake,
-                           index_state_score=fake, rope_cos=fake, rope_sin=fake,
-                           index_rope_cos=fake, index_rope_sin=fake, rope_max_pos=1000)
+                           index_state_score=fake, index_norm=fake, index_norm_max=fake,
+                           rope_cos=fake, rope_sin=fake, index_rope_cos=fake,
+                           index_rope_sin=fake, rope_max_pos=1000)
 
 
 def test_argument_checks_reject_before_launch(L):
@@ -116,6 +117,11 @@ def test_argument_checks_reject_before_launch(L):
     bad = _fake_cache()
     bad.n_rot = 1000
     assert L.ds4a_compress_append(ctypes.byref(bad), 10, 1, *P, None, None) == -2
+    # a ratio-4 cache without its row norms; the norm rebuild on another ratio
+    bad = _fake_cache()
+    bad.index_norm = None
+    assert L.ds4a_compress_append(ctypes.byref(bad), 10, 1, *P, None, None) == -1
+    assert L.ds4a_index_norms(ctypes.byref(_fake_cache(ratio=128)), None) == -1
     # index: reads beyond the appended tokens, workspace too small, bad ratio
     assert L.ds4a_index_topk(r, 10, 1, fake, fake, 64, 512, fake, fake, 1 << 30, None) == -4
     assert L.ds4a_index_topk(r, 9, 1, fake, fake, 64, 512, fake, fake, 16, None) == -8

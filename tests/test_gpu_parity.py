@@ -114,6 +114,36 @@ def test_append_chunked_equals_one_call_on_gpu_and_oracle():
     compare_cache(gc, oc, "bf16", "continuity")
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_index_norms_written_at_append(dtype):
+    """Every indexer row appended (chunk and decode paths) gets its Euclidean
+    norm, widened by 1e-4, in index_norm and the running maximum in
+    index_norm_max; ds4a_index_norms recomputes the same values from the rows
+    (the certified top-k bounds its tensor-core scores with them)."""
+    lib = lib_()
+    shape = synth.LayerShape(ratio=4, head_dim=128 if dtype == "f32" else 512,
+                             index_dim=32 if dtype == "f32" else 128, dtype=dtype)
+    wl = synth.Workload("norm", 12, 2, (shape,), 0, "prefill")
+    T, n_dec = 301, 9
+    cap = (T + n_dec) // 4 + 1
+    gc = gpu_cache(shape, 2, cap, T + n_dec + 1, synth.empty_history(wl, 0, cap), 0)
+    chunk = torch.empty((2, T, shape.head_dim), dtype=gc.torch_dtype, device=DEV)
+    lib.ds4a_compress_append(gc, 0, T, to_dev(synth.step_inputs(wl, 0, 0, T)),
+                             raw_chunk_out=chunk)
+    for p in range(T, T + n_dec):
+        lib.ds4a_compress_append(gc, p, 1, to_dev(synth.step_inputs(wl, 0, p, 1)))
+    torch.cuda.synchronize()
+    n = (T + n_dec) // 4
+    want = torch.linalg.vector_norm(gc.index_comp_kv[:, :n].double(), dim=-1) * 1.0001
+    assert torch.allclose(gc.index_norm[:, :n].double(), want, rtol=1e-5, atol=0)
+    appended = gc.index_norm[:, :n].clone()
+    assert torch.equal(gc.index_norm_max.view(torch.float32), appended.max(dim=1).values)
+    lib.ds4a_index_norms(gc)
+    torch.cuda.synchronize()
+    assert torch.allclose(gc.index_norm[:, :n].double(), want, rtol=1e-5, atol=0)
+    assert torch.equal(gc.index_norm_max.view(torch.float32), gc.index_norm[:, :n].max(dim=1).values)
+
+
 # ------------------------------------------------------------------ indexer
 
 def run_index(lib, shape, B, p0, T, seed=11, grid=False, queries=None):
