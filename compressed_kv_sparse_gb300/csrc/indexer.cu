@@ -193,6 +193,12 @@ __global__ void __launch_bounds__(kRowsPerBlock)
 }
 
 // Order-preserving unsigned key of an fp32 score (+0 and -0 share a key).
+__device__ __forceinline__ uint32_t warp_sum_u32(uint32_t v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
 __device__ __forceinline__ uint32_t score_key(float f) {
   if (f == 0.f) f = 0.f;
   const uint32_t u = __float_as_uint(f);
@@ -442,7 +448,9 @@ __global__ void __launch_bounds__(kSelectThreads)
   __shared__ uint32_t hist[256];
   __shared__ uint32_t wsum[33];
   __shared__ uint32_t sel[2];
-  __shared__ uint32_t s_misc[4];   // bin, last-block flag, band count, tie count
+  // bin of the k-th key, last-block flag, band count, tie / in count, keys above
+  // the bin, second-level bin
+  __shared__ uint32_t s_misc[6];
   __shared__ float s_red[32];
   __nv_bfloat16 *qsm = reinterpret_cast<__nv_bfloat16 *>(dyn4);   // [64][kQS]
   float *wsh = reinterpret_cast<float *>(qsm + 64 * kQS);           // [64]
@@ -520,6 +528,7 @@ __global__ void __launch_bounds__(kSelectThreads)
       for (uint32_t j = 0; j < 4; ++j) {
         if (cum + c4[j] >= k) {
           s_misc[0] = kHistBins - 1 - (4 * threadIdx.x + j);
+          s_misc[4] = cum;
           break;
         }
         cum += c4[j];
@@ -581,68 +590,129 @@ __global__ void __launch_bounds__(kSelectThreads)
     }
     const uint32_t words = (vis + 31) / 32;
     for (uint32_t i = threadIdx.x; i < words; i += blockDim.x) bitmap[i] = 0u;
+    // the k-th largest S~ lies in 12-bit key bin b* with `above` keys over it;
+    // a histogram of the next 12 key bits of the candidates in b* narrows it
+    // to one 24-bit key interval [t_lo, t_hi] (every row of b* is a candidate)
+    uint32_t *h2 = reinterpret_cast<uint32_t *>(kbuf);   // [4096], free until rescoring
+    for (uint32_t i = threadIdx.x; i < kHistBins; i += blockDim.x) h2[i] = 0u;
+    if (threadIdx.x == 0) s_misc[5] = 0xffffffffu;
     __syncthreads();
-    const float tau = key_to_float(
-        radix_kth([&](uint32_t j) { return score_key(cS[j]); }, nc, k, hist, sel, &need));
-    const float hi_cut = tau + E + fabsf(tau) * kRel;
-    const float lo_cut = tau - E - fabsf(tau) * kRel;
+    const uint32_t bstar = s_misc[0], need_b = k - s_misc[4];
     for (uint32_t j = threadIdx.x; j < nc; j += blockDim.x) {
-      const float S = cS[j], e = ce[j];
-      if (S - e > hi_cut)
-        cS[j] = INFINITY;
-      else if (S + e < lo_cut)
-        cS[j] = -INFINITY;
+      const uint32_t kk = score_key(cS[j]);
+      if ((kk >> 20) == bstar) atomicAdd(&h2[(kk >> 8) & (kHistBins - 1)], 1u);
     }
     __syncthreads();
-    for (uint32_t j = warp; j < nc; j += 32) {
-      const float v = cS[j];
-      if (v == INFINITY || v == -INFINITY) continue;
-      const float V = rescore_row(qsm, wsh, kb, rel, keys + (size_t)cidx[j] * Di, lane);
-      if (lane == 0) cS[j] = V;
-    }
-    __syncthreads();
-    auto key = [&](uint32_t j) { return score_key(cS[j]); };
-    const uint32_t kth = radix_kth(key, nc, k, hist, sel, &need);
-    // rows above the k-th key are in; of the rows at it, the `need` lowest
-    // indices (rank among tied rows by index)
-    if (threadIdx.x == 0) s_misc[3] = 0;
-    __syncthreads();
-    for (uint32_t j = threadIdx.x; j < nc; j += blockDim.x) {
-      const uint32_t kk = key(j);
-      if (kk > kth) atomicOr(&bitmap[cidx[j] >> 5], 1u << (cidx[j] & 31));
-      else if (kk == kth) atomicAdd(&s_misc[3], 1u);
-    }
-    __syncthreads();
-    if (s_misc[3] == need) {
-      for (uint32_t j = threadIdx.x; j < nc; j += blockDim.x)
-        if (key(j) == kth) atomicOr(&bitmap[cidx[j] >> 5], 1u << (cidx[j] & 31));
-    } else {
-      // more tied rows than places: keep the lowest indices
-      uint32_t nd2;
-      const uint32_t ith = radix_kth(
-          [&](uint32_t j) { return key(j) == kth ? ~cidx[j] : 0u; }, nc, need, hist, sel, &nd2);
-      for (uint32_t j = threadIdx.x; j < nc; j += blockDim.x)
-        if (key(j) == kth && ~cidx[j] >= ith) atomicOr(&bitmap[cidx[j] >> 5], 1u << (cidx[j] & 31));
-    }
-    __syncthreads();
-    // ascending output from the bitmap
-    const uint32_t per_t = (words + blockDim.x - 1) / blockDim.x;
-    const uint32_t w0 = threadIdx.x * per_t, w1 = min(words, w0 + per_t);
-    uint32_t cnt = 0;
-    for (uint32_t i = w0; i < w1; ++i) cnt += __popc(bitmap[i]);
-    uint32_t tot;
-    uint32_t pos = block_excl_scan(cnt, wsum, &tot);
-    for (uint32_t i = w0; i < w1; ++i) {
-      uint32_t m = bitmap[i];
-      while (m) {
-        const uint32_t bit = __ffs(m) - 1;
-        if (pos < k) out[pos] = (int32_t)(i * 32 + bit);
-        ++pos;
-        m &= m - 1;
+    {
+      uint32_t c4[4], loc = 0;
+#pragma unroll
+      for (uint32_t j = 0; j < 4; ++j) {
+        c4[j] = h2[kHistBins - 1 - (4 * threadIdx.x + j)];
+        loc += c4[j];
+      }
+      uint32_t tot;
+      uint32_t cum = block_excl_scan(loc, wsum, &tot);
+      if (cum < need_b && cum + loc >= need_b) {
+#pragma unroll
+        for (uint32_t j = 0; j < 4; ++j) {
+          if (cum + c4[j] >= need_b) {
+            s_misc[5] = kHistBins - 1 - (4 * threadIdx.x + j);
+            break;
+          }
+          cum += c4[j];
+        }
       }
     }
-    for (uint32_t j = tot + threadIdx.x; j < k; j += blockDim.x) out[j] = -1;
-    return;
+    __syncthreads();
+    bool ok = s_misc[5] != 0xffffffffu;
+    const uint32_t kpre = (bstar << 20) | (s_misc[5] << 8);
+    const float t_lo = key_to_float(kpre), t_hi = key_to_float(kpre | 0xffu);
+    // rows with L > t_hi + E beat the exact k-th score, rows with U < t_lo - E
+    // are beaten by k rows; only the band between can hold or tie the k-th
+    const float hi_cut = t_hi + E + fabsf(t_hi) * kRel;
+    const float lo_cut = t_lo - E - fabsf(t_lo) * kRel;
+    if (threadIdx.x == 0) {
+      s_misc[2] = 0;
+      s_misc[3] = 0;
+    }
+    __syncthreads();
+    uint32_t cls = 0;   // 2 bits per candidate of this thread: 1 in, 2 band
+    if (ok) {
+      for (uint32_t j = threadIdx.x, u = 0; j < nc; j += blockDim.x, ++u) {
+        const float S = cS[j], e = ce[j];
+        if (S - e > hi_cut) {
+          cls |= 1u << (2 * u);
+          atomicOr(&bitmap[cidx[j] >> 5], 1u << (cidx[j] & 31));
+        } else if (S + e >= lo_cut) {
+          cls |= 2u << (2 * u);
+        }
+      }
+      const uint32_t n_in = __popc(cls & 0x55555555u), n_band = __popc(cls & 0xaaaaaaaau);
+      const uint32_t wi = warp_sum_u32(n_in), wb = warp_sum_u32(n_band);
+      if (lane == 0) {
+        if (wi) atomicAdd(&s_misc[3], wi);
+        if (wb) atomicAdd(&s_misc[2], wb);
+      }
+    }
+    __syncthreads();   // ce is free from here: it holds the band's candidate slots
+    const uint32_t nband = s_misc[2], n_in = s_misc[3];
+    ok = ok && n_in <= k && k - n_in <= nband && nband <= 2048;
+    if (ok) {
+      if (threadIdx.x == 0) s_misc[2] = 0;
+      __syncthreads();
+      uint32_t *band = reinterpret_cast<uint32_t *>(ce);
+      for (uint32_t j = threadIdx.x, u = 0; j < nc; j += blockDim.x, ++u)
+        if ((cls >> (2 * u)) & 2u) band[atomicAdd(&s_misc[2], 1u)] = j;
+      __syncthreads();
+      // exact scores of the band
+      for (uint32_t i = warp; i < nband; i += 32) {
+        const uint32_t j = band[i];
+        const float V = rescore_row(qsm, wsh, kb, rel, keys + (size_t)cidx[j] * Di, lane);
+        if (lane == 0) cS[j] = V;
+      }
+      __syncthreads();
+      float *bV = kbuf;
+      uint32_t *bI = reinterpret_cast<uint32_t *>(kbuf + 2048);
+      for (uint32_t i = threadIdx.x; i < nband; i += blockDim.x) {
+        bV[i] = cS[band[i]];
+        bI[i] = cidx[band[i]];
+      }
+      __syncthreads();
+      // the k - n_in best of the band by (exact score desc, row asc)
+      const uint32_t want = k - n_in;
+      for (uint32_t i = threadIdx.x; i < nband; i += blockDim.x) {
+        const float V = bV[i];
+        const uint32_t idx = bI[i];
+        uint32_t rank = 0;
+        for (uint32_t t = 0; t < nband; ++t) {
+          const float Vt = bV[t];
+          rank += (Vt > V || (Vt == V && bI[t] < idx)) ? 1u : 0u;
+        }
+        if (rank < want) atomicOr(&bitmap[idx >> 5], 1u << (idx & 31));
+      }
+      __syncthreads();
+      // ascending output from the bitmap
+      const uint32_t per_t = (words + blockDim.x - 1) / blockDim.x;
+      const uint32_t w0 = threadIdx.x * per_t, w1 = min(words, w0 + per_t);
+      uint32_t cnt = 0;
+      for (uint32_t i = w0; i < w1; ++i) cnt += __popc(bitmap[i]);
+      uint32_t tot;
+      uint32_t pos = block_excl_scan(cnt, wsum, &tot);
+      for (uint32_t i = w0; i < w1; ++i) {
+        uint32_t m = bitmap[i];
+        while (m) {
+          const uint32_t bit = __ffs(m) - 1;
+          if (pos < k) out[pos] = (int32_t)(i * 32 + bit);
+          ++pos;
+          m &= m - 1;
+        }
+      }
+      for (uint32_t j = tot + threadIdx.x; j < k; j += blockDim.x) out[j] = -1;
+      return;
+    }
+    // inconsistent counts (never expected): the in-place selection below
+    // recomputes everything from the scores
+    __syncthreads();
   }
 
   // ---- fallback: the same certified selection over every visible row
