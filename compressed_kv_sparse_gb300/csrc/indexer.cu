@@ -342,7 +342,7 @@ __device__ __forceinline__ float key_to_float(uint32_t k) {
 
 constexpr uint32_t kCandCap = 4096;    // candidates held in shared memory
 constexpr float kRel = 2.4e-7f;        // slack for the rounding of the bound arithmetic
-constexpr uint32_t kQS = 136;          // padded row stride (bf16) of q' in shared memory
+constexpr uint32_t kQF = 132;          // padded row stride (fp32) of q' in shared memory
 
 // Block-wide exclusive prefix sum of v (every thread gets its prefix and the
 // total). `wsum` holds 33 words.
@@ -377,7 +377,7 @@ __device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t *wsum, 
 
 inline size_t select_tc_smem(uint32_t comp_cap) {
   const size_t words = (comp_cap + 31) / 32;
-  return 64 * kQS * 2 + 64 * 4 + 32 * 128 * 4 + 32 * 64 * 4 + 3 * kCandCap * 4 + words * 4;
+  return 64 * kQF * 4 + 64 * 4 + 32 * 128 * 4 + 32 * 64 * 4 + 3 * kCandCap * 4 + words * 4;
 }
 
 inline uint32_t select_groups(uint32_t nq) {
@@ -385,36 +385,77 @@ inline uint32_t select_groups(uint32_t nq) {
   return g < 1 ? 1 : (g > 16 ? 16 : g);
 }
 
+// Unbiased exponent of a nonzero fp32 value; subnormals report -140 (below
+// any of their magnitudes), inf / NaN 128.
+__device__ __forceinline__ int exp_of(float x) {
+  const int f = (int)((__float_as_uint(x) >> 23) & 0xFFu);
+  return f == 0 ? -140 : f - 127;
+}
+__device__ __forceinline__ int warp_min_i(int v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = min(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+__device__ __forceinline__ int warp_max_i(int v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = max(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
 // Exact recipe (fp32, fixed order) for key row `kr` against the 64 x 128 query
-// in shared memory; lane 0 returns the score.
-__device__ __forceinline__ float rescore_row(const __nv_bfloat16 *qsm, const float *wsh, float *kb,
-                                             float *rel, const __nv_bfloat16 *kr, uint32_t lane) {
+// in shared memory (fp32 copies of the bf16 q'); lane 0 returns the score.
+// The recipe adds fl(q * k) to the running dot product in ascending d. For
+// two bf16 factors the product has at most 16 significant bits, so fl(q * k)
+// = q * k unless it is subnormal or overflows, and then fma(q, k, acc) rounds
+// exactly like acc + fl(q * k). The exponent ranges of q' (eq_min, eq_max,
+// over nonzero entries) and of the row decide which form is used.
+__device__ __forceinline__ float rescore_row(const float *qf, const float *wsh, float *kb,
+                                             float *rel, const __nv_bfloat16 *kr, uint32_t lane,
+                                             int eq_min, int eq_max) {
   __syncwarp();
+  int emin = 1000, emax = -1000;
   {
     const uint2 v = *reinterpret_cast<const uint2 *>(kr + 4 * lane);
-    *reinterpret_cast<float4 *>(kb + 4 * lane) =
-        make_float4(__uint_as_float(v.x << 16), __uint_as_float(v.x & 0xFFFF0000u),
-                    __uint_as_float(v.y << 16), __uint_as_float(v.y & 0xFFFF0000u));
+    const float k0 = __uint_as_float(v.x << 16), k1 = __uint_as_float(v.x & 0xFFFF0000u);
+    const float k2 = __uint_as_float(v.y << 16), k3 = __uint_as_float(v.y & 0xFFFF0000u);
+    *reinterpret_cast<float4 *>(kb + 4 * lane) = make_float4(k0, k1, k2, k3);
+    const float kk[4] = {k0, k1, k2, k3};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      if (kk[e] != 0.f) {
+        emin = min(emin, exp_of(kk[e]));
+        emax = max(emax, exp_of(kk[e]));
+      }
+    }
   }
+  emin = warp_min_i(emin);
+  emax = warp_max_i(emax);
+  const bool exact = eq_min + emin >= -126 && eq_max + emax <= 125;
   __syncwarp();
+  const float4 *k4 = reinterpret_cast<const float4 *>(kb);
 #pragma unroll
   for (uint32_t j = 0; j < 2; ++j) {
     const uint32_t h = lane + 32 * j;
-    const uint4 *qrow = reinterpret_cast<const uint4 *>(qsm + (size_t)h * kQS);
+    const float4 *q4 = reinterpret_cast<const float4 *>(qf + (size_t)h * kQF);
     float acc = 0.f;
+    if (exact) {
+#pragma unroll 8
+      for (uint32_t c = 0; c < 32; ++c) {
+        const float4 q = q4[c], k = k4[c];
+        acc = fmaf(q.x, k.x, acc);
+        acc = fmaf(q.y, k.y, acc);
+        acc = fmaf(q.z, k.z, acc);
+        acc = fmaf(q.w, k.w, acc);
+      }
+    } else {
 #pragma unroll 4
-    for (uint32_t c = 0; c < 16; ++c) {
-      const uint4 q8 = qrow[c];
-      const float4 ka = *reinterpret_cast<const float4 *>(kb + 8 * c);
-      const float4 kc = *reinterpret_cast<const float4 *>(kb + 8 * c + 4);
-      acc = __fadd_rn(acc, __fmul_rn(__uint_as_float(q8.x << 16), ka.x));
-      acc = __fadd_rn(acc, __fmul_rn(__uint_as_float(q8.x & 0xFFFF0000u), ka.y));
-      acc = __fadd_rn(acc, __fmul_rn(__uint_as_float(q8.y << 16), ka.z));
-      acc = __fadd_rn(acc, __fmul_rn(__uint_as_float(q8.y & 0xFFFF0000u), ka.w));
-      acc = __fadd_rn(acc, __fmul_rn(__uint_as_float(q8.z << 16), kc.x));
-      acc = __fadd_rn(acc, __fmul_rn(__uint_as_float(q8.z & 0xFFFF0000u), kc.y));
-      acc = __fadd_rn(acc, __fmul_rn(__uint_as_float(q8.w << 16), kc.z));
-      acc = __fadd_rn(acc, __fmul_rn(__uint_as_float(q8.w & 0xFFFF0000u), kc.w));
+      for (uint32_t c = 0; c < 32; ++c) {
+        const float4 q = q4[c], k = k4[c];
+        acc = __fadd_rn(acc, __fmul_rn(q.x, k.x));
+        acc = __fadd_rn(acc, __fmul_rn(q.y, k.y));
+        acc = __fadd_rn(acc, __fmul_rn(q.z, k.z));
+        acc = __fadd_rn(acc, __fmul_rn(q.w, k.w));
+      }
     }
     rel[h] = acc > 0.f ? acc : 0.f;
   }
@@ -452,8 +493,9 @@ __global__ void __launch_bounds__(kSelectThreads)
   // the bin, second-level bin
   __shared__ uint32_t s_misc[6];
   __shared__ float s_red[32];
-  __nv_bfloat16 *qsm = reinterpret_cast<__nv_bfloat16 *>(dyn4);   // [64][kQS]
-  float *wsh = reinterpret_cast<float *>(qsm + 64 * kQS);           // [64]
+  __shared__ int s_qexp[2];        // exponent range of the nonzero q' entries
+  float *qf = reinterpret_cast<float *>(dyn4);                      // [64][kQF]
+  float *wsh = qf + 64 * kQF;                                       // [64]
   float *kbuf = wsh + 64;                                           // [32][128]
   float *relb = kbuf + 32 * 128;                                    // [32][64]
   uint32_t *cidx = reinterpret_cast<uint32_t *>(relb + 32 * 64);    // [kCandCap]
@@ -481,20 +523,41 @@ __global__ void __launch_bounds__(kSelectThreads)
   uint32_t *ctrl = w.ctrl + (size_t)qi * 4;
   uint32_t *cand = w.cand + (size_t)qi * kCandGlobal;
 
-  // A = c * sum_h |w_h| ||q'_h|| (two heads per warp); q' rows to shared memory
+  // A = c * sum_h |w_h| ||q'_h|| (two heads per warp); q' rows to shared
+  // memory as fp32, with the exponent range of their nonzero entries
+  if (threadIdx.x == 0) {
+    s_qexp[0] = 1000;
+    s_qexp[1] = -1000;
+  }
+  __syncthreads();
   {
     float part = 0.f;
+    int emin = 1000, emax = -1000;
 #pragma unroll
     for (uint32_t j = 0; j < 2; ++j) {
       const uint32_t h = warp + 32 * j;
       const uint2 v = *reinterpret_cast<const uint2 *>(qb + (size_t)h * Di + 4 * lane);
-      *reinterpret_cast<uint2 *>(qsm + (size_t)h * kQS + 4 * lane) = v;
       const float x0 = __uint_as_float(v.x << 16), x1 = __uint_as_float(v.x & 0xFFFF0000u);
       const float x2 = __uint_as_float(v.y << 16), x3 = __uint_as_float(v.y & 0xFFFF0000u);
+      *reinterpret_cast<float4 *>(qf + (size_t)h * kQF + 4 * lane) = make_float4(x0, x1, x2, x3);
+      const float xx[4] = {x0, x1, x2, x3};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        if (xx[e] != 0.f) {
+          emin = min(emin, exp_of(xx[e]));
+          emax = max(emax, exp_of(xx[e]));
+        }
+      }
       const float ss = warp_sum(x0 * x0 + x1 * x1 + x2 * x2 + x3 * x3);
       part += fabsf(__bfloat162float(wq[h])) * sqrtf(ss);
     }
-    if (lane == 0) s_red[warp] = part;
+    emin = warp_min_i(emin);
+    emax = warp_max_i(emax);
+    if (lane == 0) {
+      s_red[warp] = part;
+      atomicMin(&s_qexp[0], emin);
+      atomicMax(&s_qexp[1], emax);
+    }
     if (threadIdx.x < Hi) wsh[threadIdx.x] = __bfloat162float(wq[threadIdx.x]);
   }
   // theta_S: lower edge of the histogram bin holding the k-th largest S~
@@ -522,7 +585,7 @@ __global__ void __launch_bounds__(kSelectThreads)
       loc += c4[j];
     }
     uint32_t tot;
-    uint32_t cum = block_excl_scan(loc, wsum, &tot);   // also syncs s_red / wsh / qsm
+    uint32_t cum = block_excl_scan(loc, wsum, &tot);   // also syncs s_red / wsh / qf
     if (cum < k && cum + loc >= k) {
 #pragma unroll
       for (uint32_t j = 0; j < 4; ++j) {
@@ -541,6 +604,7 @@ __global__ void __launch_bounds__(kSelectThreads)
   const float A = At * (1.0f + 1e-5f) * cb;
   const float E = A * __uint_as_float(a.norm_max[b]);
   const float theta_s = key_to_float(s_misc[0] << 20);
+  const int eq_min = s_qexp[0], eq_max = s_qexp[1];
   const float theta = theta_s - E - fabsf(theta_s) * (2.0f * kRel);
   auto err_of = [&](float S, float nm) { return A * nm + fabsf(S) * kRel; };
 
@@ -581,8 +645,14 @@ __global__ void __launch_bounds__(kSelectThreads)
   uint32_t need;
   if (fast) {
     // ---- certified selection on the candidates
+    if (threadIdx.x == 0) s_misc[5] = 0u;
+    __syncthreads();
     for (uint32_t j = threadIdx.x; j < nc; j += blockDim.x) {
-      const uint32_t r = *(volatile uint32_t *)&cand[j];
+      uint32_t r = *(volatile uint32_t *)&cand[j];
+      if (r >= vis) {   // never expected: the selection below recomputes from the scores
+        s_misc[5] = 1u;
+        r = 0;
+      }
       const float S = sc[r];
       cidx[j] = r;
       cS[j] = S;
@@ -595,6 +665,9 @@ __global__ void __launch_bounds__(kSelectThreads)
     // to one 24-bit key interval [t_lo, t_hi] (every row of b* is a candidate)
     uint32_t *h2 = reinterpret_cast<uint32_t *>(kbuf);   // [4096], free until rescoring
     for (uint32_t i = threadIdx.x; i < kHistBins; i += blockDim.x) h2[i] = 0u;
+    __syncthreads();
+    const bool cand_ok = s_misc[5] == 0u;
+    __syncthreads();
     if (threadIdx.x == 0) s_misc[5] = 0xffffffffu;
     __syncthreads();
     const uint32_t bstar = s_misc[0], need_b = k - s_misc[4];
@@ -624,7 +697,7 @@ __global__ void __launch_bounds__(kSelectThreads)
       }
     }
     __syncthreads();
-    bool ok = s_misc[5] != 0xffffffffu;
+    bool ok = cand_ok && s_misc[5] != 0xffffffffu;
     const uint32_t kpre = (bstar << 20) | (s_misc[5] << 8);
     const float t_lo = key_to_float(kpre), t_hi = key_to_float(kpre | 0xffu);
     // rows with L > t_hi + E beat the exact k-th score, rows with U < t_lo - E
@@ -667,7 +740,8 @@ __global__ void __launch_bounds__(kSelectThreads)
       // exact scores of the band
       for (uint32_t i = warp; i < nband; i += 32) {
         const uint32_t j = band[i];
-        const float V = rescore_row(qsm, wsh, kb, rel, keys + (size_t)cidx[j] * Di, lane);
+        const float V = rescore_row(qf, wsh, kb, rel, keys + (size_t)cidx[j] * Di, lane, eq_min,
+                                  eq_max);
         if (lane == 0) cS[j] = V;
       }
       __syncthreads();
@@ -680,15 +754,16 @@ __global__ void __launch_bounds__(kSelectThreads)
       __syncthreads();
       // the k - n_in best of the band by (exact score desc, row asc)
       const uint32_t want = k - n_in;
-      for (uint32_t i = threadIdx.x; i < nband; i += blockDim.x) {
+      for (uint32_t i = warp; i < nband; i += 32) {   // one warp per band row
         const float V = bV[i];
         const uint32_t idx = bI[i];
         uint32_t rank = 0;
-        for (uint32_t t = 0; t < nband; ++t) {
+        for (uint32_t t = lane; t < nband; t += 32) {
           const float Vt = bV[t];
           rank += (Vt > V || (Vt == V && bI[t] < idx)) ? 1u : 0u;
         }
-        if (rank < want) atomicOr(&bitmap[idx >> 5], 1u << (idx & 31));
+        rank = warp_sum_u32(rank);
+        if (lane == 0 && rank < want) atomicOr(&bitmap[idx >> 5], 1u << (idx & 31));
       }
       __syncthreads();
       // ascending output from the bitmap
@@ -740,14 +815,14 @@ __global__ void __launch_bounds__(kSelectThreads)
   if (nband <= kCandCap) {
     for (uint32_t i = warp; i < nband; i += 32) {
       const uint32_t s = band[i];
-      const float V = rescore_row(qsm, wsh, kb, rel, keys + (size_t)s * Di, lane);
+      const float V = rescore_row(qf, wsh, kb, rel, keys + (size_t)s * Di, lane, eq_min, eq_max);
       if (lane == 0) sc[s] = V;
     }
   } else {
     for (uint32_t s = warp; s < vis; s += 32) {
       const float v = sc[s];
       if (v == INFINITY || v == -INFINITY) continue;
-      const float V = rescore_row(qsm, wsh, kb, rel, keys + (size_t)s * Di, lane);
+      const float V = rescore_row(qf, wsh, kb, rel, keys + (size_t)s * Di, lane, eq_min, eq_max);
       if (lane == 0) sc[s] = V;
     }
   }
