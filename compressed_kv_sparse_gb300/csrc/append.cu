@@ -73,7 +73,8 @@ __device__ void pool_norm_rope_store(const LaneArgs &L, uint32_t W, uint32_t b, 
   ss = block_sum(ss, red);
   const float inv = 1.0f / sqrtf(ss / (float)width + kRmsEps);
   T *row = comp + ((size_t)b * comp_cap + i) * width;
-  float ss_row = 0.f;   // sum of squares of the stored (rounded) row
+  float st[kMaxPairsPerThread][2];   // the stored (rounded) values, for the row norm
+  float mx = 0.f;
 #pragma unroll
   for (int k = 0; k < kMaxPairsPerThread; ++k) {
     const uint32_t j = threadIdx.x + k * blockDim.x;
@@ -92,14 +93,26 @@ __device__ void pool_norm_rope_store(const LaneArgs &L, uint32_t W, uint32_t b, 
     }
     st_elem(row, c, a);
     st_elem(row, c + 1, bb);
-    const float sa = round_to(a, row), sb = round_to(bb, row);
-    ss_row = fmaf(sa, sa, fmaf(sb, sb, ss_row));
+    st[k][0] = round_to(a, row);
+    st[k][1] = round_to(bb, row);
+    mx = fmaxf(mx, fmaxf(fabsf(st[k][0]), fabsf(st[k][1])));
   }
   if (L.norm) {   // uniform: the indexer lane records the row's norm
-    ss_row = block_sum(ss_row, red);
+    mx = block_max(mx, red);
+    int e = 0;
+    if (mx > 0.f) frexpf(mx, &e);
+    float ss = 0.f;
+#pragma unroll
+    for (int k = 0; k < kMaxPairsPerThread; ++k) {
+      const uint32_t j = threadIdx.x + k * blockDim.x;
+      if (j < npair) {
+        const float y0 = ldexpf(st[k][0], -e), y1 = ldexpf(st[k][1], -e);
+        ss = fmaf(y0, y0, fmaf(y1, y1, ss));
+      }
+    }
+    ss = block_sum(ss, red);
     if (threadIdx.x == 0) {
-      // widened by 1e-4 for the rounding of the fp32 sum of squares
-      const float nm = sqrtf(ss_row) * 1.0001f;
+      const float nm = mx > 0.f ? norm_from_scaled(ss, e) : 0.f;
       L.norm[(size_t)b * comp_cap + i] = nm;
       atomicMax(&L.norm_max[b], __float_as_uint(nm));
     }
@@ -115,14 +128,19 @@ __global__ void index_norms_kernel(const T *rows, uint32_t dim, uint32_t comp_ca
   const uint32_t r = blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
   if (r >= n_rows) return;
   const T *row = rows + ((size_t)b * comp_cap + r) * dim;
+  float mx = 0.f;
+  for (uint32_t c = lane; c < dim; c += 32) mx = fmaxf(mx, fabsf(ld_f32(row, c)));
+  mx = warp_max(mx);
+  int e = 0;
+  if (mx > 0.f) frexpf(mx, &e);
   float ss = 0.f;
   for (uint32_t c = lane; c < dim; c += 32) {
-    const float v = ld_f32(row, c);
-    ss = fmaf(v, v, ss);
+    const float y = ldexpf(ld_f32(row, c), -e);
+    ss = fmaf(y, y, ss);
   }
   ss = warp_sum(ss);
   if (lane == 0) {
-    const float nm = sqrtf(ss) * 1.0001f;
+    const float nm = mx > 0.f ? norm_from_scaled(ss, e) : 0.f;
     norm[(size_t)b * comp_cap + r] = nm;
     atomicMax(&norm_max[b], __float_as_uint(nm));
   }

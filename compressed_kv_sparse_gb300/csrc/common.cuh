@@ -45,4 +45,26 @@ __device__ __forceinline__ float block_sum(float v, float *red) {
   return warp_sum(t);
 }
 
+// Block-wide max; every thread gets the result. `red` holds >= 32 floats.
+__device__ __forceinline__ float block_max(float v, float *red) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  const int nw = (blockDim.x + 31) >> 5;
+  v = warp_max(v);
+  __syncthreads();
+  if (lane == 0) red[wid] = v;
+  __syncthreads();
+  float t = lane < nw ? red[lane] : 0.f;
+  return warp_max(t);
+}
+
+// An upper bound of the Euclidean norm from partial sums of scaled squares:
+// the values were multiplied by 2^-e (e = exponent of the largest |value|,
+// exact) before squaring, so squares of tiny magnitudes do not underflow.
+// `ss_scaled` = sum of the scaled squares (>= 0.25 when the largest value is
+// nonzero); the result is scaled back and widened by 2^-16 for the fp32
+// roundings of at most a few hundred terms.
+__device__ __forceinline__ float norm_from_scaled(float ss_scaled, int e) {
+  return ldexpf(sqrtf(ss_scaled), e) * (1.0f + 0x1p-16f);
+}
+
 }  // namespace ds4a

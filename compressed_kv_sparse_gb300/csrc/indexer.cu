@@ -342,7 +342,8 @@ __device__ __forceinline__ float key_to_float(uint32_t k) {
 
 constexpr uint32_t kCandCap = 4096;    // candidates held in shared memory
 constexpr float kRel = 2.4e-7f;        // slack for the rounding of the bound arithmetic
-constexpr uint32_t kQF = 132;          // padded row stride (fp32) of q' in shared memory
+constexpr uint32_t kQB = 132;          // row stride (bf16) of q' in shared memory: the 8-byte
+                                        // loads of 16 lanes at 16 rows hit 32 distinct banks
 
 // Block-wide exclusive prefix sum of v (every thread gets its prefix and the
 // total). `wsum` holds 33 words.
@@ -377,11 +378,12 @@ __device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t *wsum, 
 
 inline size_t select_tc_smem(uint32_t comp_cap) {
   const size_t words = (comp_cap + 31) / 32;
-  return 64 * kQF * 4 + 64 * 4 + 32 * 128 * 4 + 32 * 64 * 4 + 3 * kCandCap * 4 + words * 4;
+  return 64 * kQB * 2 + 64 * 4 + 64 * 128 * 4 + 64 * 64 * 4 + 3 * kCandCap * 4 + words * 4;
 }
 
+// Blocks per query: one wave of 1024-thread blocks (one per SM), at most 16.
 inline uint32_t select_groups(uint32_t nq) {
-  uint32_t g = 256 / (nq ? nq : 1);
+  uint32_t g = (uint32_t)num_sms() / (nq ? nq : 1);
   return g < 1 ? 1 : (g > 16 ? 16 : g);
 }
 
@@ -402,59 +404,74 @@ __device__ __forceinline__ int warp_max_i(int v) {
   return v;
 }
 
-// Exact recipe (fp32, fixed order) for key row `kr` against the 64 x 128 query
-// in shared memory (fp32 copies of the bf16 q'); lane 0 returns the score.
-// The recipe adds fl(q * k) to the running dot product in ascending d. For
-// two bf16 factors the product has at most 16 significant bits, so fl(q * k)
-// = q * k unless it is subnormal or overflows, and then fma(q, k, acc) rounds
-// exactly like acc + fl(q * k). The exponent ranges of q' (eq_min, eq_max,
-// over nonzero entries) and of the row decide which form is used.
-__device__ __forceinline__ float rescore_row(const float *qf, const float *wsh, float *kb,
-                                             float *rel, const __nv_bfloat16 *kr, uint32_t lane,
-                                             int eq_min, int eq_max) {
-  __syncwarp();
-  int emin = 1000, emax = -1000;
-  {
-    const uint2 v = *reinterpret_cast<const uint2 *>(kr + 4 * lane);
-    const float k0 = __uint_as_float(v.x << 16), k1 = __uint_as_float(v.x & 0xFFFF0000u);
-    const float k2 = __uint_as_float(v.y << 16), k3 = __uint_as_float(v.y & 0xFFFF0000u);
-    *reinterpret_cast<float4 *>(kb + 4 * lane) = make_float4(k0, k1, k2, k3);
-    const float kk[4] = {k0, k1, k2, k3};
+// The exact recipe adds fl(q * k) to the running dot product in ascending d.
+// For two bf16 factors the product has at most 16 significant bits, so
+// fl(q * k) = q * k unless it is subnormal or overflows, and then
+// fma(q, k, acc) rounds exactly like acc + fl(q * k). The exponent ranges of
+// q' (eq_min, eq_max, over nonzero entries) and of the key rows decide which
+// form is used.
+__device__ __forceinline__ bool fma_exact(int eq_min, int eq_max, int ek_min, int ek_max) {
+  return eq_min + ek_min >= -126 && eq_max + ek_max <= 125;
+}
+
+// Exponent range of the nonzero entries among four key values, over the warp.
+__device__ __forceinline__ void key_exp_range(const float (&kk)[4], int &emin, int &emax) {
+  emin = 1000;
+  emax = -1000;
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      if (kk[e] != 0.f) {
-        emin = min(emin, exp_of(kk[e]));
-        emax = max(emax, exp_of(kk[e]));
-      }
+  for (int e = 0; e < 4; ++e) {
+    if (kk[e] != 0.f) {
+      emin = min(emin, exp_of(kk[e]));
+      emax = max(emax, exp_of(kk[e]));
     }
   }
   emin = warp_min_i(emin);
   emax = warp_max_i(emax);
-  const bool exact = eq_min + emin >= -126 && eq_max + emax <= 125;
+}
+
+__device__ __forceinline__ void bf16x4(uint2 v, float &a, float &b, float &c, float &d) {
+  a = __uint_as_float(v.x << 16);
+  b = __uint_as_float(v.x & 0xFFFF0000u);
+  c = __uint_as_float(v.y << 16);
+  d = __uint_as_float(v.y & 0xFFFF0000u);
+}
+
+// Exact recipe for key row `kr` against the 64 x 128 query in shared memory
+// (one warp, two heads per lane); lane 0 returns the score.
+__device__ __forceinline__ float rescore_row(const __nv_bfloat16 *qsm, const float *wsh, float *kb,
+                                             float *rel, const __nv_bfloat16 *kr, uint32_t lane,
+                                             int eq_min, int eq_max) {
+  __syncwarp();
+  int emin, emax;
+  {
+    float kk[4];
+    bf16x4(*reinterpret_cast<const uint2 *>(kr + 4 * lane), kk[0], kk[1], kk[2], kk[3]);
+    *reinterpret_cast<float4 *>(kb + 4 * lane) = make_float4(kk[0], kk[1], kk[2], kk[3]);
+    key_exp_range(kk, emin, emax);
+  }
+  const bool exact = fma_exact(eq_min, eq_max, emin, emax);
   __syncwarp();
   const float4 *k4 = reinterpret_cast<const float4 *>(kb);
 #pragma unroll
   for (uint32_t j = 0; j < 2; ++j) {
     const uint32_t h = lane + 32 * j;
-    const float4 *q4 = reinterpret_cast<const float4 *>(qf + (size_t)h * kQF);
+    const uint2 *q2 = reinterpret_cast<const uint2 *>(qsm + (size_t)h * kQB);
     float acc = 0.f;
-    if (exact) {
-#pragma unroll 8
-      for (uint32_t c = 0; c < 32; ++c) {
-        const float4 q = q4[c], k = k4[c];
-        acc = fmaf(q.x, k.x, acc);
-        acc = fmaf(q.y, k.y, acc);
-        acc = fmaf(q.z, k.z, acc);
-        acc = fmaf(q.w, k.w, acc);
-      }
-    } else {
 #pragma unroll 4
-      for (uint32_t c = 0; c < 32; ++c) {
-        const float4 q = q4[c], k = k4[c];
-        acc = __fadd_rn(acc, __fmul_rn(q.x, k.x));
-        acc = __fadd_rn(acc, __fmul_rn(q.y, k.y));
-        acc = __fadd_rn(acc, __fmul_rn(q.z, k.z));
-        acc = __fadd_rn(acc, __fmul_rn(q.w, k.w));
+    for (uint32_t c = 0; c < 32; ++c) {
+      float q0, q1, q2v, q3;
+      bf16x4(q2[c], q0, q1, q2v, q3);
+      const float4 k = k4[c];
+      if (exact) {
+        acc = fmaf(q0, k.x, acc);
+        acc = fmaf(q1, k.y, acc);
+        acc = fmaf(q2v, k.z, acc);
+        acc = fmaf(q3, k.w, acc);
+      } else {
+        acc = __fadd_rn(acc, __fmul_rn(q0, k.x));
+        acc = __fadd_rn(acc, __fmul_rn(q1, k.y));
+        acc = __fadd_rn(acc, __fmul_rn(q2v, k.z));
+        acc = __fadd_rn(acc, __fmul_rn(q3, k.w));
       }
     }
     rel[h] = acc > 0.f ? acc : 0.f;
@@ -466,6 +483,90 @@ __device__ __forceinline__ float rescore_row(const float *qf, const float *wsh, 
     for (uint32_t h = 0; h < 64; ++h) tot = __fadd_rn(tot, __fmul_rn(wsh[h], rel[h]));
   }
   return tot;
+}
+
+// Exact recipe for the band rows (whole block): rounds of 64 rows; their keys
+// go to `kbuf` as fp32, warp pair (2g, 2g + 1) runs rows 4g .. 4g + 3 of the
+// round against heads 32 (warp & 1) + lane, so one q' load serves four rows
+// and one key load all 32 heads of a warp. Per-head ReLU dots land in `relb`
+// [64 rows][64 heads]; one thread per row sums them in ascending h. Results
+// replace cS[band[i]].
+__device__ __forceinline__ void rescore_band(const __nv_bfloat16 *qsm, const float *wsh,
+                                             float *kbuf, float *relb, const uint32_t *band,
+                                             uint32_t nband, const uint32_t *cidx, float *cS,
+                                             const __nv_bfloat16 *keys, uint32_t *rexact,
+                                             int eq_min, int eq_max) {
+  const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (uint32_t base = 0; base < nband; base += 64) {
+    const uint32_t nr = min(64u, nband - base);
+#pragma unroll
+    for (uint32_t t = 0; t < 2; ++t) {
+      const uint32_t rr = 2 * warp + t;
+      if (rr < nr) {   // warp-uniform
+        float kk[4];
+        bf16x4(*reinterpret_cast<const uint2 *>(keys + (size_t)cidx[band[base + rr]] * 128 +
+                                                4 * lane),
+               kk[0], kk[1], kk[2], kk[3]);
+        *reinterpret_cast<float4 *>(kbuf + rr * 128 + 4 * lane) =
+            make_float4(kk[0], kk[1], kk[2], kk[3]);
+        int emin, emax;
+        key_exp_range(kk, emin, emax);
+        if (lane == 0) rexact[rr] = fma_exact(eq_min, eq_max, emin, emax) ? 1u : 0u;
+      }
+    }
+    __syncthreads();
+    const uint32_t g4 = (warp >> 1) * 4, h = 32 * (warp & 1) + lane;
+    if (g4 < nr) {   // warp-uniform
+      bool exact = true;
+#pragma unroll
+      for (uint32_t rr = 0; rr < 4; ++rr)
+        if (g4 + rr < nr) exact = exact && rexact[g4 + rr] != 0u;
+      const uint2 *q2 = reinterpret_cast<const uint2 *>(qsm + (size_t)h * kQB);
+      const float4 *k4 = reinterpret_cast<const float4 *>(kbuf + g4 * 128);
+      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+      if (exact) {
+#pragma unroll 4
+        for (uint32_t c = 0; c < 32; ++c) {
+          float q0, q1, q2v, q3;
+          bf16x4(q2[c], q0, q1, q2v, q3);
+#pragma unroll
+          for (uint32_t rr = 0; rr < 4; ++rr) {
+            const float4 k = k4[rr * 32 + c];
+            acc[rr] = fmaf(q0, k.x, acc[rr]);
+            acc[rr] = fmaf(q1, k.y, acc[rr]);
+            acc[rr] = fmaf(q2v, k.z, acc[rr]);
+            acc[rr] = fmaf(q3, k.w, acc[rr]);
+          }
+        }
+      } else {
+#pragma unroll 2
+        for (uint32_t c = 0; c < 32; ++c) {
+          float q0, q1, q2v, q3;
+          bf16x4(q2[c], q0, q1, q2v, q3);
+#pragma unroll
+          for (uint32_t rr = 0; rr < 4; ++rr) {
+            const float4 k = k4[rr * 32 + c];
+            acc[rr] = __fadd_rn(acc[rr], __fmul_rn(q0, k.x));
+            acc[rr] = __fadd_rn(acc[rr], __fmul_rn(q1, k.y));
+            acc[rr] = __fadd_rn(acc[rr], __fmul_rn(q2v, k.z));
+            acc[rr] = __fadd_rn(acc[rr], __fmul_rn(q3, k.w));
+          }
+        }
+      }
+#pragma unroll
+      for (uint32_t rr = 0; rr < 4; ++rr)
+        relb[(g4 + rr) * 64 + h] = acc[rr] > 0.f ? acc[rr] : 0.f;
+    }
+    __syncthreads();
+    if (threadIdx.x < nr) {
+      const float *rl = relb + threadIdx.x * 64;
+      float tot = 0.f;
+#pragma unroll 16
+      for (uint32_t hh = 0; hh < 64; ++hh) tot = __fadd_rn(tot, __fmul_rn(wsh[hh], rl[hh]));
+      cS[band[base + threadIdx.x]] = tot;
+    }
+    __syncthreads();
+  }
 }
 
 // Certified selection for bf16 layers (64 heads x 128 dims).
@@ -492,13 +593,14 @@ __global__ void __launch_bounds__(kSelectThreads)
   // bin of the k-th key, last-block flag, band count, tie / in count, keys above
   // the bin, second-level bin
   __shared__ uint32_t s_misc[6];
-  __shared__ float s_red[32];
+  __shared__ float s_red[32], s_wabs[32];
   __shared__ int s_qexp[2];        // exponent range of the nonzero q' entries
-  float *qf = reinterpret_cast<float *>(dyn4);                      // [64][kQF]
-  float *wsh = qf + 64 * kQF;                                       // [64]
-  float *kbuf = wsh + 64;                                           // [32][128]
-  float *relb = kbuf + 32 * 128;                                    // [32][64]
-  uint32_t *cidx = reinterpret_cast<uint32_t *>(relb + 32 * 64);    // [kCandCap]
+  __shared__ uint32_t s_rexact[64];  // band round: fma is exact for the row
+  __nv_bfloat16 *qsm = reinterpret_cast<__nv_bfloat16 *>(dyn4);   // [64][kQB]
+  float *wsh = reinterpret_cast<float *>(qsm + 64 * kQB);           // [64]
+  float *kbuf = wsh + 64;                                           // [64][128]
+  float *relb = kbuf + 64 * 128;                                    // [64][64]
+  uint32_t *cidx = reinterpret_cast<uint32_t *>(relb + 64 * 64);    // [kCandCap]
   float *cS = reinterpret_cast<float *>(cidx + kCandCap);           // [kCandCap]
   float *ce = cS + kCandCap;                                        // [kCandCap]
   uint32_t *bitmap = reinterpret_cast<uint32_t *>(ce + kCandCap);   // [comp_cap / 32]
@@ -531,7 +633,7 @@ __global__ void __launch_bounds__(kSelectThreads)
   }
   __syncthreads();
   {
-    float part = 0.f;
+    float part = 0.f, wabs = 0.f;
     int emin = 1000, emax = -1000;
 #pragma unroll
     for (uint32_t j = 0; j < 2; ++j) {
@@ -539,7 +641,7 @@ __global__ void __launch_bounds__(kSelectThreads)
       const uint2 v = *reinterpret_cast<const uint2 *>(qb + (size_t)h * Di + 4 * lane);
       const float x0 = __uint_as_float(v.x << 16), x1 = __uint_as_float(v.x & 0xFFFF0000u);
       const float x2 = __uint_as_float(v.y << 16), x3 = __uint_as_float(v.y & 0xFFFF0000u);
-      *reinterpret_cast<float4 *>(qf + (size_t)h * kQF + 4 * lane) = make_float4(x0, x1, x2, x3);
+      *reinterpret_cast<uint2 *>(qsm + (size_t)h * kQB + 4 * lane) = v;
       const float xx[4] = {x0, x1, x2, x3};
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
@@ -548,13 +650,23 @@ __global__ void __launch_bounds__(kSelectThreads)
           emax = max(emax, exp_of(xx[e]));
         }
       }
-      const float ss = warp_sum(x0 * x0 + x1 * x1 + x2 * x2 + x3 * x3);
-      part += fabsf(__bfloat162float(wq[h])) * sqrtf(ss);
+      // ||q'_h|| from power-of-two scaled squares (tiny magnitudes would
+      // underflow), an upper bound
+      const float mx = warp_max(fmaxf(fmaxf(fabsf(x0), fabsf(x1)), fmaxf(fabsf(x2), fabsf(x3))));
+      int eh = 0;
+      if (mx > 0.f) frexpf(mx, &eh);
+      const float y0 = ldexpf(x0, -eh), y1 = ldexpf(x1, -eh);
+      const float y2 = ldexpf(x2, -eh), y3 = ldexpf(x3, -eh);
+      const float ss = warp_sum(fmaf(y0, y0, fmaf(y1, y1, fmaf(y2, y2, y3 * y3))));
+      const float wa = fabsf(__bfloat162float(wq[h]));
+      part += wa * (mx > 0.f ? norm_from_scaled(ss, eh) : 0.f);
+      wabs += wa;
     }
     emin = warp_min_i(emin);
     emax = warp_max_i(emax);
     if (lane == 0) {
       s_red[warp] = part;
+      s_wabs[warp] = wabs;
       atomicMin(&s_qexp[0], emin);
       atomicMax(&s_qexp[1], emax);
     }
@@ -585,7 +697,7 @@ __global__ void __launch_bounds__(kSelectThreads)
       loc += c4[j];
     }
     uint32_t tot;
-    uint32_t cum = block_excl_scan(loc, wsum, &tot);   // also syncs s_red / wsh / qf
+    uint32_t cum = block_excl_scan(loc, wsum, &tot);   // also syncs s_red / wsh / qsm
     if (cum < k && cum + loc >= k) {
 #pragma unroll
       for (uint32_t j = 0; j < 4; ++j) {
@@ -599,14 +711,21 @@ __global__ void __launch_bounds__(kSelectThreads)
     }
   }
   __syncthreads();
-  float At = 0.f;
-  for (uint32_t i = 0; i < 32; ++i) At += s_red[i];
+  float At = 0.f, Wt = 0.f;
+  for (uint32_t i = 0; i < 32; ++i) {
+    At += s_red[i];
+    Wt += s_wabs[i];
+  }
   const float A = At * (1.0f + 1e-5f) * cb;
-  const float E = A * __uint_as_float(a.norm_max[b]);
+  // absolute term for underflow: tensor-core products and partial sums that
+  // flush to zero (each off by < 2^-126) and the subnormal roundings of both
+  // computations, for 4 Di operations per head dot and 4 Hi per score
+  const float eta = (4.0f * (float)Di * Wt * (1.0f + 1e-5f) + 4.0f * (float)Hi) * 0x1p-126f;
+  const float E = A * __uint_as_float(a.norm_max[b]) + eta;
   const float theta_s = key_to_float(s_misc[0] << 20);
   const int eq_min = s_qexp[0], eq_max = s_qexp[1];
   const float theta = theta_s - E - fabsf(theta_s) * (2.0f * kRel);
-  auto err_of = [&](float S, float nm) { return A * nm + fabsf(S) * kRel; };
+  auto err_of = [&](float S, float nm) { return A * nm + fabsf(S) * kRel + eta; };
 
   // ---- this block's share of the rows: candidates with U >= theta
   {
@@ -738,13 +857,7 @@ __global__ void __launch_bounds__(kSelectThreads)
         if ((cls >> (2 * u)) & 2u) band[atomicAdd(&s_misc[2], 1u)] = j;
       __syncthreads();
       // exact scores of the band
-      for (uint32_t i = warp; i < nband; i += 32) {
-        const uint32_t j = band[i];
-        const float V = rescore_row(qf, wsh, kb, rel, keys + (size_t)cidx[j] * Di, lane, eq_min,
-                                  eq_max);
-        if (lane == 0) cS[j] = V;
-      }
-      __syncthreads();
+      rescore_band(qsm, wsh, kbuf, relb, band, nband, cidx, cS, keys, s_rexact, eq_min, eq_max);
       float *bV = kbuf;
       uint32_t *bI = reinterpret_cast<uint32_t *>(kbuf + 2048);
       for (uint32_t i = threadIdx.x; i < nband; i += blockDim.x) {
@@ -815,14 +928,14 @@ __global__ void __launch_bounds__(kSelectThreads)
   if (nband <= kCandCap) {
     for (uint32_t i = warp; i < nband; i += 32) {
       const uint32_t s = band[i];
-      const float V = rescore_row(qf, wsh, kb, rel, keys + (size_t)s * Di, lane, eq_min, eq_max);
+      const float V = rescore_row(qsm, wsh, kb, rel, keys + (size_t)s * Di, lane, eq_min, eq_max);
       if (lane == 0) sc[s] = V;
     }
   } else {
     for (uint32_t s = warp; s < vis; s += 32) {
       const float v = sc[s];
       if (v == INFINITY || v == -INFINITY) continue;
-      const float V = rescore_row(qf, wsh, kb, rel, keys + (size_t)s * Di, lane, eq_min, eq_max);
+      const float V = rescore_row(qsm, wsh, kb, rel, keys + (size_t)s * Di, lane, eq_min, eq_max);
       if (lane == 0) sc[s] = V;
     }
   }
