@@ -171,6 +171,8 @@ __device__ void raw_row(const T *src, T *dst, uint32_t D, uint32_t n_rot, uint32
 template <typename T>
 __global__ void __launch_bounds__(kThreads) append_step_kernel(AppendArgs a) {
   __shared__ float red[32];
+  pdl_wait();
+  pdl_trigger();
   const uint32_t b = blockIdx.x, p = a.pos0;
   if (blockIdx.y == 0) {
     const T *src = static_cast<const T *>(a.raw_in) + (size_t)b * a.head_dim;
@@ -333,7 +335,9 @@ __global__ void state_reset_kernel(float *kv, float *score, size_t n) {
 template <typename T>
 cudaError_t launch_append_t(const AppendArgs &a, cudaStream_t s) {
   if (a.T == 1 && a.direct) {
-    append_step_kernel<T><<<dim3(a.batch, 1 + a.n_lanes), kThreads, 0, s>>>(a);
+    cudaError_t e = launch_pdl(append_step_kernel<T>, dim3(a.batch, 1 + a.n_lanes),
+                               dim3(kThreads), 0, s, a);
+    if (e != cudaSuccess) return e;
     note_launches(1);
     return cudaGetLastError();
   }

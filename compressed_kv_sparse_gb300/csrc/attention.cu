@@ -330,13 +330,11 @@ cudaError_t launch_attention_t(const AttnArgs &a, cudaStream_t s) {
 }
 
 // bf16 Flash shape: tcgen05 kernel (decode merges its splits inside a
-// thread-block cluster); word 0 of the workspace is its error word.
+// thread-block cluster); word 0 of the workspace is its error word (never
+// reset: a launch compares it with its value at the start).
 cudaError_t launch_attention_tc_path(const AttnArgs &a, cudaStream_t s) {
   const uint32_t rmax = rows_max(a.ratio, a.cap_raw, a.comp_cap, a.top_k);
-  int *err = static_cast<int *>(a.ws);
-  cudaError_t e = cudaMemsetAsync(err, 0, sizeof(int), s);
-  if (e != cudaSuccess) return e;
-  return launch_attention_tc(a, rmax, err, s);
+  return launch_attention_tc(a, rmax, static_cast<int *>(a.ws), s);
 }
 
 }  // namespace

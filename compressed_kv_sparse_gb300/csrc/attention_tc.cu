@@ -279,6 +279,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(TcAttnParams P) {
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  pdl_wait();
+  pdl_trigger();
+  // this launch's view of the error word (see ErrWord)
+  const ErrWord ew{P.err, *(volatile int *)P.err};
 
   if (warp >= 4 && warp < 8) {
     // ------------------------------------------------------------ loaders
@@ -293,7 +297,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(TcAttnParams P) {
         src[i] = row_src(P, g, tile * kRows + lw * 32 + (lane >> 3) + 4 * i);
       const uint32_t cc = lane & 7;
       for (uint32_t kb = 0; kb < 8; ++kb) {
-        if (!mbar_wait_warp(&S.kv_empty[kb], (n & 1) ^ 1, P.err)) return false;
+        if (!mbar_wait_warp(&S.kv_empty[kb], (n & 1) ^ 1, ew)) return false;
         uint8_t *slot = S.kv + kb * kKBlk;
 #pragma unroll
         for (uint32_t i = 0; i < 8; ++i) {
@@ -308,7 +312,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(TcAttnParams P) {
     };
     for (uint32_t qi = q_first; qi < P.n_q; qi += q_step) {
       if (rank * kRows >= rows_bound(P, qi)) continue;   // no rows for this rank
-      if (!mbar_wait_warp(&S.q_empty, (qn & 1) ^ 1, P.err)) goto done_loader;
+      if (!mbar_wait_warp(&S.q_empty, (qn & 1) ^ 1, ew)) goto done_loader;
       {
         // Q first (it needs no list): warp lw loads heads 16 lw .. 16 lw + 15
         const __nv_bfloat16 *q = P.q + (size_t)qi * kH * kD;
@@ -345,7 +349,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(TcAttnParams P) {
           }
         }
         asm volatile("cp.async.wait_group 8;" ::: "memory");   // Q landed
-        if (!group_sync(&S.ld_bar, ld_phase, P.err)) goto done_loader;
+        if (!group_sync(&S.ld_bar, ld_phase, ew)) goto done_loader;
         // rotate the tail (dims 448..511 = block 7) at position p, in place
 #pragma unroll
         for (uint32_t i = 0; i < 4; ++i) {
@@ -396,11 +400,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(TcAttnParams P) {
       const QueryGeo g = query_geo(P, qi, rank, C, lane);
       if (g.t0 >= g.t1) continue;
       if (lane == 0) {
-        ok = mbar_wait(&S.q_full, qn & 1, P.err);
+        ok = mbar_wait(&S.q_full, qn & 1, ew);
         for (uint32_t tile = g.t0; ok && tile < g.t1; tile += g.ts, ++n) {
           const bool first = tile == g.t0, last = tile + g.ts >= g.t1;
           for (uint32_t kb = 0; kb < 8 && ok; ++kb) {
-            ok = mbar_wait(&S.kv_full[kb], n & 1, P.err);
+            ok = mbar_wait(&S.kv_full[kb], n & 1, ew);
             if (!ok) break;
             tc_fence_after();
 #pragma unroll
@@ -411,8 +415,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(TcAttnParams P) {
           if (!ok) break;
           mma_commit(&S.s_full);
           if (last) mma_commit(&S.q_empty);
-          ok = mbar_wait(&S.p_full, n & 1, P.err);
-          if (ok && first) ok = mbar_wait(&S.o_empty, (qn & 1) ^ 1, P.err);
+          ok = mbar_wait(&S.p_full, n & 1, ew);
+          if (ok && first) ok = mbar_wait(&S.o_empty, (qn & 1) ^ 1, ew);
           if (!ok) break;
           tc_fence_after();
 #pragma unroll 1
@@ -483,14 +487,14 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(TcAttnParams P) {
         const uint32_t row = tile * kRows + r;
         bool valid = row < g.n_w;
         if (!valid && row < g.N) valid = P.ratio != 4 || g.tk[row - g.n_w] >= 0;
-        if (!mbar_wait_warp(&S.s_full, n & 1, P.err)) goto done_softmax;
+        if (!mbar_wait_warp(&S.s_full, n & 1, ew)) goto done_softmax;
         tc_fence_after();
         if (first) {
           // running maxima start at the scores of the first valid row
           if (r == 0) S.first_row = kNoRow;
-          if (!group_sync(&S.sm_bar, sm_phase, P.err)) goto done_softmax;
+          if (!group_sync(&S.sm_bar, sm_phase, ew)) goto done_softmax;
           if (valid) atomicMin(&S.first_row, r);
-          if (!group_sync(&S.sm_bar, sm_phase, P.err)) goto done_softmax;
+          if (!group_sync(&S.sm_bar, sm_phase, ew)) goto done_softmax;
           const uint32_t fr = S.first_row;
           // (tcgen05.ld is warp-collective: every lane loads, one lane keeps)
 #pragma unroll 1
@@ -508,15 +512,15 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(TcAttnParams P) {
             for (int h = 0; h < kH; ++h) S.mref[h] = 0.f;
           }
           any_valid = fr != kNoRow;
-          if (!group_sync(&S.sm_bar, sm_phase, P.err)) goto done_softmax;
+          if (!group_sync(&S.sm_bar, sm_phase, ew)) goto done_softmax;
         }
         // P of this tile (the previous PV must be done with the buffer)
-        if (!mbar_wait_warp(&S.p_empty, (n & 1) ^ 1, P.err)) goto done_softmax;
+        if (!mbar_wait_warp(&S.p_empty, (n & 1) ^ 1, ew)) goto done_softmax;
         const bool flag = write_p(valid);
         const uint32_t fc = n % 3;
         if (r == 0) S.flagcnt[(n + 1) % 3] = 0;
         if (flag) atomicAdd(&S.flagcnt[fc], 1u);
-        if (!group_sync(&S.sm_bar, sm_phase, P.err)) goto done_softmax;
+        if (!group_sync(&S.sm_bar, sm_phase, ew)) goto done_softmax;
         if (S.flagcnt[fc] != 0) {
           // rare path: exact tile max per head, raise the running max, rescale
           // O and L, rewrite P
@@ -531,14 +535,14 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(TcAttnParams P) {
               if (lane == (uint32_t)h) S.tmax[warp][32 * hf + h] = v;
             }
           }
-          if (!group_sync(&S.sm_bar, sm_phase, P.err)) goto done_softmax;
+          if (!group_sync(&S.sm_bar, sm_phase, ew)) goto done_softmax;
           if (r < kH) {
             const float M = fmaxf(fmaxf(S.tmax[0][r], S.tmax[1][r]), fmaxf(S.tmax[2][r], S.tmax[3][r]));
             const float mo = S.mref[r], mn = fmaxf(mo, M);
             S.alpha[r] = exp2f(mo - mn);
             S.mref[r] = mn;
           }
-          if (!group_sync(&S.sm_bar, sm_phase, P.err)) goto done_softmax;
+          if (!group_sync(&S.sm_bar, sm_phase, ew)) goto done_softmax;
           if (!first) {
 #pragma unroll 1
             for (uint32_t m = 0; m < 10; ++m) {   // O^T (8 x 32 columns) then L (2 x 32)
@@ -561,7 +565,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(TcAttnParams P) {
       }
       // ---- query end: per-head sums (any lane of L), then the output
       if (has_tiles) {
-        if (!mbar_wait_warp(&S.o_full, qn & 1, P.err)) goto done_softmax;
+        if (!mbar_wait_warp(&S.o_full, qn & 1, ew)) goto done_softmax;
         tc_fence_after();
         if (warp < 2) {   // every row of L holds the sums: warp w keeps heads 32w + lane
           uint32_t a[32];
@@ -575,7 +579,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(TcAttnParams P) {
           S.linv[32 * warp + lane] = l > 0.f ? 1.f / l : 0.f;
         }
       }
-      if (!group_sync(&S.sm_bar, sm_phase, P.err)) goto done_softmax;
+      if (!group_sync(&S.sm_bar, sm_phase, ew)) goto done_softmax;
       if (dec && C > 1) {
         // (max, sum) of this rank for the cluster merge; O follows from TMEM
         if (r < kH) {
@@ -618,7 +622,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(TcAttnParams P) {
                 srow[h * 128] = __float2bfloat16_rn(__uint_as_float(a[h]) * S.linv[32 * hf + h]);
             }
           }
-          if (!group_sync(&S.sm_bar, sm_phase, P.err)) goto done_softmax;
+          if (!group_sync(&S.sm_bar, sm_phase, ew)) goto done_softmax;
           __nv_bfloat16 *o = P.out + (size_t)qi * kH * kD + m * 128;
 #pragma unroll
           for (uint32_t i = 0; i < 8; ++i) {
@@ -626,7 +630,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(TcAttnParams P) {
             *reinterpret_cast<uint4 *>(o + (size_t)h * kD + seg * 8) =
                 *reinterpret_cast<const uint4 *>(stage + h * 256 + seg * 16);
           }
-          if (!group_sync(&S.sm_bar, sm_phase, P.err)) goto done_softmax;
+          if (!group_sync(&S.sm_bar, sm_phase, ew)) goto done_softmax;
         }
       }
       if (has_tiles) {
@@ -636,7 +640,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(TcAttnParams P) {
         ++qn;
       }
       // keep the shared sums alive until every thread has read them
-      if (!group_sync(&S.sm_bar, sm_phase, P.err)) goto done_softmax;
+      if (!group_sync(&S.sm_bar, sm_phase, ew)) goto done_softmax;
     }
   done_softmax:;
   }
@@ -764,7 +768,7 @@ cudaError_t launch_attention_tc(const AttnArgs &a, uint32_t rows_max, int *err, 
     const uint32_t n_tiles = (rows_max + kRows - 1) / kRows;
     P.cluster = pick_cluster(n_tiles, P.n_q, smem);
     cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute at[1];
+    cudaLaunchAttribute at[2];
     at[0].id = cudaLaunchAttributeClusterDimension;
     at[0].val.clusterDim.x = P.cluster;
     at[0].val.clusterDim.y = 1;
@@ -773,17 +777,19 @@ cudaError_t launch_attention_tc(const AttnArgs &a, uint32_t rows_max, int *err, 
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
+    at[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = at;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     e = cudaLaunchKernelEx(&cfg, attn_tc_kernel, P);
     note_launches(1);
     return e != cudaSuccess ? e : cudaGetLastError();
   }
   P.cluster = 0;
   const uint32_t grid = min(P.n_q, (uint32_t)num_sms());
-  attn_tc_kernel<<<grid, kThreads, smem, s>>>(P);
+  e = launch_pdl(attn_tc_kernel, dim3(grid), dim3(kThreads), smem, s, P);
   note_launches(1);
-  return cudaGetLastError();
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace ds4a

@@ -8,6 +8,16 @@
 
 namespace ds4a {
 
+// Programmatic dependent launch. Kernels launched with launch_pdl may start
+// while the previous kernel in the stream is still running: each calls
+// pdl_wait() (the previous grid has completed and its writes are visible)
+// before its first global memory access, then pdl_trigger() so that the next
+// kernel can be scheduled as soon as SMs free up.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ float ld_f32(const float *p, size_t i) { return p[i]; }
 __device__ __forceinline__ float ld_f32(const __nv_bfloat16 *p, size_t i) {
   return __bfloat162float(p[i]);

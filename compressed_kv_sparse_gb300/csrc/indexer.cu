@@ -83,6 +83,8 @@ inline TcWs tc_ws_split(void *ws, uint32_t nq, uint32_t B, uint32_t Hi, uint32_t
 // per pair of dims; the same grid clears the call's counters (error word,
 // control words and, when the scorer builds them, histograms).
 __global__ void index_qbf_kernel(IndexArgs a, TcWs w, bool clear_hist) {
+  pdl_wait();
+  pdl_trigger();
   const uint32_t Hi = a.n_heads, Di = a.dim, n_nope = Di - a.rot;
   const size_t nq = (size_t)a.batch * a.T;
   const size_t npair = nq * Hi * Di / 2;
@@ -586,6 +588,8 @@ __device__ __forceinline__ void rescore_band(const __nv_bfloat16 *qsm, const flo
 // every visible row in place.
 __global__ void __launch_bounds__(kSelectThreads)
     topk_select_tc_kernel(IndexArgs a, TcWs w, float cb, uint32_t G, bool local_hist) {
+  pdl_wait();
+  pdl_trigger();
   extern __shared__ float4 dyn4[];
   __shared__ uint32_t hist[256];
   __shared__ uint32_t wsum[33];
@@ -981,7 +985,9 @@ cudaError_t launch_index_tc(const IndexArgs &a, cudaStream_t s) {
   size_t nthreads = npair;
   if (scorer_hist && (size_t)nq * kHistBins > nthreads) nthreads = (size_t)nq * kHistBins;
   if ((size_t)nq * 4 > nthreads) nthreads = (size_t)nq * 4;
-  index_qbf_kernel<<<(unsigned)((nthreads + 255) / 256), 256, 0, s>>>(a, w, scorer_hist);
+  cudaError_t eq = launch_pdl(index_qbf_kernel, dim3((unsigned)((nthreads + 255) / 256)),
+                              dim3(256), 0, s, a, w, scorer_hist);
+  if (eq != cudaSuccess) return eq;
   note_launches(1);
   const uint32_t vis_max = min((a.pos0 + a.T) / 4, a.n_comp);
   if (vis_max > a.top_k) {
@@ -1010,7 +1016,9 @@ cudaError_t launch_index_tc(const IndexArgs &a, cudaStream_t s) {
   cudaError_t e = ensure_smem(topk_select_tc_kernel, smem, &smem_set);
   if (e != cudaSuccess) return e;
   const uint32_t G = scorer_hist ? select_groups(nq) : 1;
-  topk_select_tc_kernel<<<nq * G, kSelectThreads, smem, s>>>(a, w, (float)cb, G, !scorer_hist);
+  e = launch_pdl(topk_select_tc_kernel, dim3(nq * G), dim3(kSelectThreads), smem, s, a, w,
+                 (float)cb, G, !scorer_hist);
+  if (e != cudaSuccess) return e;
   note_launches(1);
   return cudaGetLastError();
 }

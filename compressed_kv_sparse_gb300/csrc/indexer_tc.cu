@@ -121,6 +121,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  pdl_wait();
+  pdl_trigger();
 
   if (warp == 0) {
     if (lane == 0) {
@@ -336,7 +338,8 @@ cudaError_t launch_qg(const IndexTcArgs &a, cudaStream_t s) {
   e = ensure_smem(index_score_tc_kernel<QG>, C::kSmem, &smem_set);
   if (e != cudaSuccess) return e;
   const uint32_t grid = min(P.total_items, (uint32_t)num_sms());
-  index_score_tc_kernel<QG><<<grid, kThreads, C::kSmem, s>>>(tk, tq, P);
+  e = launch_pdl(index_score_tc_kernel<QG>, dim3(grid), dim3(kThreads), C::kSmem, s, tk, tq, P);
+  if (e != cudaSuccess) return e;
   note_launches(1);
   return cudaGetLastError();
 }

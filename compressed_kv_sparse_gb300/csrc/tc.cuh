@@ -58,7 +58,14 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
 // lasted kErrPollNs: a read costs an L2 round trip, during which this thread
 // would not see the phase complete.
 constexpr uint64_t kErrPollNs = 20000ull;   // 20 us
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, int *err) {
+// The kernel's error word: a timed-out wait adds 1; the kernel gives up when
+// the word differs from `base`, its value when the kernel started (so the
+// word never needs resetting between launches).
+struct ErrWord {
+  int *p;
+  int base;
+};
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, ErrWord err) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_ns();
   for (uint32_t i = 1;; ++i) {
@@ -66,18 +73,23 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, int *e
     if ((i & 63) == 0) {
       const uint64_t dt = global_ns() - t0;
       if (dt > kWaitLimitNs) {
-        atomicExch(err, 1);
+        atomicAdd(err.p, 1);
         return false;
       }
-      if (dt > kErrPollNs && (i & 1023) == 0 && *(volatile int *)err) return false;
+      if (dt > kErrPollNs && (i & 1023) == 0 && *(volatile int *)err.p != err.base) return false;
     }
   }
+}
+// A word zeroed before the launch.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, int *err) {
+  return mbar_wait(bar, parity, ErrWord{err, 0});
 }
 
 // The same wait with one outcome for the whole (converged) warp: a lane that
 // gave up makes every lane give up, so warp-collective instructions after it
 // are never reached by part of a warp.
-__device__ __forceinline__ bool mbar_wait_warp(uint64_t *bar, uint32_t parity, int *err) {
+template <typename E>
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t *bar, uint32_t parity, E err) {
   return __all_sync(0xffffffffu, mbar_wait(bar, parity, err));
 }
 
@@ -126,7 +138,8 @@ __device__ __forceinline__ void fence_proxy_async() {
 
 // A group barrier over `count` threads built on an mbarrier (bounded wait).
 // Every member calls it the same number of times; `phase` is per thread.
-__device__ __forceinline__ bool group_sync(uint64_t *bar, uint32_t &phase, int *err) {
+template <typename E>
+__device__ __forceinline__ bool group_sync(uint64_t *bar, uint32_t &phase, E err) {
   mbar_arrive(bar);
   const bool ok = mbar_wait_warp(bar, phase, err);
   phase ^= 1;
