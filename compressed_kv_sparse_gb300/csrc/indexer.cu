@@ -588,8 +588,6 @@ __device__ __forceinline__ void rescore_band(const __nv_bfloat16 *qsm, const flo
 // every visible row in place.
 __global__ void __launch_bounds__(kSelectThreads)
     topk_select_tc_kernel(IndexArgs a, TcWs w, float cb, uint32_t G, bool local_hist) {
-  pdl_wait();
-  pdl_trigger();
   extern __shared__ float4 dyn4[];
   __shared__ uint32_t hist[256];
   __shared__ uint32_t wsum[33];
@@ -615,11 +613,11 @@ __global__ void __launch_bounds__(kSelectThreads)
   const uint32_t vis = min((p + 1) / 4, a.n_comp), k = a.top_k;
   const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   int32_t *out = a.topk + (size_t)qi * k;
-  if (vis <= k || *(volatile int *)w.err) {
-    const bool bad = vis > k;
+  if (vis <= k) {
+    pdl_wait();
+    pdl_trigger();
     if (g == 0)
-      for (uint32_t j = threadIdx.x; j < k; j += blockDim.x)
-        out[j] = (!bad && j < vis) ? (int32_t)j : -1;
+      for (uint32_t j = threadIdx.x; j < k; j += blockDim.x) out[j] = j < vis ? (int32_t)j : -1;
     return;
   }
   float *sc = w.scores + (size_t)qi * a.comp_cap;
@@ -675,6 +673,15 @@ __global__ void __launch_bounds__(kSelectThreads)
       atomicMax(&s_qexp[1], emax);
     }
     if (threadIdx.x < Hi) wsh[threadIdx.x] = __bfloat162float(wq[threadIdx.x]);
+  }
+  // everything above read only what was written two or more launches back
+  // (q', head weights, row norms); the scores and histograms need the scorer
+  pdl_wait();
+  pdl_trigger();
+  if (*(volatile int *)w.err) {   // the scorer gave up: no list
+    if (g == 0)
+      for (uint32_t j = threadIdx.x; j < k; j += blockDim.x) out[j] = -1;
+    return;
   }
   // theta_S: lower edge of the histogram bin holding the k-th largest S~
   {

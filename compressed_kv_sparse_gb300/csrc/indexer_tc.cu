@@ -121,8 +121,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  pdl_wait();
-  pdl_trigger();
+  if (threadIdx.x != 0) {   // the TMA producer waits after its first key loads
+    pdl_wait();
+    pdl_trigger();
+  }
 
   if (warp == 0) {
     if (lane == 0) {
@@ -131,6 +133,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       int32_t cur = -1;
       int issued[C::kStages];
       for (int s = 0; s < C::kStages; ++s) issued[s] = -1;
+      // the key tiles of the first stages load before the wait for the
+      // previous launch: the rows were written two or more launches back
+      uint32_t pre = 0;
+      for (uint32_t it = it0; it < it1 && pre < (uint32_t)C::kStages; ++it) {
+        uint32_t b, g, tile;
+        if (!decode_item<QG>(P, it, b, g, tile)) continue;
+        mbar_arrive_expect_tx(&a_full[pre], kABytes);
+        tma_load_3d(sA + (size_t)pre * kABytes, &tmap_k, &a_full[pre], 0, (int)(tile * kRows),
+                    (int)b);
+        tma_load_3d(sA + (size_t)pre * kABytes + kKBlockBytes, &tmap_k, &a_full[pre], 64,
+                    (int)(tile * kRows), (int)b);
+        issued[pre] = 0;
+        ++pre;
+      }
+      pdl_wait();
+      pdl_trigger();
+      uint32_t n_vis = 0;
       for (uint32_t it = it0; it < it1; ++it) {
         uint32_t b, g, tile;
         if (!decode_item<QG>(P, it, b, g, tile)) continue;
@@ -146,13 +165,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_2d(sB + C::kBBytes / 2, &tmap_q, b_full, 64, row0);
           cur = bg;
         }
-        if (!mbar_wait(&a_empty[stage], phase ^ 1, P.err)) break;
-        mbar_arrive_expect_tx(&a_full[stage], kABytes);
-        tma_load_3d(sA + (size_t)stage * kABytes, &tmap_k, &a_full[stage], 0, (int)(tile * kRows),
-                    (int)b);
-        tma_load_3d(sA + (size_t)stage * kABytes + kKBlockBytes, &tmap_k, &a_full[stage], 64,
-                    (int)(tile * kRows), (int)b);
-        issued[stage] = (int)phase;
+        if (n_vis++ >= pre) {   // (the first `pre` are in flight already)
+          if (!mbar_wait(&a_empty[stage], phase ^ 1, P.err)) break;
+          mbar_arrive_expect_tx(&a_full[stage], kABytes);
+          tma_load_3d(sA + (size_t)stage * kABytes, &tmap_k, &a_full[stage], 0,
+                      (int)(tile * kRows), (int)b);
+          tma_load_3d(sA + (size_t)stage * kABytes + kKBlockBytes, &tmap_k, &a_full[stage], 64,
+                      (int)(tile * kRows), (int)b);
+          issued[stage] = (int)phase;
+        }
         if (++stage == C::kStages) {
           stage = 0;
           phase ^= 1;
