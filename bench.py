@@ -166,44 +166,54 @@ class Runner:
             self.layers.append(L)
         torch.cuda.synchronize(device)
 
-    # one layer; `ev` = optional list of (name, start_event, end_event) to record
-    def layer_step(self, L, ev=None):
+    # the library calls of one layer's step, in order: (name, fn)
+    def layer_calls(self, L):
         lib, s, c, inp = self.lib, L["s"], L["cache"], L["inp"]
-        c.n_tokens = self.p0
         k, scale = s.top_k, lib.default_scale(s.head_dim)
+        p0, T, end = self.p0, self.T, self.p0 + self.T
 
-        def timed(name, fn):
-            if ev is None:
+        def at(n, fn):          # the host position mirror each call expects
+            def run():
+                c.n_tokens = n
                 fn()
-                return
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record()
-            fn()
-            e1.record()
-            ev.append((name, e0, e1))
+            return run
 
+        calls = []
         if self.decode:
-            timed("append", lambda: lib.ds4a_compress_append(c, self.p0, 1, inp))
+            calls.append(("append", at(p0, lambda: lib.ds4a_compress_append(c, p0, 1, inp))))
             if s.ratio == 4:
-                timed("index_topk", lambda: lib.ds4a_index_topk(
-                    c, self.p0, 1, inp["q_idx"], inp["w"], s.index_heads, k, L["topk"],
-                    L["ws_idx"]))
-            timed(f"attn_r{s.ratio}", lambda: lib.ds4a_sparse_attn_decode(
-                c, self.p0, L["q"], s.n_heads, L.get("topk"), k, scale, L["out"], L["ws_attn"]))
+                calls.append(("index_topk", at(end, lambda: lib.ds4a_index_topk(
+                    c, p0, 1, inp["q_idx"], inp["w"], s.index_heads, k, L["topk"],
+                    L["ws_idx"]))))
+            calls.append((f"attn_r{s.ratio}", at(end, lambda: lib.ds4a_sparse_attn_decode(
+                c, p0, L["q"], s.n_heads, L.get("topk"), k, scale, L["out"], L["ws_attn"]))))
         else:
-            timed("append", lambda: lib.ds4a_compress_append(c, self.p0, self.T, inp,
-                                                             raw_chunk_out=L["chunk"]))
+            calls.append(("append", at(p0, lambda: lib.ds4a_compress_append(
+                c, p0, T, inp, raw_chunk_out=L["chunk"]))))
             if s.ratio == 4:
-                timed("index_topk", lambda: lib.ds4a_index_topk(
-                    c, self.p0, self.T, inp["q_idx"], inp["w"], s.index_heads, k, L["topk"],
-                    L["ws_idx"]))
-            timed(f"attn_r{s.ratio}", lambda: lib.ds4a_sparse_attn_prefill_chunk(
-                c, self.p0, self.T, L["q"], s.n_heads, L["chunk"], L.get("topk"), k, scale,
-                L["out"], L["ws_attn"]))
+                calls.append(("index_topk", at(end, lambda: lib.ds4a_index_topk(
+                    c, p0, T, inp["q_idx"], inp["w"], s.index_heads, k, L["topk"],
+                    L["ws_idx"]))))
+            calls.append((f"attn_r{s.ratio}", at(end, lambda: lib.ds4a_sparse_attn_prefill_chunk(
+                c, p0, T, L["q"], s.n_heads, L["chunk"], L.get("topk"), k, scale, L["out"],
+                L["ws_attn"]))))
+        return calls
 
-    def step(self, ev=None):
+    def layer_step(self, L):
+        for _, fn in self.layer_calls(L):
+            fn()
+
+    def step(self):
         for L in self.layers:
-            self.layer_step(L, ev)
+            self.layer_step(L)
+
+    # every call of one kind, over all layers in order: (name, [fn, ...])
+    def calls_by_kind(self):
+        kinds = {}
+        for L in self.layers:
+            for name, fn in self.layer_calls(L):
+                kinds.setdefault(name, []).append(fn)
+        return kinds
 
     def tokens_per_step(self):
         return self.wl.batch * self.T
@@ -381,31 +391,36 @@ def run_gpu(args, wl, rank, world, device):
         ms_step = float(t.item())
     value = world * R.tokens_per_step() / (ms_step / 1e3)
 
-    # per-call device time: an eager pass with events around each call on the
-    # launching stream. The GPU first spins on a sleep kernel long enough for the
-    # host to enqueue the whole step, so the events bracket back-to-back device
-    # work and not the host's argument checks and launch calls.
-    ev = []
-    torch.cuda.synchronize(device)
-    t_host = time.perf_counter()
-    R.step()
-    torch.cuda.synchronize(device)
-    t_host = time.perf_counter() - t_host
-    sleep_cycles = int(min(4.0, 3.0 * t_host + 0.002) * 2.2e9)
-    for _ in range(max(1, min(args.steps, 5))):
-        torch.cuda._sleep(sleep_cycles)
-        R.step(ev)
-        if flush is not None:
-            flush_l2(flush)
-        torch.cuda.synchronize(device)
+    # per-call device time: for each call kind, one CUDA graph runs that call on
+    # every layer that has it (layer order, as in a step); replays are timed
+    # with CUDA events on the launching stream, with the L2 flush between
+    # replays (when the step flushes) timed separately and subtracted
     per_call = {}
-    for name, a, b in ev:
-        per_call.setdefault(name, []).append(a.elapsed_time(b))
+    torch.cuda.synchronize(device)
+    reps = max(3, min(args.steps, 10))
+    for name, fns in R.calls_by_kind().items():
+        gk = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gk):
+            for fn in fns:
+                fn()
+        for _ in range(2):
+            gk.replay()
+        torch.cuda.synchronize(device)
+        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a0.record()
+        for _ in range(reps):
+            if flush is not None:
+                flush_l2(flush)
+            gk.replay()
+        a1.record()
+        torch.cuda.synchronize(device)
+        per_call[name] = [(a0.elapsed_time(a1) - flush_ms * reps) / (reps * len(fns))]
+        del gk
     alg = R.algorithmic()
     calls = {}
     for name, ts in per_call.items():
         n_per_step = alg[name][2]
-        t_launch = sum(ts) / len(ts) / 1e3          # seconds per call
+        t_launch = max(ts[0], 1e-6) / 1e3           # seconds per call
         by = alg[name][0] / n_per_step
         fl = alg[name][1] / n_per_step
         calls[name] = {"ms_per_call": t_launch * 1e3, "calls_per_step": n_per_step,
