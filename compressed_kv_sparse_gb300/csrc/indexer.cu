@@ -378,10 +378,26 @@ __device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t *wsum, 
   return r;
 }
 
-inline size_t select_tc_smem(uint32_t comp_cap) {
-  const size_t words = (comp_cap + 31) / 32;
-  return 64 * kQB * 2 + 64 * 4 + 64 * 128 * 4 + 64 * 64 * 4 + 3 * kCandCap * 4 + words * 4;
-}
+// Select kernel configurations: 1024 threads when several blocks share a
+// query (decode), 256 when each query has one block (prefill, large batches;
+// four blocks per SM then overlap their latency chains).
+template <int NT>
+struct SelCfg {
+  static constexpr int NW = NT / 32;                  // warps
+  static constexpr int HPW = 64 / NW;                 // q' heads per warp (A term)
+  static constexpr int BPT = 4096 / NT;               // histogram bins per thread
+  static constexpr int RPR = 2 * NW;                  // band rows per rescoring round
+  static constexpr uint32_t CAP = NT == 1024 ? 4096u : 1536u;   // candidates in smem
+  static constexpr uint32_t BANDCAP = CAP < 2048u ? CAP : 2048u;
+  static constexpr size_t kScratch =
+      (size_t)(4096 * 4 > RPR * 192 * 4 ? (4096 * 4 > BANDCAP * 8 ? 4096 * 4 : BANDCAP * 8)
+                                        : (RPR * 192 * 4 > BANDCAP * 8 ? RPR * 192 * 4
+                                                                      : BANDCAP * 8));
+  static size_t smem(uint32_t comp_cap) {
+    const size_t words = (comp_cap + 31) / 32;
+    return 64 * kQB * 2 + 64 * 4 + kScratch + 3 * (size_t)CAP * 4 + words * 4;
+  }
+};
 
 // Blocks per query: one wave of 1024-thread blocks (one per SM), at most 16.
 inline uint32_t select_groups(uint32_t nq) {
@@ -487,20 +503,22 @@ __device__ __forceinline__ float rescore_row(const __nv_bfloat16 *qsm, const flo
   return tot;
 }
 
-// Exact recipe for the band rows (whole block): rounds of 64 rows; their keys
-// go to `kbuf` as fp32, warp pair (2g, 2g + 1) runs rows 4g .. 4g + 3 of the
-// round against heads 32 (warp & 1) + lane, so one q' load serves four rows
-// and one key load all 32 heads of a warp. Per-head ReLU dots land in `relb`
-// [64 rows][64 heads]; one thread per row sums them in ascending h. Results
-// replace cS[band[i]].
+// Exact recipe for the band rows (whole block, NW warps): rounds of 2 NW rows;
+// their keys go to `kbuf` as fp32, warp pair (2g, 2g + 1) runs rows
+// 4g .. 4g + 3 of the round against heads 32 (warp & 1) + lane, so one q'
+// load serves four rows and one key load all 32 heads of a warp. Per-head
+// ReLU dots land in `relb` [2 NW rows][64 heads]; one thread per row sums them
+// in ascending h. Results replace cS[band[i]].
+template <int NW>
 __device__ __forceinline__ void rescore_band(const __nv_bfloat16 *qsm, const float *wsh,
                                              float *kbuf, float *relb, const uint32_t *band,
                                              uint32_t nband, const uint32_t *cidx, float *cS,
                                              const __nv_bfloat16 *keys, uint32_t *rexact,
                                              int eq_min, int eq_max) {
   const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (uint32_t base = 0; base < nband; base += 64) {
-    const uint32_t nr = min(64u, nband - base);
+  constexpr uint32_t RPR = 2 * NW;
+  for (uint32_t base = 0; base < nband; base += RPR) {
+    const uint32_t nr = min(RPR, nband - base);
 #pragma unroll
     for (uint32_t t = 0; t < 2; ++t) {
       const uint32_t rr = 2 * warp + t;
@@ -586,8 +604,11 @@ __device__ __forceinline__ void rescore_band(const __nv_bfloat16 *qsm, const flo
 // rescored with the exact recipe and the final selection is exact (ties to
 // the lower index). If the candidates overflow, the same selection runs over
 // every visible row in place.
-__global__ void __launch_bounds__(kSelectThreads)
-    topk_select_tc_kernel(IndexArgs a, TcWs w, float cb, uint32_t G, bool local_hist) {
+template <int NT>
+__global__ void __launch_bounds__(NT, NT == 256 ? 4 : 1)
+    topk_select_tc_kernel(IndexArgs a, TcWs w, float cb, uint32_t G) {
+  using SC = SelCfg<NT>;
+  constexpr uint32_t CAP = SC::CAP;
   extern __shared__ float4 dyn4[];
   __shared__ uint32_t hist[256];
   __shared__ uint32_t wsum[33];
@@ -597,15 +618,18 @@ __global__ void __launch_bounds__(kSelectThreads)
   __shared__ uint32_t s_misc[6];
   __shared__ float s_red[32], s_wabs[32];
   __shared__ int s_qexp[2];        // exponent range of the nonzero q' entries
-  __shared__ uint32_t s_rexact[64];  // band round: fma is exact for the row
+  __shared__ uint32_t s_rexact[SC::RPR];  // band round: fma is exact for the row
   __nv_bfloat16 *qsm = reinterpret_cast<__nv_bfloat16 *>(dyn4);   // [64][kQB]
   float *wsh = reinterpret_cast<float *>(qsm + 64 * kQB);           // [64]
-  float *kbuf = wsh + 64;                                           // [64][128]
-  float *relb = kbuf + 64 * 128;                                    // [64][64]
-  uint32_t *cidx = reinterpret_cast<uint32_t *>(relb + 64 * 64);    // [kCandCap]
-  float *cS = reinterpret_cast<float *>(cidx + kCandCap);           // [kCandCap]
-  float *ce = cS + kCandCap;                                        // [kCandCap]
-  uint32_t *bitmap = reinterpret_cast<uint32_t *>(ce + kCandCap);   // [comp_cap / 32]
+  // scratch, used in turn by: the second-level histogram [4096]; the band
+  // rescoring's keys [RPR][128] and ReLU dots [RPR][64]; the band values and
+  // rows [BANDCAP] + [BANDCAP]
+  float *scratch = wsh + 64;
+  float *kbuf = scratch, *relb = scratch + SC::RPR * 128;
+  uint32_t *cidx = reinterpret_cast<uint32_t *>(scratch + SC::kScratch / 4);   // [CAP]
+  float *cS = reinterpret_cast<float *>(cidx + CAP);                           // [CAP]
+  float *ce = cS + CAP;                                                        // [CAP]
+  uint32_t *bitmap = reinterpret_cast<uint32_t *>(ce + CAP);   // [comp_cap / 32]
 
   const uint32_t Hi = 64, Di = 128;
   const uint32_t qi = blockIdx.x / G, g = blockIdx.x % G;
@@ -627,7 +651,7 @@ __global__ void __launch_bounds__(kSelectThreads)
   uint32_t *ctrl = w.ctrl + (size_t)qi * 4;
   uint32_t *cand = w.cand + (size_t)qi * kCandGlobal;
 
-  // A = c * sum_h |w_h| ||q'_h|| (two heads per warp); q' rows to shared
+  // A = c * sum_h |w_h| ||q'_h|| (HPW heads per warp); q' rows to shared
   // memory as fp32, with the exponent range of their nonzero entries
   if (threadIdx.x == 0) {
     s_qexp[0] = 1000;
@@ -638,8 +662,8 @@ __global__ void __launch_bounds__(kSelectThreads)
     float part = 0.f, wabs = 0.f;
     int emin = 1000, emax = -1000;
 #pragma unroll
-    for (uint32_t j = 0; j < 2; ++j) {
-      const uint32_t h = warp + 32 * j;
+    for (uint32_t j = 0; j < (uint32_t)SC::HPW; ++j) {
+      const uint32_t h = warp + SC::NW * j;
       const uint2 v = *reinterpret_cast<const uint2 *>(qb + (size_t)h * Di + 4 * lane);
       const float x0 = __uint_as_float(v.x << 16), x1 = __uint_as_float(v.x & 0xFFFF0000u);
       const float x2 = __uint_as_float(v.y << 16), x3 = __uint_as_float(v.y & 0xFFFF0000u);
@@ -684,46 +708,32 @@ __global__ void __launch_bounds__(kSelectThreads)
     return;
   }
   // theta_S: lower edge of the histogram bin holding the k-th largest S~
+  if (threadIdx.x == 0) s_misc[2] = 0;   // candidate count (one block per query)
   {
     const uint32_t *hq = w.hist + (size_t)qi * kHistBins;
-    if (local_hist) {
-      // one block per query: count the keys' top 12 bits of every visible row
-      uint32_t *lh = reinterpret_cast<uint32_t *>(cS);   // free until the candidates load
-      for (uint32_t i = threadIdx.x; i < kHistBins; i += blockDim.x) lh[i] = 0u;
-      __syncthreads();
-      for (uint32_t base = 0; base < vis; base += blockDim.x) {
-        const uint32_t r = base + threadIdx.x;
-        const uint32_t bin = r < vis ? score_key(sc[r]) >> 20 : kHistBins;
-        const uint32_t peers = __match_any_sync(0xffffffffu, bin);
-        if (bin < kHistBins && lane == (uint32_t)(__ffs(peers) - 1))
-          atomicAdd(&lh[bin], (uint32_t)__popc(peers));
-      }
-      __syncthreads();
-      hq = lh;
-    }
-    uint32_t c4[4], loc = 0;
+    uint32_t cb4[SC::BPT], loc = 0;
 #pragma unroll
-    for (uint32_t j = 0; j < 4; ++j) {
-      c4[j] = hq[kHistBins - 1 - (4 * threadIdx.x + j)];
-      loc += c4[j];
+    for (uint32_t j = 0; j < (uint32_t)SC::BPT; ++j) {
+      cb4[j] = hq[kHistBins - 1 - (SC::BPT * threadIdx.x + j)];
+      loc += cb4[j];
     }
     uint32_t tot;
     uint32_t cum = block_excl_scan(loc, wsum, &tot);   // also syncs s_red / wsh / qsm
     if (cum < k && cum + loc >= k) {
 #pragma unroll
-      for (uint32_t j = 0; j < 4; ++j) {
-        if (cum + c4[j] >= k) {
-          s_misc[0] = kHistBins - 1 - (4 * threadIdx.x + j);
+      for (uint32_t j = 0; j < (uint32_t)SC::BPT; ++j) {
+        if (cum + cb4[j] >= k) {
+          s_misc[0] = kHistBins - 1 - (SC::BPT * threadIdx.x + j);
           s_misc[4] = cum;
           break;
         }
-        cum += c4[j];
+        cum += cb4[j];
       }
     }
   }
   __syncthreads();
   float At = 0.f, Wt = 0.f;
-  for (uint32_t i = 0; i < 32; ++i) {
+  for (uint32_t i = 0; i < (uint32_t)SC::NW; ++i) {
     At += s_red[i];
     Wt += s_wabs[i];
   }
@@ -738,7 +748,9 @@ __global__ void __launch_bounds__(kSelectThreads)
   const float theta = theta_s - E - fabsf(theta_s) * (2.0f * kRel);
   auto err_of = [&](float S, float nm) { return A * nm + fabsf(S) * kRel + eta; };
 
-  // ---- this block's share of the rows: candidates with U >= theta
+  // ---- this block's share of the rows: candidates with U >= theta; with one
+  // block per query they go straight to shared memory, else to the query's
+  // list in global memory for the last block to finish
   {
     const uint32_t per = ((vis + G * 32 - 1) / (G * 32)) * 32;
     const uint32_t r0 = g * per, r1 = min(vis, r0 + per);
@@ -746,47 +758,63 @@ __global__ void __launch_bounds__(kSelectThreads)
       const uint32_t r = base + lane;
       const bool ok = r < r1;
       const float S = ok ? sc[r] : 0.f;
-      const bool c = ok && S + err_of(S, nr[r]) >= theta;
+      const float e = ok ? err_of(S, nr[r]) : 0.f;
+      const bool c = ok && S + e >= theta;
       const uint32_t bal = __ballot_sync(0xffffffffu, c);
       if (bal) {
         uint32_t slot = 0;
-        if (lane == 0) slot = atomicAdd(&ctrl[0], (uint32_t)__popc(bal));
+        if (lane == 0)
+          slot = G == 1 ? atomicAdd(&s_misc[2], (uint32_t)__popc(bal))
+                        : atomicAdd(&ctrl[0], (uint32_t)__popc(bal));
         slot = __shfl_sync(0xffffffffu, slot, 0) + __popc(bal & ((1u << lane) - 1u));
         if (c) {
-          if (slot < kCandGlobal)
+          if (G == 1) {
+            if (slot < CAP) {
+              cidx[slot] = r;
+              cS[slot] = S;
+              ce[slot] = e;
+            }
+          } else if (slot < kCandGlobal) {
             cand[slot] = r;
-          else
+          } else {
             ctrl[2] = 1u;
+          }
         }
       }
     }
   }
-  __threadfence();
-  __syncthreads();
-  if (threadIdx.x == 0) s_misc[1] = atomicAdd(&ctrl[1], 1u) == G - 1 ? 1u : 0u;
-  __syncthreads();
-  if (!s_misc[1]) return;
-  __threadfence();
+  if (G > 1) {
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) s_misc[1] = atomicAdd(&ctrl[1], 1u) == G - 1 ? 1u : 0u;
+    __syncthreads();
+    if (!s_misc[1]) return;
+    __threadfence();
+  } else {
+    __syncthreads();
+  }
 
   const __nv_bfloat16 *keys = static_cast<const __nv_bfloat16 *>(a.keys) + (size_t)b * a.comp_cap * Di;
   float *kb = kbuf + warp * 128, *rel = relb + warp * 64;
-  const uint32_t nc = *(volatile uint32_t *)&ctrl[0];
-  const bool fast = *(volatile uint32_t *)&ctrl[2] == 0u && nc <= kCandCap;
+  const uint32_t nc = G == 1 ? s_misc[2] : *(volatile uint32_t *)&ctrl[0];
+  const bool fast = nc <= CAP && (G == 1 || *(volatile uint32_t *)&ctrl[2] == 0u);
   uint32_t need;
   if (fast) {
     // ---- certified selection on the candidates
     if (threadIdx.x == 0) s_misc[5] = 0u;
     __syncthreads();
-    for (uint32_t j = threadIdx.x; j < nc; j += blockDim.x) {
-      uint32_t r = *(volatile uint32_t *)&cand[j];
-      if (r >= vis) {   // never expected: the selection below recomputes from the scores
-        s_misc[5] = 1u;
-        r = 0;
+    if (G > 1) {
+      for (uint32_t j = threadIdx.x; j < nc; j += blockDim.x) {
+        uint32_t r = *(volatile uint32_t *)&cand[j];
+        if (r >= vis) {   // never expected: the selection below recomputes from the scores
+          s_misc[5] = 1u;
+          r = 0;
+        }
+        const float S = sc[r];
+        cidx[j] = r;
+        cS[j] = S;
+        ce[j] = err_of(S, nr[r]);
       }
-      const float S = sc[r];
-      cidx[j] = r;
-      cS[j] = S;
-      ce[j] = err_of(S, nr[r]);
     }
     const uint32_t words = (vis + 31) / 32;
     for (uint32_t i = threadIdx.x; i < words; i += blockDim.x) bitmap[i] = 0u;
@@ -807,22 +835,22 @@ __global__ void __launch_bounds__(kSelectThreads)
     }
     __syncthreads();
     {
-      uint32_t c4[4], loc = 0;
+      uint32_t cb4[SC::BPT], loc = 0;
 #pragma unroll
-      for (uint32_t j = 0; j < 4; ++j) {
-        c4[j] = h2[kHistBins - 1 - (4 * threadIdx.x + j)];
-        loc += c4[j];
+      for (uint32_t j = 0; j < (uint32_t)SC::BPT; ++j) {
+        cb4[j] = h2[kHistBins - 1 - (SC::BPT * threadIdx.x + j)];
+        loc += cb4[j];
       }
       uint32_t tot;
       uint32_t cum = block_excl_scan(loc, wsum, &tot);
       if (cum < need_b && cum + loc >= need_b) {
 #pragma unroll
-        for (uint32_t j = 0; j < 4; ++j) {
-          if (cum + c4[j] >= need_b) {
-            s_misc[5] = kHistBins - 1 - (4 * threadIdx.x + j);
+        for (uint32_t j = 0; j < (uint32_t)SC::BPT; ++j) {
+          if (cum + cb4[j] >= need_b) {
+            s_misc[5] = kHistBins - 1 - (SC::BPT * threadIdx.x + j);
             break;
           }
-          cum += c4[j];
+          cum += cb4[j];
         }
       }
     }
@@ -835,11 +863,13 @@ __global__ void __launch_bounds__(kSelectThreads)
     const float hi_cut = t_hi + E + fabsf(t_hi) * kRel;
     const float lo_cut = t_lo - E - fabsf(t_lo) * kRel;
     if (threadIdx.x == 0) {
+      s_misc[1] = 0;   // band compaction slots (the ticket flag is no longer read)
       s_misc[2] = 0;
       s_misc[3] = 0;
     }
     __syncthreads();
     uint32_t cls = 0;   // 2 bits per candidate of this thread: 1 in, 2 band
+    static_assert(CAP / NT <= 16, "two class bits per candidate of a thread");
     if (ok) {
       for (uint32_t j = threadIdx.x, u = 0; j < nc; j += blockDim.x, ++u) {
         const float S = cS[j], e = ce[j];
@@ -859,18 +889,19 @@ __global__ void __launch_bounds__(kSelectThreads)
     }
     __syncthreads();   // ce is free from here: it holds the band's candidate slots
     const uint32_t nband = s_misc[2], n_in = s_misc[3];
-    ok = ok && n_in <= k && k - n_in <= nband && nband <= 2048;
+    ok = ok && n_in <= k && k - n_in <= nband && nband <= SC::BANDCAP;
     if (ok) {
-      if (threadIdx.x == 0) s_misc[2] = 0;
-      __syncthreads();
+      // (s_misc[2] keeps the band count every thread read above: the slots
+      // come from a counter zeroed before that read's barrier)
       uint32_t *band = reinterpret_cast<uint32_t *>(ce);
       for (uint32_t j = threadIdx.x, u = 0; j < nc; j += blockDim.x, ++u)
-        if ((cls >> (2 * u)) & 2u) band[atomicAdd(&s_misc[2], 1u)] = j;
+        if ((cls >> (2 * u)) & 2u) band[atomicAdd(&s_misc[1], 1u)] = j;
       __syncthreads();
       // exact scores of the band
-      rescore_band(qsm, wsh, kbuf, relb, band, nband, cidx, cS, keys, s_rexact, eq_min, eq_max);
-      float *bV = kbuf;
-      uint32_t *bI = reinterpret_cast<uint32_t *>(kbuf + 2048);
+      rescore_band<SC::NW>(qsm, wsh, kbuf, relb, band, nband, cidx, cS, keys, s_rexact, eq_min,
+                           eq_max);
+      float *bV = scratch;
+      uint32_t *bI = reinterpret_cast<uint32_t *>(scratch + SC::BANDCAP);
       for (uint32_t i = threadIdx.x; i < nband; i += blockDim.x) {
         bV[i] = cS[band[i]];
         bI[i] = cidx[band[i]];
@@ -878,7 +909,7 @@ __global__ void __launch_bounds__(kSelectThreads)
       __syncthreads();
       // the k - n_in best of the band by (exact score desc, row asc)
       const uint32_t want = k - n_in;
-      for (uint32_t i = warp; i < nband; i += 32) {   // one warp per band row
+      for (uint32_t i = warp; i < nband; i += SC::NW) {   // one warp per band row
         const float V = bV[i];
         const uint32_t idx = bI[i];
         uint32_t rank = 0;
@@ -931,19 +962,19 @@ __global__ void __launch_bounds__(kSelectThreads)
       sc[s] = -INFINITY;
     } else {
       const uint32_t i = atomicAdd(&s_misc[2], 1u);
-      if (i < kCandCap) band[i] = s;
+      if (i < CAP) band[i] = s;
     }
   }
   __syncthreads();
   const uint32_t nband = s_misc[2];
-  if (nband <= kCandCap) {
-    for (uint32_t i = warp; i < nband; i += 32) {
+  if (nband <= CAP) {
+    for (uint32_t i = warp; i < nband; i += SC::NW) {
       const uint32_t s = band[i];
       const float V = rescore_row(qsm, wsh, kb, rel, keys + (size_t)s * Di, lane, eq_min, eq_max);
       if (lane == 0) sc[s] = V;
     }
   } else {
-    for (uint32_t s = warp; s < vis; s += 32) {
+    for (uint32_t s = warp; s < vis; s += SC::NW) {
       const float v = sc[s];
       if (v == INFINITY || v == -INFINITY) continue;
       const float V = rescore_row(qsm, wsh, kb, rel, keys + (size_t)s * Di, lane, eq_min, eq_max);
@@ -988,7 +1019,7 @@ cudaError_t launch_index_tc(const IndexArgs &a, cudaStream_t s) {
   const uint32_t nq = a.batch * a.T;
   TcWs w = tc_ws_split(a.ws, nq, a.batch, a.n_heads, a.dim, a.comp_cap, nullptr);
   const size_t npair = (size_t)nq * a.n_heads * a.dim / 2;
-  const bool scorer_hist = a.T < 4;   // the 1-query scorer builds the histograms
+  const bool scorer_hist = true;   // the scorer builds the key histograms
   size_t nthreads = npair;
   if (scorer_hist && (size_t)nq * kHistBins > nthreads) nthreads = (size_t)nq * kHistBins;
   if ((size_t)nq * 4 > nthreads) nthreads = (size_t)nq * 4;
@@ -1018,14 +1049,32 @@ cudaError_t launch_index_tc(const IndexArgs &a, cudaStream_t s) {
   // roundings) plus the fp32 epilogue; widened for the fp32 norms.
   const double cb = (gamma_n(a.dim + a.n_heads + 1) + gamma_n(4.0 * a.dim + a.n_heads + 1)) *
                     (1.0 + std::ldexp(1.0, -8));
-  const size_t smem = select_tc_smem(a.comp_cap);
-  static int smem_set = 0;
-  cudaError_t e = ensure_smem(topk_select_tc_kernel, smem, &smem_set);
-  if (e != cudaSuccess) return e;
-  const uint32_t G = scorer_hist ? select_groups(nq) : 1;
-  e = launch_pdl(topk_select_tc_kernel, dim3(nq * G), dim3(kSelectThreads), smem, s, a, w,
-                 (float)cb, G, !scorer_hist);
-  if (e != cudaSuccess) return e;
+  const uint32_t G = select_groups(nq);
+  if (G == 1) {
+    const size_t smem = SelCfg<256>::smem(a.comp_cap);
+    static int smem_set = 0;
+    cudaError_t e = ensure_smem(topk_select_tc_kernel<256>, smem, &smem_set);
+    if (e != cudaSuccess) return e;
+    // four blocks per SM: the largest shared-memory carveout
+    static int carve = 0;
+    if (!carve) {
+      e = cudaFuncSetAttribute(topk_select_tc_kernel<256>,
+                               cudaFuncAttributePreferredSharedMemoryCarveout,
+                               cudaSharedmemCarveoutMaxShared);
+      if (e != cudaSuccess) return e;
+      carve = 1;
+    }
+    e = launch_pdl(topk_select_tc_kernel<256>, dim3(nq), dim3(256), smem, s, a, w, (float)cb, G);
+    if (e != cudaSuccess) return e;
+  } else {
+    const size_t smem = SelCfg<1024>::smem(a.comp_cap);
+    static int smem_set = 0;
+    cudaError_t e = ensure_smem(topk_select_tc_kernel<1024>, smem, &smem_set);
+    if (e != cudaSuccess) return e;
+    e = launch_pdl(topk_select_tc_kernel<1024>, dim3(nq * G), dim3(1024), smem, s, a, w, (float)cb,
+                   G);
+    if (e != cudaSuccess) return e;
+  }
   note_launches(1);
   return cudaGetLastError();
 }

@@ -32,18 +32,22 @@ constexpr int kDim = 128;          // Di (MMA K)
 constexpr int kHeads = 64;         // Hi
 constexpr int kKBlockBytes = kRows * 128;          // one 64-column K block of A
 constexpr int kABytes = 2 * kKBlockBytes;          // 32 KiB per A stage
-constexpr int kThreads = 192;
 
 template <int QG>
 struct Cfg {
   static constexpr int N = kHeads * QG;
+  // epilogue warps: 4 (one per TMEM lane quarter) for one query, 8 for four
+  // (two per quarter, two queries each)
+  static constexpr int kEpiWarps = QG == 1 ? 4 : 8;
+  static constexpr int kQPW = QG * 4 / kEpiWarps;   // queries per epilogue warp
+  static constexpr int kThreads = 64 + 32 * kEpiWarps;
   static constexpr int kStages = QG == 1 ? 5 : 4;
   static constexpr int kHistBytes = QG == 1 ? 4096 * 4 : 0;   // per-CTA key histogram
   static constexpr int kBBytes = N * kDim * 2;
   // two accumulators of N columns (the allocation is a power of two >= 32)
   static constexpr int kTmemCols = QG == 1 ? 128 : 512;
   static constexpr size_t kSmem = 1024 + (size_t)kStages * kABytes + kBBytes + 1024 +
-                                  4 * QG * kHeads * 4 + kHistBytes;
+                                  kEpiWarps * QG * kHeads * 4 + kHistBytes;
 };
 
 struct ScoreParams {
@@ -77,7 +81,7 @@ __device__ __forceinline__ bool decode_item(const ScoreParams &P, uint32_t item,
 }
 
 template <int QG>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(Cfg<QG>::kThreads, 1)
     index_score_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
                           const __grid_constant__ CUtensorMap tmap_q, ScoreParams P) {
   using C = Cfg<QG>;
@@ -91,8 +95,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t *acc_full = a_empty + C::kStages, *acc_empty = acc_full + 2;
   uint64_t *b_full = acc_empty + 2, *b_empty = b_full + 1;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(b_empty + 1);
-  float *sw_all = reinterpret_cast<float *>(sB + C::kBBytes + 1024);   // [4 warps][QG][64]
-  uint32_t *shist = reinterpret_cast<uint32_t *>(sw_all + 4 * QG * kHeads);   // [4096] (QG == 1)
+  float *sw_all = reinterpret_cast<float *>(sB + C::kBBytes + 1024);   // [epi warps][QG][64]
+  uint32_t *shist = reinterpret_cast<uint32_t *>(sw_all + C::kEpiWarps * QG * kHeads);   // QG == 1
   uint64_t *epi_bar = reinterpret_cast<uint64_t *>(tmem_slot + 2);
 
   const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -107,7 +111,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&acc_full[s], 1);
-      mbar_init(&acc_empty[s], 4);
+      mbar_init(&acc_empty[s], C::kEpiWarps);
     }
     mbar_init(b_full, 1);
     mbar_init(b_empty, 1);
@@ -228,8 +232,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else {
-    // ---------------- epilogue: warps 2..5, TMEM lanes 32 * (warp % 4) ..
-    const uint32_t lg = warp & 3;
+    // ---------------- epilogue: warps 2.., TMEM lanes 32 * (warp % 4) ..,
+    // queries kQPW * ((warp - 2) / 4) .. + kQPW - 1
+    const uint32_t lg = warp & 3, q0 = C::kQPW * ((warp - 2) >> 2);
     const uint32_t row = lg * 32 + lane;
     float *sw = sw_all + (warp - 2) * QG * kHeads;   // this warp's copy of the weights
     const uint32_t et = threadIdx.x - 64;             // 0..127
@@ -277,7 +282,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const uint32_t grow = tile * kRows + row;
 #pragma unroll 1
-      for (int q = 0; q < QG; ++q) {
+      for (int q = (int)q0; q < (int)q0 + C::kQPW; ++q) {
         uint32_t r0[32], r1[32];
         const uint32_t taddr = tmem + ((lg * 32) << 16) + acc * C::N + q * kHeads;
         tmem_ld32(taddr, r0);
@@ -304,12 +309,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t t = g * QG + q;
         const bool valid = t < P.T && grow < vis_of(P, t);
         if (valid) P.scores[((size_t)b * P.T + t) * P.comp_cap + grow] = s;
-        if (QG == 1) {
-          // histogram of the keys' top 12 bits (lanes in one bin add once)
-          const uint32_t bin = valid ? score_key_tc(s) >> 20 : 4096u;
-          const uint32_t peers = __match_any_sync(0xffffffffu, bin);
-          if (bin < 4096u && lane == (uint32_t)(__ffs(peers) - 1))
+        // histogram of the keys' top 12 bits (lanes in one bin add once): per
+        // CTA in shared memory for one query, else straight to the query's
+        // histogram in global memory
+        const uint32_t bin = valid ? score_key_tc(s) >> 20 : 4096u;
+        const uint32_t peers = __match_any_sync(0xffffffffu, bin);
+        if (bin < 4096u && lane == (uint32_t)(__ffs(peers) - 1)) {
+          if (QG == 1)
             atomicAdd(&shist[bin], (uint32_t)__popc(peers));
+          else
+            atomicAdd(&P.hist[((size_t)b * P.T + t) * 4096 + bin], (uint32_t)__popc(peers));
         }
       }
       tc_fence_before();
@@ -359,7 +368,7 @@ cudaError_t launch_qg(const IndexTcArgs &a, cudaStream_t s) {
   e = ensure_smem(index_score_tc_kernel<QG>, C::kSmem, &smem_set);
   if (e != cudaSuccess) return e;
   const uint32_t grid = min(P.total_items, (uint32_t)num_sms());
-  e = launch_pdl(index_score_tc_kernel<QG>, dim3(grid), dim3(kThreads), C::kSmem, s, tk, tq, P);
+  e = launch_pdl(index_score_tc_kernel<QG>, dim3(grid), dim3(C::kThreads), C::kSmem, s, tk, tq, P);
   if (e != cudaSuccess) return e;
   note_launches(1);
   return cudaGetLastError();
