@@ -707,9 +707,17 @@ __global__ void __launch_bounds__(NT, NT == 256 ? 4 : 1)
       for (uint32_t j = threadIdx.x; j < k; j += blockDim.x) out[j] = -1;
     return;
   }
-  // theta_S: lower edge of the histogram bin holding the k-th largest S~
-  if (threadIdx.x == 0) s_misc[2] = 0;   // candidate count (one block per query)
-  {
+  // theta_S: at least k rows have S~ >= theta_S. Several blocks per query:
+  // the lower edge of the scorer's histogram bin holding the k-th largest.
+  // One block per query: a value of an evenly strided sample of the scores at
+  // a rank that leaves ~1.25 k rows above it; the filter below counts the rows
+  // at or above it exactly, and too few sends the block to the full pass.
+  if (threadIdx.x == 0) {
+    s_misc[2] = 0;   // candidate count (one block per query)
+    s_misc[3] = 0;   // rows with S~ >= theta_S (one block per query)
+  }
+  float theta_s;
+  if (G > 1) {
     const uint32_t *hq = w.hist + (size_t)qi * kHistBins;
     uint32_t cb4[SC::BPT], loc = 0;
 #pragma unroll
@@ -730,6 +738,19 @@ __global__ void __launch_bounds__(NT, NT == 256 ? 4 : 1)
         cum += cb4[j];
       }
     }
+    __syncthreads();
+    theta_s = key_to_float(s_misc[0] << 20);
+  } else {
+    constexpr uint32_t kSampleCap = (uint32_t)(SC::kScratch / 4);
+    const uint32_t stride = max(16u, (vis + kSampleCap - 1) / kSampleCap);
+    const uint32_t ns = vis / stride;   // >= 32: vis > k >= 512
+    float *smp = scratch;
+    for (uint32_t j = threadIdx.x; j < ns; j += blockDim.x) smp[j] = sc[j * stride + stride / 2];
+    __syncthreads();   // (also syncs s_red / wsh / qsm)
+    const uint32_t rs = min(ns, ((k + stride - 1) / stride) * 5 / 4 + 4);
+    uint32_t need_s;
+    theta_s = key_to_float(radix_kth([&](uint32_t j) { return score_key(smp[j]); }, ns, rs,
+                                     hist, sel, &need_s));
   }
   __syncthreads();
   float At = 0.f, Wt = 0.f;
@@ -743,7 +764,6 @@ __global__ void __launch_bounds__(NT, NT == 256 ? 4 : 1)
   // computations, for 4 Di operations per head dot and 4 Hi per score
   const float eta = (4.0f * (float)Di * Wt * (1.0f + 1e-5f) + 4.0f * (float)Hi) * 0x1p-126f;
   const float E = A * __uint_as_float(a.norm_max[b]) + eta;
-  const float theta_s = key_to_float(s_misc[0] << 20);
   const int eq_min = s_qexp[0], eq_max = s_qexp[1];
   const float theta = theta_s - E - fabsf(theta_s) * (2.0f * kRel);
   auto err_of = [&](float S, float nm) { return A * nm + fabsf(S) * kRel + eta; };
@@ -760,6 +780,10 @@ __global__ void __launch_bounds__(NT, NT == 256 ? 4 : 1)
       const float S = ok ? sc[r] : 0.f;
       const float e = ok ? err_of(S, nr[r]) : 0.f;
       const bool c = ok && S + e >= theta;
+      if (G == 1) {
+        const uint32_t ge = __ballot_sync(0xffffffffu, ok && S >= theta_s);
+        if (lane == 0 && ge) atomicAdd(&s_misc[3], (uint32_t)__popc(ge));
+      }
       const uint32_t bal = __ballot_sync(0xffffffffu, c);
       if (bal) {
         uint32_t slot = 0;
@@ -797,7 +821,7 @@ __global__ void __launch_bounds__(NT, NT == 256 ? 4 : 1)
   const __nv_bfloat16 *keys = static_cast<const __nv_bfloat16 *>(a.keys) + (size_t)b * a.comp_cap * Di;
   float *kb = kbuf + warp * 128, *rel = relb + warp * 64;
   const uint32_t nc = G == 1 ? s_misc[2] : *(volatile uint32_t *)&ctrl[0];
-  const bool fast = nc <= CAP && (G == 1 || *(volatile uint32_t *)&ctrl[2] == 0u);
+  const bool fast = nc <= CAP && (G == 1 ? s_misc[3] >= k : *(volatile uint32_t *)&ctrl[2] == 0u);
   uint32_t need;
   if (fast) {
     // ---- certified selection on the candidates
@@ -818,6 +842,37 @@ __global__ void __launch_bounds__(NT, NT == 256 ? 4 : 1)
     }
     const uint32_t words = (vis + 31) / 32;
     for (uint32_t i = threadIdx.x; i < words; i += blockDim.x) bitmap[i] = 0u;
+    if (G == 1) {
+      // every row with S~ >= theta_S (at least k) is a candidate, so the k-th
+      // largest S~ is the candidates' k-th: its 12-bit key bin b* and the
+      // count above it from a histogram of the candidates
+      uint32_t *h1 = reinterpret_cast<uint32_t *>(scratch);   // [4096]
+      for (uint32_t i = threadIdx.x; i < kHistBins; i += blockDim.x) h1[i] = 0u;
+      __syncthreads();
+      for (uint32_t j = threadIdx.x; j < nc; j += blockDim.x)
+        atomicAdd(&h1[score_key(cS[j]) >> 20], 1u);
+      __syncthreads();
+      uint32_t cb4[SC::BPT], loc = 0;
+#pragma unroll
+      for (uint32_t j = 0; j < (uint32_t)SC::BPT; ++j) {
+        cb4[j] = h1[kHistBins - 1 - (SC::BPT * threadIdx.x + j)];
+        loc += cb4[j];
+      }
+      uint32_t tot;
+      uint32_t cum = block_excl_scan(loc, wsum, &tot);
+      if (cum < k && cum + loc >= k) {
+#pragma unroll
+        for (uint32_t j = 0; j < (uint32_t)SC::BPT; ++j) {
+          if (cum + cb4[j] >= k) {
+            s_misc[0] = kHistBins - 1 - (SC::BPT * threadIdx.x + j);
+            s_misc[4] = cum;
+            break;
+          }
+          cum += cb4[j];
+        }
+      }
+      __syncthreads();
+    }
     // the k-th largest S~ lies in 12-bit key bin b* with `above` keys over it;
     // a histogram of the next 12 key bits of the candidates in b* narrows it
     // to one 24-bit key interval [t_lo, t_hi] (every row of b* is a candidate)
@@ -1019,7 +1074,9 @@ cudaError_t launch_index_tc(const IndexArgs &a, cudaStream_t s) {
   const uint32_t nq = a.batch * a.T;
   TcWs w = tc_ws_split(a.ws, nq, a.batch, a.n_heads, a.dim, a.comp_cap, nullptr);
   const size_t npair = (size_t)nq * a.n_heads * a.dim / 2;
-  const bool scorer_hist = true;   // the scorer builds the key histograms
+  // the scorer builds key histograms when several select blocks share a
+  // query; with one block per query the selection samples its threshold
+  const bool scorer_hist = select_groups(nq) > 1;
   size_t nthreads = npair;
   if (scorer_hist && (size_t)nq * kHistBins > nthreads) nthreads = (size_t)nq * kHistBins;
   if ((size_t)nq * 4 > nthreads) nthreads = (size_t)nq * 4;
@@ -1039,7 +1096,7 @@ cudaError_t launch_index_tc(const IndexArgs &a, cudaStream_t s) {
     t.qbf = w.qbf;
     t.w = a.w;
     t.scores = w.scores;
-    t.hist = w.hist;
+    t.hist = scorer_hist ? w.hist : nullptr;
     t.err = w.err;
     cudaError_t e = launch_index_score_tc(t, s);
     if (e != cudaSuccess) return e;

@@ -248,7 +248,7 @@ __global__ void __launch_bounds__(Cfg<QG>::kThreads, 1)
       for (uint32_t i = et; i < 4096; i += 128) {
         const uint32_t c = shist[i];
         if (c) {
-          if (q >= 0) atomicAdd(&P.hist[(size_t)q * 4096 + i], c);
+          if (q >= 0 && P.hist) atomicAdd(&P.hist[(size_t)q * 4096 + i], c);
           shist[i] = 0;
         }
       }
@@ -309,16 +309,13 @@ __global__ void __launch_bounds__(Cfg<QG>::kThreads, 1)
         const uint32_t t = g * QG + q;
         const bool valid = t < P.T && grow < vis_of(P, t);
         if (valid) P.scores[((size_t)b * P.T + t) * P.comp_cap + grow] = s;
-        // histogram of the keys' top 12 bits (lanes in one bin add once): per
-        // CTA in shared memory for one query, else straight to the query's
-        // histogram in global memory
-        const uint32_t bin = valid ? score_key_tc(s) >> 20 : 4096u;
-        const uint32_t peers = __match_any_sync(0xffffffffu, bin);
-        if (bin < 4096u && lane == (uint32_t)(__ffs(peers) - 1)) {
-          if (QG == 1)
+        // histogram of the keys' top 12 bits (lanes in one bin add once), per
+        // CTA in shared memory, added to the query's when the query changes
+        if (QG == 1) {   // (the selection samples its threshold otherwise)
+          const uint32_t bin = valid ? score_key_tc(s) >> 20 : 4096u;
+          const uint32_t peers = __match_any_sync(0xffffffffu, bin);
+          if (bin < 4096u && lane == (uint32_t)(__ffs(peers) - 1))
             atomicAdd(&shist[bin], (uint32_t)__popc(peers));
-          else
-            atomicAdd(&P.hist[((size_t)b * P.T + t) * 4096 + bin], (uint32_t)__popc(peers));
         }
       }
       tc_fence_before();
