@@ -65,7 +65,7 @@ struct Smem {
   uint8_t q[8 * kQBlk];     // 64 KiB
   uint8_t kv[8 * kKBlk];    // 128 KiB; decode merge: afterwards the pulled slices (with p)
   uint8_t p[kRows * 128];   // 16 KiB; direct output: afterwards staging, [64 heads][128] bf16
-  uint64_t kv_full[8], kv_empty[8];
+  uint64_t kv_full, kv_empty[4];   // kv_full: the whole tile landed; kv_empty[m]: blocks 2m, 2m+1 free
   uint64_t q_full, q_empty, s_full, p_full, p_empty, o_full, o_empty, sm_bar, ld_bar;
   float mref[kH], alpha[kH], lsh[kH], linv[kH];
   float tmax[4][kH];
@@ -245,10 +245,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(TcAttnParams P) {
   const uint32_t q_step = dec ? P.n_q : gridDim.x;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < 8; ++i) {
-      mbar_init(&S.kv_full[i], 128);
-      mbar_init(&S.kv_empty[i], 1);
-    }
+    mbar_init(&S.kv_full, 128);
+    for (int i = 0; i < 4; ++i) mbar_init(&S.kv_empty[i], 1);
     mbar_init(&S.q_full, 128);
     mbar_init(&S.q_empty, 1);
     mbar_init(&S.s_full, 1);
@@ -297,7 +295,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(TcAttnParams P) {
         src[i] = row_src(P, g, tile * kRows + lw * 32 + (lane >> 3) + 4 * i);
       const uint32_t cc = lane & 7;
       for (uint32_t kb = 0; kb < 8; ++kb) {
-        if (!mbar_wait_warp(&S.kv_empty[kb], (n & 1) ^ 1, ew)) return false;
+        if ((kb & 1) == 0 && !mbar_wait_warp(&S.kv_empty[kb >> 1], (n & 1) ^ 1, ew)) return false;
         uint8_t *slot = S.kv + kb * kKBlk;
 #pragma unroll
         for (uint32_t i = 0; i < 8; ++i) {
@@ -369,19 +367,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(TcAttnParams P) {
         mbar_arrive(&S.q_full);
         for (uint32_t tile = g.t0; tile < g.t1; tile += g.ts, ++n) {
           if (tile != g.t0 && !issue_tile(g, tile, n)) goto done_loader;
-#define DS4A_KV_LANDED(NPEND, KB)                                   \
-  asm volatile("cp.async.wait_group " #NPEND ";" ::: "memory");     \
-  fence_proxy_async();                                              \
-  mbar_arrive(&S.kv_full[KB]);
-          DS4A_KV_LANDED(7, 0)
-          DS4A_KV_LANDED(6, 1)
-          DS4A_KV_LANDED(5, 2)
-          DS4A_KV_LANDED(4, 3)
-          DS4A_KV_LANDED(3, 4)
-          DS4A_KV_LANDED(2, 5)
-          DS4A_KV_LANDED(1, 6)
-          DS4A_KV_LANDED(0, 7)
-#undef DS4A_KV_LANDED
+          // one arrival per thread once all its rows of the tile landed: the
+          // MMA issuer takes the tile whole (waits between the MMAs of one
+          // accumulation halve their rate)
+          cp_async_wait_all();
+          fence_proxy_async();
+          mbar_arrive(&S.kv_full);
         }
       }
       ++qn;
@@ -403,16 +394,14 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(TcAttnParams P) {
         ok = mbar_wait(&S.q_full, qn & 1, ew);
         for (uint32_t tile = g.t0; ok && tile < g.t1; tile += g.ts, ++n) {
           const bool first = tile == g.t0, last = tile + g.ts >= g.t1;
-          for (uint32_t kb = 0; kb < 8 && ok; ++kb) {
-            ok = mbar_wait(&S.kv_full[kb], n & 1, ew);
-            if (!ok) break;
-            tc_fence_after();
+          ok = mbar_wait(&S.kv_full, n & 1, ew);
+          if (!ok) break;
+          tc_fence_after();
+          for (uint32_t kb = 0; kb < 8; ++kb)
 #pragma unroll
             for (uint32_t kk = 0; kk < 4; ++kk)
               mma_bf16(tmS, sdesc_sw128(kv_base + kb * kKBlk + kk * 32),
                        sdesc_sw128(q_base + kb * kQBlk + kk * 32), idS, (kb | kk) ? 1u : 0u);
-          }
-          if (!ok) break;
           mma_commit(&S.s_full);
           if (last) mma_commit(&S.q_empty);
           ok = mbar_wait(&S.p_full, n & 1, ew);
@@ -427,8 +416,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(TcAttnParams P) {
               const uint64_t bd = sdesc_sw128_mn(p_base + kk * 2048, 8192, 1024);
               mma_bf16(tmO + m * kH, ad, bd, idPV, (first && kk == 0) ? 0u : 1u);
             }
-            mma_commit(&S.kv_empty[2 * m]);
-            mma_commit(&S.kv_empty[2 * m + 1]);
+            mma_commit(&S.kv_empty[m]);
           }
           // per-head row sums of P on the tensor core: every row of L = 1^T P^T
           constexpr uint32_t idL = idesc_bf16_f32(kRows, kH) | kIdescMajorB_MN;
