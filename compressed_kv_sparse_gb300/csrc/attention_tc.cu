@@ -66,7 +66,8 @@ struct Smem {
   uint8_t kv[8 * kKBlk];    // 128 KiB; decode merge: afterwards the pulled slices (with p)
   uint8_t p[kRows * 128];   // 16 KiB; direct output: afterwards staging, [64 heads][128] bf16
   uint64_t kv_full, kv_empty[4];   // kv_full: the whole tile landed; kv_empty[m]: blocks 2m, 2m+1 free
-  uint64_t q_full, q_empty, s_full, p_full, p_empty, o_full, o_empty, sm_bar, ld_bar;
+  uint64_t q_full, q_empty, s_full, p_full, p_empty, o_full, o_empty, sm_bar;
+  uint64_t q_tma;   // the query's eight Q blocks landed (TMA transaction count)
   float mref[kH], alpha[kH], lsh[kH], linv[kH];
   float tmax[4][kH];
   float mw[kH][kMaxCluster];        // decode merge: weight of each rank, per owned head
@@ -231,7 +232,8 @@ __device__ __forceinline__ void merge_heads(const TcAttnParams &P, Smem &S, uint
   }
 }
 
-__global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(TcAttnParams P) {
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, TcAttnParams P) {
   extern __shared__ uint8_t smem_raw[];
   Smem &S = *reinterpret_cast<Smem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                       ~(uintptr_t)1023);
@@ -255,9 +257,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(TcAttnParams P) {
     mbar_init(&S.o_full, 1);
     mbar_init(&S.o_empty, 4);
     mbar_init(&S.sm_bar, 128);
-    mbar_init(&S.ld_bar, 128);
+    mbar_init(&S.q_tma, 1);
     S.flagcnt[0] = S.flagcnt[1] = S.flagcnt[2] = 0;
     fence_mbar_init();
+    prefetch_tmap(&tmap_q);
   }
   if (warp == 8) tmem_alloc(&S.tmem, 512);
   tc_fence_before();
@@ -285,7 +288,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(TcAttnParams P) {
   if (warp >= 4 && warp < 8) {
     // ------------------------------------------------------------ loaders
     const uint32_t lt = threadIdx.x - 128, lw = warp - 4;
-    uint32_t n = 0, qn = 0, ld_phase = 0;
+    uint32_t n = 0, qn = 0, qt = 0;   // qt: Q loads issued (q_tma phases)
     // issue all eight 64-dim blocks of a tile (one cp.async group each) as
     // their slots free up; rows of this lane: lw*32 + lane/8 + 4i, chunk lane%8
     auto issue_tile = [&](const QueryGeo &g, uint32_t tile, uint32_t n) -> bool {
@@ -311,25 +314,20 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(TcAttnParams P) {
     for (uint32_t qi = q_first; qi < P.n_q; qi += q_step) {
       if (rank * kRows >= rows_bound(P, qi)) continue;   // no rows for this rank
       if (!mbar_wait_warp(&S.q_empty, (qn & 1) ^ 1, ew)) goto done_loader;
-      {
-        // Q first (it needs no list): warp lw loads heads 16 lw .. 16 lw + 15
-        const __nv_bfloat16 *q = P.q + (size_t)qi * kH * kD;
-        for (uint32_t hh = 0; hh < 16; ++hh) {
-          const uint32_t h = lw * 16 + hh;
+      // Q first (it needs no list): eight TMA boxes of 64 heads x 64 dims, in
+      // the 128-byte swizzled K-major layout the S MMAs read
+      if (lt == 0) {
+        mbar_arrive_expect_tx(&S.q_tma, 8 * kQBlk);
 #pragma unroll
-          for (uint32_t half = 0; half < 2; ++half) {
-            const uint32_t ch = lane + 32 * half;           // 16-byte chunk 0..63 of the row
-            const uint32_t kb = ch >> 3, c = ch & 7;
-            uint8_t *dst = S.q + kb * kQBlk + h * 128 + ((c ^ (h & 7)) << 4);
-            cp_async16(dst, q + (size_t)h * kD + ch * 8, 16);
-          }
-        }
-        asm volatile("cp.async.commit_group;" ::: "memory");
+        for (uint32_t kb = 0; kb < 8; ++kb)
+          tma_load_2d(S.q + kb * kQBlk, &tmap_q, &S.q_tma, (int)(64 * kb), (int)(qi * kH));
       }
       {
         const QueryGeo g = query_geo(P, qi, rank, C, lane);
         if (g.t0 >= g.t1) {          // the list is shorter than the bound: nothing to do
-          cp_async_wait_all();
+          // (Q still lands: wait for it so the buffer is never written twice at once)
+          if (!mbar_wait_warp(&S.q_tma, qt & 1, ew)) goto done_loader;
+          ++qt;
           continue;
         }
         // the first tile's rows start loading before Q is rotated
@@ -346,8 +344,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(TcAttnParams P) {
             si[4 * i + e] = P.sin[(size_t)g.p * 32 + 4 * lc + e];
           }
         }
-        asm volatile("cp.async.wait_group 8;" ::: "memory");   // Q landed
-        if (!group_sync(&S.ld_bar, ld_phase, ew)) goto done_loader;
+        if (!mbar_wait_warp(&S.q_tma, qt & 1, ew)) goto done_loader;   // Q landed
+        ++qt;
         // rotate the tail (dims 448..511 = block 7) at position p, in place
 #pragma unroll
         for (uint32_t i = 0; i < 4; ++i) {
@@ -752,6 +750,13 @@ cudaError_t launch_attention_tc(const AttnArgs &a, uint32_t rows_max, int *err, 
   static int smem_set = 0;
   cudaError_t e = ensure_smem(attn_tc_kernel, smem, &smem_set);
   if (e != cudaSuccess) return e;
+  // Q as [n_q * 64 heads][512] bf16 rows; boxes of 64 heads x 64 dims
+  CUtensorMap tq;
+  const uint64_t qd[2] = {(uint64_t)kD, (uint64_t)P.n_q * kH};
+  const uint64_t qs[1] = {(uint64_t)kD * 2};
+  const uint32_t qb[2] = {64, (uint32_t)kH};
+  e = make_tmap_bf16(&tq, a.q, 2, qd, qs, qb);
+  if (e != cudaSuccess) return e;
   if (a.T == 1) {
     const uint32_t n_tiles = (rows_max + kRows - 1) / kRows;
     P.cluster = pick_cluster(n_tiles, P.n_q, smem);
@@ -769,13 +774,13 @@ cudaError_t launch_attention_tc(const AttnArgs &a, uint32_t rows_max, int *err, 
     at[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = at;
     cfg.numAttrs = 2;
-    e = cudaLaunchKernelEx(&cfg, attn_tc_kernel, P);
+    e = cudaLaunchKernelEx(&cfg, attn_tc_kernel, tq, P);
     note_launches(1);
     return e != cudaSuccess ? e : cudaGetLastError();
   }
   P.cluster = 0;
   const uint32_t grid = min(P.n_q, (uint32_t)num_sms());
-  e = launch_pdl(attn_tc_kernel, dim3(grid), dim3(kThreads), smem, s, P);
+  e = launch_pdl(attn_tc_kernel, dim3(grid), dim3(kThreads), smem, s, tq, P);
   note_launches(1);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
