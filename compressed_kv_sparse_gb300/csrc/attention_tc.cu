@@ -45,7 +45,6 @@ constexpr int kQBlk = kH * 128;        // one 64-dim block of Q: 64 heads x 128 
 constexpr int kKBlk = kRows * 128;     // one 64-dim block of the row tile
 constexpr int kThreads = 288;
 constexpr uint32_t kMaxCluster = 8;    // portable cluster size
-constexpr uint32_t kNoRow = 0x7fffffffu;
 constexpr float kRaiseLog2 = 8.0f;     // raise the running max beyond 2^8
 
 struct TcAttnParams {
@@ -68,10 +67,11 @@ struct Smem {
   uint64_t kv_full, kv_empty[4];   // kv_full: the whole tile landed; kv_empty[m]: blocks 2m, 2m+1 free
   uint64_t q_full, q_empty, s_full, p_full, p_empty, o_full, o_empty, sm_bar;
   uint64_t q_tma;   // the query's eight Q blocks landed (TMA transaction count)
+  uint64_t mg_bar;  // decode merge: the peers' partial O slices landed
   float mref[kH], alpha[kH], lsh[kH], linv[kH];
   float tmax[4][kH];
   float mw[kH][kMaxCluster];        // decode merge: weight of each rank, per owned head
-  uint32_t first_row, flagcnt[3], tmem, has_tiles;
+  uint32_t flagcnt[3], tmem, has_tiles;
 };
 // the merge pulls at most C * ceil(64 / C) rows of 2 KiB (140 KiB at C = 7)
 static_assert(8 * kKBlk + kRows * 128 >= 7 * 10 * kD * 4, "pulled slices fit kv + p");
@@ -162,19 +162,21 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 // row-tile buffer as [j][i][512] fp32 and are combined in rank order with
 // weights 2^(m_j - M) / sum_j 2^(m_j - M) l_j. A rank without rows left
 // m = -inf and zeros; one with only masked rows left m = -inf and O = 0.
-__device__ __forceinline__ void merge_heads(const TcAttnParams &P, Smem &S, uint32_t qi,
-                                            uint32_t rank, uint32_t C) {
+__device__ __forceinline__ bool merge_heads(const TcAttnParams &P, Smem &S, uint32_t qi,
+                                            uint32_t rank, uint32_t C, ErrWord ew) {
   const uint32_t t = threadIdx.x;
   const uint32_t h0 = rank * kH / C, h1 = (rank + 1) * kH / C, nh = h1 - h0;
   const float *part = P.part + (size_t)qi * C * kH * kD;
   const float *ml = P.part + (size_t)P.n_q * C * kH * kD + (size_t)qi * C * kH * 2;
   float *recv = reinterpret_cast<float *>(S.kv);
-  const uint32_t n_chunks = C * nh * (kD / 4);
-  for (uint32_t c = t; c < n_chunks; c += 256) {
-    const uint32_t row = c >> 7, ch = c & 127, j = row / nh, i = row - j * nh;
-    cp_async16(recv + row * kD + ch * 4, part + ((size_t)j * kH + h0 + i) * kD + ch * 4, 16);
+  // rank j's rows h0 .. h1 - 1 are contiguous: one bulk copy per rank
+  if (t == 0) {
+    fence_proxy_async_global();
+    mbar_arrive_expect_tx(&S.mg_bar, C * nh * kD * 4);
+    for (uint32_t j = 0; j < C; ++j)
+      bulk_load(recv + (size_t)j * nh * kD, part + ((size_t)j * kH + h0) * kD, nh * kD * 4,
+                &S.mg_bar);
   }
-  asm volatile("cp.async.commit_group;" ::: "memory");
   if (t < nh) {
     const uint32_t h = h0 + t;
     float m[kMaxCluster], l[kMaxCluster], M = -INFINITY;
@@ -194,8 +196,9 @@ __device__ __forceinline__ void merge_heads(const TcAttnParams &P, Smem &S, uint
     }
     S.linv[t] = L > 0.f ? 1.f / L : 0.f;
   }
-  cp_async_wait_all();
+  const bool ok = mbar_wait(&S.mg_bar, 0, ew);
   named_bar_sync(1, 256);
+  if (!ok) return false;
   const uint32_t p = P.pos0 + qi % P.T, c = t & 127, d = 4 * c;
   float co0 = 1.f, si0 = 0.f, co1 = 1.f, si1 = 0.f;
   if (d >= (uint32_t)kNope) {
@@ -230,6 +233,7 @@ __device__ __forceinline__ void merge_heads(const TcAttnParams &P, Smem &S, uint
     *reinterpret_cast<uint2 *>(P.out + ((size_t)qi * kH + h0 + i) * kD + d) =
         make_uint2(pack_bf16(r0, r1), pack_bf16(r2, r3));
   }
+  return true;
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -245,6 +249,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t rank = dec ? cluster_ctarank() : 0u;
   const uint32_t q_first = dec ? blockIdx.x / C : blockIdx.x;
   const uint32_t q_step = dec ? P.n_q : gridDim.x;
+  const int err_base = *(volatile int *)P.err;
 
   if (threadIdx.x == 0) {
     mbar_init(&S.kv_full, 128);
@@ -258,6 +263,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&S.o_empty, 4);
     mbar_init(&S.sm_bar, 128);
     mbar_init(&S.q_tma, 1);
+    mbar_init(&S.mg_bar, 1);
     S.flagcnt[0] = S.flagcnt[1] = S.flagcnt[2] = 0;
     fence_mbar_init();
     prefetch_tmap(&tmap_q);
@@ -282,8 +288,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   pdl_wait();
   pdl_trigger();
-  // this launch's view of the error word (see ErrWord)
-  const ErrWord ew{P.err, *(volatile int *)P.err};
+  // this launch's view of the error word (see ErrWord), read before the wait
+  // so that its latency overlaps the previous launch
+  const ErrWord ew{P.err, err_base};
 
   if (warp >= 4 && warp < 8) {
     // ------------------------------------------------------------ loaders
@@ -476,28 +483,32 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!mbar_wait_warp(&S.s_full, n & 1, ew)) goto done_softmax;
         tc_fence_after();
         if (first) {
-          // running maxima start at the scores of the first valid row
-          if (r == 0) S.first_row = kNoRow;
-          if (!group_sync(&S.sm_bar, sm_phase, ew)) goto done_softmax;
-          if (valid) atomicMin(&S.first_row, r);
-          if (!group_sync(&S.sm_bar, sm_phase, ew)) goto done_softmax;
-          const uint32_t fr = S.first_row;
-          // (tcgen05.ld is warp-collective: every lane loads, one lane keeps)
+          // running maxima start at the exact per-head maxima of the first
+          // tile's scaled scores (so its P never needs a raise): warp maxima
+          // of order-keyed values, then the largest of the four warps
+          uint32_t *tkey = reinterpret_cast<uint32_t *>(&S.tmax[0][0]);   // [4][kH]
 #pragma unroll 1
           for (uint32_t hf = 0; hf < 2; ++hf) {
             uint32_t a[32];
             tmem_ld32(tmS + lane_base + 32 * hf, a);
             tmem_ld_wait();
-            if (fr == r) {
 #pragma unroll
-              for (int h = 0; h < 32; ++h) S.mref[32 * hf + h] = __uint_as_float(a[h]) * P.c2;
+            for (int h = 0; h < 32; ++h) {
+              const uint32_t u = __float_as_uint(__uint_as_float(a[h]) * P.c2);
+              const uint32_t key = valid ? ((u & 0x80000000u) ? ~u : (u | 0x80000000u)) : 0u;
+              const uint32_t mk = redux_max_u32(key);
+              if (lane == (uint32_t)h) tkey[warp * kH + 32 * hf + h] = mk;
             }
           }
-          if (fr == kNoRow && r == 0) {
-#pragma unroll
-            for (int h = 0; h < kH; ++h) S.mref[h] = 0.f;
+          if (!group_sync(&S.sm_bar, sm_phase, ew)) goto done_softmax;
+          const uint32_t k0 = max(max(tkey[0 * kH], tkey[1 * kH]), max(tkey[2 * kH], tkey[3 * kH]));
+          any_valid = k0 != 0u;   // a valid row has a key above 0 for every head
+          if (r < kH) {
+            const uint32_t mk = max(max(tkey[0 * kH + r], tkey[1 * kH + r]),
+                                    max(tkey[2 * kH + r], tkey[3 * kH + r]));
+            const float mx = __uint_as_float((mk & 0x80000000u) ? (mk & 0x7fffffffu) : ~mk);
+            S.mref[r] = any_valid ? mx : 0.f;
           }
-          any_valid = fr != kNoRow;
           if (!group_sync(&S.sm_bar, sm_phase, ew)) goto done_softmax;
         }
         // P of this tile (the previous PV must be done with the buffer)
@@ -633,24 +644,39 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (dec && C > 1 && warp < 8) {
-    // this rank's unnormalised O: warp w reads TMEM lanes 32 (w % 4) .. + 31
-    // (dims) for heads 32 (w / 4) .. + 31; a warp stores 128 contiguous bytes
-    const uint32_t qw = warp & 3, hf = warp >> 2, dl = 32 * qw + lane;
-    float *dst = P.part + ((size_t)q_first * C + rank) * kH * kD + (size_t)(32 * hf) * kD;
-    const bool had = S.has_tiles != 0;
+  if (dec && C > 1) {
+    // this rank's unnormalised O as [64 heads][512] fp32 in the row buffer
+    // (free: the last PV is done), then one bulk store to the workspace. Warp
+    // w reads TMEM lanes 32 (w % 4) .. + 31 (dims) for heads 32 (w / 4) .. + 31
+    float *stg = reinterpret_cast<float *>(S.kv);
+    if (warp < 8) {
+      const uint32_t qw = warp & 3, hf = warp >> 2, dl = 32 * qw + lane;
+      const bool had = S.has_tiles != 0;
 #pragma unroll 1
-    for (uint32_t m = 0; m < 4; ++m) {
-      uint32_t a[32];
-      if (had) {
-        tmem_ld32(tmO + ((32 * qw) << 16) + m * kH + 32 * hf, a);
-        tmem_ld_wait();
-      } else {
+      for (uint32_t m = 0; m < 4; ++m) {
+        uint32_t a[32];
+        if (had) {
+          tmem_ld32(tmO + ((32 * qw) << 16) + m * kH + 32 * hf, a);
+          tmem_ld_wait();
+        } else {
 #pragma unroll
-        for (int h = 0; h < 32; ++h) a[h] = 0u;
+          for (int h = 0; h < 32; ++h) a[h] = 0u;
+        }
+#pragma unroll
+        for (int h = 0; h < 32; ++h)
+          stg[(size_t)(32 * hf + h) * kD + m * 128 + dl] = __uint_as_float(a[h]);
       }
-#pragma unroll
-      for (int h = 0; h < 32; ++h) dst[(size_t)h * kD + m * 128 + dl] = __uint_as_float(a[h]);
+    }
+    fence_proxy_async();
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      float *dst = P.part + ((size_t)q_first * C + rank) * kH * kD;
+#pragma unroll 1
+      for (uint32_t i = 0; i < 8; ++i)   // 8 heads (16 KiB) per copy
+        bulk_store(dst + (size_t)i * 8 * kD, stg + (size_t)i * 8 * kD, 8 * kD * 4);
+      bulk_commit();
+      bulk_wait_all();
+      fence_proxy_async_global();
     }
   }
   tc_fence_before();
@@ -658,7 +684,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 8) tmem_dealloc(tmem, 512);
   if (dec && C > 1) {
     cluster_sync_all();   // every rank's O and (max, sum) are in the workspace
-    if (warp < 8) merge_heads(P, S, q_first, rank, C);
+    if (warp < 8) merge_heads(P, S, q_first, rank, C, ew);
   }
 }
 

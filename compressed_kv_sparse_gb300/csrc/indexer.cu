@@ -702,11 +702,8 @@ __global__ void __launch_bounds__(NT, NT == 256 ? 4 : 1)
   // (q', head weights, row norms); the scores and histograms need the scorer
   pdl_wait();
   pdl_trigger();
-  if (*(volatile int *)w.err) {   // the scorer gave up: no list
-    if (g == 0)
-      for (uint32_t j = threadIdx.x; j < k; j += blockDim.x) out[j] = -1;
-    return;
-  }
+  // did the scorer give up? (tested once the threshold's loads are in flight)
+  const int scorer_err = *(volatile int *)w.err;
   // theta_S: at least k rows have S~ >= theta_S. Several blocks per query:
   // the lower edge of the scorer's histogram bin holding the k-th largest.
   // One block per query: a value of an evenly strided sample of the scores at
@@ -751,6 +748,11 @@ __global__ void __launch_bounds__(NT, NT == 256 ? 4 : 1)
     uint32_t need_s;
     theta_s = key_to_float(radix_kth([&](uint32_t j) { return score_key(smp[j]); }, ns, rs,
                                      hist, sel, &need_s));
+  }
+  if (scorer_err) {   // no scores: no list
+    if (g == 0)
+      for (uint32_t j = threadIdx.x; j < k; j += blockDim.x) out[j] = -1;
+    return;
   }
   __syncthreads();
   float At = 0.f, Wt = 0.f;
