@@ -56,7 +56,10 @@ struct TcAttnParams {
   const int32_t *topk;
   const float *cos, *sin;
   __nv_bfloat16 *out;
-  float *part;        // decode, C > 1: [n_q][C][64][512] O, then [n_q][C][64] (max, sum)
+  // decode, C > 1: each rank's O / L as [n_q][C][64][512] bf16, and its
+  // (max, sum) per head as [n_q][C][64][2] fp32
+  __nv_bfloat16 *part;
+  float *ml;
   int *err;
 };
 
@@ -73,8 +76,8 @@ struct Smem {
   float mw[kH][kMaxCluster];        // decode merge: weight of each rank, per owned head
   uint32_t flagcnt[3], tmem, has_tiles;
 };
-// the merge pulls at most C * ceil(64 / C) rows of 2 KiB (140 KiB at C = 7)
-static_assert(8 * kKBlk + kRows * 128 >= 7 * 10 * kD * 4, "pulled slices fit kv + p");
+// the merge pulls at most C * ceil(64 / C) rows of 1 KiB (70 KiB at C = 7)
+static_assert(8 * kKBlk >= 7 * 10 * kD * 2, "pulled slices fit the row buffer");
 static_assert(2 * kH * 128 == kRows * 128, "output staging fills the P buffer");
 
 // Rows that a query can have at most, without reading its top-k list.
@@ -166,15 +169,15 @@ __device__ __forceinline__ bool merge_heads(const TcAttnParams &P, Smem &S, uint
                                             uint32_t rank, uint32_t C, ErrWord ew) {
   const uint32_t t = threadIdx.x;
   const uint32_t h0 = rank * kH / C, h1 = (rank + 1) * kH / C, nh = h1 - h0;
-  const float *part = P.part + (size_t)qi * C * kH * kD;
-  const float *ml = P.part + (size_t)P.n_q * C * kH * kD + (size_t)qi * C * kH * 2;
-  float *recv = reinterpret_cast<float *>(S.kv);
+  const __nv_bfloat16 *part = P.part + (size_t)qi * C * kH * kD;
+  const float *ml = P.ml + (size_t)qi * C * kH * 2;
+  __nv_bfloat16 *recv = reinterpret_cast<__nv_bfloat16 *>(S.kv);
   // rank j's rows h0 .. h1 - 1 are contiguous: one bulk copy per rank
   if (t == 0) {
     fence_proxy_async_global();
-    mbar_arrive_expect_tx(&S.mg_bar, C * nh * kD * 4);
+    mbar_arrive_expect_tx(&S.mg_bar, C * nh * kD * 2);
     for (uint32_t j = 0; j < C; ++j)
-      bulk_load(recv + (size_t)j * nh * kD, part + ((size_t)j * kH + h0) * kD, nh * kD * 4,
+      bulk_load(recv + (size_t)j * nh * kD, part + ((size_t)j * kH + h0) * kD, nh * kD * 2,
                 &S.mg_bar);
   }
   if (t < nh) {
@@ -187,14 +190,16 @@ __device__ __forceinline__ bool merge_heads(const TcAttnParams &P, Smem &S, uint
     }
 #pragma unroll
     for (uint32_t j = 0; j < kMaxCluster; ++j) M = fmaxf(M, m[j]);
-    float L = 0.f;
+    // O = sum_j f_j (O_j / L_j) with f_j = 2^(m_j - M) L_j / sum_i 2^(m_i - M) L_i
+    float f[kMaxCluster], L = 0.f;
 #pragma unroll
     for (uint32_t j = 0; j < kMaxCluster; ++j) {
-      const float f = m[j] == -INFINITY ? 0.f : exp2f(m[j] - M);
-      S.mw[t][j] = f;
-      L = fmaf(f, l[j], L);
+      f[j] = m[j] == -INFINITY ? 0.f : exp2f(m[j] - M) * l[j];
+      L += f[j];
     }
-    S.linv[t] = L > 0.f ? 1.f / L : 0.f;
+    const float li = L > 0.f ? 1.f / L : 0.f;
+#pragma unroll
+    for (uint32_t j = 0; j < kMaxCluster; ++j) S.mw[t][j] = f[j] * li;
   }
   const bool ok = mbar_wait(&S.mg_bar, 0, ew);
   named_bar_sync(1, 256);
@@ -215,18 +220,13 @@ __device__ __forceinline__ bool merge_heads(const TcAttnParams &P, Smem &S, uint
     for (uint32_t j = 0; j < kMaxCluster; ++j) {
       const float f = S.mw[i][j];
       if (j < C && f != 0.f) {
-        const float4 v = *reinterpret_cast<const float4 *>(recv + (j * nh + i) * kD + d);
-        a0 = fmaf(f, v.x, a0);
-        a1 = fmaf(f, v.y, a1);
-        a2 = fmaf(f, v.z, a2);
-        a3 = fmaf(f, v.w, a3);
+        const uint2 v = *reinterpret_cast<const uint2 *>(recv + (j * nh + i) * kD + d);
+        a0 = fmaf(f, bf16lo(v.x), a0);
+        a1 = fmaf(f, bf16hi(v.x), a1);
+        a2 = fmaf(f, bf16lo(v.y), a2);
+        a3 = fmaf(f, bf16hi(v.y), a3);
       }
     }
-    const float li = S.linv[i];
-    a0 *= li;
-    a1 *= li;
-    a2 *= li;
-    a3 *= li;
     // rotate back by -p: (x0, x1) -> (x0 c + x1 s, -x0 s + x1 c)
     const float r0 = a0 * co0 + a1 * si0, r1 = -a0 * si0 + a1 * co0;
     const float r2 = a2 * co1 + a3 * si1, r3 = -a2 * si1 + a3 * co1;
@@ -580,7 +580,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (dec && C > 1) {
         // (max, sum) of this rank for the cluster merge; O follows from TMEM
         if (r < kH) {
-          float *ml = P.part + (size_t)P.n_q * C * kH * kD + ((size_t)(qi * C + rank) * kH + r) * 2;
+          float *ml = P.ml + ((size_t)(qi * C + rank) * kH + r) * 2;
           ml[0] = (has_tiles && any_valid) ? S.mref[r] : -INFINITY;
           ml[1] = has_tiles ? S.lsh[r] : 0.f;
         }
@@ -645,13 +645,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   if (dec && C > 1) {
-    // this rank's unnormalised O as [64 heads][512] fp32 in the row buffer
-    // (free: the last PV is done), then one bulk store to the workspace. Warp
-    // w reads TMEM lanes 32 (w % 4) .. + 31 (dims) for heads 32 (w / 4) .. + 31
-    float *stg = reinterpret_cast<float *>(S.kv);
+    // this rank's O / L as [64 heads][512] bf16 in the row buffer (free: the
+    // last PV is done), then bulk stores to the workspace. Warp w reads TMEM
+    // lanes 32 (w % 4) .. + 31 (dims) for heads 32 (w / 4) .. + 31
+    __nv_bfloat16 *stg = reinterpret_cast<__nv_bfloat16 *>(S.kv);
     if (warp < 8) {
       const uint32_t qw = warp & 3, hf = warp >> 2, dl = 32 * qw + lane;
-      const bool had = S.has_tiles != 0;
+      const bool had = S.has_tiles != 0, odd = lane & 1;
+      float li[32];
+#pragma unroll
+      for (int h = 0; h < 32; ++h) li[h] = had ? S.linv[32 * hf + h] : 0.f;
 #pragma unroll 1
       for (uint32_t m = 0; m < 4; ++m) {
         uint32_t a[32];
@@ -662,18 +665,25 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int h = 0; h < 32; ++h) a[h] = 0u;
         }
+        // lanes 2i, 2i + 1 hold dims d, d + 1: the even lane writes the bf16
+        // pair of head h, the odd lane that of head h + 1 (one swap each)
 #pragma unroll
-        for (int h = 0; h < 32; ++h)
-          stg[(size_t)(32 * hf + h) * kD + m * 128 + dl] = __uint_as_float(a[h]);
+        for (int h = 0; h < 32; h += 2) {
+          const float v0 = __uint_as_float(a[h]) * li[h], v1 = __uint_as_float(a[h + 1]) * li[h + 1];
+          const float other = __shfl_xor_sync(0xffffffffu, odd ? v0 : v1, 1);
+          const uint32_t row = 32 * hf + h + (odd ? 1 : 0);
+          const uint32_t w = odd ? pack_bf16(other, v1) : pack_bf16(v0, other);
+          *reinterpret_cast<uint32_t *>(stg + (size_t)row * kD + m * 128 + (dl & ~1u)) = w;
+        }
       }
     }
     fence_proxy_async();
     __syncthreads();
     if (threadIdx.x == 0) {
-      float *dst = P.part + ((size_t)q_first * C + rank) * kH * kD;
+      __nv_bfloat16 *dst = P.part + ((size_t)q_first * C + rank) * kH * kD;
 #pragma unroll 1
-      for (uint32_t i = 0; i < 8; ++i)   // 8 heads (16 KiB) per copy
-        bulk_store(dst + (size_t)i * 8 * kD, stg + (size_t)i * 8 * kD, 8 * kD * 4);
+      for (uint32_t i = 0; i < 4; ++i)   // 16 heads (16 KiB) per copy
+        bulk_store(dst + (size_t)i * 16 * kD, stg + (size_t)i * 16 * kD, 16 * kD * 2);
       bulk_commit();
       bulk_wait_all();
       fence_proxy_async_global();
@@ -747,7 +757,7 @@ size_t attn_tc_ws_bytes(uint32_t batch, uint32_t T, uint32_t rows_max) {
   const uint32_t n_tiles = (rows_max + kRows - 1) / kRows;
   const uint32_t cmax = n_tiles < kMaxCluster ? (n_tiles ? n_tiles : 1u) : kMaxCluster;
   if (cmax < 2) return 256;
-  return 256 + (size_t)batch * cmax * kH * (kD + 2) * sizeof(float);
+  return 256 + (size_t)batch * cmax * kH * (kD * sizeof(__nv_bfloat16) + 2 * sizeof(float));
 }
 
 cudaError_t launch_attention_tc(const AttnArgs &a, uint32_t rows_max, int *err, cudaStream_t s) {
@@ -770,7 +780,8 @@ cudaError_t launch_attention_tc(const AttnArgs &a, uint32_t rows_max, int *err, 
   P.cos = a.cos;
   P.sin = a.sin;
   P.out = static_cast<__nv_bfloat16 *>(a.out);
-  P.part = reinterpret_cast<float *>(static_cast<uint8_t *>(a.ws) + 256);
+  P.part = reinterpret_cast<__nv_bfloat16 *>(static_cast<uint8_t *>(a.ws) + 256);
+  P.ml = nullptr;
   P.err = err;
   const size_t smem = sizeof(Smem) + 1024;
   static int smem_set = 0;
@@ -786,6 +797,7 @@ cudaError_t launch_attention_tc(const AttnArgs &a, uint32_t rows_max, int *err, 
   if (a.T == 1) {
     const uint32_t n_tiles = (rows_max + kRows - 1) / kRows;
     P.cluster = pick_cluster(n_tiles, P.n_q, smem);
+    P.ml = reinterpret_cast<float *>(P.part + (size_t)P.n_q * P.cluster * kH * kD);
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute at[2];
     at[0].id = cudaLaunchAttributeClusterDimension;
