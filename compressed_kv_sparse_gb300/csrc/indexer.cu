@@ -47,8 +47,9 @@ __host__ __device__ inline IndexWs index_ws_split(void *ws, uint32_t nq, uint32_
 // Workspace of bf16 layers: err word, qbf [nq][Hi][Di] bf16, scores
 // [nq][comp_cap] (fp32), per-query histograms of the scores' top 12 key bits
 // [nq][4096], per-query control words [nq][4] (candidate count, finished-block
-// ticket, overflow) and candidate rows [nq][kCandGlobal]. The row norms of the
-// error bound live in the cache (written when rows are appended).
+// ticket, overflow) and candidates [nq][3][kCandGlobal] (row, S~, error bound).
+// The row norms of the error bound live in the cache (written when rows are
+// appended).
 constexpr uint32_t kHistBins = 4096;
 constexpr uint32_t kCandGlobal = 4096;
 struct TcWs {
@@ -74,7 +75,7 @@ inline TcWs tc_ws_split(void *ws, uint32_t nq, uint32_t B, uint32_t Hi, uint32_t
   w.ctrl = reinterpret_cast<uint32_t *>(base + off);
   off = align_up(off + (size_t)nq * 16, 256);
   w.cand = reinterpret_cast<uint32_t *>(base + off);
-  off += (size_t)nq * kCandGlobal * 4;
+  off += (size_t)nq * 3 * kCandGlobal * 4;
   if (total) *total = off;
   return w;
 }
@@ -503,12 +504,52 @@ __device__ __forceinline__ float rescore_row(const __nv_bfloat16 *qsm, const flo
   return tot;
 }
 
+// Per-head ReLU dots of RPP band rows (fp32 keys at k4, RPP x 128) against
+// head h of q': one q' load serves RPP rows. `exact`: every product is exact,
+// so the fused form rounds like the separate one.
+template <int RPP>
+__device__ __forceinline__ void band_dots(const uint2 *q2, const float4 *k4, bool exact,
+                                          float (&acc)[RPP]) {
+#pragma unroll
+  for (int rr = 0; rr < RPP; ++rr) acc[rr] = 0.f;
+  if (exact) {
+#pragma unroll 4
+    for (uint32_t c = 0; c < 32; ++c) {
+      float q0, q1, q2v, q3;
+      bf16x4(q2[c], q0, q1, q2v, q3);
+#pragma unroll
+      for (int rr = 0; rr < RPP; ++rr) {
+        const float4 k = k4[rr * 32 + c];
+        acc[rr] = fmaf(q0, k.x, acc[rr]);
+        acc[rr] = fmaf(q1, k.y, acc[rr]);
+        acc[rr] = fmaf(q2v, k.z, acc[rr]);
+        acc[rr] = fmaf(q3, k.w, acc[rr]);
+      }
+    }
+  } else {
+#pragma unroll 2
+    for (uint32_t c = 0; c < 32; ++c) {
+      float q0, q1, q2v, q3;
+      bf16x4(q2[c], q0, q1, q2v, q3);
+#pragma unroll
+      for (int rr = 0; rr < RPP; ++rr) {
+        const float4 k = k4[rr * 32 + c];
+        acc[rr] = __fadd_rn(acc[rr], __fmul_rn(q0, k.x));
+        acc[rr] = __fadd_rn(acc[rr], __fmul_rn(q1, k.y));
+        acc[rr] = __fadd_rn(acc[rr], __fmul_rn(q2v, k.z));
+        acc[rr] = __fadd_rn(acc[rr], __fmul_rn(q3, k.w));
+      }
+    }
+  }
+}
+
 // Exact recipe for the band rows (whole block, NW warps): rounds of 2 NW rows;
-// their keys go to `kbuf` as fp32, warp pair (2g, 2g + 1) runs rows
-// 4g .. 4g + 3 of the round against heads 32 (warp & 1) + lane, so one q'
-// load serves four rows and one key load all 32 heads of a warp. Per-head
-// ReLU dots land in `relb` [2 NW rows][64 heads]; one thread per row sums them
-// in ascending h. Results replace cS[band[i]].
+// their keys go to `kbuf` as fp32. The NW / 2 warp pairs split a round's rows
+// evenly, RPP = ceil(rows / (NW / 2)) <= 4 consecutive rows per pair; warp
+// 2g + t of pair g takes heads 32 t + lane, so one q' load serves RPP rows
+// and one key load all 32 heads of a warp. Per-head ReLU dots land in `relb`
+// [2 NW rows][64 heads]; one thread per row sums them in ascending h.
+// Results replace cS[band[i]].
 template <int NW>
 __device__ __forceinline__ void rescore_band(const __nv_bfloat16 *qsm, const float *wsh,
                                              float *kbuf, float *relb, const uint32_t *band,
@@ -516,7 +557,7 @@ __device__ __forceinline__ void rescore_band(const __nv_bfloat16 *qsm, const flo
                                              const __nv_bfloat16 *keys, uint32_t *rexact,
                                              int eq_min, int eq_max) {
   const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  constexpr uint32_t RPR = 2 * NW;
+  constexpr uint32_t RPR = 2 * NW, NP = NW / 2;
   for (uint32_t base = 0; base < nband; base += RPR) {
     const uint32_t nr = min(RPR, nband - base);
 #pragma unroll
@@ -535,47 +576,37 @@ __device__ __forceinline__ void rescore_band(const __nv_bfloat16 *qsm, const flo
       }
     }
     __syncthreads();
-    const uint32_t g4 = (warp >> 1) * 4, h = 32 * (warp & 1) + lane;
-    if (g4 < nr) {   // warp-uniform
+    const uint32_t rpp = (nr + NP - 1) / NP;   // 1 .. 4
+    const uint32_t g0 = (warp >> 1) * rpp, h = 32 * (warp & 1) + lane;
+    if (g0 < nr) {   // warp-uniform
+      const uint32_t cnt = min(rpp, nr - g0);
       bool exact = true;
-#pragma unroll
-      for (uint32_t rr = 0; rr < 4; ++rr)
-        if (g4 + rr < nr) exact = exact && rexact[g4 + rr] != 0u;
+      for (uint32_t rr = 0; rr < cnt; ++rr) exact = exact && rexact[g0 + rr] != 0u;
       const uint2 *q2 = reinterpret_cast<const uint2 *>(qsm + (size_t)h * kQB);
-      const float4 *k4 = reinterpret_cast<const float4 *>(kbuf + g4 * 128);
-      float acc[4] = {0.f, 0.f, 0.f, 0.f};
-      if (exact) {
-#pragma unroll 4
-        for (uint32_t c = 0; c < 32; ++c) {
-          float q0, q1, q2v, q3;
-          bf16x4(q2[c], q0, q1, q2v, q3);
-#pragma unroll
-          for (uint32_t rr = 0; rr < 4; ++rr) {
-            const float4 k = k4[rr * 32 + c];
-            acc[rr] = fmaf(q0, k.x, acc[rr]);
-            acc[rr] = fmaf(q1, k.y, acc[rr]);
-            acc[rr] = fmaf(q2v, k.z, acc[rr]);
-            acc[rr] = fmaf(q3, k.w, acc[rr]);
-          }
-        }
+      const float4 *k4 = reinterpret_cast<const float4 *>(kbuf + g0 * 128);
+      // (rows past cnt read keys of the next pair or stale data: never stored)
+      float acc[4];
+      if (rpp == 1) {
+        float a1[1];
+        band_dots<1>(q2, k4, exact, a1);
+        acc[0] = a1[0];
+      } else if (rpp == 2) {
+        float a2[2];
+        band_dots<2>(q2, k4, exact, a2);
+        acc[0] = a2[0];
+        acc[1] = a2[1];
+      } else if (rpp == 3) {
+        float a3[3];
+        band_dots<3>(q2, k4, exact, a3);
+        acc[0] = a3[0];
+        acc[1] = a3[1];
+        acc[2] = a3[2];
       } else {
-#pragma unroll 2
-        for (uint32_t c = 0; c < 32; ++c) {
-          float q0, q1, q2v, q3;
-          bf16x4(q2[c], q0, q1, q2v, q3);
-#pragma unroll
-          for (uint32_t rr = 0; rr < 4; ++rr) {
-            const float4 k = k4[rr * 32 + c];
-            acc[rr] = __fadd_rn(acc[rr], __fmul_rn(q0, k.x));
-            acc[rr] = __fadd_rn(acc[rr], __fmul_rn(q1, k.y));
-            acc[rr] = __fadd_rn(acc[rr], __fmul_rn(q2v, k.z));
-            acc[rr] = __fadd_rn(acc[rr], __fmul_rn(q3, k.w));
-          }
-        }
+        band_dots<4>(q2, k4, exact, acc);
       }
 #pragma unroll
       for (uint32_t rr = 0; rr < 4; ++rr)
-        relb[(g4 + rr) * 64 + h] = acc[rr] > 0.f ? acc[rr] : 0.f;
+        if (rr < cnt) relb[(g0 + rr) * 64 + h] = acc[rr] > 0.f ? acc[rr] : 0.f;
     }
     __syncthreads();
     if (threadIdx.x < nr) {
@@ -649,7 +680,10 @@ __global__ void __launch_bounds__(NT, NT == 256 ? 4 : 1)
   const __nv_bfloat16 *qb = w.qbf + (size_t)qi * Hi * Di;
   const __nv_bfloat16 *wq = static_cast<const __nv_bfloat16 *>(a.w) + (size_t)qi * Hi;
   uint32_t *ctrl = w.ctrl + (size_t)qi * 4;
-  uint32_t *cand = w.cand + (size_t)qi * kCandGlobal;
+  // candidates of a query (several blocks per query): rows, S~, error bounds
+  uint32_t *cand = w.cand + (size_t)qi * 3 * kCandGlobal;
+  float *cand_s = reinterpret_cast<float *>(cand + kCandGlobal);
+  float *cand_e = cand_s + kCandGlobal;
 
   // A = c * sum_h |w_h| ||q'_h|| (HPW heads per warp); q' rows to shared
   // memory as fp32, with the exponent range of their nonzero entries
@@ -710,7 +744,7 @@ __global__ void __launch_bounds__(NT, NT == 256 ? 4 : 1)
   // a rank that leaves ~1.25 k rows above it; the filter below counts the rows
   // at or above it exactly, and too few sends the block to the full pass.
   if (threadIdx.x == 0) {
-    s_misc[2] = 0;   // candidate count (one block per query)
+    s_misc[2] = 0;   // this block's candidate count
     s_misc[3] = 0;   // rows with S~ >= theta_S (one block per query)
   }
   float theta_s;
@@ -770,46 +804,62 @@ __global__ void __launch_bounds__(NT, NT == 256 ? 4 : 1)
   const float theta = theta_s - E - fabsf(theta_s) * (2.0f * kRel);
   auto err_of = [&](float S, float nm) { return A * nm + fabsf(S) * kRel + eta; };
 
-  // ---- this block's share of the rows: candidates with U >= theta; with one
-  // block per query they go straight to shared memory, else to the query's
-  // list in global memory for the last block to finish
+  // ---- this block's share of the rows: candidates with U >= theta, gathered
+  // in shared memory (four rows per thread loaded before any is classified);
+  // with several blocks per query each block then reserves one range of the
+  // query's list in global memory for the last block to finish
   {
     const uint32_t per = ((vis + G * 32 - 1) / (G * 32)) * 32;
     const uint32_t r0 = g * per, r1 = min(vis, r0 + per);
-    for (uint32_t base = r0 + warp * 32; base < r1; base += blockDim.x) {
-      const uint32_t r = base + lane;
-      const bool ok = r < r1;
-      const float S = ok ? sc[r] : 0.f;
-      const float e = ok ? err_of(S, nr[r]) : 0.f;
-      const bool c = ok && S + e >= theta;
-      if (G == 1) {
-        const uint32_t ge = __ballot_sync(0xffffffffu, ok && S >= theta_s);
-        if (lane == 0 && ge) atomicAdd(&s_misc[3], (uint32_t)__popc(ge));
+    constexpr uint32_t J = 4;
+    for (uint32_t pass = r0; pass < r1; pass += J * NT) {
+      float Sv[J], Nv[J];
+#pragma unroll
+      for (uint32_t j = 0; j < J; ++j) {
+        const uint32_t r = pass + j * NT + threadIdx.x;
+        Sv[j] = r < r1 ? sc[r] : 0.f;
+        Nv[j] = r < r1 ? nr[r] : 0.f;
       }
-      const uint32_t bal = __ballot_sync(0xffffffffu, c);
-      if (bal) {
-        uint32_t slot = 0;
-        if (lane == 0)
-          slot = G == 1 ? atomicAdd(&s_misc[2], (uint32_t)__popc(bal))
-                        : atomicAdd(&ctrl[0], (uint32_t)__popc(bal));
-        slot = __shfl_sync(0xffffffffu, slot, 0) + __popc(bal & ((1u << lane) - 1u));
-        if (c) {
-          if (G == 1) {
-            if (slot < CAP) {
-              cidx[slot] = r;
-              cS[slot] = S;
-              ce[slot] = e;
-            }
-          } else if (slot < kCandGlobal) {
-            cand[slot] = r;
-          } else {
-            ctrl[2] = 1u;
+#pragma unroll
+      for (uint32_t j = 0; j < J; ++j) {
+        const uint32_t r = pass + j * NT + threadIdx.x;
+        const bool ok = r < r1;
+        const float S = Sv[j];
+        const float e = ok ? err_of(S, Nv[j]) : 0.f;
+        const bool c = ok && S + e >= theta;
+        if (G == 1) {
+          const uint32_t ge = __ballot_sync(0xffffffffu, ok && S >= theta_s);
+          if (lane == 0 && ge) atomicAdd(&s_misc[3], (uint32_t)__popc(ge));
+        }
+        const uint32_t bal = __ballot_sync(0xffffffffu, c);
+        if (bal) {
+          uint32_t slot = 0;
+          if (lane == 0) slot = atomicAdd(&s_misc[2], (uint32_t)__popc(bal));
+          slot = __shfl_sync(0xffffffffu, slot, 0) + __popc(bal & ((1u << lane) - 1u));
+          if (c && slot < CAP) {
+            cidx[slot] = r;
+            cS[slot] = S;
+            ce[slot] = e;
           }
         }
       }
     }
   }
   if (G > 1) {
+    __syncthreads();
+    const uint32_t nb = s_misc[2];
+    if (threadIdx.x == 0) {
+      const uint32_t at = atomicAdd(&ctrl[0], nb);
+      s_misc[5] = at;
+      if (nb > CAP || at + nb > kCandGlobal) ctrl[2] = 1u;   // overflow: full pass
+    }
+    __syncthreads();
+    const uint32_t at = s_misc[5], nbc = min(nb, CAP);
+    for (uint32_t i = threadIdx.x; i < nbc && at + i < kCandGlobal; i += NT) {
+      cand[at + i] = cidx[i];
+      cand_s[at + i] = cS[i];
+      cand_e[at + i] = ce[i];
+    }
     __threadfence();
     __syncthreads();
     if (threadIdx.x == 0) s_misc[1] = atomicAdd(&ctrl[1], 1u) == G - 1 ? 1u : 0u;
@@ -831,15 +881,15 @@ __global__ void __launch_bounds__(NT, NT == 256 ? 4 : 1)
     __syncthreads();
     if (G > 1) {
       for (uint32_t j = threadIdx.x; j < nc; j += blockDim.x) {
-        uint32_t r = *(volatile uint32_t *)&cand[j];
+        uint32_t r = __ldcg(&cand[j]);
+        const float S = __ldcg(&cand_s[j]), e = __ldcg(&cand_e[j]);
         if (r >= vis) {   // never expected: the selection below recomputes from the scores
           s_misc[5] = 1u;
           r = 0;
         }
-        const float S = sc[r];
         cidx[j] = r;
         cS[j] = S;
-        ce[j] = err_of(S, nr[r]);
+        ce[j] = e;
       }
     }
     const uint32_t words = (vis + 31) / 32;
