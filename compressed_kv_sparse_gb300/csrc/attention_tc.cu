@@ -44,7 +44,8 @@ constexpr int kH = 64, kD = 512, kNope = 448, kRows = 128;
 constexpr int kQBlk = kH * 128;        // one 64-dim block of Q: 64 heads x 128 B
 constexpr int kKBlk = kRows * 128;     // one 64-dim block of the row tile
 constexpr int kThreads = 288;
-constexpr uint32_t kMaxCluster = 8;    // portable cluster size
+constexpr uint32_t kMaxCluster = 16;   // cluster size; beyond 8 (the portable limit) when the
+                                       // device allows non-portable sizes
 constexpr float kRaiseLog2 = 8.0f;     // raise the running max beyond 2^8
 
 struct TcAttnParams {
@@ -76,8 +77,13 @@ struct Smem {
   float mw[kH][kMaxCluster];        // decode merge: weight of each rank, per owned head
   uint32_t flagcnt[3], tmem, has_tiles;
 };
-// the merge pulls at most C * ceil(64 / C) rows of 1 KiB (70 KiB at C = 7)
-static_assert(8 * kKBlk >= 7 * 10 * kD * 2, "pulled slices fit the row buffer");
+// the merge pulls at most C * ceil(64 / C) rows of 1 KiB (75 at C = 15)
+constexpr uint32_t max_pulled_rows(uint32_t C = 1) {
+  return C > kMaxCluster ? 0u
+                         : (C * ((kH + C - 1) / C) > max_pulled_rows(C + 1) ? C * ((kH + C - 1) / C)
+                                                                             : max_pulled_rows(C + 1));
+}
+static_assert(8 * kKBlk >= max_pulled_rows() * kD * 2, "pulled slices fit the row buffer");
 static_assert(2 * kH * 128 == kRows * 128, "output staging fills the P buffer");
 
 // Rows that a query can have at most, without reading its top-k list.
@@ -698,15 +704,32 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-// Largest number of clusters of each size (1..8) that fit on the device at
-// once, per device; 0 = not yet asked.
+// Largest number of clusters of each size (1..16) that fit on the device at
+// once, per device; 0 = not yet asked, -1 = the size cannot be launched.
 std::atomic<int> g_max_clusters[64][kMaxCluster + 1];
+// Per device: 1 = cluster sizes above 8 allowed for the kernel, -1 = refused.
+std::atomic<int> g_nonportable[64];
 
 int max_active_clusters(uint32_t C, size_t smem) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
   int v = g_max_clusters[dev][C].load(std::memory_order_relaxed);
-  if (v > 0) return v;
+  if (v != 0) return v;
+  if (C > 8) {
+    int np = g_nonportable[dev].load(std::memory_order_relaxed);
+    if (np == 0) {
+      np = cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) ==
+                   cudaSuccess
+               ? 1
+               : -1;
+      (void)cudaGetLastError();
+      g_nonportable[dev].store(np, std::memory_order_relaxed);
+    }
+    if (np < 0) {
+      g_max_clusters[dev][C].store(-1, std::memory_order_relaxed);
+      return -1;
+    }
+  }
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute at[1];
   at[0].id = cudaLaunchAttributeClusterDimension;
@@ -720,9 +743,10 @@ int max_active_clusters(uint32_t C, size_t smem) {
   cfg.numAttrs = 1;
   if (cudaOccupancyMaxActiveClusters(&v, attn_tc_kernel, &cfg) != cudaSuccess || v <= 0) {
     (void)cudaGetLastError();
-    v = num_sms() / (int)C;
+    // beyond the portable size an unanswered query means the size is not used
+    v = C > 8 ? -1 : num_sms() / (int)C;
   }
-  if (v < 1) v = 1;
+  if (v == 0) v = 1;
   g_max_clusters[dev][C].store(v, std::memory_order_relaxed);
   return v;
 }
@@ -734,7 +758,9 @@ uint32_t pick_cluster(uint32_t n_tiles, uint32_t n_q, size_t smem) {
   uint32_t best = 1, best_cost = 0xffffffffu;
   const uint32_t cmax = n_tiles < kMaxCluster ? (n_tiles ? n_tiles : 1u) : kMaxCluster;
   for (uint32_t C = 1; C <= cmax; ++C) {
-    const uint32_t act = (uint32_t)max_active_clusters(C, smem);
+    const int actv = max_active_clusters(C, smem);
+    if (actv < 1) continue;
+    const uint32_t act = (uint32_t)actv;
     const uint32_t waves = (n_q + act - 1) / act, tiles = (n_tiles + C - 1) / C;
     const uint32_t cost = waves * (tiles + 2);
     if (cost < best_cost) {
