@@ -171,6 +171,8 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 // row-tile buffer as [j][i][512] fp32 and are combined in rank order with
 // weights 2^(m_j - M) / sum_j 2^(m_j - M) l_j. A rank without rows left
 // m = -inf and zeros; one with only masked rows left m = -inf and O = 0.
+// CM: compile-time bound on the cluster size C (the loops over ranks unroll)
+template <uint32_t CM>
 __device__ __forceinline__ bool merge_heads(const TcAttnParams &P, Smem &S, uint32_t qi,
                                             uint32_t rank, uint32_t C, ErrWord ew) {
   const uint32_t t = threadIdx.x;
@@ -188,24 +190,24 @@ __device__ __forceinline__ bool merge_heads(const TcAttnParams &P, Smem &S, uint
   }
   if (t < nh) {
     const uint32_t h = h0 + t;
-    float m[kMaxCluster], l[kMaxCluster], M = -INFINITY;
+    float m[CM], l[CM], M = -INFINITY;
 #pragma unroll
-    for (uint32_t j = 0; j < kMaxCluster; ++j) {
+    for (uint32_t j = 0; j < CM; ++j) {
       m[j] = j < C ? __ldcg(ml + ((size_t)j * kH + h) * 2) : -INFINITY;   // written by peers
       l[j] = j < C ? __ldcg(ml + ((size_t)j * kH + h) * 2 + 1) : 0.f;
     }
 #pragma unroll
-    for (uint32_t j = 0; j < kMaxCluster; ++j) M = fmaxf(M, m[j]);
+    for (uint32_t j = 0; j < CM; ++j) M = fmaxf(M, m[j]);
     // O = sum_j f_j (O_j / L_j) with f_j = 2^(m_j - M) L_j / sum_i 2^(m_i - M) L_i
-    float f[kMaxCluster], L = 0.f;
+    float f[CM], L = 0.f;
 #pragma unroll
-    for (uint32_t j = 0; j < kMaxCluster; ++j) {
+    for (uint32_t j = 0; j < CM; ++j) {
       f[j] = m[j] == -INFINITY ? 0.f : exp2f(m[j] - M) * l[j];
       L += f[j];
     }
     const float li = L > 0.f ? 1.f / L : 0.f;
 #pragma unroll
-    for (uint32_t j = 0; j < kMaxCluster; ++j) S.mw[t][j] = f[j] * li;
+    for (uint32_t j = 0; j < CM; ++j) S.mw[t][j] = f[j] * li;
   }
   const bool ok = mbar_wait(&S.mg_bar, 0, ew);
   named_bar_sync(1, 256);
@@ -223,7 +225,7 @@ __device__ __forceinline__ bool merge_heads(const TcAttnParams &P, Smem &S, uint
   for (uint32_t i = t >> 7; i < nh; i += 2) {
     float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
 #pragma unroll
-    for (uint32_t j = 0; j < kMaxCluster; ++j) {
+    for (uint32_t j = 0; j < CM; ++j) {
       const float f = S.mw[i][j];
       if (j < C && f != 0.f) {
         const uint2 v = *reinterpret_cast<const uint2 *>(recv + (j * nh + i) * kD + d);
@@ -700,7 +702,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 8) tmem_dealloc(tmem, 512);
   if (dec && C > 1) {
     cluster_sync_all();   // every rank's O and (max, sum) are in the workspace
-    if (warp < 8) merge_heads(P, S, q_first, rank, C, ew);
+    if (warp < 8) {
+      if (C <= 8)
+        merge_heads<8>(P, S, q_first, rank, C, ew);
+      else
+        merge_heads<kMaxCluster>(P, S, q_first, rank, C, ew);
+    }
   }
 }
 
