@@ -81,35 +81,49 @@ inline TcWs tc_ws_split(void *ws, uint32_t nq, uint32_t B, uint32_t Hi, uint32_t
 }
 
 // bf16 layers: q' = rotated query rounded to bf16 (fp32 recipe), one thread
-// per pair of dims; the same grid clears the call's counters (error word,
-// control words and, when the scorer builds them, histograms).
-__global__ void index_qbf_kernel(IndexArgs a, TcWs w, bool clear_hist) {
+// per `per` dims (a 16-byte unit of 8, or a pair when the query is not 16-byte
+// aligned); the same grid clears the call's counters (error word, control
+// words and, when the scorer builds them, histograms).
+__global__ void index_qbf_kernel(IndexArgs a, TcWs w, bool clear_hist, uint32_t per) {
   pdl_wait();
   pdl_trigger();
   const uint32_t Hi = a.n_heads, Di = a.dim, n_nope = Di - a.rot;
-  const size_t nq = (size_t)a.batch * a.T;
-  const size_t npair = nq * Hi * Di / 2;
-  const size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x;
+  const uint32_t nq = a.batch * a.T;
+  const uint32_t upr = Di / per;                  // units (per dims each) per head row
+  const uint32_t n_units = nq * Hi * upr;
+  const uint32_t i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i == 0) *w.err = 0;
   if (i < nq * 4) w.ctrl[i] = 0u;
-  if (clear_hist && i < nq * kHistBins) w.hist[i] = 0u;
-  if (i >= npair) return;
-  const uint32_t c = (uint32_t)(2 * (i % (Di / 2)));
-  const size_t qi = i / ((size_t)Hi * Di / 2);
-  const uint32_t p = a.pos0 + (uint32_t)(qi % a.T);
-  const uint32_t *src = reinterpret_cast<const uint32_t *>(a.q_idx);
-  uint32_t v = src[i];
-  if (c >= n_nope) {
-    const float x0 = __uint_as_float(v << 16), x1 = __uint_as_float(v & 0xFFFF0000u);
-    const uint32_t fi = (c - n_nope) / 2;
-    const float co = a.cos[(size_t)p * (a.rot / 2) + fi];
-    const float si = a.sin[(size_t)p * (a.rot / 2) + fi];
-    const float r0 = __fsub_rn(__fmul_rn(x0, co), __fmul_rn(x1, si));
-    const float r1 = __fadd_rn(__fmul_rn(x0, si), __fmul_rn(x1, co));
-    const __nv_bfloat162 r = __floats2bfloat162_rn(r0, r1);
-    v = *reinterpret_cast<const uint32_t *>(&r);
+  if (clear_hist && i < nq * (kHistBins / 4))
+    reinterpret_cast<uint4 *>(w.hist)[i] = make_uint4(0u, 0u, 0u, 0u);
+  if (i >= n_units) return;
+  const uint32_t row = i / upr, c0 = (i - row * upr) * per;   // row = query * Hi + head
+  const uint32_t p = a.pos0 + (row / Hi) % a.T;
+  // rotate the pairs of w4 (dims c0, c0 + 1, ...) that lie in the tail
+  auto rot = [&](uint32_t *w4, uint32_t n) {
+    for (uint32_t e = 0; e < n; ++e) {
+      const uint32_t c = c0 + 2 * e;
+      if (c < n_nope) continue;
+      const float x0 = __uint_as_float(w4[e] << 16), x1 = __uint_as_float(w4[e] & 0xFFFF0000u);
+      const uint32_t fi = (c - n_nope) / 2;
+      const float co = a.cos[(size_t)p * (a.rot / 2) + fi];
+      const float si = a.sin[(size_t)p * (a.rot / 2) + fi];
+      const float r0 = __fsub_rn(__fmul_rn(x0, co), __fmul_rn(x1, si));
+      const float r1 = __fadd_rn(__fmul_rn(x0, si), __fmul_rn(x1, co));
+      const __nv_bfloat162 r = __floats2bfloat162_rn(r0, r1);
+      w4[e] = *reinterpret_cast<const uint32_t *>(&r);
+    }
+  };
+  if (per == 8) {
+    const uint4 v = reinterpret_cast<const uint4 *>(a.q_idx)[i];
+    uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+    if (c0 + 8 > n_nope) rot(w4, 4);
+    reinterpret_cast<uint4 *>(w.qbf)[i] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+  } else {
+    uint32_t w1[1] = {reinterpret_cast<const uint32_t *>(a.q_idx)[i]};
+    rot(w1, 1);
+    reinterpret_cast<uint32_t *>(w.qbf)[i] = w1[0];
   }
-  reinterpret_cast<uint32_t *>(w.qbf)[i] = v;
 }
 
 template <typename T>
@@ -1125,15 +1139,18 @@ inline double gamma_n(double n) {
 cudaError_t launch_index_tc(const IndexArgs &a, cudaStream_t s) {
   const uint32_t nq = a.batch * a.T;
   TcWs w = tc_ws_split(a.ws, nq, a.batch, a.n_heads, a.dim, a.comp_cap, nullptr);
-  const size_t npair = (size_t)nq * a.n_heads * a.dim / 2;
+  // q' in 16-byte units of 8 dims (4-byte pairs when the query is not
+  // 16-byte aligned)
+  const uint32_t per = reinterpret_cast<uintptr_t>(a.q_idx) % 16 == 0 && a.dim % 8 == 0 ? 8u : 2u;
+  if ((size_t)nq * a.n_heads * a.dim >= (1ull << 31)) return cudaErrorInvalidValue;
   // the scorer builds key histograms when several select blocks share a
   // query; with one block per query the selection samples its threshold
   const bool scorer_hist = select_groups(nq) > 1;
-  size_t nthreads = npair;
-  if (scorer_hist && (size_t)nq * kHistBins > nthreads) nthreads = (size_t)nq * kHistBins;
+  size_t nthreads = (size_t)nq * a.n_heads * a.dim / per;
+  if (scorer_hist && (size_t)nq * (kHistBins / 4) > nthreads) nthreads = (size_t)nq * (kHistBins / 4);
   if ((size_t)nq * 4 > nthreads) nthreads = (size_t)nq * 4;
   cudaError_t eq = launch_pdl(index_qbf_kernel, dim3((unsigned)((nthreads + 255) / 256)),
-                              dim3(256), 0, s, a, w, scorer_hist);
+                              dim3(256), 0, s, a, w, scorer_hist, per);
   if (eq != cudaSuccess) return eq;
   note_launches(1);
   const uint32_t vis_max = min((a.pos0 + a.T) / 4, a.n_comp);
