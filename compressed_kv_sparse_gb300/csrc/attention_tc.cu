@@ -653,11 +653,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   if (dec && C > 1) {
-    // this rank's O / L as [64 heads][512] bf16 in the row buffer (free: the
-    // last PV is done), then bulk stores to the workspace. Warp w reads TMEM
-    // lanes 32 (w % 4) .. + 31 (dims) for heads 32 (w / 4) .. + 31
-    __nv_bfloat16 *stg = reinterpret_cast<__nv_bfloat16 *>(S.kv);
+    // this rank's O / L as [64 heads][512] bf16 straight to the workspace.
+    // Warp w reads TMEM lanes 32 (w % 4) .. + 31 (dims) for heads 32 (w / 4)
+    // .. + 31; lanes 2i, 2i + 1 hold dims d, d + 1: the even lane stores the
+    // bf16 pair of head h, the odd lane that of head h + 1 (one swap each)
     if (warp < 8) {
+      __nv_bfloat16 *dst = P.part + ((size_t)q_first * C + rank) * kH * kD;
       const uint32_t qw = warp & 3, hf = warp >> 2, dl = 32 * qw + lane;
       const bool had = S.has_tiles != 0, odd = lane & 1;
       float li[32];
@@ -673,28 +674,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int h = 0; h < 32; ++h) a[h] = 0u;
         }
-        // lanes 2i, 2i + 1 hold dims d, d + 1: the even lane writes the bf16
-        // pair of head h, the odd lane that of head h + 1 (one swap each)
 #pragma unroll
         for (int h = 0; h < 32; h += 2) {
           const float v0 = __uint_as_float(a[h]) * li[h], v1 = __uint_as_float(a[h + 1]) * li[h + 1];
           const float other = __shfl_xor_sync(0xffffffffu, odd ? v0 : v1, 1);
           const uint32_t row = 32 * hf + h + (odd ? 1 : 0);
           const uint32_t w = odd ? pack_bf16(other, v1) : pack_bf16(v0, other);
-          *reinterpret_cast<uint32_t *>(stg + (size_t)row * kD + m * 128 + (dl & ~1u)) = w;
+          *reinterpret_cast<uint32_t *>(dst + (size_t)row * kD + m * 128 + (dl & ~1u)) = w;
         }
       }
-    }
-    fence_proxy_async();
-    __syncthreads();
-    if (threadIdx.x == 0) {
-      __nv_bfloat16 *dst = P.part + ((size_t)q_first * C + rank) * kH * kD;
-#pragma unroll 1
-      for (uint32_t i = 0; i < 4; ++i)   // 16 heads (16 KiB) per copy
-        bulk_store(dst + (size_t)i * 16 * kD, stg + (size_t)i * 16 * kD, 16 * kD * 2);
-      bulk_commit();
-      bulk_wait_all();
-      fence_proxy_async_global();
     }
   }
   tc_fence_before();
