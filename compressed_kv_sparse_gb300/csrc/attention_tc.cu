@@ -244,6 +244,9 @@ __device__ __forceinline__ bool merge_heads(const TcAttnParams &P, Smem &S, uint
   return true;
 }
 
+// DEC: decode (clusters of P.cluster CTAs per query) or prefill (persistent
+// CTAs); two instantiations keep each path's code to itself
+template <bool DEC>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, TcAttnParams P) {
   extern __shared__ uint8_t smem_raw[];
@@ -252,7 +255,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // decode: cluster of C CTAs per query, rank c takes tiles c, c + C, ...;
   // prefill: one whole query at a time per CTA
-  const bool dec = P.cluster != 0;
+  constexpr bool dec = DEC;
   const uint32_t C = dec ? P.cluster : 1u;
   const uint32_t rank = dec ? cluster_ctarank() : 0u;
   const uint32_t q_first = dec ? blockIdx.x / C : blockIdx.x;
@@ -713,7 +716,7 @@ int max_active_clusters(uint32_t C, size_t smem) {
   if (C > 8) {
     int np = g_nonportable[dev].load(std::memory_order_relaxed);
     if (np == 0) {
-      np = cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) ==
+      np = cudaFuncSetAttribute(attn_tc_kernel<true>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) ==
                    cudaSuccess
                ? 1
                : -1;
@@ -736,7 +739,7 @@ int max_active_clusters(uint32_t C, size_t smem) {
   cfg.dynamicSmemBytes = smem;
   cfg.attrs = at;
   cfg.numAttrs = 1;
-  if (cudaOccupancyMaxActiveClusters(&v, attn_tc_kernel, &cfg) != cudaSuccess || v <= 0) {
+  if (cudaOccupancyMaxActiveClusters(&v, attn_tc_kernel<true>, &cfg) != cudaSuccess || v <= 0) {
     (void)cudaGetLastError();
     // beyond the portable size an unanswered query means the size is not used
     v = C > 8 ? -1 : num_sms() / (int)C;
@@ -805,8 +808,9 @@ cudaError_t launch_attention_tc(const AttnArgs &a, uint32_t rows_max, int *err, 
   P.ml = nullptr;
   P.err = err;
   const size_t smem = sizeof(Smem) + 1024;
-  static int smem_set = 0;
-  cudaError_t e = ensure_smem(attn_tc_kernel, smem, &smem_set);
+  static int smem_dec = 0, smem_pf = 0;
+  cudaError_t e = a.T == 1 ? ensure_smem(attn_tc_kernel<true>, smem, &smem_dec)
+                           : ensure_smem(attn_tc_kernel<false>, smem, &smem_pf);
   if (e != cudaSuccess) return e;
   // Q as [n_q * 64 heads][512] bf16 rows; boxes of 64 heads x 64 dims
   CUtensorMap tq;
@@ -833,13 +837,13 @@ cudaError_t launch_attention_tc(const AttnArgs &a, uint32_t rows_max, int *err, 
     at[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = at;
     cfg.numAttrs = 2;
-    e = cudaLaunchKernelEx(&cfg, attn_tc_kernel, tq, P);
+    e = cudaLaunchKernelEx(&cfg, attn_tc_kernel<true>, tq, P);
     note_launches(1);
     return e != cudaSuccess ? e : cudaGetLastError();
   }
   P.cluster = 0;
   const uint32_t grid = min(P.n_q, (uint32_t)num_sms());
-  e = launch_pdl(attn_tc_kernel, dim3(grid), dim3(kThreads), smem, s, tq, P);
+  e = launch_pdl(attn_tc_kernel<false>, dim3(grid), dim3(kThreads), smem, s, tq, P);
   note_launches(1);
   return e != cudaSuccess ? e : cudaGetLastError();
 }

@@ -357,7 +357,6 @@ __device__ __forceinline__ float key_to_float(uint32_t k) {
   return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
 }
 
-constexpr uint32_t kCandCap = 4096;    // candidates held in shared memory
 constexpr float kRel = 2.4e-7f;        // slack for the rounding of the bound arithmetic
 constexpr uint32_t kQB = 132;          // row stride (bf16) of q' in shared memory: the 8-byte
                                         // loads of 16 lanes at 16 rows hit 32 distinct banks
