@@ -873,12 +873,13 @@ __global__ void __launch_bounds__(NT, NT == 256 ? 4 : 1)
       cand_s[at + i] = cS[i];
       cand_e[at + i] = ce[i];
     }
-    __threadfence();
+    // the ticket: an acquire-release add at GPU scope publishes this block's
+    // candidates (ordered before it by the barrier) and, in the last block,
+    // makes every other block's visible to the threads after the next barrier
     __syncthreads();
-    if (threadIdx.x == 0) s_misc[1] = atomicAdd(&ctrl[1], 1u) == G - 1 ? 1u : 0u;
+    if (threadIdx.x == 0) s_misc[1] = atom_add_acq_rel_gpu(&ctrl[1], 1u) == G - 1 ? 1u : 0u;
     __syncthreads();
     if (!s_misc[1]) return;
-    __threadfence();
   } else {
     __syncthreads();
   }
