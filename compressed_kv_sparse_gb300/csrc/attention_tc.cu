@@ -209,9 +209,7 @@ __device__ __forceinline__ bool merge_heads(const TcAttnParams &P, Smem &S, uint
 #pragma unroll
     for (uint32_t j = 0; j < CM; ++j) S.mw[t][j] = f[j] * li;
   }
-  const bool ok = mbar_wait(&S.mg_bar, 0, ew);
-  named_bar_sync(1, 256);
-  if (!ok) return false;
+  // rotation coefficients load while the slices land
   const uint32_t p = P.pos0 + qi % P.T, c = t & 127, d = 4 * c;
   float co0 = 1.f, si0 = 0.f, co1 = 1.f, si1 = 0.f;
   if (d >= (uint32_t)kNope) {
@@ -221,6 +219,9 @@ __device__ __forceinline__ bool merge_heads(const TcAttnParams &P, Smem &S, uint
     co1 = P.cos[(size_t)p * 32 + fi + 1];
     si1 = P.sin[(size_t)p * 32 + fi + 1];
   }
+  const bool ok = mbar_wait(&S.mg_bar, 0, ew);
+  named_bar_sync(1, 256);
+  if (!ok) return false;
 #pragma unroll 1
   for (uint32_t i = t >> 7; i < nh; i += 2) {
     float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
@@ -453,16 +454,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t r = threadIdx.x;          // tile row / TMEM lane, then dim within a block
     const uint32_t lane_base = (warp * 32) << 16;
     uint32_t n = 0, qn = 0, sm_phase = 0;
-    // P row r from the scores in TMEM with the current running maxima;
-    // returns whether a score exceeds its head's maximum by more than 2^8
-    auto write_p = [&](bool valid) {
-      bool flag = false;
+    // P of heads 32 hf .. + 31 of row r from their scores `a` with the current
+    // running maxima; flags a score above its head's maximum by more than 2^8
+    auto p_half = [&](bool valid, const uint32_t (&a)[32], uint32_t hf, bool &flag) {
       uint8_t *prow = S.p + (r >> 3) * 1024 + (r & 7) * 128;
-#pragma unroll
-      for (uint32_t hf = 0; hf < 2; ++hf) {
-        uint32_t a[32];
-        tmem_ld32(tmS + lane_base + 32 * hf, a);
-        tmem_ld_wait();
 #pragma unroll
         for (uint32_t c4 = 0; c4 < 4; ++c4) {
           uint32_t w4[4];
@@ -477,6 +472,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           *reinterpret_cast<uint4 *>(prow + (((4 * hf + c4) ^ (r & 7)) << 4)) =
               make_uint4(w4[0], w4[1], w4[2], w4[3]);
         }
+    };
+    // P row r from the scores in TMEM; returns whether a score exceeds its
+    // head's running maximum by more than 2^8
+    auto write_p = [&](bool valid) {
+      bool flag = false;
+#pragma unroll
+      for (uint32_t hf = 0; hf < 2; ++hf) {
+        uint32_t a[32];
+        tmem_ld32(tmS + lane_base + 32 * hf, a);
+        tmem_ld_wait();
+        p_half(valid, a, hf, flag);
       }
       return flag;
     };
@@ -495,22 +501,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         if (first) {
           // running maxima start at the exact per-head maxima of the first
-          // tile's scaled scores (so its P never needs a raise): warp maxima
-          // of order-keyed values, then the largest of the four warps
+          // tile's scaled scores: warp maxima of order-keyed values, then the
+          // largest of the four warps. The scores stay in registers for P,
+          // which then has no score above its maximum (no raise to check).
+          uint32_t a0[32], a1[32];
+          tmem_ld32(tmS + lane_base, a0);
+          tmem_ld32(tmS + lane_base + 32, a1);
+          tmem_ld_wait();
           uint32_t *tkey = reinterpret_cast<uint32_t *>(&S.tmax[0][0]);   // [4][kH]
-#pragma unroll 1
-          for (uint32_t hf = 0; hf < 2; ++hf) {
-            uint32_t a[32];
-            tmem_ld32(tmS + lane_base + 32 * hf, a);
-            tmem_ld_wait();
 #pragma unroll
-            for (int h = 0; h < 32; ++h) {
-              const uint32_t u = __float_as_uint(__uint_as_float(a[h]) * P.c2);
-              const uint32_t key = valid ? ((u & 0x80000000u) ? ~u : (u | 0x80000000u)) : 0u;
-              const uint32_t mk = redux_max_u32(key);
-              if (lane == (uint32_t)h) tkey[warp * kH + 32 * hf + h] = mk;
-            }
+          for (int h = 0; h < 64; ++h) {
+            const uint32_t u = __float_as_uint(__uint_as_float(h < 32 ? a0[h] : a1[h - 32]) * P.c2);
+            const uint32_t key = valid ? ((u & 0x80000000u) ? ~u : (u | 0x80000000u)) : 0u;
+            const uint32_t mk = redux_max_u32(key);
+            if (lane == (uint32_t)(h & 31)) tkey[warp * kH + h] = mk;
           }
+          if (r == 0) S.flagcnt[(n + 1) % 3] = 0;   // the next tile's raise count
           if (!group_sync(&S.sm_bar, sm_phase, ew)) goto done_softmax;
           const uint32_t k0 = max(max(tkey[0 * kH], tkey[1 * kH]), max(tkey[2 * kH], tkey[3 * kH]));
           any_valid = k0 != 0u;   // a valid row has a key above 0 for every head
@@ -521,6 +527,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             S.mref[r] = any_valid ? mx : 0.f;
           }
           if (!group_sync(&S.sm_bar, sm_phase, ew)) goto done_softmax;
+          if (!mbar_wait_warp(&S.p_empty, (n & 1) ^ 1, ew)) goto done_softmax;
+          bool unused = false;
+          p_half(valid, a0, 0, unused);
+          p_half(valid, a1, 1, unused);
+          fence_proxy_async();
+          tc_fence_before();
+          mbar_arrive(&S.p_full);
+          continue;
         }
         // P of this tile (the previous PV must be done with the buffer)
         if (!mbar_wait_warp(&S.p_empty, (n & 1) ^ 1, ew)) goto done_softmax;
