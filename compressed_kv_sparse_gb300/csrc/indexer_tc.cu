@@ -36,9 +36,9 @@ constexpr int kABytes = 2 * kKBlockBytes;          // 32 KiB per A stage
 template <int QG>
 struct Cfg {
   static constexpr int N = kHeads * QG;
-  // epilogue warps: 4 (one per TMEM lane quarter) for one query, 8 for four
-  // (two per quarter, two queries each)
-  static constexpr int kEpiWarps = QG == 1 ? 4 : 8;
+  // epilogue warps: 4 (one per TMEM lane quarter) for one query, 16 for four
+  // (four per quarter, one query each)
+  static constexpr int kEpiWarps = QG == 1 ? 4 : 16;
   static constexpr int kQPW = QG * 4 / kEpiWarps;   // queries per epilogue warp
   static constexpr int kThreads = 64 + 32 * kEpiWarps;
   static constexpr int kStages = QG == 1 ? 5 : 4;
