@@ -8,13 +8,15 @@
 // (M = 128, K = Di = 128, TMA-loaded with the 128-byte swizzle), B = the QG x 64
 // rotated query heads (N = 64 QG); the fp32 accumulator sits in TMEM (two
 // buffers so the epilogue of one tile overlaps the MMA of the next). Each
-// epilogue thread owns one TMEM lane = one key row: it reads its QG x 64 head
-// dots and applies ReLU and the head weights; with QG = 1 (decode) it also
+// epilogue thread owns one TMEM lane = one key row of its warp's queries: it
+// reads their 64 head dots each and applies ReLU and the head weights; with
+// QG = 1 (decode) it also
 // counts the top 12 bits of each score key into a per-CTA histogram that the
 // selection uses to place its threshold.
 //
-// Persistent kernel, one CTA per SM, 6 warps: warp 0 issues TMA, warp 1 issues
-// MMAs (one thread each), warps 2..5 run the epilogue. Work items are
+// Persistent kernel, one CTA per SM: warp 0 issues TMA, warp 1 issues MMAs
+// (one thread each), warps 2.. run the epilogue (4 for one query per group,
+// 16 for four: one query each, four per TMEM lane quarter). Work items are
 // (sequence, query group, 128-row tile), split into contiguous ranges so the
 // B operand (the query group's heads) is reloaded only when the group changes.
 // Every wait is bounded (tc.cuh); on a timeout the kernel sets *err and winds
