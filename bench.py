@@ -85,7 +85,9 @@ def write_traffic(csv_path: str, workload: str, captured_on: str, calls: int):
     for r in rows[hi + 1:]:
         if len(r) <= vi or r[mi] not in ("dram__bytes_read.sum", "dram__bytes_write.sum"):
             continue
-        name = re.sub(r"^.*?<unnamed>::", "", re.sub(r"\(.*", "", r[ki]).replace("void ", ""))
+        # (the anonymous namespace prints as "(anonymous namespace)::" or "<unnamed>::")
+        name = re.sub(r"\(.*", "", r[ki]).replace("void ", "")
+        name = re.sub(r"^.*?(unnamed>|anonymous namespace\))::", "", name)
         v = float(r[vi].replace(",", "")) * scale.get(r[ui] if ui is not None else "byte", 1)
         for call, prefixes in CALL_KERNELS.items():
             if name.startswith(prefixes):
