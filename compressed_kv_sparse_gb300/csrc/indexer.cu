@@ -754,7 +754,7 @@ __global__ void __launch_bounds__(NT, NT == 256 ? 4 : 1)
   // theta_S: at least k rows have S~ >= theta_S. Several blocks per query:
   // the lower edge of the scorer's histogram bin holding the k-th largest.
   // One block per query: a value of an evenly strided sample of the scores at
-  // a rank that leaves ~1.25 k rows above it; the filter below counts the rows
+  // a rank that leaves ~1.6 k rows above it; the filter below counts the rows
   // at or above it exactly, and too few sends the block to the full pass.
   if (threadIdx.x == 0) {
     s_misc[2] = 0;   // this block's candidate count
@@ -791,7 +791,10 @@ __global__ void __launch_bounds__(NT, NT == 256 ? 4 : 1)
     float *smp = scratch;
     for (uint32_t j = threadIdx.x; j < ns; j += blockDim.x) smp[j] = sc[j * stride + stride / 2];
     __syncthreads();   // (also syncs s_red / wsh / qsm)
-    const uint32_t rs = min(ns, ((k + stride - 1) / stride) * 5 / 4 + 4);
+    // (the sample's rank-r value has ~stride * r rows above it, give or take
+    // ~stride * sqrt(r): 1.6 k leaves about three of those above k, so the
+    // exact count rarely sends the block to the full pass)
+    const uint32_t rs = min(ns, ((k + stride - 1) / stride) * 8 / 5 + 8);
     uint32_t need_s;
     theta_s = key_to_float(radix_kth([&](uint32_t j) { return score_key(smp[j]); }, ns, rs,
                                      hist, sel, &need_s));
