@@ -8,8 +8,8 @@ Follows "【#3】ds4.c を読み解く":
 * §4 the per-token compressor steps: candidate (wkv) and score (wgate) come in
   projected; APE bias; store in the recurrent state; at a ratio boundary pool
   with per-channel softmax weights exp(score - max) (denominator 0 gives 0);
-  RMS normalisation; tail-only RoPE. Step 8 (FP8 / FP4 round trips) is not
-  part of this layer's definition here;
+  RMS normalisation; tail-only RoPE; step 8, the FP8 (attention lane) or
+  FP4 QAT (indexer lane) round trip, when the cache enables it (``qat.py``);
 * §5 ratio 4 keeps an 8-row frontier: token p is written to row 4 + p % 4, at
   (p + 1) % 4 == 0 the 8 rows are pooled into one row and rows 4..7 move to
   rows 0..3. With vLLM's page (c4a: one compressed token is a weighted sum of
@@ -30,6 +30,7 @@ Readings:
 import numpy as np
 
 from .numerics import round_store
+from .qat import attn_row_round_trip, index_row_round_trip
 from .rope import rope_tail
 
 RMS_EPS = 1e-6
@@ -64,13 +65,15 @@ def rms_norm(c, gamma, eps: float = RMS_EPS) -> np.ndarray:
 class Lane:
     """One compressor lane's recurrent state and output rows (numpy views)."""
 
-    def __init__(self, state_kv, state_score, comp, ape, gamma, n_rot):
+    def __init__(self, state_kv, state_score, comp, ape, gamma, n_rot, quant=None, pre=None):
         self.state_kv = state_kv          # [B, W, width] float32
         self.state_score = state_score    # [B, W, width] float32, pre-APE
         self.comp = comp                  # [B, cap, width] float64 (storage-exact)
         self.ape = ape                    # [W, width]
         self.gamma = gamma                # [width]
         self.n_rot = n_rot
+        self.quant = quant                # None, "fp8" (attention) or "fp4" (indexer)
+        self.pre = pre                    # optional [B, cap, width]: rows before step 8
 
 
 def lane_step(lane: Lane, ratio: int, p: int, cand, score, base: float, dtype: str):
@@ -83,6 +86,12 @@ def lane_step(lane: Lane, ratio: int, p: int, cand, score, base: float, dtype: s
     i = (p + 1) // ratio - 1
     pooled = softmax_pool(lane.state_kv, lane.state_score, lane.ape)
     row = rope_tail(rms_norm(pooled, lane.gamma), i * ratio, base, lane.n_rot)
+    if lane.pre is not None:
+        lane.pre[:, i] = row
+    if lane.quant == "fp8":
+        row = attn_row_round_trip(row, lane.n_rot)
+    elif lane.quant == "fp4":
+        row = index_row_round_trip(row)
     lane.comp[:, i] = round_store(row, dtype)
     if ratio == 4:
         lane.state_kv[:, 0:4] = lane.state_kv[:, 4:8]

@@ -16,6 +16,8 @@ Readings (the pages give no formula):
   r_h = dot_h if dot_h > 0 else +0; I = ((w_0 r_0) + (w_1 r_1)) + ... in
   ascending h, starting from +0. The rotated query is rounded to the storage
   dtype before scoring (it is a bf16 activation in the bf16 workloads).
+  With the QAT round trip enabled (§9: the indexer query takes it too), it
+  runs on the fp32 rotated query before that rounding (``qat.py``).
 * Visible rows for a query at position p: s < floor((p + 1) / 4) (a row emitted
   at p is visible to p: the append runs before the indexer).
 * Top-k: the k largest scores, ties to the lower row index; the kept indices
@@ -24,6 +26,7 @@ Readings (the pages give no formula):
 import numpy as np
 
 from .numerics import round_f32_to_bf16
+from .qat import fp4_qat_round_trip
 from .rope import rope_tail_f32
 
 
@@ -31,9 +34,13 @@ def visible_rows(ratio: int, p: int) -> int:
     return (p + 1) // ratio
 
 
-def rotate_index_query(q_idx, p, base: float, index_rot: int, dtype: str) -> np.ndarray:
-    """q' = tail rotation of q_idx[..., Hi, Di] at p (fp32 recipe), stored dtype."""
+def rotate_index_query(q_idx, p, base: float, index_rot: int, dtype: str,
+                       qat: bool = False) -> np.ndarray:
+    """q' = tail rotation of q_idx[..., Hi, Di] at p (fp32 recipe), then the
+    FP4 QAT round trip when enabled, stored dtype."""
     q = rope_tail_f32(np.asarray(q_idx, np.float32), p, base, index_rot)
+    if qat:
+        q = fp4_qat_round_trip(q)
     return round_f32_to_bf16(q) if dtype == "bf16" else q
 
 
@@ -68,10 +75,10 @@ def topk_select(scores, vis: int, k: int) -> np.ndarray:
 
 
 def index_topk_query(q_idx, w, keys, p: int, base: float, index_rot: int, dtype: str,
-                     k: int) -> np.ndarray:
+                     k: int, qat: bool = False) -> np.ndarray:
     """Top-k row list of one query at position p."""
     vis = min(visible_rows(4, p), keys.shape[0])
     if vis <= k:
         return topk_select(None, vis, k)
-    q_rot = rotate_index_query(q_idx, p, base, index_rot, dtype)
+    q_rot = rotate_index_query(q_idx, p, base, index_rot, dtype, qat)
     return topk_select(index_scores(q_rot, w, keys[:vis]), vis, k)

@@ -8,12 +8,20 @@ step (§4-§7): append (raw row, both lanes' compressor) -> indexer top-k
 (ratio 4) -> attention. A prefill chunk keeps the ring as it was before the
 chunk until its attention is done (early queries of the chunk still need the
 older window rows) and then writes the chunk's last rows into the ring.
+
+``qat`` enables step 8 of the compressor (§4, §9): bit 0 the FP8 round trip of
+compressed attention rows, bit 1 the FP4 QAT round trip of compressed indexer
+rows and of the indexer query (``qat.py``). ``keep_pre`` records every
+compressed row as it was before that step (``attn_pre`` / ``index_pre``).
 """
 import numpy as np
 
 from .attention import attention_query, comp_row_ids, window_positions
 from .compressor import Lane, lane_step, raw_rows
 from .indexer import index_topk_query
+
+QAT_FP8_ATTN = 1
+QAT_FP4_INDEX = 2
 
 
 class OracleCache:
@@ -25,7 +33,7 @@ class OracleCache:
     def __init__(self, *, ratio, head_dim, n_rot, cap_raw, base, dtype, n_tokens,
                  raw_kv, index_dim=0, index_rot=0, attn_comp_kv=None, attn_state_kv=None,
                  attn_state_score=None, index_comp_kv=None, index_state_kv=None,
-                 index_state_score=None):
+                 index_state_score=None, qat=0, keep_pre=False):
         self.ratio, self.head_dim, self.n_rot = ratio, head_dim, n_rot
         self.cap_raw, self.base, self.dtype = cap_raw, base, dtype
         self.index_dim, self.index_rot = index_dim, index_rot
@@ -36,6 +44,9 @@ class OracleCache:
         self.attn_comp_kv, self.index_comp_kv = f64(attn_comp_kv), f64(index_comp_kv)
         self.attn_state_kv, self.attn_state_score = f32(attn_state_kv), f32(attn_state_score)
         self.index_state_kv, self.index_state_score = f32(index_state_kv), f32(index_state_score)
+        self.qat = qat
+        pre = lambda a: None if (a is None or not keep_pre) else np.full(a.shape, np.nan)
+        self.attn_pre, self.index_pre = pre(self.attn_comp_kv), pre(self.index_comp_kv)
 
     @property
     def n_comp(self) -> int:
@@ -45,11 +56,13 @@ class OracleCache:
         out = []
         if self.ratio:
             out.append((Lane(self.attn_state_kv, self.attn_state_score, self.attn_comp_kv,
-                             w["ape_attn"], w["gamma_attn"], self.n_rot),
+                             w["ape_attn"], w["gamma_attn"], self.n_rot,
+                             "fp8" if self.qat & QAT_FP8_ATTN else None, self.attn_pre),
                         "attn_cand", "attn_score"))
         if self.ratio == 4:
             out.append((Lane(self.index_state_kv, self.index_state_score, self.index_comp_kv,
-                             w["ape_idx"], w["gamma_idx"], self.index_rot),
+                             w["ape_idx"], w["gamma_idx"], self.index_rot,
+                             "fp4" if self.qat & QAT_FP4_INDEX else None, self.index_pre),
                         "idx_cand", "idx_score"))
         return out
 
@@ -91,7 +104,8 @@ def index_topk(c: OracleCache, pos0: int, q_idx, w, k: int, queries=None) -> np.
     todo = queries if queries is not None else [(b, t) for b in range(B) for t in range(T)]
     for b, t in todo:
         out[b, t] = index_topk_query(q_idx[b, t], w[b, t], c.index_comp_kv[b], pos0 + t,
-                                     c.base, c.index_rot, c.dtype, k)
+                                     c.base, c.index_rot, c.dtype, k,
+                                     bool(c.qat & QAT_FP4_INDEX))
     return out
 
 

@@ -30,12 +30,13 @@ def gpu_cache(shape: synth.LayerShape, batch: int, comp_cap: int, rope_max_pos: 
     return c
 
 
-def oracle_cache(shape: synth.LayerShape, hist, n_tokens: int):
+def oracle_cache(shape: synth.LayerShape, hist, n_tokens: int, qat: int = 0,
+                 keep_pre: bool = False):
     from oracle.layer import OracleCache
     return OracleCache(ratio=shape.ratio, head_dim=shape.head_dim, n_rot=shape.n_rot,
                        cap_raw=shape.cap_raw, base=shape.rope_base, dtype=shape.dtype,
                        n_tokens=n_tokens, index_dim=shape.index_dim, index_rot=shape.index_rot,
-                       **{k: np_(v) for k, v in hist.items()})
+                       qat=qat, keep_pre=keep_pre, **{k: np_(v) for k, v in hist.items()})
 
 
 def to_dev(inp, device="cuda"):
