@@ -123,7 +123,7 @@ def peaks():
 class Runner:
     """Builds every layer's cache and inputs on the device and runs steps."""
 
-    def __init__(self, wl: synth.Workload, device, rank: int = 0):
+    def __init__(self, wl: synth.Workload, device, rank: int = 0, qat: bool = False):
         from compressed_kv_sparse_gb300 import lib
         self.lib, self.wl, self.dev = lib, wl, device
         self.decode = wl.mode == "decode"
@@ -140,7 +140,8 @@ class Runner:
             c = lib.LayerCache(ratio=s.ratio, head_dim=s.head_dim, n_rot=s.n_rot, batch=B,
                                comp_cap=cap, dtype=s.dtype, base=s.rope_base,
                                rope_max_pos=end + 1, index_dim=s.index_dim,
-                               index_rot=s.index_rot, cap_raw=s.cap_raw, device=device)
+                               index_rot=s.index_rot, cap_raw=s.cap_raw,
+                               qat=qat_flags(s.ratio) if qat else 0, device=device)
             hist = synth.cache_history(seed_wl, il, self.p0, comp_cap=cap, device=device)
             c.load_state(hist, self.p0)
             del hist
@@ -321,10 +322,17 @@ def flush_l2(buf):
     buf.add_(1)
 
 
+def qat_flags(ratio: int) -> int:
+    """Step-8 flags of a layer: FP8 attention rows on compressed layers, FP4
+    QAT of the indexer lane on ratio-4 layers."""
+    from compressed_kv_sparse_gb300 import lib
+    return (lib.QAT_FP8_ATTN if ratio else 0) | (lib.QAT_FP4_INDEX if ratio == 4 else 0)
+
+
 def run_gpu(args, wl, rank, world, device):
     hbm, bf16, bf16s, peak_kind = peaks()
     lib_mod = __import__("compressed_kv_sparse_gb300.lib", fromlist=["lib"])
-    R = Runner(wl, device, rank)
+    R = Runner(wl, device, rank, qat=args.qat)
     step_bytes = sum(v[0] for v in R.algorithmic().values())
     flush = None
     if step_bytes < 512e6:      # working set below ~4x L2: flush between steps
@@ -492,6 +500,8 @@ def run_gpu(args, wl, rank, world, device):
                       "l2": "flushed between steps" if flush is not None
                       else "inputs larger than L2 (algorithmic %.2f GB per step)" % (step_bytes / 1e9),
                       "cuda_graph": use_graph, "parallelism": f"replicas x{world}",
+                      "step8_round_trips": "fp8 attention rows + fp4 indexer rows/queries"
+                      if args.qat else "off",
                       "algorithmic_GB_per_step": step_bytes / 1e9,
                       "step_GB/s": step_bytes / (ms_step / 1e3) / 1e9},
            "roofline": roof, "calls": calls,
@@ -604,6 +614,9 @@ def main():
     ap.add_argument("--workload", default="flash43", choices=sorted(WORKLOADS))
     ap.add_argument("--impl", default="gpu", choices=["gpu", "reference"])
     ap.add_argument("--no-graph", action="store_true")
+    ap.add_argument("--qat", action="store_true",
+                    help="compressor step 8 on: FP8 round trip of attention rows, FP4 QAT "
+                         "round trip of indexer rows and queries")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--write-traffic", metavar="NCU_CSV",
                     help="record per-call DRAM bytes of --workload from an ncu CSV and exit")

@@ -42,12 +42,21 @@ ds4a_status check_cache(const ds4a_layer_cache *c) {
     if (!c->index_norm || !c->index_norm_max) return DS4A_ERR_ARG;
     if (!c->index_rope_cos || !c->index_rope_sin) return DS4A_ERR_ARG;
   }
+  if (c->qat & ~(DS4A_QAT_FP8_ATTN | DS4A_QAT_FP4_INDEX)) return DS4A_ERR_ARG;
+  if ((c->qat & DS4A_QAT_FP8_ATTN) && c->ratio == 0) return DS4A_ERR_ARG;
+  if (c->qat & DS4A_QAT_FP4_INDEX) {
+    if (c->ratio != 4) return DS4A_ERR_ARG;
+    if (c->index_dim < 32 || (c->index_dim & (c->index_dim - 1))) return DS4A_ERR_SHAPE;
+  }
   return DS4A_OK;
 }
 
 ds4a_status cuda_status(cudaError_t e) {
   return note_error(e) == cudaSuccess ? DS4A_OK : DS4A_ERR_CUDA;
 }
+
+// c = 1/sqrt(n) rounded to fp32, the Hadamard normalisation of the FP4 round trip.
+float hadamard_scale(uint32_t n) { return (float)(1.0 / std::sqrt((double)n)); }
 
 uint32_t comp_rows(const ds4a_layer_cache *c, uint32_t n_tokens) {
   return c->ratio ? n_tokens / c->ratio : 0;
@@ -181,12 +190,14 @@ ds4a_status ds4a_compress_append(ds4a_layer_cache *c, uint32_t pos0, uint32_t T,
   if (c->ratio) {
     a.lane[0] = LaneArgs{c->head_dim, c->n_rot, c->attn_comp_kv, c->attn_state_kv,
                          c->attn_state_score, c->rope_cos, c->rope_sin, attn_cand, attn_score,
-                         ape_attn, gamma_attn, nullptr, nullptr};
+                         ape_attn, gamma_attn, nullptr, nullptr,
+                         (c->qat & DS4A_QAT_FP8_ATTN) ? 1u : 0u, 0.f};
   }
   if (c->ratio == 4) {
     a.lane[1] = LaneArgs{c->index_dim, c->index_rot, c->index_comp_kv, c->index_state_kv,
                          c->index_state_score, c->index_rope_cos, c->index_rope_sin, idx_cand,
-                         idx_score, ape_idx, gamma_idx, c->index_norm, c->index_norm_max};
+                         idx_score, ape_idx, gamma_idx, c->index_norm, c->index_norm_max,
+                         (c->qat & DS4A_QAT_FP4_INDEX) ? 2u : 0u, hadamard_scale(c->index_dim)};
   }
   st = cuda_status(launch_append(a, reinterpret_cast<cudaStream_t>(stream)));
   if (st) return st;
@@ -246,6 +257,8 @@ ds4a_status ds4a_index_topk(const ds4a_layer_cache *c, uint32_t pos0, uint32_t T
   a.topk = topk;
   a.ws = ws;
   a.ws_bytes = ws_bytes;
+  a.qat = (c->qat & DS4A_QAT_FP4_INDEX) != 0;
+  a.had_c = hadamard_scale(c->index_dim);
   return cuda_status(launch_index_topk(a, reinterpret_cast<cudaStream_t>(stream)));
 }
 

@@ -15,12 +15,13 @@
 // parallel, one block per row, reading window tokens from the chunk inputs or,
 // for tokens before pos0, from the state as it was before the chunk; a second
 // launch then writes the state as the token-by-token process would leave it.
-#include "common.cuh"
+#include "quant.cuh"
 
 namespace ds4a {
 namespace {
 
 constexpr int kThreads = 256;
+constexpr int kMaxQatWidth = 256;      // indexer rows with the FP4 round trip
 constexpr float kRmsEps = 1e-6f;
 constexpr int kMaxPairsPerThread = 2;  // width <= 1024
 
@@ -28,9 +29,10 @@ struct SlotVal {
   float kv, score;
 };
 
-// Pool window slots per channel, RMS-normalise, rotate at `pos` and store row
-// i of the lane. get(s, c) returns slot s of channel c (score without APE,
-// -inf when empty). Called by every thread of the block (uniform).
+// Pool window slots per channel, RMS-normalise, rotate at `pos`, apply the
+// lane's step-8 round trip (if any) and store row i of the lane. get(s, c)
+// returns slot s of channel c (score without APE, -inf when empty). Called by
+// every thread of the block (uniform).
 template <typename T, typename Get>
 __device__ void pool_norm_rope_store(const LaneArgs &L, uint32_t W, uint32_t b, uint32_t i,
                                      uint32_t comp_cap, uint32_t pos, Get get, float *red) {
@@ -73,8 +75,6 @@ __device__ void pool_norm_rope_store(const LaneArgs &L, uint32_t W, uint32_t b, 
   ss = block_sum(ss, red);
   const float inv = 1.0f / sqrtf(ss / (float)width + kRmsEps);
   T *row = comp + ((size_t)b * comp_cap + i) * width;
-  float st[kMaxPairsPerThread][2];   // the stored (rounded) values, for the row norm
-  float mx = 0.f;
 #pragma unroll
   for (int k = 0; k < kMaxPairsPerThread; ++k) {
     const uint32_t j = threadIdx.x + k * blockDim.x;
@@ -91,10 +91,56 @@ __device__ void pool_norm_rope_store(const LaneArgs &L, uint32_t W, uint32_t b, 
       a = ra;
       bb = rb;
     }
-    st_elem(row, c, a);
-    st_elem(row, c + 1, bb);
-    st[k][0] = round_to(a, row);
-    st[k][1] = round_to(bb, row);
+    y[k][0] = a;
+    y[k][1] = bb;
+  }
+  // step 8 (uniform branch): FP8 on the non-RoPE dims, one warp per 64-dim
+  // block (thread j holds dims 2j, 2j + 1), or the FP4 QAT round trip of the
+  // whole row through shared memory
+  if (L.quant == 1) {
+#pragma unroll
+    for (int k = 0; k < kMaxPairsPerThread; ++k) {
+      const uint32_t j = threadIdx.x + k * blockDim.x, c = 2 * j;
+      const bool in = j < npair && c < n_nope;
+      const float am = warp_max(in ? fmaxf(fabsf(y[k][0]), fabsf(y[k][1])) : 0.f);
+      const int ke = block_scale_exp(am, kE4M3);
+      if (in) {
+        y[k][0] = quant_dequant(y[k][0], ke, kE4M3);
+        y[k][1] = quant_dequant(y[k][1], ke, kE4M3);
+      }
+    }
+  } else if (L.quant == 2) {
+    __shared__ float qbuf[kMaxQatWidth];
+#pragma unroll
+    for (int k = 0; k < kMaxPairsPerThread; ++k) {
+      const uint32_t j = threadIdx.x + k * blockDim.x;
+      if (j < npair) {
+        qbuf[2 * j] = y[k][0];
+        qbuf[2 * j + 1] = y[k][1];
+      }
+    }
+    __syncthreads();
+    fp4_qat_smem(qbuf, width, L.had_c);
+#pragma unroll
+    for (int k = 0; k < kMaxPairsPerThread; ++k) {
+      const uint32_t j = threadIdx.x + k * blockDim.x;
+      if (j < npair) {
+        y[k][0] = qbuf[2 * j];
+        y[k][1] = qbuf[2 * j + 1];
+      }
+    }
+  }
+  float st[kMaxPairsPerThread][2];   // the stored (rounded) values, for the row norm
+  float mx = 0.f;
+#pragma unroll
+  for (int k = 0; k < kMaxPairsPerThread; ++k) {
+    const uint32_t j = threadIdx.x + k * blockDim.x;
+    if (j >= npair) continue;
+    const uint32_t c = 2 * j;
+    st_elem(row, c, y[k][0]);
+    st_elem(row, c + 1, y[k][1]);
+    st[k][0] = round_to(y[k][0], row);
+    st[k][1] = round_to(y[k][1], row);
     mx = fmaxf(mx, fmaxf(fabsf(st[k][0]), fabsf(st[k][1])));
   }
   if (L.norm) {   // uniform: the indexer lane records the row's norm

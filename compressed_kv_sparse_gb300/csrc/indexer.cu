@@ -23,7 +23,7 @@
 // radix select. The kept set is therefore the exact one.
 #include <cmath>
 
-#include "common.cuh"
+#include "quant.cuh"
 
 namespace ds4a {
 namespace {
@@ -83,8 +83,10 @@ inline TcWs tc_ws_split(void *ws, uint32_t nq, uint32_t B, uint32_t Hi, uint32_t
 // bf16 layers: q' = rotated query rounded to bf16 (fp32 recipe), one thread
 // per `per` dims (a 16-byte unit of 8, or a pair when the query is not 16-byte
 // aligned); the same grid clears the call's counters (error word, control
-// words and, when the scorer builds them, histograms).
-__global__ void index_qbf_kernel(IndexArgs a, TcWs w, bool clear_hist, uint32_t per) {
+// words and, when the scorer builds them, histograms). With the FP4 QAT round
+// trip, units are always 8 dims (loaded one by one when `vec` is false) and
+// the Di / 8 lanes of a head row run the transform together.
+__global__ void index_qbf_kernel(IndexArgs a, TcWs w, bool clear_hist, uint32_t per, bool vec) {
   pdl_wait();
   pdl_trigger();
   const uint32_t Hi = a.n_heads, Di = a.dim, n_nope = Di - a.rot;
@@ -114,7 +116,43 @@ __global__ void index_qbf_kernel(IndexArgs a, TcWs w, bool clear_hist, uint32_t 
       w4[e] = *reinterpret_cast<const uint32_t *>(&r);
     }
   };
-  if (per == 8) {
+  if (a.qat) {   // uniform; per == 8, a head row is an aligned group of upr lanes
+    float v[8];
+    if (vec) {
+      const uint4 q4 = reinterpret_cast<const uint4 *>(a.q_idx)[i];
+      const uint32_t w4[4] = {q4.x, q4.y, q4.z, q4.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        v[2 * e] = __uint_as_float(w4[e] << 16);
+        v[2 * e + 1] = __uint_as_float(w4[e] & 0xFFFF0000u);
+      }
+    } else {
+      const __nv_bfloat16 *q = static_cast<const __nv_bfloat16 *>(a.q_idx) + (size_t)i * 8;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) v[e] = __bfloat162float(q[e]);
+    }
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const uint32_t c = c0 + 2 * e;
+      if (c < n_nope) continue;
+      const uint32_t fi = (c - n_nope) / 2;
+      const float co = a.cos[(size_t)p * (a.rot / 2) + fi];
+      const float si = a.sin[(size_t)p * (a.rot / 2) + fi];
+      const float x0 = v[2 * e], x1 = v[2 * e + 1];
+      v[2 * e] = __fsub_rn(__fmul_rn(x0, co), __fmul_rn(x1, si));
+      v[2 * e + 1] = __fadd_rn(__fmul_rn(x0, si), __fmul_rn(x1, co));
+    }
+    const uint32_t lane = threadIdx.x & 31;
+    const uint32_t mask = upr == 32 ? 0xffffffffu : ((1u << upr) - 1u) << (lane & ~(upr - 1u));
+    fp4_qat_lanes8(v, lane & (upr - 1u), upr, mask, a.had_c);
+    uint32_t o4[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const __nv_bfloat162 r = __floats2bfloat162_rn(v[2 * e], v[2 * e + 1]);
+      o4[e] = *reinterpret_cast<const uint32_t *>(&r);
+    }
+    reinterpret_cast<uint4 *>(w.qbf)[i] = make_uint4(o4[0], o4[1], o4[2], o4[3]);
+  } else if (per == 8) {
     const uint4 v = reinterpret_cast<const uint4 *>(a.q_idx)[i];
     uint32_t w4[4] = {v.x, v.y, v.z, v.w};
     if (c0 + 8 > n_nope) rot(w4, 4);
@@ -133,6 +171,36 @@ __global__ void index_qrot_kernel(IndexArgs a, float *qrot) {
   const T *q = static_cast<const T *>(a.q_idx) + (size_t)qi * Hi * Di;
   float *dst = qrot + (size_t)qi * Di * Hp;
   const T *tag = nullptr;
+  if (a.qat) {   // uniform: one head at a time through shared memory
+    __shared__ float buf[256];
+    for (uint32_t h = 0; h < Hp; ++h) {
+      if (h >= Hi) {
+        for (uint32_t c = threadIdx.x; c < Di; c += blockDim.x) dst[(size_t)c * Hp + h] = 0.f;
+        continue;
+      }
+      for (uint32_t pr = threadIdx.x; pr < Di / 2; pr += blockDim.x) {
+        const uint32_t c = 2 * pr;
+        float x0 = ld_f32(q, (size_t)h * Di + c), x1 = ld_f32(q, (size_t)h * Di + c + 1);
+        if (c >= n_nope) {
+          const uint32_t fi = (c - n_nope) / 2;
+          const float co = a.cos[(size_t)p * (a.rot / 2) + fi];
+          const float si = a.sin[(size_t)p * (a.rot / 2) + fi];
+          const float r0 = __fsub_rn(__fmul_rn(x0, co), __fmul_rn(x1, si));
+          const float r1 = __fadd_rn(__fmul_rn(x0, si), __fmul_rn(x1, co));
+          x0 = r0;
+          x1 = r1;
+        }
+        buf[c] = x0;
+        buf[c + 1] = x1;
+      }
+      __syncthreads();
+      fp4_qat_smem(buf, Di, a.had_c);
+      for (uint32_t c = threadIdx.x; c < Di; c += blockDim.x)
+        dst[(size_t)c * Hp + h] = round_to(buf[c], tag);
+      __syncthreads();
+    }
+    return;
+  }
   for (uint32_t pr = threadIdx.x; pr < Hp * Di / 2; pr += blockDim.x) {
     const uint32_t h = pr / (Di / 2), c = 2 * (pr % (Di / 2));
     float x0 = 0.f, x1 = 0.f;
@@ -1144,7 +1212,8 @@ cudaError_t launch_index_tc(const IndexArgs &a, cudaStream_t s) {
   TcWs w = tc_ws_split(a.ws, nq, a.batch, a.n_heads, a.dim, a.comp_cap, nullptr);
   // q' in 16-byte units of 8 dims (4-byte pairs when the query is not
   // 16-byte aligned)
-  const uint32_t per = reinterpret_cast<uintptr_t>(a.q_idx) % 16 == 0 && a.dim % 8 == 0 ? 8u : 2u;
+  const bool vec = reinterpret_cast<uintptr_t>(a.q_idx) % 16 == 0 && a.dim % 8 == 0;
+  const uint32_t per = vec || a.qat ? 8u : 2u;
   if ((size_t)nq * a.n_heads * a.dim >= (1ull << 31)) return cudaErrorInvalidValue;
   // the scorer builds key histograms when several select blocks share a
   // query; with one block per query the selection samples its threshold
@@ -1153,7 +1222,7 @@ cudaError_t launch_index_tc(const IndexArgs &a, cudaStream_t s) {
   if (scorer_hist && (size_t)nq * (kHistBins / 4) > nthreads) nthreads = (size_t)nq * (kHistBins / 4);
   if ((size_t)nq * 4 > nthreads) nthreads = (size_t)nq * 4;
   cudaError_t eq = launch_pdl(index_qbf_kernel, dim3((unsigned)((nthreads + 255) / 256)),
-                              dim3(256), 0, s, a, w, scorer_hist, per);
+                              dim3(256), 0, s, a, w, scorer_hist, per, vec);
   if (eq != cudaSuccess) return eq;
   note_launches(1);
   const uint32_t vis_max = min((a.pos0 + a.T) / 4, a.n_comp);

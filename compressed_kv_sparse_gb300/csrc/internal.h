@@ -58,6 +58,8 @@ struct LaneArgs {
   const void *ape, *gamma;        // [W][width], [width]
   float *norm;                    // [B][comp_cap] row norms (indexer lane) or NULL
   uint32_t *norm_max;             // [B] float bits of the largest norm
+  uint32_t quant;                 // step 8: 0 none, 1 FP8 non-RoPE dims, 2 FP4 QAT
+  float had_c;                    // 1/sqrt(width) in fp32 (quant 2)
 };
 
 struct AppendArgs {
@@ -82,6 +84,8 @@ struct IndexArgs {
   int32_t *topk;
   void *ws;
   size_t ws_bytes;
+  bool qat;                       // FP4 QAT round trip of the rotated query
+  float had_c;                    // 1/sqrt(dim) in fp32
 };
 size_t index_ws_bytes(int dtype, uint32_t batch, uint32_t T, uint32_t n_heads, uint32_t dim,
                       uint32_t comp_cap);

@@ -44,7 +44,11 @@ class LayerCacheC(ctypes.Structure):
         ("index_state_score", ctypes.c_void_p), ("index_norm", ctypes.c_void_p),
         ("index_norm_max", ctypes.c_void_p), ("rope_cos", ctypes.c_void_p),
         ("rope_sin", ctypes.c_void_p), ("index_rope_cos", ctypes.c_void_p),
-        ("index_rope_sin", ctypes.c_void_p), ("rope_max_pos", ctypes.c_uint32)]
+        ("index_rope_sin", ctypes.c_void_p), ("rope_max_pos", ctypes.c_uint32),
+        ("qat", ctypes.c_uint32)]
+
+QAT_FP8_ATTN = 1    # DS4A_QAT_FP8_ATTN
+QAT_FP4_INDEX = 2   # DS4A_QAT_FP4_INDEX
 
 
 EXPORTS = {
@@ -143,7 +147,7 @@ class LayerCache:
 
     def __init__(self, *, ratio: int, head_dim: int, n_rot: int, batch: int, comp_cap: int,
                  dtype: str, base: float, rope_max_pos: int, index_dim: int = 0,
-                 index_rot: int = 0, cap_raw: int = 128, device="cuda"):
+                 index_rot: int = 0, cap_raw: int = 128, qat: int = 0, device="cuda"):
         td = {"f32": torch.float32, "bf16": torch.bfloat16}[dtype]
         self.dtype, self.torch_dtype = dtype, td
         self.ratio, self.head_dim, self.n_rot = ratio, head_dim, n_rot
@@ -182,7 +186,7 @@ class LayerCache:
             index_state_score=_ptr(self.index_state_score), index_norm=_ptr(self.index_norm),
             index_norm_max=_ptr(self.index_norm_max), rope_cos=_ptr(self.rope_cos),
             rope_sin=_ptr(self.rope_sin), index_rope_cos=_ptr(self.index_rope_cos),
-            index_rope_sin=_ptr(self.index_rope_sin), rope_max_pos=rope_max_pos)
+            index_rope_sin=_ptr(self.index_rope_sin), rope_max_pos=rope_max_pos, qat=qat)
 
     @property
     def n_tokens(self) -> int:

@@ -91,6 +91,14 @@ typedef enum { DS4A_F32 = 0, DS4A_BF16 = 1 } ds4a_dtype;
  *                    layers with ratio != 0, normal base otherwise (page §8).
  *  index_rope_cos/sin [rope_max_pos][index_rot/2] fp32 (same base), ratio 4.
  *  rope_max_pos      rows of the tables; every position used must be below it.
+ *  qat               step 8 of the compressor (page §4 step 8, §9), a bit set:
+ *                    DS4A_QAT_FP8_ATTN (ratio != 0): every compressed attention
+ *                    row is quantised to FP8 E4M3 and back on its leading
+ *                    head_dim - n_rot dims before it is stored;
+ *                    DS4A_QAT_FP4_INDEX (ratio 4, Di a power of two >= 32):
+ *                    compressed indexer rows, and in ds4a_index_topk the
+ *                    rotated queries, take the FP4 QAT round trip. 0 = off.
+ *                    Scales and arithmetic: see DS4A_QAT_FP8_ATTN below.
  *
  * State layout: ratio 4 keeps the last complete group of 4 tokens in slots
  * 0..3 and token p of the current group in slot 4 + p % 4 (page §5's 8-row
@@ -111,7 +119,28 @@ typedef struct {
   const float *rope_cos, *rope_sin;
   const float *index_rope_cos, *index_rope_sin;
   uint32_t rope_max_pos;
+  uint32_t qat;
 } ds4a_layer_cache;
+
+/*
+ * Step-8 round trips (page §9: E4M3 FP8 on the non-RoPE part of attention
+ * rows; Hadamard-128 plus FP4 activation quantisation on indexer rows and the
+ * indexer query). The pages give no granularity; this library fixes it:
+ *  FP8: blocks of 64 consecutive non-RoPE dims (the last may be shorter), each
+ *       with the scale 2^k, k the smallest integer >= -127 such that
+ *       amax <= 448 * 2^k; each dim becomes the E4M3 value nearest x / 2^k
+ *       (ties to the even code) times 2^k. RoPE dims are unchanged.
+ *  FP4: z = c * H x, with H the Sylvester Hadamard matrix of order Di,
+ *       applied as radix-2 butterflies over stages h = 1, 2, ..., Di/2 in fp32,
+ *       and c = 1/sqrt(Di) rounded to fp32. z is cut into blocks of 32, each
+ *       with the scale 2^k (amax <= 6 * 2^k, k >= -127) and the nearest E2M1
+ *       value. The result is x' = c * H z'.
+ * The input is the fp32 row (after RMSNorm and tail RoPE) or query (after its
+ * tail rotation). The output is rounded once to dtype; FP8 values are exact in
+ * both dtypes. The cache keeps the dequantised values in dtype.
+ */
+#define DS4A_QAT_FP8_ATTN 1u
+#define DS4A_QAT_FP4_INDEX 2u
 
 /* Workspace selectors for ds4a_workspace_bytes. */
 enum { DS4A_CALL_APPEND = 0, DS4A_CALL_INDEX_TOPK = 1, DS4A_CALL_ATTN_DECODE = 2,
@@ -180,7 +209,8 @@ ds4a_status ds4a_compress_append(ds4a_layer_cache *cache, uint32_t pos0, uint32_
  *  ws      workspace of ds4a_workspace_bytes(DS4A_CALL_INDEX_TOPK, ...) bytes.
  *
  * q' = tail rotation of q_idx at p, computed in fp32 (one rounding per
- * operation) and rounded to dtype. The selection is exact with respect to the
+ * operation), then the FP4 QAT round trip when cache->qat has
+ * DS4A_QAT_FP4_INDEX, and rounded to dtype. The selection is exact with respect to the
  * fp32 score defined by: dot_h accumulated in ascending d with separately
  * rounded products and sums, ReLU to +0, then w_h * relu_h summed in ascending
  * h from +0. Requires pos0 + T <= n_tokens.

@@ -19,12 +19,12 @@ def rel_l2(got, want):
 
 
 def gpu_cache(shape: synth.LayerShape, batch: int, comp_cap: int, rope_max_pos: int,
-              hist=None, n_tokens: int = 0, device="cuda"):
+              hist=None, n_tokens: int = 0, device="cuda", qat: int = 0):
     from compressed_kv_sparse_gb300 import lib
     c = lib.LayerCache(ratio=shape.ratio, head_dim=shape.head_dim, n_rot=shape.n_rot,
                        batch=batch, comp_cap=comp_cap, dtype=shape.dtype, base=shape.rope_base,
                        rope_max_pos=rope_max_pos, index_dim=shape.index_dim,
-                       index_rot=shape.index_rot, cap_raw=shape.cap_raw, device=device)
+                       index_rot=shape.index_rot, cap_raw=shape.cap_raw, qat=qat, device=device)
     if hist is not None:
         c.load_state({k: v.to(device) for k, v in hist.items()}, n_tokens)
     return c

@@ -92,6 +92,28 @@ def _fake_cache(ratio=4, n_tokens=10, dtype=lib.DS4A_BF16):
                            index_rope_sin=fake, rope_max_pos=1000)
 
 
+def test_cache_struct_layout_matches_header(tmp_path):
+    """The binding's struct has the header's field offsets and size (a C
+    program compiled against include/ds4a.h prints them)."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    fields = [f[0] for f in lib.LayerCacheC._fields_]
+    src = tmp_path / "layout.c"
+    src.write_text('#include <stddef.h>\n#include <stdio.h>\n#include "ds4a.h"\nint main(void){'
+                   + "".join(f'printf("%zu ", offsetof(ds4a_layer_cache, {f}));' for f in fields)
+                   + 'printf("%zu\\n", sizeof(ds4a_layer_cache));return 0;}\n')
+    inc = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include")
+    exe = tmp_path / "layout"
+    subprocess.run([cc, "-I", inc, str(src), "-o", str(exe)], check=True)
+    got = [int(x) for x in subprocess.run([str(exe)], check=True, capture_output=True,
+                                          text=True).stdout.split()]
+    want = [getattr(lib.LayerCacheC, f).offset for f in fields] + [ctypes.sizeof(lib.LayerCacheC)]
+    assert got == want
+
+
 def test_argument_checks_reject_before_launch(L):
     fake = 0x1000
     c = _fake_cache()
@@ -129,6 +151,16 @@ def test_argument_checks_reject_before_launch(L):
     c128 = _fake_cache(ratio=128)
     assert L.ds4a_index_topk(ctypes.byref(c128), 9, 1, fake, fake, 64, 512, fake, fake,
                              1 << 30, None) == -1
+    # step-8 flags: unknown bit, FP4 off ratio 4, FP4 with Di not a power of two,
+    # FP8 on a window-only layer
+    for ratio, q, dim, want in ((4, 4, 128, -1), (128, 2, 128, -1), (4, 2, 96, -2),
+                                (0, 1, 128, -1)):
+        bad = _fake_cache(ratio=ratio)
+        bad.qat, bad.index_dim = q, dim
+        assert L.ds4a_compress_append(ctypes.byref(bad), 10, 1, *P, None, None) == want
+    ok = _fake_cache()
+    ok.qat = lib.QAT_FP8_ATTN | lib.QAT_FP4_INDEX
+    assert L.ds4a_compress_append(ctypes.byref(ok), 9, 1, *P, None, None) == -4  # past the flag check
     # attention: position, missing top-k on a ratio-4 layer, workspace
     assert L.ds4a_sparse_attn_decode(r, 8, fake, 64, fake, 512, 0.1, fake, fake, 1 << 30,
                                      None) == -4
