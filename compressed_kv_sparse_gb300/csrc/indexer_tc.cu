@@ -54,6 +54,7 @@ struct Cfg {
 
 struct ScoreParams {
   uint32_t batch, T, pos0, comp_cap, n_comp, n_groups, tiles_per, total_items;
+  uint32_t cta_per_group;   // > 0: that many CTAs per (sequence, group), none crossing one
   const __nv_bfloat16 *w;   // [B][T][Hi]
   float *scores;            // [B][T][comp_cap]
   uint32_t *hist;           // [B*T][4096] counts of the top 12 bits of the score keys
@@ -102,9 +103,20 @@ __global__ void __launch_bounds__(Cfg<QG>::kThreads, 1)
   uint64_t *epi_bar = reinterpret_cast<uint64_t *>(tmem_slot + 2);
 
   const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const uint32_t per = (P.total_items + gridDim.x - 1) / gridDim.x;
-  const uint32_t it0 = blockIdx.x * per;
-  const uint32_t it1 = min(P.total_items, it0 + per);
+  // work range: contiguous items, or (cta_per_group > 0) an even share of one
+  // (sequence, group)'s visible tiles, so that no CTA changes query mid-range
+  uint32_t it0, it1;
+  if (P.cta_per_group) {
+    const uint32_t bg = blockIdx.x / P.cta_per_group, j = blockIdx.x % P.cta_per_group;
+    const uint32_t last = min(P.T, (bg % P.n_groups + 1) * QG) - 1;
+    const uint32_t nt = min(P.tiles_per, (vis_of(P, last) + kRows - 1) / kRows);
+    it0 = bg * P.tiles_per + j * nt / P.cta_per_group;
+    it1 = bg * P.tiles_per + (j + 1) * nt / P.cta_per_group;
+  } else {
+    const uint32_t per = (P.total_items + gridDim.x - 1) / gridDim.x;
+    it0 = min(P.total_items, blockIdx.x * per);
+    it1 = min(P.total_items, it0 + per);
+  }
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kStages; ++s) {
@@ -247,12 +259,20 @@ __global__ void __launch_bounds__(Cfg<QG>::kThreads, 1)
     // added to the global one when the query changes
     auto flush_hist = [&](int32_t q) {
       if (!group_sync(epi_bar, epi_phase, P.err)) return false;
-      for (uint32_t i = et; i < 4096; i += 128) {
-        const uint32_t c = shist[i];
-        if (c) {
-          if (q >= 0 && P.hist) atomicAdd(&P.hist[(size_t)q * 4096 + i], c);
-          shist[i] = 0;
-        }
+      // eight 16-byte loads per thread in flight at once, then the adds
+      uint4 *h4 = reinterpret_cast<uint4 *>(shist);
+      uint4 v[8];
+#pragma unroll
+      for (uint32_t j = 0; j < 8; ++j) v[j] = h4[et + 128 * j];
+#pragma unroll
+      for (uint32_t j = 0; j < 8; ++j) {
+        const uint32_t c[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+        if ((c[0] | c[1] | c[2] | c[3]) == 0u) continue;
+        const uint32_t i0 = 4 * (et + 128 * j);
+#pragma unroll
+        for (uint32_t e = 0; e < 4; ++e)
+          if (c[e] && q >= 0 && P.hist) atomicAdd(&P.hist[(size_t)q * 4096 + i0 + e], c[e]);
+        h4[et + 128 * j] = make_uint4(0u, 0u, 0u, 0u);
       }
       return group_sync(epi_bar, epi_phase, P.err);
     };
@@ -366,7 +386,20 @@ cudaError_t launch_qg(const IndexTcArgs &a, cudaStream_t s) {
   static int smem_set = 0;
   e = ensure_smem(index_score_tc_kernel<QG>, C::kSmem, &smem_set);
   if (e != cudaSuccess) return e;
-  const uint32_t grid = min(P.total_items, (uint32_t)num_sms());
+  // one group per CTA range when that costs no more tiles per CTA than the
+  // contiguous split (a CTA that changes query reloads its heads and flushes
+  // its histogram in between)
+  const uint32_t sms = (uint32_t)num_sms(), n_bg = a.batch * P.n_groups;
+  uint32_t grid = min(P.total_items, sms);
+  P.cta_per_group = 0;
+  if (n_bg <= sms) {
+    const uint32_t cpg = sms / n_bg;
+    const uint32_t max_contig = (P.total_items + grid - 1) / grid;
+    if ((P.tiles_per + cpg - 1) / cpg <= max_contig) {
+      P.cta_per_group = cpg;
+      grid = n_bg * cpg;
+    }
+  }
   e = launch_pdl(index_score_tc_kernel<QG>, dim3(grid), dim3(C::kThreads), C::kSmem, s, tk, tq, P);
   if (e != cudaSuccess) return e;
   note_launches(1);
