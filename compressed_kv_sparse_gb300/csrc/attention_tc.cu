@@ -386,7 +386,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (tile != g.t0 && !issue_tile(g, tile, n)) goto done_loader;
           // one arrival per thread once all its rows of the tile landed: the
           // MMA issuer takes the tile whole (waits between the MMAs of one
-          // accumulation halve their rate)
+          // accumulation halve their rate; issuing S pair by pair as the
+          // blocks land measured slower)
           cp_async_wait_all();
           fence_proxy_async();
           mbar_arrive(&S.kv_full);
@@ -492,6 +493,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (maybe) g = query_geo(P, qi, rank, C, lane);
       const bool has_tiles = maybe && g.t0 < g.t1;
       bool any_valid = false;
+      // the rotation coefficients of this thread's tail dim in the direct
+      // output (dim 384 + r of the last chunk), loaded while the tiles run
+      float ep_co = 1.f, ep_si = 0.f;
+      if (!(dec && C > 1) && has_tiles && 384 + r >= (uint32_t)kNope) {
+        const uint32_t fi = (384 + r - kNope) >> 1;
+        ep_co = P.cos[(size_t)g.p * 32 + fi];
+        ep_si = P.sin[(size_t)g.p * 32 + fi];
+      }
       for (uint32_t tile = g.t0; has_tiles && tile < g.t1; tile += g.ts, ++n) {
         const bool first = tile == g.t0;
         const uint32_t row = tile * kRows + r;
@@ -617,12 +626,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll 1
         for (uint32_t m = 0; m < 4; ++m) {
           const uint32_t d = m * 128 + r;
-          float co = 1.f, si = 0.f;
-          if (d >= (uint32_t)kNope) {
-            const uint32_t fi = (d - kNope) >> 1;
-            co = P.cos[(size_t)g.p * 32 + fi];
-            si = P.sin[(size_t)g.p * 32 + fi];
-          }
+          const float co = ep_co, si = ep_si;   // used by the tail dims only (m = 3)
 #pragma unroll 1
           for (uint32_t hf = 0; hf < 2; ++hf) {
             uint32_t a[32];

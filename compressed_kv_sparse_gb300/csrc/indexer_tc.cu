@@ -303,13 +303,19 @@ __global__ void __launch_bounds__(Cfg<QG>::kThreads, 1)
       }
       tc_fence_after();
       const uint32_t grow = tile * kRows + row;
-#pragma unroll 1
-      for (int q = (int)q0; q < (int)q0 + C::kQPW; ++q) {
+      static_assert(C::kQPW == 1, "one query per epilogue warp");
+      {
+        const int q = (int)q0;
         uint32_t r0[32], r1[32];
         const uint32_t taddr = tmem + ((lg * 32) << 16) + acc * C::N + q * kHeads;
         tmem_ld32(taddr, r0);
         tmem_ld32(taddr + 32, r1);
         tmem_ld_wait();
+        // the accumulator is free once its columns are in registers: the
+        // MMA two items on may start while this warp finishes the scores
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&acc_empty[acc]);
         // approximate score: any summation order is covered by the error
         // bound, so eight independent chains and vector loads of the weights
         const float4 *wq4 = reinterpret_cast<const float4 *>(sw + q * kHeads);
@@ -340,9 +346,6 @@ __global__ void __launch_bounds__(Cfg<QG>::kThreads, 1)
             atomicAdd(&shist[bin], (uint32_t)__popc(peers));
         }
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&acc_empty[acc]);
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1;
     }
