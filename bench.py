@@ -123,9 +123,15 @@ def peaks():
 class Runner:
     """Builds every layer's cache and inputs on the device and runs steps."""
 
-    def __init__(self, wl: synth.Workload, device, rank: int = 0, qat: bool = False):
+    def __init__(self, wl: synth.Workload, device, rank: int = 0, qat: bool = False,
+                 streams: int = 1):
         from compressed_kv_sparse_gb300 import lib
         self.lib, self.wl, self.dev = lib, wl, device
+        # streams == 2 (decode): the indexer lane's append and the top-k of a
+        # c4a layer run on a second stream beside the raw insert and the
+        # attention lane's append
+        self.streams = streams
+        self.aux = torch.cuda.Stream(device=device) if streams == 2 else None
         self.decode = wl.mode == "decode"
         self.T = 1 if self.decode else wl.chunk
         self.p0 = wl.context
@@ -203,8 +209,31 @@ class Runner:
         return calls
 
     def layer_step(self, L):
+        if self.streams == 2 and self.decode and L["s"].ratio == 4:
+            self.layer_step_two_streams(L)
+            return
         for _, fn in self.layer_calls(L):
             fn()
+
+    def layer_step_two_streams(self, L):
+        """c4a decode layer with the indexer pipeline on its own stream (vLLM's
+        multi-stream partitioning): fork, [index-lane append -> top-k] beside
+        [raw insert + attention-lane append], join, attention."""
+        lib, s, c, inp = self.lib, L["s"], L["cache"], L["inp"]
+        k, p0 = s.top_k, self.p0
+        main = torch.cuda.current_stream()
+        self.aux.wait_stream(main)
+        c.n_tokens = p0
+        with torch.cuda.stream(self.aux):
+            lib.ds4a_compress_append_lanes(c, p0, 1, lib.LANE_INDEX, inp)
+        lib.ds4a_compress_append_lanes(c, p0, 1, lib.LANE_RAW | lib.LANE_ATTN, inp)
+        c.n_tokens = p0 + 1
+        with torch.cuda.stream(self.aux):
+            lib.ds4a_index_topk(c, p0, 1, inp["q_idx"], inp["w"], s.index_heads, k, L["topk"],
+                                L["ws_idx"])
+        main.wait_stream(self.aux)
+        lib.ds4a_sparse_attn_decode(c, p0, L["q"], s.n_heads, L["topk"], k,
+                                    lib.default_scale(s.head_dim), L["out"], L["ws_attn"])
 
     def step(self):
         for L in self.layers:
@@ -332,7 +361,7 @@ def qat_flags(ratio: int) -> int:
 def run_gpu(args, wl, rank, world, device):
     hbm, bf16, bf16s, peak_kind = peaks()
     lib_mod = __import__("compressed_kv_sparse_gb300.lib", fromlist=["lib"])
-    R = Runner(wl, device, rank, qat=args.qat)
+    R = Runner(wl, device, rank, qat=args.qat, streams=args.streams)
     step_bytes = sum(v[0] for v in R.algorithmic().values())
     flush = None
     if step_bytes < 512e6:      # working set below ~4x L2: flush between steps
@@ -502,6 +531,7 @@ def run_gpu(args, wl, rank, world, device):
                       "cuda_graph": use_graph, "parallelism": f"replicas x{world}",
                       "step8_round_trips": "fp8 attention rows + fp4 indexer rows/queries"
                       if args.qat else "off",
+                      "streams": args.streams,
                       "algorithmic_GB_per_step": step_bytes / 1e9,
                       "step_GB/s": step_bytes / (ms_step / 1e3) / 1e9},
            "roofline": roof, "calls": calls,
@@ -614,6 +644,8 @@ def main():
     ap.add_argument("--workload", default="flash43", choices=sorted(WORKLOADS))
     ap.add_argument("--impl", default="gpu", choices=["gpu", "reference"])
     ap.add_argument("--no-graph", action="store_true")
+    ap.add_argument("--streams", type=int, default=1, choices=[1, 2],
+                    help="2: c4a decode layers run the indexer pipeline on a second stream")
     ap.add_argument("--qat", action="store_true",
                     help="compressor step 8 on: FP8 round trip of attention rows, FP4 QAT "
                          "round trip of indexer rows and queries")

@@ -152,22 +152,29 @@ ds4a_status ds4a_index_norms(ds4a_layer_cache *c, ds4a_stream_t stream) {
                                         c->index_norm_max, s));
 }
 
-ds4a_status ds4a_compress_append(ds4a_layer_cache *c, uint32_t pos0, uint32_t T,
-                                 const void *raw_kv_in, const void *attn_cand,
-                                 const void *attn_score, const void *ape_attn,
-                                 const void *gamma_attn, const void *idx_cand,
-                                 const void *idx_score, const void *ape_idx,
-                                 const void *gamma_idx, void *raw_chunk_out,
-                                 ds4a_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// The append of the parts in `lanes` (DS4A_LANE_*); `advance`: set n_tokens.
+ds4a_status append_parts(ds4a_layer_cache *c, uint32_t pos0, uint32_t T, uint32_t lanes,
+                         bool advance, const void *raw_kv_in, const void *attn_cand,
+                         const void *attn_score, const void *ape_attn, const void *gamma_attn,
+                         const void *idx_cand, const void *idx_score, const void *ape_idx,
+                         const void *gamma_idx, void *raw_chunk_out, ds4a_stream_t stream) {
   ds4a_status st = check_cache(c);
   if (st) return st;
   if (T == 0) return DS4A_ERR_SHAPE;
-  if (!raw_kv_in) return DS4A_ERR_ARG;
+  if (!lanes || (lanes & ~(DS4A_LANE_RAW | DS4A_LANE_ATTN | DS4A_LANE_INDEX))) return DS4A_ERR_ARG;
+  const bool raw = lanes & DS4A_LANE_RAW;
+  const bool la = lanes & DS4A_LANE_ATTN, li = lanes & DS4A_LANE_INDEX;
+  if ((la && c->ratio == 0) || (li && c->ratio != 4)) return DS4A_ERR_ARG;
+  if (raw && !raw_kv_in) return DS4A_ERR_ARG;
   if (pos0 != c->n_tokens) return DS4A_ERR_POSITION;
   if ((uint64_t)pos0 + T > c->rope_max_pos) return DS4A_ERR_CAPACITY;
   if (c->ratio && comp_rows(c, pos0 + T) > c->comp_cap) return DS4A_ERR_CAPACITY;
-  if (c->ratio && (!attn_cand || !attn_score || !ape_attn || !gamma_attn)) return DS4A_ERR_ARG;
-  if (c->ratio == 4 && (!idx_cand || !idx_score || !ape_idx || !gamma_idx)) return DS4A_ERR_ARG;
+  if (la && (!attn_cand || !attn_score || !ape_attn || !gamma_attn)) return DS4A_ERR_ARG;
+  if (li && (!idx_cand || !idx_score || !ape_idx || !gamma_idx)) return DS4A_ERR_ARG;
 
   AppendArgs a;
   std::memset(&a, 0, sizeof(a));
@@ -186,23 +193,54 @@ ds4a_status ds4a_compress_append(ds4a_layer_cache *c, uint32_t pos0, uint32_t T,
   a.raw_dst = a.direct ? c->raw_kv : raw_chunk_out;
   a.cos = c->rope_cos;
   a.sin = c->rope_sin;
-  a.n_lanes = c->ratio == 0 ? 0 : c->ratio == 4 ? 2 : 1;
-  if (c->ratio) {
-    a.lane[0] = LaneArgs{c->head_dim, c->n_rot, c->attn_comp_kv, c->attn_state_kv,
-                         c->attn_state_score, c->rope_cos, c->rope_sin, attn_cand, attn_score,
-                         ape_attn, gamma_attn, nullptr, nullptr,
-                         (c->qat & DS4A_QAT_FP8_ATTN) ? 1u : 0u, 0.f};
+  a.y0 = raw ? 0u : 1u;
+  a.n_lanes = 0;
+  if (la) {
+    a.lane[a.n_lanes++] =
+        LaneArgs{c->head_dim, c->n_rot, c->attn_comp_kv, c->attn_state_kv, c->attn_state_score,
+                 c->rope_cos, c->rope_sin, attn_cand, attn_score, ape_attn, gamma_attn,
+                 nullptr, nullptr, (c->qat & DS4A_QAT_FP8_ATTN) ? 1u : 0u, 0.f};
   }
-  if (c->ratio == 4) {
-    a.lane[1] = LaneArgs{c->index_dim, c->index_rot, c->index_comp_kv, c->index_state_kv,
-                         c->index_state_score, c->index_rope_cos, c->index_rope_sin, idx_cand,
-                         idx_score, ape_idx, gamma_idx, c->index_norm, c->index_norm_max,
-                         (c->qat & DS4A_QAT_FP4_INDEX) ? 2u : 0u, hadamard_scale(c->index_dim)};
+  if (li) {
+    a.lane[a.n_lanes++] =
+        LaneArgs{c->index_dim, c->index_rot, c->index_comp_kv, c->index_state_kv,
+                 c->index_state_score, c->index_rope_cos, c->index_rope_sin, idx_cand,
+                 idx_score, ape_idx, gamma_idx, c->index_norm, c->index_norm_max,
+                 (c->qat & DS4A_QAT_FP4_INDEX) ? 2u : 0u, hadamard_scale(c->index_dim)};
   }
   st = cuda_status(launch_append(a, reinterpret_cast<cudaStream_t>(stream)));
   if (st) return st;
-  c->n_tokens = pos0 + T;
+  if (advance) c->n_tokens = pos0 + T;
   return DS4A_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+ds4a_status ds4a_compress_append(ds4a_layer_cache *c, uint32_t pos0, uint32_t T,
+                                 const void *raw_kv_in, const void *attn_cand,
+                                 const void *attn_score, const void *ape_attn,
+                                 const void *gamma_attn, const void *idx_cand,
+                                 const void *idx_score, const void *ape_idx,
+                                 const void *gamma_idx, void *raw_chunk_out,
+                                 ds4a_stream_t stream) {
+  if (!c) return DS4A_ERR_ARG;
+  const uint32_t lanes = DS4A_LANE_RAW | (c->ratio ? DS4A_LANE_ATTN : 0u) |
+                         (c->ratio == 4 ? DS4A_LANE_INDEX : 0u);
+  return append_parts(c, pos0, T, lanes, true, raw_kv_in, attn_cand, attn_score, ape_attn,
+                      gamma_attn, idx_cand, idx_score, ape_idx, gamma_idx, raw_chunk_out, stream);
+}
+
+ds4a_status ds4a_compress_append_lanes(ds4a_layer_cache *c, uint32_t pos0, uint32_t T,
+                                       uint32_t lanes, const void *raw_kv_in,
+                                       const void *attn_cand, const void *attn_score,
+                                       const void *ape_attn, const void *gamma_attn,
+                                       const void *idx_cand, const void *idx_score,
+                                       const void *ape_idx, const void *gamma_idx,
+                                       void *raw_chunk_out, ds4a_stream_t stream) {
+  return append_parts(c, pos0, T, lanes, false, raw_kv_in, attn_cand, attn_score, ape_attn,
+                      gamma_attn, idx_cand, idx_score, ape_idx, gamma_idx, raw_chunk_out, stream);
 }
 
 size_t ds4a_workspace_bytes(int call, const ds4a_layer_cache *c, uint32_t T, uint32_t n_heads,

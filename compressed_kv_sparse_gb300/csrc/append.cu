@@ -8,7 +8,8 @@
 // only the RMS of the pooled row needs a block reduction.
 //
 // Decode (T = 1): one launch, grid (B, 1 + lanes). Block y = 0 rotates the raw
-// row into the ring; block y = 1 + l stores the token into lane l's state and,
+// row into the ring (absent when the raw rows are not part of the call, y0 = 1);
+// block y = 1 + l stores the token into lane l's state and,
 // at a ratio boundary, pools, normalises, rotates and appends the compressed
 // row, then (ratio 4) moves slots 4..7 to 0..3.
 // Chunk (T > 1): every compressed row completed inside the chunk is built in
@@ -219,15 +220,15 @@ __global__ void __launch_bounds__(kThreads) append_step_kernel(AppendArgs a) {
   __shared__ float red[32];
   pdl_wait();
   pdl_trigger();
-  const uint32_t b = blockIdx.x, p = a.pos0;
-  if (blockIdx.y == 0) {
+  const uint32_t b = blockIdx.x, p = a.pos0, role = blockIdx.y + a.y0;
+  if (role == 0) {
     const T *src = static_cast<const T *>(a.raw_in) + (size_t)b * a.head_dim;
     T *dst = static_cast<T *>(a.raw_dst) +
              ((size_t)b * a.cap_raw + p % a.cap_raw) * a.head_dim;
     raw_row(src, dst, a.head_dim, a.n_rot, p, a.cos, a.sin);
     return;
   }
-  const LaneArgs &L = a.lane[blockIdx.y - 1];
+  const LaneArgs &L = a.lane[role - 1];
   const uint32_t r = a.ratio, W = a.window, width = L.width;
   const uint32_t slot = r == 4 ? 4 + p % 4 : p % r;
   const T *cand = static_cast<const T *>(L.cand) + (size_t)b * width;
@@ -381,13 +382,15 @@ __global__ void state_reset_kernel(float *kv, float *score, size_t n) {
 template <typename T>
 cudaError_t launch_append_t(const AppendArgs &a, cudaStream_t s) {
   if (a.T == 1 && a.direct) {
-    cudaError_t e = launch_pdl(append_step_kernel<T>, dim3(a.batch, 1 + a.n_lanes),
-                               dim3(kThreads), 0, s, a);
+    const uint32_t roles = (a.y0 ? 0u : 1u) + (uint32_t)a.n_lanes;
+    if (!roles) return cudaSuccess;
+    cudaError_t e = launch_pdl(append_step_kernel<T>, dim3(a.batch, roles), dim3(kThreads), 0,
+                               s, a);
     if (e != cudaSuccess) return e;
     note_launches(1);
     return cudaGetLastError();
   }
-  const uint32_t n_raw = a.direct ? (a.T < a.cap_raw ? a.T : a.cap_raw) : a.T;
+  const uint32_t n_raw = a.y0 ? 0u : a.direct ? (a.T < a.cap_raw ? a.T : a.cap_raw) : a.T;
   const uint32_t n_emit = a.ratio ? (a.pos0 + a.T) / a.ratio - a.pos0 / a.ratio : 0;
   const uint32_t nblk = n_raw + n_emit * a.n_lanes;
   if (nblk) {

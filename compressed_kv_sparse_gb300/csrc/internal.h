@@ -69,8 +69,9 @@ struct AppendArgs {
   void *raw_dst;          // ring [B][cap][D] (direct) or chunk [B][T][D]
   bool direct;            // raw rows go to the ring
   const float *cos, *sin; // attention-lane / raw-row table
-  int n_lanes;
+  int n_lanes;             // lanes to append (lane[0 .. n_lanes-1])
   LaneArgs lane[2];
+  uint32_t y0;             // 1: the raw rows are not part of this append
 };
 cudaError_t launch_append(const AppendArgs &a, cudaStream_t s);
 

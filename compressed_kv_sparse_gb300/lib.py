@@ -56,6 +56,9 @@ EXPORTS = {
     "ds4a_index_norms": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p]),
     "ds4a_compress_append": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_uint32, ctypes.c_uint32]
                              + [ctypes.c_void_p] * 11),
+    "ds4a_compress_append_lanes": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_uint32,
+                                                  ctypes.c_uint32, ctypes.c_uint32]
+                                   + [ctypes.c_void_p] * 11),
     "ds4a_index_topk": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_uint32, ctypes.c_uint32,
                                        ctypes.c_void_p, ctypes.c_void_p, ctypes.c_uint32,
                                        ctypes.c_uint32, ctypes.c_void_p, ctypes.c_void_p,
@@ -237,6 +240,21 @@ def ds4a_compress_append(cache: LayerCache, pos0: int, T: int, inp: Dict[str, to
         _ptr(g("ape_attn")), _ptr(g("gamma_attn")), _ptr(g("idx_cand")), _ptr(g("idx_score")),
         _ptr(g("ape_idx")), _ptr(g("gamma_idx")), _ptr(raw_chunk_out), _stream(stream)),
         "ds4a_compress_append")
+
+
+LANE_RAW, LANE_ATTN, LANE_INDEX = 1, 2, 4   # DS4A_LANE_*
+
+
+def ds4a_compress_append_lanes(cache: LayerCache, pos0: int, T: int, lanes: int,
+                               inp: Dict[str, torch.Tensor],
+                               raw_chunk_out: Optional[torch.Tensor] = None, stream=None):
+    """The parts `lanes` of an append; n_tokens is left for the caller to set."""
+    g = inp.get
+    _check(load().ds4a_compress_append_lanes(
+        cache.ref(), pos0, T, lanes, _ptr(g("raw_kv_in")), _ptr(g("attn_cand")),
+        _ptr(g("attn_score")), _ptr(g("ape_attn")), _ptr(g("gamma_attn")), _ptr(g("idx_cand")),
+        _ptr(g("idx_score")), _ptr(g("ape_idx")), _ptr(g("gamma_idx")), _ptr(raw_chunk_out),
+        _stream(stream)), "ds4a_compress_append_lanes")
 
 
 def ds4a_index_topk(cache: LayerCache, pos0: int, T: int, q_idx: torch.Tensor, w: torch.Tensor,

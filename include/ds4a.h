@@ -5,6 +5,7 @@
  * engine runs for every token of a DeepSeek-V4-style model:
  *
  *   ds4a_compress_append          raw-window insert + KV compressor
+ *                                 (ds4a_compress_append_lanes: a part of it)
  *   ds4a_index_topk               ratio-4 indexer scores + exact top-k
  *   ds4a_sparse_attn_decode       attention of one new token per sequence
  *   ds4a_sparse_attn_prefill_chunk attention of a chunk of T tokens
@@ -195,6 +196,30 @@ ds4a_status ds4a_compress_append(ds4a_layer_cache *cache, uint32_t pos0, uint32_
                                  const void *idx_score, const void *ape_idx,
                                  const void *gamma_idx, void *raw_chunk_out,
                                  ds4a_stream_t stream);
+
+/* Parts of an append, for ds4a_compress_append_lanes. */
+#define DS4A_LANE_RAW 1u    /* the raw-window rows (raw_kv or raw_chunk_out) */
+#define DS4A_LANE_ATTN 2u   /* the attention lane: state and compressed rows */
+#define DS4A_LANE_INDEX 4u  /* the indexer lane (ratio 4): state, rows, row norms */
+
+/*
+ * ds4a_compress_append restricted to the parts in `lanes` (a nonzero set of
+ * DS4A_LANE_*; lanes the layer does not have are an error). The parts touch
+ * disjoint memory, so they may run on different streams at once. vLLM's page
+ * runs the indexer pipeline of a c4a layer on its own stream, beside the main
+ * KV compression and the SWA insert ("Multi-stream Partitioning"). Inputs of
+ * parts not selected may be NULL. Requires pos0 == n_tokens and leaves n_tokens
+ * unchanged: once every part the caller needs is appended, it sets
+ * cache->n_tokens = pos0 + T itself. Errors as for ds4a_compress_append, plus
+ * DS4A_ERR_ARG for an empty or invalid lane set.
+ */
+ds4a_status ds4a_compress_append_lanes(ds4a_layer_cache *cache, uint32_t pos0, uint32_t T,
+                                       uint32_t lanes, const void *raw_kv_in,
+                                       const void *attn_cand, const void *attn_score,
+                                       const void *ape_attn, const void *gamma_attn,
+                                       const void *idx_cand, const void *idx_score,
+                                       const void *ape_idx, const void *gamma_idx,
+                                       void *raw_chunk_out, ds4a_stream_t stream);
 
 /*
  * Indexer top-k for queries at positions pos0 .. pos0+T-1 (ratio 4 only;

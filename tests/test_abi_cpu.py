@@ -151,6 +151,16 @@ def test_argument_checks_reject_before_launch(L):
     c128 = _fake_cache(ratio=128)
     assert L.ds4a_index_topk(ctypes.byref(c128), 9, 1, fake, fake, 64, 512, fake, fake,
                              1 << 30, None) == -1
+    # lane-selective append: empty or unknown lane set, a lane the layer lacks,
+    # and the position check (n_tokens stays for the caller to set)
+    assert L.ds4a_compress_append_lanes(r, 10, 1, 0, *P, None, None) == -1
+    assert L.ds4a_compress_append_lanes(r, 10, 1, 8, *P, None, None) == -1
+    assert L.ds4a_compress_append_lanes(ctypes.byref(_fake_cache(ratio=128)), 10, 1,
+                                        lib.LANE_INDEX, *P, None, None) == -1
+    assert L.ds4a_compress_append_lanes(ctypes.byref(_fake_cache(ratio=0)), 10, 1,
+                                        lib.LANE_ATTN, *P, None, None) == -1
+    assert L.ds4a_compress_append_lanes(r, 9, 1, lib.LANE_RAW, *P, None, None) == -4
+    assert c.n_tokens == 10
     # step-8 flags: unknown bit, FP4 off ratio 4, FP4 with Di not a power of two,
     # FP8 on a window-only layer
     for ratio, q, dim, want in ((4, 4, 128, -1), (128, 2, 128, -1), (4, 2, 96, -2),

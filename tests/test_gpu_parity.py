@@ -114,6 +114,40 @@ def test_append_chunked_equals_one_call_on_gpu_and_oracle():
     compare_cache(gc, oc, "bf16", "continuity")
 
 
+@pytest.mark.parametrize("T", [1, 37])
+def test_append_lanes_on_two_streams_equal_one_call(T):
+    """The indexer lane on one stream and the raw rows plus attention lane on
+    another (ds4a_compress_append_lanes, then n_tokens set by the caller) leave
+    exactly the cache of one ds4a_compress_append."""
+    lib = lib_()
+    shape = synth.LayerShape(ratio=4)
+    p0 = 1023 if T == 1 else 1021
+    wl = synth.Workload("lanes", 14, 2, (shape,), p0, "decode" if T == 1 else "prefill")
+    cap = (p0 + T) // 4 + 1
+    hist = synth.cache_history(wl, 0, p0, comp_cap=cap)
+    inp = to_dev(synth.step_inputs(wl, 0, p0, T))
+    ref = gpu_cache(shape, 2, cap, p0 + T + 1, hist, p0)
+    got = gpu_cache(shape, 2, cap, p0 + T + 1, hist, p0)
+    mk = lambda: torch.empty((2, T, 512), dtype=torch.bfloat16, device=DEV) if T > 1 else None
+    chunk_ref, chunk_got = mk(), mk()
+    lib.ds4a_compress_append(ref, p0, T, inp, raw_chunk_out=chunk_ref)
+    main, aux = torch.cuda.current_stream(), torch.cuda.Stream()
+    aux.wait_stream(main)
+    with torch.cuda.stream(aux):
+        lib.ds4a_compress_append_lanes(got, p0, T, lib.LANE_INDEX, inp)
+    lib.ds4a_compress_append_lanes(got, p0, T, lib.LANE_RAW | lib.LANE_ATTN, inp,
+                                   raw_chunk_out=chunk_got)
+    main.wait_stream(aux)
+    assert got.n_tokens == p0
+    got.n_tokens = p0 + T
+    torch.cuda.synchronize()
+    for name in ("raw_kv", "attn_comp_kv", "attn_state_kv", "attn_state_score", "index_comp_kv",
+                 "index_state_kv", "index_state_score", "index_norm", "index_norm_max"):
+        assert torch.equal(getattr(ref, name), getattr(got, name)), name
+    if T > 1:
+        assert torch.equal(chunk_ref, chunk_got)
+
+
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
 def test_index_norms_written_at_append(dtype):
     """Every indexer row appended (chunk and decode paths) gets an upper bound
