@@ -511,19 +511,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (first) {
           // running maxima start at the exact per-head maxima of the first
           // tile's scaled scores: warp maxima of order-keyed values, then the
-          // largest of the four warps. The scores stay in registers for P,
-          // which then has no score above its maximum (no raise to check).
-          uint32_t a0[32], a1[32];
-          tmem_ld32(tmS + lane_base, a0);
-          tmem_ld32(tmS + lane_base + 32, a1);
-          tmem_ld_wait();
+          // largest of the four warps. P of this tile then has no score above
+          // its maximum (no raise to check).
           uint32_t *tkey = reinterpret_cast<uint32_t *>(&S.tmax[0][0]);   // [4][kH]
+          // eight heads per step of a short loop: this runs once per query,
+          // its code is fetched cold, and an unrolled form measured ~2 us of
+          // instruction fetch
+#pragma unroll 1
+          for (uint32_t c = 0; c < (uint32_t)kH; c += 8) {
+            uint32_t a8[8];
+            tmem_ld8(tmS + lane_base + c, a8);
+            tmem_ld_wait();
 #pragma unroll
-          for (int h = 0; h < 64; ++h) {
-            const uint32_t u = __float_as_uint(__uint_as_float(h < 32 ? a0[h] : a1[h - 32]) * P.c2);
-            const uint32_t key = valid ? ((u & 0x80000000u) ? ~u : (u | 0x80000000u)) : 0u;
-            const uint32_t mk = redux_max_u32(key);
-            if (lane == (uint32_t)(h & 31)) tkey[warp * kH + h] = mk;
+            for (uint32_t j = 0; j < 8; ++j) {
+              const uint32_t u = __float_as_uint(__uint_as_float(a8[j]) * P.c2);
+              const uint32_t key = valid ? ((u & 0x80000000u) ? ~u : (u | 0x80000000u)) : 0u;
+              const uint32_t mk = redux_max_u32(key);
+              if (lane == ((c + j) & 31)) tkey[warp * kH + c + j] = mk;
+            }
           }
           if (r == 0) S.flagcnt[(n + 1) % 3] = 0;   // the next tile's raise count
           if (!group_sync(&S.sm_bar, sm_phase, ew)) goto done_softmax;
@@ -537,6 +542,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           if (!group_sync(&S.sm_bar, sm_phase, ew)) goto done_softmax;
           if (!mbar_wait_warp(&S.p_empty, (n & 1) ^ 1, ew)) goto done_softmax;
+          // the scores (S stays until this tile's P is done)
+          uint32_t a0[32], a1[32];
+          tmem_ld32(tmS + lane_base, a0);
+          tmem_ld32(tmS + lane_base + 32, a1);
+          tmem_ld_wait();
           bool unused = false;
           p_half(valid, a0, 0, unused);
           p_half(valid, a1, 1, unused);

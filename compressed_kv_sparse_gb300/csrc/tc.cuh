@@ -274,13 +274,6 @@ __device__ __forceinline__ void mma_bf16_ta(uint32_t d_tmem, uint32_t a_tmem, ui
       : "memory");
 }
 
-// Largest value of the warp (all lanes active).
-__device__ __forceinline__ uint32_t redux_max_u32(uint32_t v) {
-  uint32_t r;
-  asm volatile("redux.sync.max.u32 %0, %1, 0xffffffff;" : "=r"(r) : "r"(v));
-  return r;
-}
-
 // 2^x, hardware approximation (relative error ~2^-22; flushes denormals).
 __device__ __forceinline__ float ex2_approx(float x) {
   float y;
@@ -297,6 +290,19 @@ __device__ __forceinline__ void mma_commit(uint64_t *bar) {
 }
 
 // Each thread of the warp reads 32 consecutive 32-bit columns of its TMEM lane.
+// Eight consecutive 32-bit columns of this warp's 32 TMEM lanes.
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t (&r)[8]) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
+                 "=r"(r[6]), "=r"(r[7])
+               : "r"(taddr));
+}
+// Largest value of the warp (all lanes active).
+__device__ __forceinline__ uint32_t redux_max_u32(uint32_t v) {
+  uint32_t r;
+  asm volatile("redux.sync.max.u32 %0, %1, 0xffffffff;" : "=r"(r) : "r"(v));
+  return r;
+}
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
