@@ -124,7 +124,7 @@ class Runner:
     """Builds every layer's cache and inputs on the device and runs steps."""
 
     def __init__(self, wl: synth.Workload, device, rank: int = 0, qat: bool = False,
-                 streams: int = 1):
+                 streams: int = 1, paged: bool = False):
         from compressed_kv_sparse_gb300 import lib
         self.lib, self.wl, self.dev = lib, wl, device
         # streams == 2 (decode): the indexer lane's append and the top-k of a
@@ -143,11 +143,20 @@ class Runner:
         end = self.p0 + self.T
         for il, s in enumerate(wl.layers):
             cap = end // s.ratio + 1 if s.ratio else 0
+            table, n_blocks = None, 0
+            if paged and s.ratio:
+                # 256-position blocks in a random order of one shared pool
+                rpb = 256 // s.ratio
+                max_blocks = cap // rpb + 1
+                cap, n_blocks = max_blocks * rpb, B * max_blocks
+                perm = torch.randperm(n_blocks, generator=torch.Generator().manual_seed(il))
+                table = perm.to(torch.int32).reshape(B, max_blocks).to(device)
             c = lib.LayerCache(ratio=s.ratio, head_dim=s.head_dim, n_rot=s.n_rot, batch=B,
                                comp_cap=cap, dtype=s.dtype, base=s.rope_base,
                                rope_max_pos=end + 1, index_dim=s.index_dim,
                                index_rot=s.index_rot, cap_raw=s.cap_raw,
-                               qat=qat_flags(s.ratio) if qat else 0, device=device)
+                               qat=qat_flags(s.ratio) if qat else 0, device=device,
+                               block_table=table, n_blocks=n_blocks)
             hist = synth.cache_history(seed_wl, il, self.p0, comp_cap=cap, device=device)
             c.load_state(hist, self.p0)
             del hist
@@ -361,7 +370,7 @@ def qat_flags(ratio: int) -> int:
 def run_gpu(args, wl, rank, world, device):
     hbm, bf16, bf16s, peak_kind = peaks()
     lib_mod = __import__("compressed_kv_sparse_gb300.lib", fromlist=["lib"])
-    R = Runner(wl, device, rank, qat=args.qat, streams=args.streams)
+    R = Runner(wl, device, rank, qat=args.qat, streams=args.streams, paged=args.paged)
     step_bytes = sum(v[0] for v in R.algorithmic().values())
     flush = None
     if step_bytes < 512e6:      # working set below ~4x L2: flush between steps
@@ -532,6 +541,7 @@ def run_gpu(args, wl, rank, world, device):
                       "step8_round_trips": "fp8 attention rows + fp4 indexer rows/queries"
                       if args.qat else "off",
                       "streams": args.streams,
+                      "cache_layout": "paged, 256-position blocks" if args.paged else "contiguous",
                       "algorithmic_GB_per_step": step_bytes / 1e9,
                       "step_GB/s": step_bytes / (ms_step / 1e3) / 1e9},
            "roofline": roof, "calls": calls,
@@ -646,6 +656,8 @@ def main():
     ap.add_argument("--no-graph", action="store_true")
     ap.add_argument("--streams", type=int, default=1, choices=[1, 2],
                     help="2: c4a decode layers run the indexer pipeline on a second stream")
+    ap.add_argument("--paged", action="store_true",
+                    help="compressed rows in 256-position blocks behind a block table")
     ap.add_argument("--qat", action="store_true",
                     help="compressor step 8 on: FP8 round trip of attention rows, FP4 QAT "
                          "round trip of indexer rows and queries")

@@ -42,6 +42,10 @@ ds4a_status check_cache(const ds4a_layer_cache *c) {
     if (!c->index_norm || !c->index_norm_max) return DS4A_ERR_ARG;
     if (!c->index_rope_cos || !c->index_rope_sin) return DS4A_ERR_ARG;
   }
+  if (c->block_table) {
+    if (c->ratio == 0 || c->max_blocks == 0 || c->n_blocks == 0) return DS4A_ERR_ARG;
+    if ((uint64_t)c->max_blocks * (256u / c->ratio) != c->comp_cap) return DS4A_ERR_SHAPE;
+  }
   if (c->qat & ~(DS4A_QAT_FP8_ATTN | DS4A_QAT_FP4_INDEX)) return DS4A_ERR_ARG;
   if ((c->qat & DS4A_QAT_FP8_ATTN) && c->ratio == 0) return DS4A_ERR_ARG;
   if (c->qat & DS4A_QAT_FP4_INDEX) {
@@ -53,6 +57,16 @@ ds4a_status check_cache(const ds4a_layer_cache *c) {
 
 ds4a_status cuda_status(cudaError_t e) {
   return note_error(e) == cudaSuccess ? DS4A_OK : DS4A_ERR_CUDA;
+}
+
+// Row maps of the attention lane (256/ratio rows per block) and the indexer
+// lane (64 rows per block).
+RowMap attn_map(const ds4a_layer_cache *c) {
+  const uint32_t rpb = c->ratio ? 256u / c->ratio : 1u;
+  return RowMap{c->block_table, c->comp_cap, c->max_blocks, rpb, c->n_blocks};
+}
+RowMap index_map(const ds4a_layer_cache *c) {
+  return RowMap{c->block_table, c->comp_cap, c->max_blocks, 64u, c->n_blocks};
 }
 
 // c = 1/sqrt(n) rounded to fp32, the Hadamard normalisation of the FP4 round trip.
@@ -147,8 +161,8 @@ ds4a_status ds4a_index_norms(ds4a_layer_cache *c, ds4a_stream_t stream) {
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   st = cuda_status(cudaMemsetAsync(c->index_norm_max, 0, sizeof(uint32_t) * c->batch, s));
   if (st) return st;
-  return cuda_status(launch_index_norms(c->dtype, c->index_comp_kv, c->index_dim, c->batch,
-                                        c->comp_cap, comp_rows(c, c->n_tokens), c->index_norm,
+  return cuda_status(launch_index_norms(c->dtype, c->index_comp_kv, index_map(c), c->index_dim,
+                                        c->batch, comp_rows(c, c->n_tokens), c->index_norm,
                                         c->index_norm_max, s));
 }
 
@@ -199,14 +213,15 @@ ds4a_status append_parts(ds4a_layer_cache *c, uint32_t pos0, uint32_t T, uint32_
     a.lane[a.n_lanes++] =
         LaneArgs{c->head_dim, c->n_rot, c->attn_comp_kv, c->attn_state_kv, c->attn_state_score,
                  c->rope_cos, c->rope_sin, attn_cand, attn_score, ape_attn, gamma_attn,
-                 nullptr, nullptr, (c->qat & DS4A_QAT_FP8_ATTN) ? 1u : 0u, 0.f};
+                 nullptr, nullptr, (c->qat & DS4A_QAT_FP8_ATTN) ? 1u : 0u, 0.f, attn_map(c)};
   }
   if (li) {
     a.lane[a.n_lanes++] =
         LaneArgs{c->index_dim, c->index_rot, c->index_comp_kv, c->index_state_kv,
                  c->index_state_score, c->index_rope_cos, c->index_rope_sin, idx_cand,
                  idx_score, ape_idx, gamma_idx, c->index_norm, c->index_norm_max,
-                 (c->qat & DS4A_QAT_FP4_INDEX) ? 2u : 0u, hadamard_scale(c->index_dim)};
+                 (c->qat & DS4A_QAT_FP4_INDEX) ? 2u : 0u, hadamard_scale(c->index_dim),
+                 index_map(c)};
   }
   st = cuda_status(launch_append(a, reinterpret_cast<cudaStream_t>(stream)));
   if (st) return st;
@@ -297,6 +312,7 @@ ds4a_status ds4a_index_topk(const ds4a_layer_cache *c, uint32_t pos0, uint32_t T
   a.ws_bytes = ws_bytes;
   a.qat = (c->qat & DS4A_QAT_FP4_INDEX) != 0;
   a.had_c = hadamard_scale(c->index_dim);
+  a.map = index_map(c);
   return cuda_status(launch_index_topk(a, reinterpret_cast<cudaStream_t>(stream)));
 }
 
@@ -335,6 +351,7 @@ static ds4a_status attn_common(const ds4a_layer_cache *c, uint32_t pos0, uint32_
   a.out = out;
   a.ws = ws;
   a.ws_bytes = ws_bytes;
+  a.map = attn_map(c);
   return cuda_status(launch_attention(a, s));
 }
 

@@ -36,7 +36,7 @@ struct SlotVal {
 // every thread of the block (uniform).
 template <typename T, typename Get>
 __device__ void pool_norm_rope_store(const LaneArgs &L, uint32_t W, uint32_t b, uint32_t i,
-                                     uint32_t comp_cap, uint32_t pos, Get get, float *red) {
+                                     uint32_t pos, Get get, float *red) {
   const T *ape = static_cast<const T *>(L.ape);
   const T *gamma = static_cast<const T *>(L.gamma);
   T *comp = static_cast<T *>(L.comp);
@@ -75,7 +75,9 @@ __device__ void pool_norm_rope_store(const LaneArgs &L, uint32_t W, uint32_t b, 
   }
   ss = block_sum(ss, red);
   const float inv = 1.0f / sqrtf(ss / (float)width + kRmsEps);
-  T *row = comp + ((size_t)b * comp_cap + i) * width;
+  size_t prow;
+  const bool mapped = L.map.phys(b, i, prow);   // uniform; unmapped: computed, not stored
+  T *row = comp + prow * width;
 #pragma unroll
   for (int k = 0; k < kMaxPairsPerThread; ++k) {
     const uint32_t j = threadIdx.x + k * blockDim.x;
@@ -138,8 +140,10 @@ __device__ void pool_norm_rope_store(const LaneArgs &L, uint32_t W, uint32_t b, 
     const uint32_t j = threadIdx.x + k * blockDim.x;
     if (j >= npair) continue;
     const uint32_t c = 2 * j;
-    st_elem(row, c, y[k][0]);
-    st_elem(row, c + 1, y[k][1]);
+    if (mapped) {
+      st_elem(row, c, y[k][0]);
+      st_elem(row, c + 1, y[k][1]);
+    }
     st[k][0] = round_to(y[k][0], row);
     st[k][1] = round_to(y[k][1], row);
     mx = fmaxf(mx, fmaxf(fabsf(st[k][0]), fabsf(st[k][1])));
@@ -158,9 +162,9 @@ __device__ void pool_norm_rope_store(const LaneArgs &L, uint32_t W, uint32_t b, 
       }
     }
     ss = block_sum(ss, red);
-    if (threadIdx.x == 0) {
+    if (threadIdx.x == 0 && mapped) {
       const float nm = mx > 0.f ? norm_from_scaled(ss, e) : 0.f;
-      L.norm[(size_t)b * comp_cap + i] = nm;
+      L.norm[prow] = nm;
       atomicMax(&L.norm_max[b], __float_as_uint(nm));
     }
   }
@@ -169,12 +173,14 @@ __device__ void pool_norm_rope_store(const LaneArgs &L, uint32_t W, uint32_t b, 
 // Euclidean norm of stored indexer rows (rebuild after the caller wrote rows):
 // one warp per row, the same widening as at append time.
 template <typename T>
-__global__ void index_norms_kernel(const T *rows, uint32_t dim, uint32_t comp_cap,
-                                   uint32_t n_rows, float *norm, uint32_t *norm_max) {
+__global__ void index_norms_kernel(const T *rows, RowMap map, uint32_t dim, uint32_t n_rows,
+                                   float *norm, uint32_t *norm_max) {
   const uint32_t b = blockIdx.y, lane = threadIdx.x & 31;
   const uint32_t r = blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
   if (r >= n_rows) return;
-  const T *row = rows + ((size_t)b * comp_cap + r) * dim;
+  size_t prow;
+  if (!map.phys(b, r, prow)) return;   // warp-uniform
+  const T *row = rows + prow * dim;
   float mx = 0.f;
   for (uint32_t c = lane; c < dim; c += 32) mx = fmaxf(mx, fabsf(ld_f32(row, c)));
   mx = warp_max(mx);
@@ -188,7 +194,7 @@ __global__ void index_norms_kernel(const T *rows, uint32_t dim, uint32_t comp_ca
   ss = warp_sum(ss);
   if (lane == 0) {
     const float nm = mx > 0.f ? norm_from_scaled(ss, e) : 0.f;
-    norm[(size_t)b * comp_cap + r] = nm;
+    norm[prow] = nm;
     atomicMax(&norm_max[b], __float_as_uint(nm));
   }
 }
@@ -247,7 +253,7 @@ __global__ void __launch_bounds__(kThreads) append_step_kernel(AppendArgs a) {
   // The store above gives thread t channel t; the pool gives it channels 2t
   // and 2t + 1, written by other threads: make the stores visible first.
   __syncthreads();
-  pool_norm_rope_store<T>(L, W, b, i, a.comp_cap, i * r, get, red);
+  pool_norm_rope_store<T>(L, W, b, i, i * r, get, red);
   if (r == 4) {
     __syncthreads();  // every pool read of slots 0..3 is done
     for (uint32_t c = threadIdx.x; c < width; c += blockDim.x) {
@@ -307,7 +313,7 @@ __global__ void __launch_bounds__(kThreads)
   const LaneArgs &L = a.lane[l];
   const uint32_t r = a.ratio, i = a.pos0 / r + e;
   ChunkSlot<T> get{&L, r, a.window, b, i, a.pos0, a.T};
-  pool_norm_rope_store<T>(L, a.window, b, i, a.comp_cap, i * r, get, red);
+  pool_norm_rope_store<T>(L, a.window, b, i, i * r, get, red);
 }
 
 // State after the chunk, as the token-by-token process leaves it.
@@ -418,17 +424,17 @@ cudaError_t launch_state_reset(float *kv, float *score, size_t n, cudaStream_t s
   return cudaGetLastError();
 }
 
-cudaError_t launch_index_norms(int dtype, const void *rows, uint32_t dim, uint32_t batch,
-                               uint32_t comp_cap, uint32_t n_rows, float *norm,
-                               uint32_t *norm_max, cudaStream_t s) {
+cudaError_t launch_index_norms(int dtype, const void *rows, const RowMap &map, uint32_t dim,
+                               uint32_t batch, uint32_t n_rows, float *norm, uint32_t *norm_max,
+                               cudaStream_t s) {
   if (n_rows == 0) return cudaSuccess;
   const dim3 grid((n_rows + 7) / 8, batch);
   if (dtype == DS4A_BF16)
-    index_norms_kernel<<<grid, 256, 0, s>>>(static_cast<const __nv_bfloat16 *>(rows), dim,
-                                            comp_cap, n_rows, norm, norm_max);
-  else
-    index_norms_kernel<<<grid, 256, 0, s>>>(static_cast<const float *>(rows), dim, comp_cap,
+    index_norms_kernel<<<grid, 256, 0, s>>>(static_cast<const __nv_bfloat16 *>(rows), map, dim,
                                             n_rows, norm, norm_max);
+  else
+    index_norms_kernel<<<grid, 256, 0, s>>>(static_cast<const float *>(rows), map, dim, n_rows,
+                                            norm, norm_max);
   note_launches(1);
   return cudaGetLastError();
 }

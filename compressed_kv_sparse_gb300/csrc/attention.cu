@@ -126,7 +126,7 @@ __global__ void __launch_bounds__(kThreads)
 
   const T *ring = static_cast<const T *>(a.ring) + (size_t)b * a.cap_raw * D;
   const T *chunk = a.chunk ? static_cast<const T *>(a.chunk) + (size_t)b * a.T * D : nullptr;
-  const T *comp = a.comp ? static_cast<const T *>(a.comp) + (size_t)b * a.comp_cap * D : nullptr;
+  const T *comp = static_cast<const T *>(a.comp);   // pool base: rows via a.map
   const uint32_t lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
 
   for (uint32_t r0 = r_begin; r0 < r_end; r0 += S) {
@@ -146,7 +146,7 @@ __global__ void __launch_bounds__(kThreads)
         } else {
           const uint32_t j = g - n_w;
           const int32_t idx = a.ratio == 4 ? tk[j] : (int32_t)j;
-          if (idx >= 0) off = (1ll << 61) | (long long)idx * D;
+          if (idx >= 0) off = (1ll << 61) | (long long)(a.map.row_of(b, (uint32_t)idx) * D);
         }
       }
       roff[r] = off;

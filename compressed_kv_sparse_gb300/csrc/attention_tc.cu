@@ -50,6 +50,7 @@ constexpr float kRaiseLog2 = 8.0f;     // raise the running max beyond 2^8
 
 struct TcAttnParams {
   uint32_t ratio, batch, T, pos0, cap_raw, comp_cap, n_comp, top_k;
+  RowMap map;         // rows of comp
   uint32_t cluster;   // decode: CTAs per query (one cluster); 0: prefill, persistent CTAs
   uint32_t n_q;       // queries = batch * T
   float c2;           // softmax scale * log2(e)
@@ -154,7 +155,7 @@ __device__ __forceinline__ const __nv_bfloat16 *row_src(const TcAttnParams &P, c
   if (r < g.N) {
     const uint32_t j = r - g.n_w;
     const int32_t idx = P.ratio == 4 ? g.tk[j] : (int32_t)j;
-    if (idx >= 0) return P.comp + ((size_t)g.b * P.comp_cap + (uint32_t)idx) * kD;
+    if (idx >= 0) return P.comp + P.map.row_of(g.b, (uint32_t)idx) * kD;
   }
   return nullptr;
 }
@@ -820,6 +821,7 @@ cudaError_t launch_attention_tc(const AttnArgs &a, uint32_t rows_max, int *err, 
   P.pos0 = a.pos0;
   P.cap_raw = a.cap_raw;
   P.comp_cap = a.comp_cap;
+  P.map = a.map;
   P.n_comp = a.n_comp;
   P.top_k = a.top_k;
   P.n_q = a.batch * a.T;

@@ -238,11 +238,11 @@ __global__ void __launch_bounds__(kRowsPerBlock)
   for (uint32_t i = threadIdx.x; i < Di * Hp; i += blockDim.x) qs[i] = qsrc[i];
   const T *w = static_cast<const T *>(a.w) + (size_t)qi * Hi;
   for (uint32_t h = threadIdx.x; h < Hp; h += blockDim.x) ws[h] = h < Hi ? ld_f32(w, h) : 0.f;
-  const T *keys = static_cast<const T *>(a.keys) + (size_t)b * a.comp_cap * Di;
+  const T *keys = static_cast<const T *>(a.keys);
   const uint32_t nrow = min((uint32_t)kRowsPerBlock, vis - row0);
   for (uint32_t i = threadIdx.x; i < nrow * Di; i += blockDim.x) {
     const uint32_t r = i / Di, d = i % Di;
-    ks[(size_t)r * ks_stride + d] = ld_f32(keys, (size_t)(row0 + r) * Di + d);
+    ks[(size_t)r * ks_stride + d] = ld_f32(keys, a.map.row_of(b, row0 + r) * Di + d);
   }
   __syncthreads();
   const uint32_t s = threadIdx.x;
@@ -635,7 +635,8 @@ template <int NW>
 __device__ __forceinline__ void rescore_band(const __nv_bfloat16 *qsm, const float *wsh,
                                              float *kbuf, float *relb, const uint32_t *band,
                                              uint32_t nband, const uint32_t *cidx, float *cS,
-                                             const __nv_bfloat16 *keys, uint32_t *rexact,
+                                             const __nv_bfloat16 *keys, const RowMap &map,
+                                             uint32_t b, uint32_t *rexact,
                                              int eq_min, int eq_max) {
   const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   constexpr uint32_t RPR = 2 * NW, NP = NW / 2;
@@ -646,7 +647,7 @@ __device__ __forceinline__ void rescore_band(const __nv_bfloat16 *qsm, const flo
       const uint32_t rr = 2 * warp + t;
       if (rr < nr) {   // warp-uniform
         float kk[4];
-        bf16x4(*reinterpret_cast<const uint2 *>(keys + (size_t)cidx[band[base + rr]] * 128 +
+        bf16x4(*reinterpret_cast<const uint2 *>(keys + map.row_of(b, cidx[band[base + rr]]) * 128 +
                                                 4 * lane),
                kk[0], kk[1], kk[2], kk[3]);
         *reinterpret_cast<float4 *>(kbuf + rr * 128 + 4 * lane) =
@@ -757,7 +758,7 @@ __global__ void __launch_bounds__(NT, NT == 256 ? 4 : 1)
     return;
   }
   float *sc = w.scores + (size_t)qi * a.comp_cap;
-  const float *nr = a.norms + (size_t)b * a.comp_cap;
+  const float *nr = a.norms;   // row r of this sequence: nr[a.map.row_of(b, r)]
   const __nv_bfloat16 *qb = w.qbf + (size_t)qi * Hi * Di;
   const __nv_bfloat16 *wq = static_cast<const __nv_bfloat16 *>(a.w) + (size_t)qi * Hi;
   uint32_t *ctrl = w.ctrl + (size_t)qi * 4;
@@ -902,7 +903,7 @@ __global__ void __launch_bounds__(NT, NT == 256 ? 4 : 1)
       for (uint32_t j = 0; j < J; ++j) {
         const uint32_t r = pass + j * NT + threadIdx.x;
         Sv[j] = r < r1 ? sc[r] : 0.f;
-        Nv[j] = r < r1 ? nr[r] : 0.f;
+        Nv[j] = r < r1 ? nr[a.map.row_of(b, r)] : 0.f;
       }
 #pragma unroll
       for (uint32_t j = 0; j < J; ++j) {
@@ -955,7 +956,7 @@ __global__ void __launch_bounds__(NT, NT == 256 ? 4 : 1)
     __syncthreads();
   }
 
-  const __nv_bfloat16 *keys = static_cast<const __nv_bfloat16 *>(a.keys) + (size_t)b * a.comp_cap * Di;
+  const __nv_bfloat16 *keys = static_cast<const __nv_bfloat16 *>(a.keys);   // rows via a.map
   float *kb = kbuf + warp * 128, *rel = relb + warp * 64;
   const uint32_t nc = G == 1 ? s_misc[2] : *(volatile uint32_t *)&ctrl[0];
   const bool fast = nc <= CAP && (G == 1 ? s_misc[3] >= k : *(volatile uint32_t *)&ctrl[2] == 0u);
@@ -1090,8 +1091,8 @@ __global__ void __launch_bounds__(NT, NT == 256 ? 4 : 1)
         if ((cls >> (2 * u)) & 2u) band[atomicAdd(&s_misc[1], 1u)] = j;
       __syncthreads();
       // exact scores of the band
-      rescore_band<SC::NW>(qsm, wsh, kbuf, relb, band, nband, cidx, cS, keys, s_rexact, eq_min,
-                           eq_max);
+      rescore_band<SC::NW>(qsm, wsh, kbuf, relb, band, nband, cidx, cS, keys, a.map, b, s_rexact,
+                           eq_min, eq_max);
       float *bV = scratch;
       uint32_t *bI = reinterpret_cast<uint32_t *>(scratch + SC::BANDCAP);
       for (uint32_t i = threadIdx.x; i < nband; i += blockDim.x) {
@@ -1147,7 +1148,7 @@ __global__ void __launch_bounds__(NT, NT == 256 ? 4 : 1)
   __syncthreads();
   for (uint32_t s = threadIdx.x; s < vis; s += blockDim.x) {
     const float S = sc[s];
-    const float e = err_of(S, nr[s]);
+    const float e = err_of(S, nr[a.map.row_of(b, s)]);
     if (S - e > hi_cut) {
       sc[s] = INFINITY;
     } else if (S + e < lo_cut) {
@@ -1162,14 +1163,16 @@ __global__ void __launch_bounds__(NT, NT == 256 ? 4 : 1)
   if (nband <= CAP) {
     for (uint32_t i = warp; i < nband; i += SC::NW) {
       const uint32_t s = band[i];
-      const float V = rescore_row(qsm, wsh, kb, rel, keys + (size_t)s * Di, lane, eq_min, eq_max);
+      const float V = rescore_row(qsm, wsh, kb, rel, keys + a.map.row_of(b, s) * Di, lane, eq_min,
+                                  eq_max);
       if (lane == 0) sc[s] = V;
     }
   } else {
     for (uint32_t s = warp; s < vis; s += SC::NW) {
       const float v = sc[s];
       if (v == INFINITY || v == -INFINITY) continue;
-      const float V = rescore_row(qsm, wsh, kb, rel, keys + (size_t)s * Di, lane, eq_min, eq_max);
+      const float V = rescore_row(qsm, wsh, kb, rel, keys + a.map.row_of(b, s) * Di, lane, eq_min,
+                                  eq_max);
       if (lane == 0) sc[s] = V;
     }
   }
@@ -1239,6 +1242,7 @@ cudaError_t launch_index_tc(const IndexArgs &a, cudaStream_t s) {
     t.scores = w.scores;
     t.hist = scorer_hist ? w.hist : nullptr;
     t.err = w.err;
+    t.map = a.map;
     cudaError_t e = launch_index_score_tc(t, s);
     if (e != cudaSuccess) return e;
   }

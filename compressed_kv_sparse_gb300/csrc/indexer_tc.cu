@@ -55,6 +55,7 @@ struct Cfg {
 struct ScoreParams {
   uint32_t batch, T, pos0, comp_cap, n_comp, n_groups, tiles_per, total_items;
   uint32_t cta_per_group;   // > 0: that many CTAs per (sequence, group), none crossing one
+  RowMap map;               // paged keys (map.table != NULL): 64-row blocks of the pool
   const __nv_bfloat16 *w;   // [B][T][Hi]
   float *scores;            // [B][T][comp_cap]
   uint32_t *hist;           // [B*T][4096] counts of the top 12 bits of the score keys
@@ -151,17 +152,31 @@ __global__ void __launch_bounds__(Cfg<QG>::kThreads, 1)
       int32_t cur = -1;
       int issued[C::kStages];
       for (int s = 0; s < C::kStages; ++s) issued[s] = -1;
+      // one 128-row key tile: two 64-dim K blocks, each one box of 128 rows
+      // (contiguous keys) or two boxes of 64 rows from the tile's two
+      // physical blocks (paged)
+      auto issue_a = [&](uint32_t st, uint32_t b, uint32_t tile) {
+        uint8_t *dst = sA + (size_t)st * kABytes;
+        mbar_arrive_expect_tx(&a_full[st], kABytes);
+        if (!P.map.table) {
+          tma_load_3d(dst, &tmap_k, &a_full[st], 0, (int)(tile * kRows), (int)b);
+          tma_load_3d(dst + kKBlockBytes, &tmap_k, &a_full[st], 64, (int)(tile * kRows), (int)b);
+        } else {
+#pragma unroll
+          for (uint32_t hb = 0; hb < 2; ++hb) {
+            const int y = (int)P.map.row_of(b, tile * kRows + 64 * hb);
+            tma_load_2d(dst + hb * (kKBlockBytes / 2), &tmap_k, &a_full[st], 0, y);
+            tma_load_2d(dst + kKBlockBytes + hb * (kKBlockBytes / 2), &tmap_k, &a_full[st], 64, y);
+          }
+        }
+      };
       // the key tiles of the first stages load before the wait for the
       // previous launch: the rows were written two or more launches back
       uint32_t pre = 0;
       for (uint32_t it = it0; it < it1 && pre < (uint32_t)C::kStages; ++it) {
         uint32_t b, g, tile;
         if (!decode_item<QG>(P, it, b, g, tile)) continue;
-        mbar_arrive_expect_tx(&a_full[pre], kABytes);
-        tma_load_3d(sA + (size_t)pre * kABytes, &tmap_k, &a_full[pre], 0, (int)(tile * kRows),
-                    (int)b);
-        tma_load_3d(sA + (size_t)pre * kABytes + kKBlockBytes, &tmap_k, &a_full[pre], 64,
-                    (int)(tile * kRows), (int)b);
+        issue_a(pre, b, tile);
         issued[pre] = 0;
         ++pre;
       }
@@ -185,11 +200,7 @@ __global__ void __launch_bounds__(Cfg<QG>::kThreads, 1)
         }
         if (n_vis++ >= pre) {   // (the first `pre` are in flight already)
           if (!mbar_wait(&a_empty[stage], phase ^ 1, P.err)) break;
-          mbar_arrive_expect_tx(&a_full[stage], kABytes);
-          tma_load_3d(sA + (size_t)stage * kABytes, &tmap_k, &a_full[stage], 0,
-                      (int)(tile * kRows), (int)b);
-          tma_load_3d(sA + (size_t)stage * kABytes + kKBlockBytes, &tmap_k, &a_full[stage], 64,
-                      (int)(tile * kRows), (int)b);
+          issue_a(stage, b, tile);
           issued[stage] = (int)phase;
         }
         if (++stage == C::kStages) {
@@ -361,10 +372,18 @@ template <int QG>
 cudaError_t launch_qg(const IndexTcArgs &a, cudaStream_t s) {
   using C = Cfg<QG>;
   CUtensorMap tk, tq;
-  const uint64_t kd[3] = {kDim, a.comp_cap, a.batch};
-  const uint64_t ks[2] = {(uint64_t)kDim * 2, (uint64_t)a.comp_cap * kDim * 2};
-  const uint32_t kb[3] = {64, kRows, 1};
-  cudaError_t e = make_tmap_bf16(&tk, a.keys, 3, kd, ks, kb);
+  cudaError_t e;
+  if (!a.map.table) {
+    const uint64_t kd[3] = {kDim, a.comp_cap, a.batch};
+    const uint64_t ks[2] = {(uint64_t)kDim * 2, (uint64_t)a.comp_cap * kDim * 2};
+    const uint32_t kb[3] = {64, kRows, 1};
+    e = make_tmap_bf16(&tk, a.keys, 3, kd, ks, kb);
+  } else {   // the pool as [n_blocks * 64][128], boxes of 64 rows
+    const uint64_t kd[2] = {kDim, (uint64_t)a.map.n_blocks * a.map.rpb};
+    const uint64_t ks[1] = {(uint64_t)kDim * 2};
+    const uint32_t kb[2] = {64, 64};
+    e = make_tmap_bf16(&tk, a.keys, 2, kd, ks, kb);
+  }
   if (e != cudaSuccess) return e;
   const uint64_t qd[2] = {kDim, (uint64_t)a.batch * a.T * kHeads};
   const uint64_t qs[1] = {(uint64_t)kDim * 2};
@@ -385,6 +404,7 @@ cudaError_t launch_qg(const IndexTcArgs &a, cudaStream_t s) {
   P.scores = a.scores;
   P.hist = a.hist;
   P.err = a.err;
+  P.map = a.map;
   if (P.total_items == 0) return cudaSuccess;
   static int smem_set = 0;
   e = ensure_smem(index_score_tc_kernel<QG>, C::kSmem, &smem_set);

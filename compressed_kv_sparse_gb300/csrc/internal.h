@@ -43,6 +43,37 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
   return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args &&>(args)...);
 }
 
+// Where row i of sequence b of a compressed lane lives. Contiguous (table
+// NULL): row b * cap + i. Paged: the logical block i / rpb of sequence b is
+// physical block table[b * max_blocks + i / rpb] and the row is that block's
+// row i % rpb. An entry outside [0, n_blocks) is a caller error: its rows
+// are not written, and reads of them return rows of block 0 (every access
+// stays inside the pools). phys() returns false for such rows and for rows
+// past the table's max_blocks logical blocks.
+struct RowMap {
+  const int32_t *table;
+  uint32_t cap, max_blocks, rpb, n_blocks;
+#ifdef __CUDACC__
+  __device__ __forceinline__ bool phys(uint32_t b, uint32_t i, size_t &row) const {
+    if (!table) {
+      row = (size_t)b * cap + i;
+      return true;
+    }
+    const uint32_t lb = i / rpb;   // (rows past the last logical block: block 0, not ok)
+    const uint32_t blk = lb < max_blocks ? (uint32_t)__ldg(table + (size_t)b * max_blocks + lb)
+                                         : 0xffffffffu;
+    const bool ok = blk < n_blocks;
+    row = (size_t)(ok ? blk : 0u) * rpb + i % rpb;
+    return ok;
+  }
+  __device__ __forceinline__ size_t row_of(uint32_t b, uint32_t i) const {
+    size_t r;
+    phys(b, i, r);
+    return r;
+  }
+#endif
+};
+
 // TMA tensor map over bf16 data with 128-byte swizzle (tmap.cu).
 cudaError_t make_tmap_bf16(CUtensorMap *map, const void *base, int rank, const uint64_t *dims,
                            const uint64_t *strides_bytes, const uint32_t *box);
@@ -60,6 +91,7 @@ struct LaneArgs {
   uint32_t *norm_max;             // [B] float bits of the largest norm
   uint32_t quant;                 // step 8: 0 none, 1 FP8 non-RoPE dims, 2 FP4 QAT
   float had_c;                    // 1/sqrt(width) in fp32 (quant 2)
+  RowMap map;                     // rows of comp (and norm)
 };
 
 struct AppendArgs {
@@ -87,6 +119,7 @@ struct IndexArgs {
   size_t ws_bytes;
   bool qat;                       // FP4 QAT round trip of the rotated query
   float had_c;                    // 1/sqrt(dim) in fp32
+  RowMap map;                     // rows of keys and norms
 };
 size_t index_ws_bytes(int dtype, uint32_t batch, uint32_t T, uint32_t n_heads, uint32_t dim,
                       uint32_t comp_cap);
@@ -100,6 +133,7 @@ struct IndexTcArgs {
   float *scores;      // [B][T][comp_cap]
   uint32_t *hist;     // [B*T][4096], zeroed before the call
   int *err;
+  RowMap map;         // rows of keys
 };
 bool index_tc_supported(uint32_t n_heads, uint32_t dim);
 cudaError_t launch_index_score_tc(const IndexTcArgs &a, cudaStream_t s);
@@ -118,6 +152,7 @@ struct AttnArgs {
   void *out;              // [B][T][H][D]
   void *ws;
   size_t ws_bytes;
+  RowMap map;             // rows of comp
 };
 size_t attn_ws_bytes(int dtype, uint32_t ratio, uint32_t batch, uint32_t T, uint32_t n_heads,
                      uint32_t head_dim, uint32_t n_rot, uint32_t cap_raw, uint32_t comp_cap,
@@ -132,8 +167,8 @@ cudaError_t launch_ring_commit(int dtype, uint32_t batch, uint32_t T, uint32_t p
                                uint32_t cap_raw, uint32_t head_dim, const void *chunk,
                                void *ring, cudaStream_t s);
 cudaError_t launch_state_reset(float *kv, float *score, size_t n, cudaStream_t s);
-cudaError_t launch_index_norms(int dtype, const void *rows, uint32_t dim, uint32_t batch,
-                               uint32_t comp_cap, uint32_t n_rows, float *norm,
-                               uint32_t *norm_max, cudaStream_t s);
+cudaError_t launch_index_norms(int dtype, const void *rows, const RowMap &map, uint32_t dim,
+                               uint32_t batch, uint32_t n_rows, float *norm, uint32_t *norm_max,
+                               cudaStream_t s);
 
 }  // namespace ds4a

@@ -45,7 +45,8 @@ class LayerCacheC(ctypes.Structure):
         ("index_norm_max", ctypes.c_void_p), ("rope_cos", ctypes.c_void_p),
         ("rope_sin", ctypes.c_void_p), ("index_rope_cos", ctypes.c_void_p),
         ("index_rope_sin", ctypes.c_void_p), ("rope_max_pos", ctypes.c_uint32),
-        ("qat", ctypes.c_uint32)]
+        ("qat", ctypes.c_uint32), ("block_table", ctypes.c_void_p),
+        ("max_blocks", ctypes.c_uint32), ("n_blocks", ctypes.c_uint32)]
 
 QAT_FP8_ATTN = 1    # DS4A_QAT_FP8_ATTN
 QAT_FP4_INDEX = 2   # DS4A_QAT_FP4_INDEX
@@ -146,11 +147,17 @@ def rope_table(base: float, n_rot: int, n_pos: int, device) -> tuple:
 
 
 class LayerCache:
-    """Device memory of one layer's cache (torch tensors) and its C struct."""
+    """Device memory of one layer's cache (torch tensors) and its C struct.
+
+    block_table ([B][max_blocks] int32 on the device) makes the compressed rows
+    paged: pools of n_blocks blocks of 256 token positions (256 / ratio rows);
+    comp_cap is then max_blocks * 256 / ratio. ``logical(name)`` gathers a
+    pool back into the contiguous [B][comp_cap][...] view."""
 
     def __init__(self, *, ratio: int, head_dim: int, n_rot: int, batch: int, comp_cap: int,
                  dtype: str, base: float, rope_max_pos: int, index_dim: int = 0,
-                 index_rot: int = 0, cap_raw: int = 128, qat: int = 0, device="cuda"):
+                 index_rot: int = 0, cap_raw: int = 128, qat: int = 0, device="cuda",
+                 block_table: Optional[torch.Tensor] = None, n_blocks: int = 0):
         td = {"f32": torch.float32, "bf16": torch.bfloat16}[dtype]
         self.dtype, self.torch_dtype = dtype, td
         self.ratio, self.head_dim, self.n_rot = ratio, head_dim, n_rot
@@ -158,21 +165,31 @@ class LayerCache:
         self.cap_raw, self.comp_cap, self.base = cap_raw, comp_cap, base
         W = {0: 0, 4: 8, 128: 128}[ratio]
         z = lambda *s, dt=td: torch.zeros(s, dtype=dt, device=device)
+        self.block_table, self.n_blocks = block_table, n_blocks
+        paged = block_table is not None
+        if paged:
+            assert block_table.dtype == torch.int32 and block_table.shape[0] == batch
+            assert comp_cap == block_table.shape[1] * (256 // ratio)
+        rpb = 256 // ratio if ratio else 0
+        # comp rows: [B][comp_cap][w] or a pool [n_blocks][rows per block][w]
+        rows = (lambda w, r, dt=td: z(n_blocks, r, w, dt=dt)) if paged else \
+               (lambda w, r, dt=td: z(batch, comp_cap, w, dt=dt))
         self.raw_kv = z(batch, cap_raw, head_dim)
         self.attn_comp_kv = self.attn_state_kv = self.attn_state_score = None
         self.index_comp_kv = self.index_state_kv = self.index_state_score = None
         self.index_norm = self.index_norm_max = None
         if ratio:
-            self.attn_comp_kv = z(batch, comp_cap, head_dim)
+            self.attn_comp_kv = rows(head_dim, rpb)
             self.attn_state_kv = z(batch, W, head_dim, dt=torch.float32)
             self.attn_state_score = torch.full((batch, W, head_dim), float("-inf"),
                                                device=device)
         if ratio == 4:
-            self.index_comp_kv = z(batch, comp_cap, index_dim)
+            self.index_comp_kv = rows(index_dim, 64)
             self.index_state_kv = z(batch, 8, index_dim, dt=torch.float32)
             self.index_state_score = torch.full((batch, 8, index_dim), float("-inf"),
                                                 device=device)
-            self.index_norm = z(batch, comp_cap, dt=torch.float32)
+            self.index_norm = (z(n_blocks, 64, dt=torch.float32) if paged
+                               else z(batch, comp_cap, dt=torch.float32))
             self.index_norm_max = z(batch, dt=torch.int32)
         self.rope_cos, self.rope_sin = rope_table(base, n_rot, rope_max_pos, device)
         self.index_rope_cos = self.index_rope_sin = None
@@ -189,7 +206,20 @@ class LayerCache:
             index_state_score=_ptr(self.index_state_score), index_norm=_ptr(self.index_norm),
             index_norm_max=_ptr(self.index_norm_max), rope_cos=_ptr(self.rope_cos),
             rope_sin=_ptr(self.rope_sin), index_rope_cos=_ptr(self.index_rope_cos),
-            index_rope_sin=_ptr(self.index_rope_sin), rope_max_pos=rope_max_pos, qat=qat)
+            index_rope_sin=_ptr(self.index_rope_sin), rope_max_pos=rope_max_pos, qat=qat,
+            block_table=_ptr(block_table), max_blocks=block_table.shape[1] if paged else 0,
+            n_blocks=n_blocks if paged else 0)
+
+    def logical(self, name: str) -> torch.Tensor:
+        """[B][comp_cap][...] view of compressed rows / row norms (a gather
+        through the block table when paged)."""
+        t = getattr(self, name)
+        if self.block_table is None or name not in ("attn_comp_kv", "index_comp_kv",
+                                                     "index_norm"):
+            return t
+        tb = self.block_table.long()                       # [B][max_blocks]
+        g = t[tb.clamp(0, self.n_blocks - 1)]              # [B][max_blocks][rpb](...)
+        return g.reshape((self.batch, self.comp_cap) + tuple(t.shape[2:]))
 
     @property
     def n_tokens(self) -> int:
@@ -207,7 +237,14 @@ class LayerCache:
         n_tokens and rebuild the indexer row norms (ds4a_index_norms)."""
         for name, t in hist.items():
             dst = getattr(self, name)
-            if name in ("attn_comp_kv", "index_comp_kv") and t.shape[1] < dst.shape[1]:
+            if self.block_table is not None and name in ("attn_comp_kv", "index_comp_kv"):
+                rpb, nb = dst.shape[1], (t.shape[1] + dst.shape[1] - 1) // dst.shape[1]
+                src = torch.zeros((self.batch, nb * rpb) + tuple(t.shape[2:]), dtype=t.dtype,
+                                  device=t.device)
+                src[:, :t.shape[1]] = t
+                idx = self.block_table[:, :nb].reshape(-1).long().to(dst.device)
+                dst[idx] = src.reshape((self.batch * nb, rpb) + tuple(t.shape[2:])).to(dst.device)
+            elif name in ("attn_comp_kv", "index_comp_kv") and t.shape[1] < dst.shape[1]:
                 dst[:, :t.shape[1]].copy_(t)
             else:
                 dst.copy_(t)

@@ -100,6 +100,20 @@ typedef enum { DS4A_F32 = 0, DS4A_BF16 = 1 } ds4a_dtype;
  *                    compressed indexer rows, and in ds4a_index_topk the
  *                    rotated queries, take the FP4 QAT round trip. 0 = off.
  *                    Scales and arithmetic: see DS4A_QAT_FP8_ATTN below.
+ *  block_table       NULL: compressed rows are contiguous per sequence as laid
+ *                    out above. Non-NULL (ratio != 0): a paged cache (vLLM's
+ *                    page: one logical block = 256 token positions on every
+ *                    compressed layer, i.e. 64 rows on c4a, 2 on c128a).
+ *                    [B][max_blocks] int32 DEVICE array: entry (b, j) is the
+ *                    physical block holding rows 256/ratio * j .. of sequence
+ *                    b. Then attn_comp_kv is a pool [n_blocks][256/ratio][D],
+ *                    index_comp_kv [n_blocks][64][Di] and index_norm
+ *                    [n_blocks][64], and comp_cap must equal
+ *                    max_blocks * 256/ratio. Sequences may share blocks (a
+ *                    common prefix) when nothing appends into them. Entries
+ *                    must lie in [0, n_blocks); an entry outside is not
+ *                    written to, and reads of its rows return rows of block 0.
+ *  max_blocks, n_blocks  see block_table (ignored when it is NULL).
  *
  * State layout: ratio 4 keeps the last complete group of 4 tokens in slots
  * 0..3 and token p of the current group in slot 4 + p % 4 (page §5's 8-row
@@ -121,6 +135,8 @@ typedef struct {
   const float *index_rope_cos, *index_rope_sin;
   uint32_t rope_max_pos;
   uint32_t qat;
+  const int32_t *block_table;
+  uint32_t max_blocks, n_blocks;
 } ds4a_layer_cache;
 
 /*

@@ -161,6 +161,16 @@ def test_argument_checks_reject_before_launch(L):
                                         lib.LANE_ATTN, *P, None, None) == -1
     assert L.ds4a_compress_append_lanes(r, 9, 1, lib.LANE_RAW, *P, None, None) == -4
     assert c.n_tokens == 10
+    # paged cache: a table on a window-only layer, comp_cap not max_blocks rows
+    # of 256 positions, no blocks
+    bad = _fake_cache(ratio=0)
+    bad.block_table, bad.max_blocks, bad.n_blocks = fake, 4, 8
+    assert L.ds4a_compress_append(ctypes.byref(bad), 10, 1, *P, None, None) == -1
+    bad = _fake_cache()
+    bad.block_table, bad.max_blocks, bad.n_blocks = fake, 4, 8   # 4 blocks = 256 rows != 16
+    assert L.ds4a_compress_append(ctypes.byref(bad), 10, 1, *P, None, None) == -2
+    bad.max_blocks, bad.n_blocks = 1, 0
+    assert L.ds4a_compress_append(ctypes.byref(bad), 10, 1, *P, None, None) == -1
     # step-8 flags: unknown bit, FP4 off ratio 4, FP4 with Di not a power of two,
     # FP8 on a window-only layer
     for ratio, q, dim, want in ((4, 4, 128, -1), (128, 2, 128, -1), (4, 2, 96, -2),
