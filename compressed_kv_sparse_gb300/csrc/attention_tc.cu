@@ -144,6 +144,7 @@ __device__ __forceinline__ QueryGeo query_geo(const TcAttnParams &P, uint32_t qi
 }
 
 // Source row of list entry r (nullptr: masked).
+template <bool PAGED>
 __device__ __forceinline__ const __nv_bfloat16 *row_src(const TcAttnParams &P, const QueryGeo &g,
                                                         uint32_t r) {
   if (r < g.n_w) {
@@ -155,7 +156,10 @@ __device__ __forceinline__ const __nv_bfloat16 *row_src(const TcAttnParams &P, c
   if (r < g.N) {
     const uint32_t j = r - g.n_w;
     const int32_t idx = P.ratio == 4 ? g.tk[j] : (int32_t)j;
-    if (idx >= 0) return P.comp + P.map.row_of(g.b, (uint32_t)idx) * kD;
+    if (idx >= 0) {
+      if (PAGED) return P.comp + P.map.row_of(g.b, (uint32_t)idx) * kD;
+      return P.comp + ((size_t)g.b * P.comp_cap + (uint32_t)idx) * kD;
+    }
   }
   return nullptr;
 }
@@ -248,7 +252,7 @@ __device__ __forceinline__ bool merge_heads(const TcAttnParams &P, Smem &S, uint
 
 // DEC: decode (clusters of P.cluster CTAs per query) or prefill (persistent
 // CTAs); two instantiations keep each path's code to itself
-template <bool DEC>
+template <bool DEC, bool PAGED>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, TcAttnParams P) {
   extern __shared__ uint8_t smem_raw[];
@@ -315,7 +319,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const __nv_bfloat16 *src[8];
 #pragma unroll
       for (uint32_t i = 0; i < 8; ++i)
-        src[i] = row_src(P, g, tile * kRows + lw * 32 + (lane >> 3) + 4 * i);
+        src[i] = row_src<PAGED>(P, g, tile * kRows + lw * 32 + (lane >> 3) + 4 * i);
       const uint32_t cc = lane & 7;
       for (uint32_t kb = 0; kb < 8; ++kb) {
         if ((kb & 1) == 0 && !mbar_wait_warp(&S.kv_empty[kb >> 1], (n & 1) ^ 1, ew)) return false;
@@ -745,8 +749,10 @@ int max_active_clusters(uint32_t C, size_t smem) {
   if (C > 8) {
     int np = g_nonportable[dev].load(std::memory_order_relaxed);
     if (np == 0) {
-      np = cudaFuncSetAttribute(attn_tc_kernel<true>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) ==
-                   cudaSuccess
+      np = cudaFuncSetAttribute(attn_tc_kernel<true, false>,
+                                cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess &&
+                   cudaFuncSetAttribute(attn_tc_kernel<true, true>,
+                                        cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess
                ? 1
                : -1;
       (void)cudaGetLastError();
@@ -768,7 +774,7 @@ int max_active_clusters(uint32_t C, size_t smem) {
   cfg.dynamicSmemBytes = smem;
   cfg.attrs = at;
   cfg.numAttrs = 1;
-  if (cudaOccupancyMaxActiveClusters(&v, attn_tc_kernel<true>, &cfg) != cudaSuccess || v <= 0) {
+  if (cudaOccupancyMaxActiveClusters(&v, attn_tc_kernel<true, false>, &cfg) != cudaSuccess || v <= 0) {
     (void)cudaGetLastError();
     // beyond the portable size an unanswered query means the size is not used
     v = C > 8 ? -1 : num_sms() / (int)C;
@@ -838,9 +844,14 @@ cudaError_t launch_attention_tc(const AttnArgs &a, uint32_t rows_max, int *err, 
   P.ml = nullptr;
   P.err = err;
   const size_t smem = sizeof(Smem) + 1024;
-  static int smem_dec = 0, smem_pf = 0;
-  cudaError_t e = a.T == 1 ? ensure_smem(attn_tc_kernel<true>, smem, &smem_dec)
-                           : ensure_smem(attn_tc_kernel<false>, smem, &smem_pf);
+  // paged rows: an instantiation of its own, so the contiguous gathers carry
+  // no table code
+  const bool paged = a.map.table != nullptr;
+  auto *k_dec = paged ? attn_tc_kernel<true, true> : attn_tc_kernel<true, false>;
+  auto *k_pf = paged ? attn_tc_kernel<false, true> : attn_tc_kernel<false, false>;
+  static int smem_set[2][2] = {{0, 0}, {0, 0}};
+  cudaError_t e = a.T == 1 ? ensure_smem(k_dec, smem, &smem_set[1][paged])
+                           : ensure_smem(k_pf, smem, &smem_set[0][paged]);
   if (e != cudaSuccess) return e;
   // Q as [n_q * 64 heads][512] bf16 rows; boxes of 64 heads x 64 dims
   CUtensorMap tq;
@@ -867,13 +878,13 @@ cudaError_t launch_attention_tc(const AttnArgs &a, uint32_t rows_max, int *err, 
     at[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = at;
     cfg.numAttrs = 2;
-    e = cudaLaunchKernelEx(&cfg, attn_tc_kernel<true>, tq, P);
+    e = cudaLaunchKernelEx(&cfg, k_dec, tq, P);
     note_launches(1);
     return e != cudaSuccess ? e : cudaGetLastError();
   }
   P.cluster = 0;
   const uint32_t grid = min(P.n_q, (uint32_t)num_sms());
-  e = launch_pdl(attn_tc_kernel<false>, dim3(grid), dim3(kThreads), smem, s, tq, P);
+  e = launch_pdl(k_pf, dim3(grid), dim3(kThreads), smem, s, tq, P);
   note_launches(1);
   return e != cudaSuccess ? e : cudaGetLastError();
 }

@@ -759,6 +759,7 @@ __global__ void __launch_bounds__(NT, NT == 256 ? 4 : 1)
   }
   float *sc = w.scores + (size_t)qi * a.comp_cap;
   const float *nr = a.norms;   // row r of this sequence: nr[a.map.row_of(b, r)]
+  const float *nr_c = a.map.table ? nullptr : a.norms + (size_t)b * a.comp_cap;   // contiguous
   const __nv_bfloat16 *qb = w.qbf + (size_t)qi * Hi * Di;
   const __nv_bfloat16 *wq = static_cast<const __nv_bfloat16 *>(a.w) + (size_t)qi * Hi;
   uint32_t *ctrl = w.ctrl + (size_t)qi * 4;
@@ -903,7 +904,7 @@ __global__ void __launch_bounds__(NT, NT == 256 ? 4 : 1)
       for (uint32_t j = 0; j < J; ++j) {
         const uint32_t r = pass + j * NT + threadIdx.x;
         Sv[j] = r < r1 ? sc[r] : 0.f;
-        Nv[j] = r < r1 ? nr[a.map.row_of(b, r)] : 0.f;
+        Nv[j] = r < r1 ? (nr_c ? nr_c[r] : nr[a.map.row_of(b, r)]) : 0.f;
       }
 #pragma unroll
       for (uint32_t j = 0; j < J; ++j) {
