@@ -259,7 +259,8 @@ class Runner:
     def tokens_per_step(self):
         return self.wl.batch * self.T
 
-    # algorithmic bytes / FLOPs per call kind (measurement)
+    # algorithmic bytes / FLOPs per call kind: the bytes a call must move at
+    # least (rows it reads, inputs and outputs) and its useful multiply-adds
     def algorithmic(self):
         B, T = self.wl.batch, self.T
         out = {}
