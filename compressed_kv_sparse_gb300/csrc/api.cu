@@ -179,6 +179,7 @@ ds4a_status append_parts(ds4a_layer_cache *c, uint32_t pos0, uint32_t T, uint32_
   ds4a_status st = check_cache(c);
   if (st) return st;
   if (T == 0) return DS4A_ERR_SHAPE;
+  if (c->seq_pos && T != 1) return DS4A_ERR_ARG;   // ragged batches decode one token
   if (!lanes || (lanes & ~(DS4A_LANE_RAW | DS4A_LANE_ATTN | DS4A_LANE_INDEX))) return DS4A_ERR_ARG;
   const bool raw = lanes & DS4A_LANE_RAW;
   const bool la = lanes & DS4A_LANE_ATTN, li = lanes & DS4A_LANE_INDEX;
@@ -208,6 +209,7 @@ ds4a_status append_parts(ds4a_layer_cache *c, uint32_t pos0, uint32_t T, uint32_
   a.cos = c->rope_cos;
   a.sin = c->rope_sin;
   a.y0 = raw ? 0u : 1u;
+  a.seq_pos = c->seq_pos;
   a.n_lanes = 0;
   if (la) {
     a.lane[a.n_lanes++] =
@@ -284,6 +286,7 @@ ds4a_status ds4a_index_topk(const ds4a_layer_cache *c, uint32_t pos0, uint32_t T
   if (T == 0 || n_heads == 0 || n_heads > 128 || top_k == 0 || top_k > 2048) return DS4A_ERR_SHAPE;
   if (!q_idx || !w || !topk) return DS4A_ERR_ARG;
   if ((uint64_t)pos0 + T > c->n_tokens) return DS4A_ERR_POSITION;
+  if (c->seq_pos && T != 1) return DS4A_ERR_ARG;
   const uint32_t Hp = (n_heads + 7u) & ~7u;
   if (((size_t)c->index_dim * Hp + Hp + 128 * (size_t)(c->index_dim + 1)) * 4 > 227 * 1024)
     return DS4A_ERR_SHAPE;
@@ -313,6 +316,7 @@ ds4a_status ds4a_index_topk(const ds4a_layer_cache *c, uint32_t pos0, uint32_t T
   a.qat = (c->qat & DS4A_QAT_FP4_INDEX) != 0;
   a.had_c = hadamard_scale(c->index_dim);
   a.map = index_map(c);
+  a.seq_pos = c->seq_pos;
   return cuda_status(launch_index_topk(a, reinterpret_cast<cudaStream_t>(stream)));
 }
 
@@ -322,6 +326,7 @@ static ds4a_status attn_common(const ds4a_layer_cache *c, uint32_t pos0, uint32_
                                void *ws, size_t ws_bytes, cudaStream_t s) {
   if (T == 0 || n_heads == 0 || n_heads > 128) return DS4A_ERR_SHAPE;
   if (!q || !out) return DS4A_ERR_ARG;
+  if (c->seq_pos && T != 1) return DS4A_ERR_ARG;
   if (!std::isfinite(scale)) return DS4A_ERR_ARG;
   if (c->ratio == 4 && (!topk || top_k == 0 || top_k > 2048)) return DS4A_ERR_ARG;
   const size_t need = attn_ws_bytes(c->dtype, c->ratio, c->batch, T, n_heads, c->head_dim,
@@ -352,6 +357,7 @@ static ds4a_status attn_common(const ds4a_layer_cache *c, uint32_t pos0, uint32_
   a.ws = ws;
   a.ws_bytes = ws_bytes;
   a.map = attn_map(c);
+  a.seq_pos = c->seq_pos;
   return cuda_status(launch_attention(a, s));
 }
 

@@ -226,7 +226,7 @@ __global__ void __launch_bounds__(kThreads) append_step_kernel(AppendArgs a) {
   __shared__ float red[32];
   pdl_wait();
   pdl_trigger();
-  const uint32_t b = blockIdx.x, p = a.pos0, role = blockIdx.y + a.y0;
+  const uint32_t b = blockIdx.x, p = seq_base(a.seq_pos, a.pos0, b), role = blockIdx.y + a.y0;
   if (role == 0) {
     const T *src = static_cast<const T *>(a.raw_in) + (size_t)b * a.head_dim;
     T *dst = static_cast<T *>(a.raw_dst) +

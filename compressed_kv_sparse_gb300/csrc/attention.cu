@@ -76,7 +76,8 @@ __global__ void __launch_bounds__(kThreads)
   long long *roff = reinterpret_cast<long long *>(alpha + 2 * HG);  // [S] row offsets (-1 masked)
   __shared__ uint32_t s_nlist;
 
-  const uint32_t qi = blockIdx.z, b = qi / a.T, t = qi % a.T, p = a.pos0 + t;
+  const uint32_t qi = blockIdx.z, b = qi / a.T, t = qi % a.T;
+  const uint32_t p = seq_base(a.seq_pos, a.pos0, b) + t;
   const uint32_t h0 = blockIdx.y * HG, split = blockIdx.x;
   const uint32_t n_w = min(p + 1, a.cap_raw);
   const int32_t *tk = a.topk ? a.topk + (size_t)qi * a.top_k : nullptr;
@@ -263,7 +264,8 @@ __global__ void __launch_bounds__(kThreads)
 
 template <typename T>
 __global__ void attn_merge_kernel(AttnArgs a, Plan pl, const float *part) {
-  const uint32_t h = blockIdx.x, qi = blockIdx.y, t = qi % a.T, p = a.pos0 + t;
+  const uint32_t h = blockIdx.x, qi = blockIdx.y, t = qi % a.T;
+  const uint32_t p = seq_base(a.seq_pos, a.pos0, qi / a.T) + t;
   const uint32_t D = a.head_dim, H = a.n_heads, ns = pl.n_splits, n_nope = D - a.n_rot;
   const size_t nq = (size_t)a.batch * a.T;
   const float *pml = part + nq * ns * H * D + (size_t)qi * ns * H * 2;

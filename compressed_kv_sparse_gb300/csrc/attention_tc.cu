@@ -51,6 +51,7 @@ constexpr float kRaiseLog2 = 8.0f;     // raise the running max beyond 2^8
 struct TcAttnParams {
   uint32_t ratio, batch, T, pos0, cap_raw, comp_cap, n_comp, top_k;
   RowMap map;         // rows of comp
+  const uint32_t *seq_pos;   // [B] per-sequence positions (ragged decode) or NULL
   uint32_t cluster;   // decode: CTAs per query (one cluster); 0: prefill, persistent CTAs
   uint32_t n_q;       // queries = batch * T
   float c2;           // softmax scale * log2(e)
@@ -89,7 +90,7 @@ static_assert(2 * kH * 128 == kRows * 128, "output staging fills the P buffer");
 
 // Rows that a query can have at most, without reading its top-k list.
 __device__ __forceinline__ uint32_t rows_bound(const TcAttnParams &P, uint32_t qi) {
-  const uint32_t p = P.pos0 + qi % P.T;
+  const uint32_t p = seq_base(P.seq_pos, P.pos0, qi / P.T) + qi % P.T;
   uint32_t n = min(p + 1, P.cap_raw);
   if (P.ratio == 4) n += min(P.top_k, min((p + 1) / 4, P.n_comp));
   else if (P.ratio == 128) n += min((p + 1) / 128, P.n_comp);
@@ -107,7 +108,7 @@ __device__ __forceinline__ QueryGeo query_geo(const TcAttnParams &P, uint32_t qi
   QueryGeo g;
   g.qi = qi;
   g.b = qi / P.T;
-  g.p = P.pos0 + qi % P.T;
+  g.p = seq_base(P.seq_pos, P.pos0, g.b) + qi % P.T;
   g.n_w = min(g.p + 1, P.cap_raw);
   g.tk = P.topk ? P.topk + (size_t)qi * P.top_k : nullptr;
   g.n_list = 0;
@@ -215,7 +216,7 @@ __device__ __forceinline__ bool merge_heads(const TcAttnParams &P, Smem &S, uint
     for (uint32_t j = 0; j < CM; ++j) S.mw[t][j] = f[j] * li;
   }
   // rotation coefficients load while the slices land
-  const uint32_t p = P.pos0 + qi % P.T, c = t & 127, d = 4 * c;
+  const uint32_t p = seq_base(P.seq_pos, P.pos0, qi / P.T) + qi % P.T, c = t & 127, d = 4 * c;
   float co0 = 1.f, si0 = 0.f, co1 = 1.f, si1 = 0.f;
   if (d >= (uint32_t)kNope) {
     const uint32_t fi = (d - kNope) >> 1;
@@ -828,6 +829,7 @@ cudaError_t launch_attention_tc(const AttnArgs &a, uint32_t rows_max, int *err, 
   P.cap_raw = a.cap_raw;
   P.comp_cap = a.comp_cap;
   P.map = a.map;
+  P.seq_pos = a.seq_pos;
   P.n_comp = a.n_comp;
   P.top_k = a.top_k;
   P.n_q = a.batch * a.T;

@@ -25,6 +25,12 @@ __device__ __forceinline__ void pdl_trigger() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
+// Position of sequence b's first token in this call: its own (ragged decode,
+// seq_pos non-NULL) or the call's pos0.
+__device__ __forceinline__ uint32_t seq_base(const uint32_t *seq_pos, uint32_t pos0, uint32_t b) {
+  return seq_pos ? __ldg(seq_pos + b) : pos0;
+}
+
 __device__ __forceinline__ float ld_f32(const float *p, size_t i) { return p[i]; }
 __device__ __forceinline__ float ld_f32(const __nv_bfloat16 *p, size_t i) {
   return __bfloat162float(p[i]);

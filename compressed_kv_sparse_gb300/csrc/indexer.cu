@@ -100,7 +100,7 @@ __global__ void index_qbf_kernel(IndexArgs a, TcWs w, bool clear_hist, uint32_t 
     reinterpret_cast<uint4 *>(w.hist)[i] = make_uint4(0u, 0u, 0u, 0u);
   if (i >= n_units) return;
   const uint32_t row = i / upr, c0 = (i - row * upr) * per;   // row = query * Hi + head
-  const uint32_t p = a.pos0 + (row / Hi) % a.T;
+  const uint32_t p = seq_base(a.seq_pos, a.pos0, (row / Hi) / a.T) + (row / Hi) % a.T;
   // rotate the pairs of w4 (dims c0, c0 + 1, ...) that lie in the tail
   auto rot = [&](uint32_t *w4, uint32_t n) {
     for (uint32_t e = 0; e < n; ++e) {
@@ -166,7 +166,7 @@ __global__ void index_qbf_kernel(IndexArgs a, TcWs w, bool clear_hist, uint32_t 
 
 template <typename T>
 __global__ void index_qrot_kernel(IndexArgs a, float *qrot) {
-  const uint32_t qi = blockIdx.x, t = qi % a.T, p = a.pos0 + t;
+  const uint32_t qi = blockIdx.x, t = qi % a.T, p = seq_base(a.seq_pos, a.pos0, qi / a.T) + t;
   const uint32_t Hi = a.n_heads, Di = a.dim, Hp = round_up8(Hi), n_nope = Di - a.rot;
   const T *q = static_cast<const T *>(a.q_idx) + (size_t)qi * Hi * Di;
   float *dst = qrot + (size_t)qi * Di * Hp;
@@ -226,7 +226,8 @@ template <typename T>
 __global__ void __launch_bounds__(kRowsPerBlock)
     index_score_exact_kernel(IndexArgs a, const float *qrot, float *scores) {
   extern __shared__ float4 smem4[];
-  const uint32_t qi = blockIdx.y, b = qi / a.T, t = qi % a.T, p = a.pos0 + t;
+  const uint32_t qi = blockIdx.y, b = qi / a.T, t = qi % a.T;
+  const uint32_t p = seq_base(a.seq_pos, a.pos0, b) + t;
   const uint32_t vis = min((p + 1) / 4, a.n_comp);
   const uint32_t row0 = blockIdx.x * kRowsPerBlock;
   if (vis <= a.top_k || row0 >= vis) return;
@@ -407,7 +408,7 @@ __global__ void __launch_bounds__(kSelectThreads)
   __shared__ uint32_t hist[256];
   __shared__ uint32_t wsum[33];
   __shared__ uint32_t sel[2];
-  const uint32_t qi = blockIdx.x, t = qi % a.T, p = a.pos0 + t;
+  const uint32_t qi = blockIdx.x, t = qi % a.T, p = seq_base(a.seq_pos, a.pos0, qi / a.T) + t;
   const uint32_t vis = min((p + 1) / 4, a.n_comp), k = a.top_k;
   int32_t *out = a.topk + (size_t)qi * k;
   if (vis <= k) {
@@ -746,7 +747,7 @@ __global__ void __launch_bounds__(NT, NT == 256 ? 4 : 1)
 
   const uint32_t Hi = 64, Di = 128;
   const uint32_t qi = blockIdx.x / G, g = blockIdx.x % G;
-  const uint32_t b = qi / a.T, p = a.pos0 + qi % a.T;
+  const uint32_t b = qi / a.T, p = seq_base(a.seq_pos, a.pos0, b) + qi % a.T;
   const uint32_t vis = min((p + 1) / 4, a.n_comp), k = a.top_k;
   const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   int32_t *out = a.topk + (size_t)qi * k;
@@ -1244,6 +1245,7 @@ cudaError_t launch_index_tc(const IndexArgs &a, cudaStream_t s) {
     t.hist = scorer_hist ? w.hist : nullptr;
     t.err = w.err;
     t.map = a.map;
+    t.seq_pos = a.seq_pos;
     cudaError_t e = launch_index_score_tc(t, s);
     if (e != cudaSuccess) return e;
   }

@@ -56,6 +56,7 @@ struct ScoreParams {
   uint32_t batch, T, pos0, comp_cap, n_comp, n_groups, tiles_per, total_items;
   uint32_t cta_per_group;   // > 0: that many CTAs per (sequence, group), none crossing one
   RowMap map;               // paged keys (map.table != NULL): 64-row blocks of the pool
+  const uint32_t *seq_pos;  // [B] per-sequence positions (ragged decode) or NULL
   const __nv_bfloat16 *w;   // [B][T][Hi]
   float *scores;            // [B][T][comp_cap]
   uint32_t *hist;           // [B*T][4096] counts of the top 12 bits of the score keys
@@ -69,8 +70,8 @@ __device__ __forceinline__ uint32_t score_key_tc(float f) {
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-__device__ __forceinline__ uint32_t vis_of(const ScoreParams &P, uint32_t t) {
-  return min((P.pos0 + t + 1) / 4, P.n_comp);
+__device__ __forceinline__ uint32_t vis_of(const ScoreParams &P, uint32_t b, uint32_t t) {
+  return min((seq_base(P.seq_pos, P.pos0, b) + t + 1) / 4, P.n_comp);
 }
 
 template <int QG>
@@ -81,7 +82,7 @@ __device__ __forceinline__ bool decode_item(const ScoreParams &P, uint32_t item,
   g = rest % P.n_groups;
   b = rest / P.n_groups;
   const uint32_t last = min(P.T, (g + 1) * QG) - 1;
-  return tile * kRows < vis_of(P, last);   // false: every row of the tile is invisible
+  return tile * kRows < vis_of(P, b, last);   // false: every row of the tile is invisible
 }
 
 template <int QG>
@@ -110,7 +111,8 @@ __global__ void __launch_bounds__(Cfg<QG>::kThreads, 1)
   if (P.cta_per_group) {
     const uint32_t bg = blockIdx.x / P.cta_per_group, j = blockIdx.x % P.cta_per_group;
     const uint32_t last = min(P.T, (bg % P.n_groups + 1) * QG) - 1;
-    const uint32_t nt = min(P.tiles_per, (vis_of(P, last) + kRows - 1) / kRows);
+    const uint32_t nt =
+        min(P.tiles_per, (vis_of(P, bg / P.n_groups, last) + kRows - 1) / kRows);
     it0 = bg * P.tiles_per + j * nt / P.cta_per_group;
     it1 = bg * P.tiles_per + (j + 1) * nt / P.cta_per_group;
   } else {
@@ -346,7 +348,7 @@ __global__ void __launch_bounds__(Cfg<QG>::kThreads, 1)
         const float s = ((acc8[0] + acc8[1]) + (acc8[2] + acc8[3])) +
                         ((acc8[4] + acc8[5]) + (acc8[6] + acc8[7]));
         const uint32_t t = g * QG + q;
-        const bool valid = t < P.T && grow < vis_of(P, t);
+        const bool valid = t < P.T && grow < vis_of(P, b, t);
         if (valid) P.scores[((size_t)b * P.T + t) * P.comp_cap + grow] = s;
         // histogram of the keys' top 12 bits (lanes in one bin add once), per
         // CTA in shared memory, added to the query's when the query changes
@@ -405,6 +407,7 @@ cudaError_t launch_qg(const IndexTcArgs &a, cudaStream_t s) {
   P.hist = a.hist;
   P.err = a.err;
   P.map = a.map;
+  P.seq_pos = a.seq_pos;
   if (P.total_items == 0) return cudaSuccess;
   static int smem_set = 0;
   e = ensure_smem(index_score_tc_kernel<QG>, C::kSmem, &smem_set);

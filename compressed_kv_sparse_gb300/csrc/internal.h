@@ -104,6 +104,7 @@ struct AppendArgs {
   int n_lanes;             // lanes to append (lane[0 .. n_lanes-1])
   LaneArgs lane[2];
   uint32_t y0;             // 1: the raw rows are not part of this append
+  const uint32_t *seq_pos; // [B] per-sequence positions (ragged decode) or NULL
 };
 cudaError_t launch_append(const AppendArgs &a, cudaStream_t s);
 
@@ -120,6 +121,7 @@ struct IndexArgs {
   bool qat;                       // FP4 QAT round trip of the rotated query
   float had_c;                    // 1/sqrt(dim) in fp32
   RowMap map;                     // rows of keys and norms
+  const uint32_t *seq_pos;        // [B] per-sequence positions (ragged decode) or NULL
 };
 size_t index_ws_bytes(int dtype, uint32_t batch, uint32_t T, uint32_t n_heads, uint32_t dim,
                       uint32_t comp_cap);
@@ -134,6 +136,7 @@ struct IndexTcArgs {
   uint32_t *hist;     // [B*T][4096], zeroed before the call
   int *err;
   RowMap map;         // rows of keys
+  const uint32_t *seq_pos;   // [B] per-sequence positions (ragged decode) or NULL
 };
 bool index_tc_supported(uint32_t n_heads, uint32_t dim);
 cudaError_t launch_index_score_tc(const IndexTcArgs &a, cudaStream_t s);
@@ -153,6 +156,7 @@ struct AttnArgs {
   void *ws;
   size_t ws_bytes;
   RowMap map;             // rows of comp
+  const uint32_t *seq_pos;  // [B] per-sequence positions (ragged decode) or NULL
 };
 size_t attn_ws_bytes(int dtype, uint32_t ratio, uint32_t batch, uint32_t T, uint32_t n_heads,
                      uint32_t head_dim, uint32_t n_rot, uint32_t cap_raw, uint32_t comp_cap,

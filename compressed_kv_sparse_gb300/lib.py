@@ -46,7 +46,8 @@ class LayerCacheC(ctypes.Structure):
         ("rope_sin", ctypes.c_void_p), ("index_rope_cos", ctypes.c_void_p),
         ("index_rope_sin", ctypes.c_void_p), ("rope_max_pos", ctypes.c_uint32),
         ("qat", ctypes.c_uint32), ("block_table", ctypes.c_void_p),
-        ("max_blocks", ctypes.c_uint32), ("n_blocks", ctypes.c_uint32)]
+        ("max_blocks", ctypes.c_uint32), ("n_blocks", ctypes.c_uint32),
+        ("seq_pos", ctypes.c_void_p)]
 
 QAT_FP8_ATTN = 1    # DS4A_QAT_FP8_ATTN
 QAT_FP4_INDEX = 2   # DS4A_QAT_FP4_INDEX
@@ -209,6 +210,13 @@ class LayerCache:
             index_rope_sin=_ptr(self.index_rope_sin), rope_max_pos=rope_max_pos, qat=qat,
             block_table=_ptr(block_table), max_blocks=block_table.shape[1] if paged else 0,
             n_blocks=n_blocks if paged else 0)
+
+    def set_seq_pos(self, seq_pos: Optional[torch.Tensor]):
+        """Ragged decode: [B] uint32/int32 device positions of this step's
+        tokens (None: every sequence at the call's position). The tensor must
+        stay alive while calls use it."""
+        self.seq_pos = seq_pos
+        self.c.seq_pos = _ptr(seq_pos)
 
     def logical(self, name: str) -> torch.Tensor:
         """[B][comp_cap][...] view of compressed rows / row norms (a gather

@@ -114,6 +114,14 @@ typedef enum { DS4A_F32 = 0, DS4A_BF16 = 1 } ds4a_dtype;
  *                    must lie in [0, n_blocks); an entry outside is not
  *                    written to, and reads of its rows return rows of block 0.
  *  max_blocks, n_blocks  see block_table (ignored when it is NULL).
+ *  seq_pos           NULL: every sequence is at the call's position. Non-NULL
+ *                    (ragged decode batches): [B] uint32 DEVICE array, the
+ *                    position of sequence b's token in this decode step. The
+ *                    append, top-k and attention calls of the step (T = 1
+ *                    only; T > 1 with seq_pos is DS4A_ERR_ARG) place and read
+ *                    sequence b's token at seq_pos[b] instead of pos. The
+ *                    host checks use pos and n_tokens: the caller keeps every
+ *                    seq_pos[b] <= pos, and updates the array between steps.
  *
  * State layout: ratio 4 keeps the last complete group of 4 tokens in slots
  * 0..3 and token p of the current group in slot 4 + p % 4 (page §5's 8-row
@@ -137,6 +145,7 @@ typedef struct {
   uint32_t qat;
   const int32_t *block_table;
   uint32_t max_blocks, n_blocks;
+  const uint32_t *seq_pos;
 } ds4a_layer_cache;
 
 /*
