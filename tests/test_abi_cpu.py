@@ -196,3 +196,27 @@ def test_argument_checks_reject_before_launch(L):
                                             fake, 1 << 30, None) == -4
     assert L.ds4a_sparse_attn_decode(None, 9, fake, 64, fake, 512, 0.1, fake, fake, 1 << 30,
                                      None) == -1
+
+
+def test_paged_cache_layout_helpers_on_cpu(L):
+    """The binding's paged layout without a GPU: a history scattered into the
+    pools through a block table (random order, a shared prefix) gathers back
+    to the same logical rows, and the struct carries the table."""
+    import torch
+    B, max_blocks, n_blocks, D, rpb = 3, 5, 20, 16, 2      # ratio 128: 2 rows per block
+    perm = torch.randperm(n_blocks, generator=torch.Generator().manual_seed(0))
+    table = perm[:B * max_blocks].reshape(B, max_blocks).to(torch.int32)
+    table[1:, :2] = table[0, :2]                            # shared first two blocks
+    rows = torch.randn(B, max_blocks * rpb, D)
+    rows[1:, :2 * rpb] = rows[0, :2 * rpb]
+    c = lib.LayerCache(ratio=128, head_dim=D, n_rot=8, batch=B, comp_cap=max_blocks * rpb,
+                       dtype="f32", base=10000.0, rope_max_pos=16, device="cpu",
+                       block_table=table, n_blocks=n_blocks)
+    assert c.attn_comp_kv.shape == (n_blocks, rpb, D)
+    c.load_state({"attn_comp_kv": rows}, 0)
+    assert torch.equal(c.logical("attn_comp_kv"), rows)
+    assert c.c.block_table == table.data_ptr() and c.c.max_blocks == max_blocks
+    assert c.c.n_blocks == n_blocks and c.c.seq_pos is None
+    pos = torch.tensor([5, 3, 9], dtype=torch.int32)
+    c.set_seq_pos(pos)
+    assert c.c.seq_pos == pos.data_ptr()
