@@ -229,3 +229,45 @@ def test_paged_cache_layout_helpers_on_cpu(L):
     pos = torch.tensor([5, 3, 9], dtype=torch.int32)
     c.set_seq_pos(pos)
     assert c.c.seq_pos == pos.data_ptr()
+
+
+def test_plain_c_host_links_the_library(L, tmp_path):
+    """A C program built with gcc against include/ds4a.h and linked to
+    libds4a.so (no Python, no torch) gets the same host results as the
+    oracle: the 61-layer Pro schedule's cache bytes at 1M tokens (the page's
+    9.62 GiB), a rope coefficient and an argument check."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    src = tmp_path / "host.c"
+    src.write_text(r'''
+#include <stdio.h>
+#include "ds4a.h"
+int main(void) {
+  unsigned long long tot = 0;
+  for (unsigned il = 0; il < 61; ++il)
+    tot += ds4a_cache_bytes(ds4a_layer_compress_ratio(1, il), 512, 128, 1u << 20, 1, 2);
+  float c[3 * 32], s[3 * 32];
+  const int st = ds4a_rope_table(160000.0, 64, 3, c, s);
+  const int bad = ds4a_rope_table(160000.0, 63, 3, c, s);
+  printf("%llu %d %d %.9g %.9g %s\n", tot, st, bad, c[32 + 1], s[2 * 32 + 5],
+         ds4a_status_string((ds4a_status)bad));
+  return 0;
+}
+''')
+    exe = tmp_path / "host"
+    libdir = os.path.dirname(lib.LIB_PATH)
+    subprocess.run([cc, "-I", os.path.join(root, "include"), str(src), "-o", str(exe),
+                    "-L", libdir, "-lds4a", "-Wl,-rpath," + libdir], check=True)
+    out = subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout.split()
+    tot, st, bad = int(out[0]), int(out[1]), int(out[2])
+    assert round(tot / 2**30, 2) == 9.62
+    assert tot == sum(schedule.kv_cache_bytes(schedule.layer_compress_ratio(1, il), 512, 128,
+                                              1 << 20, 1, 2) for il in range(61))
+    ref_c, ref_s = rope.rope_coeffs(np.arange(3), 160000.0, 64)
+    assert st == 0 and np.float32(float(out[3])) == ref_c[1, 1]   # %.9g round-trips fp32
+    assert np.float32(float(out[4])) == ref_s[2, 5]
+    assert bad == -1 and " ".join(out[5:]) == "invalid argument"
