@@ -85,9 +85,10 @@ def write_traffic(csv_path: str, workload: str, captured_on: str, calls: int):
     for r in rows[hi + 1:]:
         if len(r) <= vi or r[mi] not in ("dram__bytes_read.sum", "dram__bytes_write.sum"):
             continue
-        # (the anonymous namespace prints as "(anonymous namespace)::" or "<unnamed>::")
-        name = re.sub(r"\(.*", "", r[ki]).replace("void ", "")
-        name = re.sub(r"^.*?(unnamed>|anonymous namespace\))::", "", name)
+        # (the anonymous namespace prints as "(anonymous namespace)::" or
+        # "<unnamed>::": strip it before the argument list, whose "(" it shares)
+        name = re.sub(r"^.*?(unnamed>|anonymous namespace\))::", "", r[ki].replace("void ", ""))
+        name = re.sub(r"\(.*", "", name)
         v = float(r[vi].replace(",", "")) * scale.get(r[ui] if ui is not None else "byte", 1)
         for call, prefixes in CALL_KERNELS.items():
             if name.startswith(prefixes):
