@@ -64,3 +64,31 @@ def test_qat_flags_by_layer_kind():
     assert bench.qat_flags(0) == 0
     assert bench.qat_flags(128) == lib.QAT_FP8_ATTN
     assert bench.qat_flags(4) == lib.QAT_FP8_ATTN | lib.QAT_FP4_INDEX
+
+
+def test_clock_summary_median_max_and_reasons():
+    s = bench.ClockSampler(0)
+    s.lines = ["2070, 2070, 900.5, Not Active, Not Active, Not Active, Not Active",
+               "1980, 2070, 1200.0, Not Active, Not Active, Not Active, Active",
+               "2070, 2070, 1300.0, Not Active, Not Active, Not Active, Not Active",
+               "[N/A], garbage"]
+    out = s.summary()
+    assert out == {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": ["sw_power_cap"],
+                   "samples": 3}
+    s.lines = []
+    assert s.summary()["reasons"] == ["unsampled"]
+
+
+def test_reference_arm_line_keeps_the_contract():
+    """The reference arm (the oracle on host cores) prints the contract's keys
+    with its own e2e figure and no host-device bytes."""
+    line = bench.reference_arm(bench.WORKLOADS["tiny"], 1, 0, 1)
+    for k in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+              "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config"):
+        assert k in line, k
+    assert line["impl"] == "reference" and line["n_gpus"] == 1 and line["value"] > 0
+    cb = line["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["value"] == line["value"] and cb["cores"] >= 1
+    assert line["e2e"] == {"value": line["value"], "unit": line["unit"],
+                           "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+    assert line["config"]["workload"] == bench.WORKLOADS["tiny"].name
