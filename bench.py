@@ -362,6 +362,20 @@ def flush_l2(buf):
     buf.add_(1)
 
 
+def max_over_ranks(x: float, world: int, device) -> float:
+    """The slowest rank's figure (every rank gets it); x itself on one rank."""
+    if world <= 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(world: int, tokens_per_step_per_rank: int, step_s: float) -> float:
+    """Whole-job tokens/s: every rank's tokens over the slowest rank's step."""
+    return world * tokens_per_step_per_rank / step_s
+
+
 def qat_flags(ratio: int) -> int:
     """Step-8 flags of a layer: FP8 attention rows on compressed layers, FP4
     QAT of the indexer lane on ratio-4 layers."""
@@ -434,12 +448,8 @@ def run_gpu(args, wl, rank, world, device):
         f1.record()
         torch.cuda.synchronize(device)
         flush_ms = f0.elapsed_time(f1) / args.steps
-    ms_step = max(ms - flush_ms, 1e-6)
-    if world > 1:
-        t = torch.tensor([ms_step], device=device)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms_step = float(t.item())
-    value = world * R.tokens_per_step() / (ms_step / 1e3)
+    ms_step = max_over_ranks(max(ms - flush_ms, 1e-6), world, device)
+    value = job_throughput(world, R.tokens_per_step(), ms_step / 1e3)
 
     # per-call device time: for each call kind, one CUDA graph runs that call on
     # every layer that has it (layer order, as in a step); replays are timed
@@ -520,12 +530,9 @@ def run_gpu(args, wl, rank, world, device):
     for _ in range(args.steps):
         e2e_step()
         torch.cuda.synchronize(device)
-    e2e_s = (time.perf_counter() - t0) / args.steps - flush_ms / 1e3
-    if world > 1:
-        t = torch.tensor([e2e_s], device=device)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_s = float(t.item())
-    e2e = {"value": world * R.tokens_per_step() / e2e_s, "unit": "tok/s",
+    e2e_s = max_over_ranks((time.perf_counter() - t0) / args.steps - flush_ms / 1e3, world,
+                           device)
+    e2e = {"value": job_throughput(world, R.tokens_per_step(), e2e_s), "unit": "tok/s",
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
 
     res = {"metric": METRIC, "value": value, "unit": "tok/s", "n_gpus": world,
