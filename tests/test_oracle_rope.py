@@ -64,3 +64,55 @@ def test_fp32_recipe_close_to_fp64_and_exact_on_grid():
     assert np.allclose(y32, y64, rtol=0, atol=4 * 2.0**-24 * np.abs(x).max() * 2)
     # at p = 0 the recipe is exact: a*1 - b*0 = a
     assert np.array_equal(rope.rope_tail_f32(x, 0, 160000.0, 32), x)
+
+
+def _mp_f32(v, mp):
+    """fp32 nearest to the mpmath value v (v converted exactly to a binary64
+    first only when that cannot change the fp32 rounding, i.e. the value is
+    not within 2^-40 relative of an fp32 rounding midpoint)."""
+    x = float(v)
+    f = np.float32(x)
+    lo, hi = np.nextafter(f, np.float32(-np.inf)), np.nextafter(f, np.float32(np.inf))
+    for nb in (lo, hi):
+        mid = (mp.mpf(float(f)) + mp.mpf(float(nb))) / 2
+        if mid != 0 and abs((v - mid) / mid) < mp.mpf(2) ** -40:
+            return None          # too close to a midpoint to decide from a binary64 copy
+    return f
+
+
+def test_coefficients_against_independent_high_precision_evaluation():
+    """rope_coeffs (fp64 libm angle, cos and sin each rounded once to fp32) pinned
+    against mpmath at 50 digits, positions up to 131,072, both bases and both
+    rotation widths. theta_i = base^(-2i/n_rot) must be the binary64 nearest (or
+    adjacent, as C pow allows) to the exact power, and cos / sin of the fp64
+    angle p * theta_i, evaluated at 50 digits and rounded once to fp32, must
+    equal the oracle's coefficients. A wrong exponent (-i/n_rot), a swapped
+    cos / sin, an fp32 angle or a missing pair fails here."""
+    import pytest
+    mp = pytest.importorskip("mpmath").mp
+    mp.dps = 50
+    r = np.random.default_rng(5)
+    pos = np.unique(np.concatenate([np.arange(0, 70), [127, 128, 255, 256, 4095, 4096, 28671,
+                                                       28672, 32767, 32768, 65535, 65536,
+                                                       131071, 131072],
+                                    r.integers(0, 131073, 300)]))
+    undecided = 0
+    for base in (10000.0, 160000.0):
+        for n_rot in (64, 32):
+            theta = rope.inv_freq(base, n_rot)
+            for i, t in enumerate(theta):
+                exact = mp.power(mp.mpf(base), mp.mpf(-2 * i) / n_rot)
+                ulp = mp.mpf(np.spacing(t))
+                assert abs(mp.mpf(float(t)) - exact) <= ulp, (base, n_rot, i)
+            c, s = rope.rope_coeffs(pos, base, n_rot)
+            assert c.dtype == np.float32 and c.shape == (len(pos), n_rot // 2)
+            for a, p in enumerate(pos):
+                for i in range(n_rot // 2):
+                    ang = mp.mpf(float(p) * float(theta[i]))   # the reading's fp64 angle
+                    for got, fn in ((c[a, i], mp.cos), (s[a, i], mp.sin)):
+                        want = _mp_f32(fn(ang), mp)
+                        if want is None:
+                            undecided += 1
+                            continue
+                        assert got == want, (base, n_rot, int(p), i, fn.__name__, got, want)
+    assert undecided < 4
