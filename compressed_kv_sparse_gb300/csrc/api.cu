@@ -277,9 +277,14 @@ size_t ds4a_workspace_bytes(int call, const ds4a_layer_cache *c, uint32_t T, uin
   }
 }
 
-ds4a_status ds4a_index_topk(const ds4a_layer_cache *c, uint32_t pos0, uint32_t T,
-                            const void *q_idx, const void *w, uint32_t n_heads, uint32_t top_k,
-                            int32_t *topk, void *ws, size_t ws_bytes, ds4a_stream_t stream) {
+}  // extern "C"
+
+namespace ds4a {
+// Every check of ds4a_index_topk except the workspace's (shared with the
+// no-allocation variant, which checks its scratch size after these).
+ds4a_status index_topk_check(const ds4a_layer_cache *c, uint32_t pos0, uint32_t T,
+                             const void *q_idx, const void *w, uint32_t n_heads, uint32_t top_k,
+                             const int32_t *topk) {
   ds4a_status st = check_cache(c);
   if (st) return st;
   if (c->ratio != 4) return DS4A_ERR_ARG;
@@ -290,6 +295,17 @@ ds4a_status ds4a_index_topk(const ds4a_layer_cache *c, uint32_t pos0, uint32_t T
   const uint32_t Hp = (n_heads + 7u) & ~7u;
   if (((size_t)c->index_dim * Hp + Hp + 128 * (size_t)(c->index_dim + 1)) * 4 > 227 * 1024)
     return DS4A_ERR_SHAPE;
+  return DS4A_OK;
+}
+}  // namespace ds4a
+
+extern "C" {
+
+ds4a_status ds4a_index_topk(const ds4a_layer_cache *c, uint32_t pos0, uint32_t T,
+                            const void *q_idx, const void *w, uint32_t n_heads, uint32_t top_k,
+                            int32_t *topk, void *ws, size_t ws_bytes, ds4a_stream_t stream) {
+  const ds4a_status st = index_topk_check(c, pos0, T, q_idx, w, n_heads, top_k, topk);
+  if (st) return st;
   const size_t need = index_ws_bytes(c->dtype, c->batch, T, n_heads, c->index_dim, c->comp_cap);
   if (!ws || ws_bytes < need) return DS4A_ERR_WORKSPACE;
   IndexArgs a;
@@ -370,6 +386,18 @@ ds4a_status ds4a_sparse_attn_decode(const ds4a_layer_cache *c, uint32_t pos, con
   if ((uint64_t)pos + 1 != c->n_tokens) return DS4A_ERR_POSITION;
   return attn_common(c, pos, 1, q, n_heads, nullptr, topk, top_k, scale, out, ws, ws_bytes,
                      reinterpret_cast<cudaStream_t>(stream));
+}
+
+ds4a_status ds4a_set_decode_cluster(uint32_t C) {
+  if (C > 16) return DS4A_ERR_ARG;
+  attn_tc_force_cluster(C);
+  return DS4A_OK;
+}
+
+uint32_t ds4a_decode_cluster_size(const ds4a_layer_cache *c, uint32_t n_heads, uint32_t top_k) {
+  if (check_cache(c) != DS4A_OK) return 0;
+  return attn_decode_cluster(c->dtype, c->ratio, c->batch, n_heads, c->head_dim, c->n_rot,
+                             c->cap_raw, c->comp_cap, c->ratio == 4 ? top_k : 0);
 }
 
 ds4a_status ds4a_sparse_attn_prefill_chunk(ds4a_layer_cache *c, uint32_t pos0, uint32_t T,

@@ -320,7 +320,9 @@ cudaError_t launch_attention_t(const AttnArgs &a, cudaStream_t s) {
   static int smem_set = 0;
   cudaError_t e = ensure_smem(attn_kernel<T>, smem, &smem_set);
   if (e != cudaSuccess) return e;
-  float *part = static_cast<float *>(a.ws);
+  // (the first 256 bytes: the error word of the workspace; this path has no
+  // device waits and leaves it alone)
+  float *part = a.ws ? reinterpret_cast<float *>(static_cast<uint8_t *>(a.ws) + 256) : nullptr;
   dim3 grid(pl.n_splits, pl.n_hg, a.batch * a.T);
   attn_kernel<T><<<grid, kThreads, smem, s>>>(a, pl, part);
   note_launches(1);
@@ -348,7 +350,14 @@ size_t attn_ws_bytes(int dtype, uint32_t ratio, uint32_t batch, uint32_t T, uint
     return attn_tc_ws_bytes(batch, T, rows_max(ratio, cap_raw, comp_cap, top_k));
   const Plan pl = make_plan(ratio, batch, T, n_heads, head_dim, cap_raw, comp_cap, top_k);
   if (pl.n_splits == 1) return 0;
-  return (size_t)batch * T * pl.n_splits * n_heads * (head_dim + 2) * sizeof(float);
+  return 256 + (size_t)batch * T * pl.n_splits * n_heads * (head_dim + 2) * sizeof(float);
+}
+
+uint32_t attn_decode_cluster(int dtype, uint32_t ratio, uint32_t batch, uint32_t n_heads,
+                             uint32_t head_dim, uint32_t n_rot, uint32_t cap_raw,
+                             uint32_t comp_cap, uint32_t top_k) {
+  if (!attn_tc_supported(dtype, n_heads, head_dim, n_rot)) return 0;
+  return attn_tc_decode_cluster(rows_max(ratio, cap_raw, comp_cap, top_k), batch);
 }
 
 cudaError_t launch_attention(const AttnArgs &a, cudaStream_t s) {

@@ -805,7 +805,31 @@ uint32_t pick_cluster(uint32_t n_tiles, uint32_t n_q, size_t smem) {
   return best;
 }
 
+// Process-wide cluster size forced by ds4a_set_decode_cluster (0: automatic).
+std::atomic<uint32_t> g_force_cluster{0};
+
+// The cluster size a decode launch uses: the forced size (clamped to the
+// query's tile count and 16) when the device can launch it, else pick_cluster.
+uint32_t decode_cluster(uint32_t rows_max, uint32_t n_q, size_t smem) {
+  const uint32_t n_tiles = (rows_max + kRows - 1) / kRows;
+  const uint32_t cmax = n_tiles < kMaxCluster ? (n_tiles ? n_tiles : 1u) : kMaxCluster;
+  uint32_t f = g_force_cluster.load(std::memory_order_relaxed);
+  if (f) {
+    if (f > cmax) f = cmax;
+    if (max_active_clusters(f, smem) >= 1) return f;
+  }
+  return pick_cluster(n_tiles, n_q, smem);
+}
+
 }  // namespace
+
+void attn_tc_force_cluster(uint32_t C) {
+  g_force_cluster.store(C > kMaxCluster ? kMaxCluster : C, std::memory_order_relaxed);
+}
+
+uint32_t attn_tc_decode_cluster(uint32_t rows_max, uint32_t n_q) {
+  return decode_cluster(rows_max, n_q, sizeof(Smem) + 1024);
+}
 
 bool attn_tc_supported(int dtype, uint32_t H, uint32_t D, uint32_t n_rot) {
   return dtype == DS4A_BF16 && H == (uint32_t)kH && D == (uint32_t)kD && n_rot == 64;
@@ -863,8 +887,7 @@ cudaError_t launch_attention_tc(const AttnArgs &a, uint32_t rows_max, int *err, 
   e = make_tmap_bf16(&tq, a.q, 2, qd, qs, qb);
   if (e != cudaSuccess) return e;
   if (a.T == 1) {
-    const uint32_t n_tiles = (rows_max + kRows - 1) / kRows;
-    P.cluster = pick_cluster(n_tiles, P.n_q, smem);
+    P.cluster = decode_cluster(rows_max, P.n_q, smem);
     P.ml = reinterpret_cast<float *>(P.part + (size_t)P.n_q * P.cluster * kH * kD);
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute at[2];

@@ -33,15 +33,19 @@ constexpr int kSelectThreads = 1024;
 
 __host__ __device__ inline uint32_t round_up8(uint32_t x) { return (x + 7u) & ~7u; }
 
-// Workspace layout: qrot [B*T][Di][Hpad] fp32, then scores [B*T][comp_cap] fp32.
+// Workspace layout: the error word (int32, then padding to 256 bytes; this
+// path has no device waits, so the query rotation only zeroes it), qrot
+// [B*T][Di][Hpad] fp32, then scores [B*T][comp_cap] fp32.
+constexpr size_t kExactWsHeader = 256;
 struct IndexWs {
+  int *err;
   float *qrot, *scores;
 };
 __host__ __device__ inline IndexWs index_ws_split(void *ws, uint32_t nq, uint32_t Hi,
                                                   uint32_t Di) {
-  float *base = static_cast<float *>(ws);
+  float *base = reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + kExactWsHeader);
   const size_t qsz = (size_t)nq * Di * round_up8(Hi);
-  return IndexWs{base, base + ((qsz + 63) & ~(size_t)63)};
+  return IndexWs{static_cast<int *>(ws), base, base + ((qsz + 63) & ~(size_t)63)};
 }
 
 // Workspace of bf16 layers: err word, qbf [nq][Hi][Di] bf16, scores
@@ -165,7 +169,8 @@ __global__ void index_qbf_kernel(IndexArgs a, TcWs w, bool clear_hist, uint32_t 
 }
 
 template <typename T>
-__global__ void index_qrot_kernel(IndexArgs a, float *qrot) {
+__global__ void index_qrot_kernel(IndexArgs a, float *qrot, int *err) {
+  if (blockIdx.x == 0 && threadIdx.x == 0) *err = 0;
   const uint32_t qi = blockIdx.x, t = qi % a.T, p = seq_base(a.seq_pos, a.pos0, qi / a.T) + t;
   const uint32_t Hi = a.n_heads, Di = a.dim, Hp = round_up8(Hi), n_nope = Di - a.rot;
   const T *q = static_cast<const T *>(a.q_idx) + (size_t)qi * Hi * Di;
@@ -1188,7 +1193,7 @@ template <typename T>
 cudaError_t launch_index_exact(const IndexArgs &a, cudaStream_t s) {
   const uint32_t nq = a.batch * a.T;
   IndexWs w = index_ws_split(a.ws, nq, a.n_heads, a.dim);
-  index_qrot_kernel<T><<<nq, 256, 0, s>>>(a, w.qrot);
+  index_qrot_kernel<T><<<nq, 256, 0, s>>>(a, w.qrot, w.err);
   note_launches(1);
   const uint32_t Hp = round_up8(a.n_heads);
   const size_t smem = ((size_t)a.dim * Hp + Hp + (size_t)kRowsPerBlock * (a.dim + 1)) * 4;
@@ -1295,7 +1300,7 @@ size_t index_ws_bytes(int dtype, uint32_t batch, uint32_t T, uint32_t n_heads, u
     return total;
   }
   const size_t qsz = nq * dim * round_up8(n_heads);
-  return (((qsz + 63) & ~(size_t)63) + nq * comp_cap) * sizeof(float);
+  return kExactWsHeader + (((qsz + 63) & ~(size_t)63) + nq * comp_cap) * sizeof(float);
 }
 
 cudaError_t launch_index_topk(const IndexArgs &a, cudaStream_t s) {

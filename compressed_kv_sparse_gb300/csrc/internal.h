@@ -74,6 +74,11 @@ struct RowMap {
 #endif
 };
 
+// The argument checks of ds4a_index_topk other than the workspace's (api.cu).
+ds4a_status index_topk_check(const ds4a_layer_cache *c, uint32_t pos0, uint32_t T,
+                             const void *q_idx, const void *w, uint32_t n_heads, uint32_t top_k,
+                             const int32_t *topk);
+
 // TMA tensor map over bf16 data with 128-byte swizzle (tmap.cu).
 cudaError_t make_tmap_bf16(CUtensorMap *map, const void *base, int rank, const uint64_t *dims,
                            const uint64_t *strides_bytes, const uint32_t *box);
@@ -167,6 +172,15 @@ cudaError_t launch_attention(const AttnArgs &a, cudaStream_t s);
 bool attn_tc_supported(int dtype, uint32_t H, uint32_t D, uint32_t n_rot);
 size_t attn_tc_ws_bytes(uint32_t batch, uint32_t T, uint32_t rows_max);
 cudaError_t launch_attention_tc(const AttnArgs &a, uint32_t rows_max, int *err, cudaStream_t s);
+// Decode cluster size: forced process-wide (0 = automatic), and the size a
+// decode launch of `n_q` queries with at most `rows_max` rows each uses.
+void attn_tc_force_cluster(uint32_t C);
+uint32_t attn_tc_decode_cluster(uint32_t rows_max, uint32_t n_q);
+// The same for the arguments of a decode call: 0 when it does not run on the
+// tensor-core kernel.
+uint32_t attn_decode_cluster(int dtype, uint32_t ratio, uint32_t batch, uint32_t n_heads,
+                             uint32_t head_dim, uint32_t n_rot, uint32_t cap_raw,
+                             uint32_t comp_cap, uint32_t top_k);
 cudaError_t launch_ring_commit(int dtype, uint32_t batch, uint32_t T, uint32_t pos0,
                                uint32_t cap_raw, uint32_t head_dim, const void *chunk,
                                void *ring, cudaStream_t s);

@@ -40,11 +40,20 @@ extern "C" ds4a_status ds4a_index_topk_noalloc(const ds4a_layer_cache *cache, ui
                                                uint32_t T, const void *q_idx, const void *w,
                                                uint32_t n_heads, uint32_t top_k, int32_t *topk,
                                                ds4a_stream_t stream) {
-  if (!cache) return DS4A_ERR_ARG;
+  // the checks of ds4a_index_topk first, so that a malformed call gets the
+  // same status from both entry points; then the scratch size
+  const ds4a_status st = ds4a::index_topk_check(cache, pos0, T, q_idx, w, n_heads, top_k, topk);
+  if (st) return st;
   const size_t need = ds4a_workspace_bytes(DS4A_CALL_INDEX_TOPK, cache, T, n_heads, top_k);
   if (need > DS4A_STATIC_SCRATCH_BYTES) return DS4A_ERR_WORKSPACE;
   void *scratch = nullptr;
   if (ds4a::note_error(scratch_address(&scratch)) != cudaSuccess) return DS4A_ERR_CUDA;
   return ds4a_index_topk(cache, pos0, T, q_idx, w, n_heads, top_k, topk, scratch,
                          DS4A_STATIC_SCRATCH_BYTES, stream);
+}
+
+extern "C" ds4a_status ds4a_noalloc_status(uint32_t *count) {
+  void *scratch = nullptr;
+  if (ds4a::note_error(scratch_address(&scratch)) != cudaSuccess) return DS4A_ERR_CUDA;
+  return ds4a_workspace_status(scratch, DS4A_STATIC_SCRATCH_BYTES, count);
 }

@@ -80,20 +80,25 @@ struct ErrWord {
   int *p;
   int base;
 };
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, ErrWord err) {
+// (limit_ns: kWaitLimitNs in every kernel; the wait self-test passes a short one)
+__device__ __forceinline__ bool mbar_wait_for(uint64_t *bar, uint32_t parity, ErrWord err,
+                                              uint64_t limit_ns) {
   if (mbar_test_wait(bar, parity)) return true;
   const uint64_t t0 = global_ns();
   for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((i & 63) == 0) {
       const uint64_t dt = global_ns() - t0;
-      if (dt > kWaitLimitNs) {
+      if (dt > limit_ns) {
         atomicAdd(err.p, 1);
         return false;
       }
       if (dt > kErrPollNs && (i & 1023) == 0 && *(volatile int *)err.p != err.base) return false;
     }
   }
+}
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, ErrWord err) {
+  return mbar_wait_for(bar, parity, err, kWaitLimitNs);
 }
 // A word zeroed before the launch.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, int *err) {

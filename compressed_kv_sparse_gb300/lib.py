@@ -80,6 +80,15 @@ EXPORTS = {
     "ds4a_index_topk_noalloc": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_uint32, ctypes.c_uint32,
                                                ctypes.c_void_p, ctypes.c_void_p, ctypes.c_uint32,
                                                ctypes.c_uint32, ctypes.c_void_p, ctypes.c_void_p]),
+    "ds4a_noalloc_status": (ctypes.c_int, [ctypes.c_void_p]),
+    "ds4a_workspace_status": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
+    "ds4a_workspace_clear_status": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_size_t,
+                                                   ctypes.c_void_p]),
+    "ds4a_wait_selftest": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_uint32,
+                                          ctypes.c_void_p]),
+    "ds4a_set_decode_cluster": (ctypes.c_int, [ctypes.c_uint32]),
+    "ds4a_decode_cluster_size": (ctypes.c_uint32, [ctypes.c_void_p, ctypes.c_uint32,
+                                                   ctypes.c_uint32]),
     "ds4a_workspace_bytes": (ctypes.c_size_t, [ctypes.c_int, ctypes.c_void_p, ctypes.c_uint32,
                                                ctypes.c_uint32, ctypes.c_uint32]),
     "ds4a_rope_table": (ctypes.c_int, [ctypes.c_double, ctypes.c_uint32, ctypes.c_uint32,
@@ -358,10 +367,56 @@ def ds4a_launch_count() -> int:
 
 
 def workspace(nbytes: int, device="cuda") -> Optional[torch.Tensor]:
-    """A workspace buffer (uint8) of at least nbytes, 256-byte aligned by torch."""
+    """A workspace buffer (uint8) of at least nbytes, 256-byte aligned by torch.
+    Its first 256 bytes are zeroed, so its wait status starts clear."""
     if nbytes == 0:
         return None
-    return torch.empty(max(nbytes, 1), dtype=torch.uint8, device=device)
+    ws = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=device)
+    ws[:min(nbytes, 256)].zero_()
+    return ws
+
+
+def _nbytes(ws: Optional[torch.Tensor]) -> int:
+    return 0 if ws is None else ws.numel() * ws.element_size()
+
+
+def ds4a_workspace_status(ws: torch.Tensor) -> int:
+    """Timed-out device waits recorded in a workspace's error word (0: none).
+    Synchronises nothing itself: call after the calls' stream is synchronised.
+    Returns the count; the status (DS4A_OK / DS4A_ERR_TIMEOUT) follows from it."""
+    n = ctypes.c_uint32(0)
+    st = load().ds4a_workspace_status(_ptr(ws), _nbytes(ws), ctypes.byref(n))
+    if st not in (0, -7):
+        _check(st, "ds4a_workspace_status")
+    assert (st == -7) == (n.value != 0)
+    return n.value
+
+
+def ds4a_workspace_clear_status(ws: torch.Tensor, stream=None):
+    _check(load().ds4a_workspace_clear_status(_ptr(ws), _nbytes(ws), _stream(stream)),
+           "ds4a_workspace_clear_status")
+
+
+def ds4a_noalloc_status() -> int:
+    """ds4a_workspace_status of the no-allocation variant's static scratch."""
+    n = ctypes.c_uint32(0)
+    st = load().ds4a_noalloc_status(ctypes.byref(n))
+    if st not in (0, -7):
+        _check(st, "ds4a_noalloc_status")
+    return n.value
+
+
+def ds4a_wait_selftest(ws: torch.Tensor, limit_us: int, stream=None):
+    _check(load().ds4a_wait_selftest(_ptr(ws), _nbytes(ws), limit_us, _stream(stream)),
+           "ds4a_wait_selftest")
+
+
+def ds4a_set_decode_cluster(C: int):
+    _check(load().ds4a_set_decode_cluster(C), "ds4a_set_decode_cluster")
+
+
+def ds4a_decode_cluster_size(cache: "LayerCache", n_heads: int, top_k: int) -> int:
+    return load().ds4a_decode_cluster_size(cache.ref(), n_heads, top_k)
 
 
 def default_scale(head_dim: int) -> float:

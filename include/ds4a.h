@@ -256,7 +256,8 @@ ds4a_status ds4a_compress_append_lanes(ds4a_layer_cache *cache, uint32_t pos0, u
  *  topk    [B][T][k] int32 out: for the query at p, the k rows s < floor((p+1)/4)
  *          with the largest score I = sum_h w_h * ReLU(q'_h . k_s), ties to the
  *          lower index, in ascending order, padded with -1 when fewer are visible.
- *  ws      workspace of ds4a_workspace_bytes(DS4A_CALL_INDEX_TOPK, ...) bytes.
+ *  ws      workspace of ds4a_workspace_bytes(DS4A_CALL_INDEX_TOPK, ...) bytes;
+ *          its first 4 bytes are the call's wait status (ds4a_workspace_status).
  *
  * q' = tail rotation of q_idx at p, computed in fp32 (one rounding per
  * operation), then the FP4 QAT round trip when cache->qat has
@@ -283,7 +284,9 @@ ds4a_status ds4a_index_topk(const ds4a_layer_cache *cache, uint32_t pos0, uint32
  *  out     [B][H][D] (dtype): softmax over the raw rows of positions
  *          max(0, pos-cap_raw+1)..pos plus the compressed rows, V = K, with the
  *          output tail rotated back by -pos.
- *  ws      ds4a_workspace_bytes(DS4A_CALL_ATTN_DECODE, ...) bytes.
+ *  ws      ds4a_workspace_bytes(DS4A_CALL_ATTN_DECODE, ...) bytes (may be NULL when
+ *          that is 0); its first 4 bytes count timed-out device waits
+ *          (ds4a_workspace_status).
  * Requires pos + 1 == n_tokens (the token has been appended).
  */
 ds4a_status ds4a_sparse_attn_decode(const ds4a_layer_cache *cache, uint32_t pos,
@@ -342,6 +345,76 @@ ds4a_status ds4a_sparse_attn_prefill_chunk(ds4a_layer_cache *cache, uint32_t pos
 ds4a_status ds4a_index_topk_noalloc(const ds4a_layer_cache *cache, uint32_t pos0, uint32_t T,
                                     const void *q_idx, const void *w, uint32_t n_heads,
                                     uint32_t top_k, int32_t *topk, ds4a_stream_t stream);
+
+/*
+ * No-allocation variant's wait status: ds4a_workspace_status (below) applied
+ * to the static scratch of ds4a_index_topk_noalloc on the current device.
+ */
+ds4a_status ds4a_noalloc_status(uint32_t *count);
+
+/*
+ * Device wait status. Every wait inside the tensor-core kernels (on an
+ * mbarrier: TMA and cp.async arrivals, MMA completion, barriers between warps)
+ * gives up after 2 s, adds 1 to an error word and lets its thread block wind
+ * down, so a stuck call ends instead of hanging the device; the call's outputs
+ * are then invalid while the call itself has returned DS4A_OK (launches are
+ * asynchronous). The error word is the int32 at byte offset 0 of the workspace
+ * of ds4a_index_topk and of the attention calls (every workspace those calls
+ * need is at least 256 bytes; calls that need none have no device waits):
+ *  - ds4a_index_topk zeroes it at the start of every call, so after a call it
+ *    counts that call's timed-out waits;
+ *  - the attention calls never zero it (each launch compares it with its value
+ *    at the start): it counts the timed-out waits of every call since it was
+ *    last zeroed. Zero a new attention workspace once (ds4a_workspace_clear_status
+ *    or a memset of the first 4 bytes) before relying on it.
+ *
+ * ds4a_workspace_status: call after synchronising the stream of the calls
+ * that used `ws`. Copies the word to the host (a synchronous 4-byte
+ * cudaMemcpy; host memory, such as a mapped workspace or a host copy of the
+ * word, is read in place) and returns DS4A_OK when it is zero,
+ * DS4A_ERR_TIMEOUT otherwise;
+ * *count (may be NULL) receives its value. NULL ws or ws_bytes < 4:
+ * DS4A_ERR_WORKSPACE; a failed copy: DS4A_ERR_CUDA.
+ * ds4a_workspace_clear_status: zeroes the word, asynchronously on `stream`.
+ */
+ds4a_status ds4a_workspace_status(const void *ws, size_t ws_bytes, uint32_t *count);
+ds4a_status ds4a_workspace_clear_status(void *ws, size_t ws_bytes, ds4a_stream_t stream);
+
+/*
+ * Self-test of the bounded waits (the pages have no counterpart): one block of
+ * 128 threads waits, through the same bounded-wait code as the kernels but
+ * with a limit of limit_us microseconds (1 .. 1,000,000), on a barrier phase
+ * that nothing completes. No copy or MMA is in flight. Each waiting thread gives
+ * up when the limit has passed (or once another has recorded the timeout),
+ * the error word at byte offset 0 of ws grows by at least 1, and the block
+ * returns; ds4a_workspace_status then reports DS4A_ERR_TIMEOUT. Asynchronous
+ * on `stream`. Errors: DS4A_ERR_WORKSPACE (NULL ws, ws_bytes < 4),
+ * DS4A_ERR_ARG (limit out of range), DS4A_ERR_CUDA.
+ */
+ds4a_status ds4a_wait_selftest(void *ws, size_t ws_bytes, uint32_t limit_us,
+                               ds4a_stream_t stream);
+
+/*
+ * Cluster size of the tensor-core decode attention (bf16 layers, 64 heads x
+ * 512 dims, 64 rotated dims). That kernel spreads each query's 128-row tiles
+ * over a thread-block cluster of C CTAs and merges their partial outputs. C
+ * is chosen from the tile count (a bound from the cache's shape: cap_raw +
+ * top_k rows on ratio 4, cap_raw + comp_cap on ratio 128, cap_raw on ratio 0)
+ * and the device's cluster occupancy, so that the batch runs in one wave;
+ * sizes above 8 are used only where the device allows them.
+ *
+ * ds4a_set_decode_cluster(C): 0 (the default) keeps the automatic choice;
+ * 1 .. 16 forces C for every later decode launch of this process (a tuning
+ * and test hook), reduced to the call's tile count, and ignored where the
+ * device cannot launch that size. DS4A_ERR_ARG for C > 16.
+ * ds4a_decode_cluster_size: the C that ds4a_sparse_attn_decode uses for this
+ * cache and these arguments, with the current device current; 0 when the call
+ * does not run on that kernel (fp32 layers, other head shapes) or the cache
+ * fails its checks.
+ */
+ds4a_status ds4a_set_decode_cluster(uint32_t C);
+uint32_t ds4a_decode_cluster_size(const ds4a_layer_cache *cache, uint32_t n_heads,
+                                  uint32_t top_k);
 
 /* Workspace bytes a call needs for these sizes (0: none). */
 size_t ds4a_workspace_bytes(int call, const ds4a_layer_cache *cache, uint32_t T,

@@ -151,6 +151,14 @@ def test_argument_checks_reject_before_launch(L):
     c128 = _fake_cache(ratio=128)
     assert L.ds4a_index_topk(ctypes.byref(c128), 9, 1, fake, fake, 64, 512, fake, fake,
                              1 << 30, None) == -1
+    # the no-allocation variant runs the same checks before its scratch-size
+    # check: the same statuses, and nothing touches a device
+    assert L.ds4a_index_topk_noalloc(ctypes.byref(c128), 9, 1, fake, fake, 64, 512, fake,
+                                     None) == -1
+    assert L.ds4a_index_topk_noalloc(r, 10, 1, fake, fake, 64, 512, fake, None) == -4
+    assert L.ds4a_index_topk_noalloc(r, 9, 1, fake, fake, 64, 0, fake, None) == -2
+    assert L.ds4a_index_topk_noalloc(r, 9, 1, None, fake, 64, 512, fake, None) == -1
+    assert L.ds4a_index_topk_noalloc(None, 9, 1, fake, fake, 64, 512, fake, None) == -1
     # lane-selective append: empty or unknown lane set, a lane the layer lacks,
     # and the position check (n_tokens stays for the caller to set)
     assert L.ds4a_compress_append_lanes(r, 10, 1, 0, *P, None, None) == -1
@@ -271,3 +279,27 @@ int main(void) {
     assert st == 0 and np.float32(float(out[3])) == ref_c[1, 1]   # %.9g round-trips fp32
     assert np.float32(float(out[4])) == ref_s[2, 5]
     assert bad == -1 and " ".join(out[5:]) == "invalid argument"
+
+
+def test_wait_status_and_cluster_hooks_on_cpu(L):
+    """The wait status read-back maps a nonzero error word to DS4A_ERR_TIMEOUT
+    and returns the count (a host copy of the word, read in place); the
+    argument checks of the status, self-test and cluster calls reject bad
+    values before touching a device."""
+    word = (ctypes.c_int32 * 64)()
+    n = ctypes.c_uint32(99)
+    assert L.ds4a_workspace_status(ctypes.addressof(word), 256, ctypes.byref(n)) == 0
+    assert n.value == 0
+    word[0] = 3
+    assert L.ds4a_workspace_status(ctypes.addressof(word), 256, ctypes.byref(n)) == -7
+    assert n.value == 3
+    assert L.ds4a_workspace_status(ctypes.addressof(word), 256, None) == -7
+    assert L.ds4a_status_string(-7) == b"device wait timed out"
+    assert L.ds4a_workspace_status(None, 256, ctypes.byref(n)) == -8
+    assert L.ds4a_workspace_status(ctypes.addressof(word), 3, ctypes.byref(n)) == -8
+    assert L.ds4a_workspace_clear_status(None, 256, None) == -8
+    assert L.ds4a_wait_selftest(None, 256, 1000, None) == -8
+    assert L.ds4a_wait_selftest(ctypes.addressof(word), 256, 0, None) == -1
+    assert L.ds4a_wait_selftest(ctypes.addressof(word), 256, 1000001, None) == -1
+    assert L.ds4a_set_decode_cluster(17) == -1
+    assert L.ds4a_decode_cluster_size(None, 64, 512) == 0

@@ -8,6 +8,7 @@ import torch
 
 import synth
 from helpers import TOL, gpu_cache, np_, oracle_cache, rel_l2
+from test_gpu_parity import compare_cache
 from oracle import layer as olayer
 from test_gpu_parity import lib_, run_attn, run_index
 
@@ -85,42 +86,60 @@ def test_c4a_decode_full_size_sampled():
         assert rel_l2(np_(out[b]), o_ref[0]) <= TOL["bf16"], b
 
 
+def prefill_samples(T: int):
+    """Queries checked in a full chunk: every 16th, plus the four positions of
+    each residue mod 4 at both ends of the chunk."""
+    return sorted(set(range(0, T, 16)) | set(range(4)) | set(range(T - 4, T)))
+
+
 def test_c4a_prefill_full_size_sampled():
-    """One 4096-token chunk at 28,672 over a 28,672-token cache: exact top-k
-    and attention for sampled queries (first, boundary, middle, last)."""
+    """The 4096-token chunk at 28,672 over a cache built from the 28,672
+    earlier seeded tokens: on the GPU by seven 4096-token chunks of the real
+    prefill path (append, top-k, chunk attention with the window commit), in
+    the oracle by its own compressor from an empty cache. The caches must
+    agree before the chunk (state bit-identical, rows within the bf16 bound)
+    and the chunk's top-k lists and outputs must match on sampled queries
+    ("【#3】ds4.c を読み解く" §3: chunks keep absolute positions)."""
     lib = lib_()
     wl = synth.C4A_PREFILL
     s = wl.layers[0]
     p0, T = wl.context, wl.chunk
     cap = (p0 + T) // 4 + 1
-    hist = synth.cache_history(wl, 0, p0, comp_cap=cap, device=DEV)
-    inp = {k: v.contiguous() for k, v in synth.step_inputs(wl, 0, p0, T, device=DEV).items()}
-    gc = gpu_cache(s, 1, cap, p0 + T + 1, hist, p0)
-    ring0 = gc.raw_kv.clone()
+    k, scale = s.top_k, 1 / np.sqrt(s.head_dim)
+    gc = gpu_cache(s, 1, cap, p0 + T + 1, synth.empty_history(wl, 0, cap, device=DEV), 0)
+    lib.ds4a_cache_reset(gc)
+    oc = oracle_cache(s, synth.empty_history(wl, 0, cap), 0)
+    comp_keys = ("raw_kv_in", "attn_cand", "attn_score", "idx_cand", "idx_score", "ape_attn",
+                 "gamma_attn", "ape_idx", "gamma_idx")
     chunk = torch.empty((1, T, s.head_dim), dtype=torch.bfloat16, device=DEV)
-    lib.ds4a_compress_append(gc, p0, T, inp, raw_chunk_out=chunk)
-    k = s.top_k
     topk = torch.empty((1, T, k), dtype=torch.int32, device=DEV)
-    ws = lib.workspace(gc.workspace_bytes(lib.CALL_INDEX_TOPK, T, s.index_heads, k))
-    lib.ds4a_index_topk(gc, p0, T, inp["q_idx"], inp["w"], s.index_heads, k, topk, ws)
     out = torch.empty((1, T, s.n_heads, s.head_dim), dtype=torch.bfloat16, device=DEV)
+    ws = lib.workspace(gc.workspace_bytes(lib.CALL_INDEX_TOPK, T, s.index_heads, k))
     wa = lib.workspace(gc.workspace_bytes(lib.CALL_ATTN_PREFILL, T, s.n_heads, k))
-    lib.ds4a_sparse_attn_prefill_chunk(gc, p0, T, inp["q"], s.n_heads, chunk, topk, k,
-                                       1 / np.sqrt(s.head_dim), out, wa)
+    for p in range(0, p0 + 1, T):
+        inp = {n: v.contiguous() for n, v in synth.step_inputs(wl, 0, p, T, device=DEV).items()}
+        if p == p0:
+            ring0 = np_(gc.raw_kv)
+            compare_cache(gc, oc, "bf16", "history")
+        lib.ds4a_compress_append(gc, p, T, inp, raw_chunk_out=chunk)
+        lib.ds4a_index_topk(gc, p, T, inp["q_idx"], inp["w"], s.index_heads, k, topk, ws)
+        lib.ds4a_sparse_attn_prefill_chunk(gc, p, T, inp["q"], s.n_heads, chunk, topk, k,
+                                           scale, out, wa)
+        ninp = {n: np_(inp[n]) for n in comp_keys}
+        rows = olayer.compress_append(oc, p, ninp, chunk=True)
+        if p < p0:
+            olayer.commit_ring(oc, p, rows)
     torch.cuda.synchronize()
-    # the oracle on the same chunk: compressor over the whole chunk, then samples
-    oc = oracle_cache(s, {n: t.cpu() for n, t in hist.items()}, p0)
-    ninp = {n: np_(t) for n, t in inp.items()}
-    rows = olayer.compress_append(oc, p0, ninp, chunk=True)
+    assert lib.ds4a_workspace_status(ws) == 0 and lib.ds4a_workspace_status(wa) == 0
     assert rel_l2(np_(chunk), rows) <= TOL["bf16"]
     assert oc.n_comp == 8192 and gc.n_tokens == p0 + T
     assert rel_l2(np_(gc.attn_comp_kv)[:, 7168:8192], oc.attn_comp_kv[:, 7168:8192]) <= TOL["bf16"]
-    qs = [(0, t) for t in (0, 1, 2, 3, 4, 127, 128, 1000, 2047, 4092, 4094, 4095)]
-    tk_ref = olayer.index_topk(oc, p0, ninp["q_idx"], ninp["w"], k, queries=qs)
+    qs = [(0, t) for t in prefill_samples(T)]
+    tk_ref = olayer.index_topk(oc, p0, np_(inp["q_idx"]), np_(inp["w"]), k, queries=qs)
     got_tk = topk.cpu().numpy()
     for b, t in qs:
         assert np.array_equal(got_tk[b, t], tk_ref[b, t]), t
-    o_ref = olayer.attention(oc, p0, ninp["q"], tk_ref, None, ring=np_(ring0), chunk_rows=rows,
+    o_ref = olayer.attention(oc, p0, np_(inp["q"]), tk_ref, None, ring=ring0, chunk_rows=rows,
                              queries=qs)
     got = np.stack([np_(out[b, t]) for b, t in qs])
     ref = np.stack([o_ref[b, t] for b, t in qs])

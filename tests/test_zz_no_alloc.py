@@ -47,6 +47,7 @@ def test_noalloc_matches_workspace_entry_point(shape, B, p):
         lib.ds4a_index_topk_noalloc(c, p, 1, q_idx, w, shape.index_heads, k, got)
         torch.cuda.synchronize()
         assert np.array_equal(got.cpu().numpy(), ref.cpu().numpy()), f"call {call}"
+        assert lib.ds4a_noalloc_status() == 0      # no device wait gave up
 
 
 def test_noalloc_rejects_requests_beyond_the_scratch():
