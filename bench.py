@@ -10,17 +10,23 @@ A step is one pass of the whole per-layer path over one batch:
                       attention with the raw-window commit.
 Default workload: the 43-layer Flash schedule decoding 8 sequences at context
 131,072 (ratio-4 and ratio-128 layers, both lanes, every step of the path).
-`value` is whole-job tokens/s with every input resident in HBM; `e2e` adds the
-per-step host->device copy of the step's inputs (pinned) and the device->host
-read of the last layer's output. The reference arm (--impl reference) times
-the CPU oracle on a bounded sample of the same workload.
+`value` is whole-job tokens/s with every input resident in HBM, over K graph
+replays timed as one region; `median_ms_per_step` is the median of at least
+100 replays timed one by one. `e2e` adds the per-step host->device copy of the
+step's inputs (pinned) and the device->host read of the last layer's output.
+On one GPU the default line also carries, under `workloads`, the single c4a
+layer decode (32 sequences at 65,536), the single c128a layer decode (one
+sequence at 65,536) and the 4096-token prefill chunk at 28,672, each with its
+own roofline, and under `boundary_step` the Flash stack decoding at 131,071,
+where every compressed layer emits a row. `cpu_baseline` times the oracle on
+every host core and on one core; the reference arm (--impl reference) times it
+on every host core. Both time a bounded sample of the workload and scale it to
+a step by a stated factor.
 """
 import argparse
 import json
 import os
 
-os.environ.setdefault("OPENBLAS_NUM_THREADS", "1")   # the oracle legs run single-threaded
-os.environ.setdefault("OMP_NUM_THREADS", "1")
 import statistics
 import subprocess
 import sys
@@ -37,6 +43,8 @@ METRIC = ("c4a/c128a decode tok/s & HBM GB/s frac; 4096-chunk prefill tok/s (1×
 WORKLOADS = {"flash43": synth.FLASH_STACK, "c4a_decode": synth.C4A_DECODE,
              "c128a_decode": synth.C128A_DECODE, "prefill": synth.C4A_PREFILL,
              "tiny": synth.TINY, "flash_c4a_layer": synth.FLASH_C4A_LAYER}
+WORKLOADS_BY_NAME = {w.name: w for w in WORKLOADS.values()}
+SINGLE_THREAD_ENV = ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS")
 # ncu DRAM counters per call, recorded with the hash of the kernel sources they
 # were taken on; a stale record (sources changed since) reports null
 TRAFFIC_PATH = os.path.join(ROOT, "profiles", "traffic.json")
@@ -439,6 +447,20 @@ def run_gpu(args, wl, rank, world, device):
     if world > 1:
         torch.distributed.barrier()
     ms = e0.elapsed_time(e1) / args.steps
+    # the same replays timed one by one (median of at least 100), the L2
+    # flush outside each pair of events
+    rep_ms = []
+    for _ in range(max(100, args.steps)):
+        if flush is not None:
+            flush_l2(flush)
+        r0, r1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        r0.record()
+        (g.replay() if use_graph else R.step())
+        r1.record()
+        rep_ms.append((r0, r1))
+    torch.cuda.synchronize(device)
+    rep_ms = sorted(a.elapsed_time(b) for a, b in rep_ms)
+    median_ms = max_over_ranks(statistics.median(rep_ms), world, device)
     flush_ms = 0.0
     if flush is not None:        # subtract the L2 flush from the step time
         f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -537,10 +559,14 @@ def run_gpu(args, wl, rank, world, device):
 
     res = {"metric": METRIC, "value": value, "unit": "tok/s", "n_gpus": world,
            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+           "median_ms_per_step": median_ms, "timed_replays_for_median": len(rep_ms),
+           "p10_p90_ms_per_step": [rep_ms[len(rep_ms) // 10], rep_ms[(9 * len(rep_ms)) // 10]],
            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
            "dtype": wl.dtype, "data": "synthetic",
            "config": {"workload": wl.name, "mode": wl.mode, "batch_per_gpu": wl.batch,
                       "context": wl.context, "tokens_per_step_per_gpu": R.tokens_per_step(),
+                      "positions": (f"decode at p = {wl.context}" if wl.mode == "decode" else
+                                    f"chunk of {wl.chunk} at p = {wl.context}"),
                       "layers": len(wl.layers),
                       "ratios": {str(r): sum(1 for s in wl.layers if s.ratio == r)
                                  for r in (0, 4, 128)},
@@ -561,105 +587,312 @@ def run_gpu(args, wl, rank, world, device):
 
 # ----------------------------------------------------------------- CPU oracle
 # The CPU baseline and the reference arm time the oracle (test infrastructure)
-# as it stands, single-threaded numpy, on a bounded sample of the workload.
+# as it stands: plain numpy, one thread per process, on a bounded sample of the
+# workload, once on every host core (one spawned process per core, each with
+# its own units) and once on one core. The sample's time is scaled to a whole
+# step by the stated factor.
 
-def _oracle_layer_case(wl: synth.Workload, il: int):
-    """Oracle cache + step inputs of layer il for the first sequence only."""
+def _one_seq(wl: synth.Workload, b: int) -> synth.Workload:
+    """A one-sequence workload standing for sequence b (its own seeded draw)."""
+    return synth.Workload(wl.name, wl.seed * 1000 + b, 1, wl.layers, wl.context, wl.mode,
+                          wl.chunk, wl.hidden)
+
+
+def _oracle_cache(s, hist, n_tokens):
     from oracle.layer import OracleCache
-    s = wl.layers[il]
-    one = synth.Workload(wl.name, wl.seed, 1, wl.layers, wl.context, wl.mode, wl.chunk, wl.hidden)
-    T = 1 if wl.mode == "decode" else wl.chunk
-    cap = (wl.context + T) // s.ratio + 1 if s.ratio else 0
-    hist = synth.cache_history(one, il, wl.context, comp_cap=cap)
-    inp = synth.step_inputs(one, il, wl.context, T)
-    np_ = lambda t: t.float().numpy()
-    oc = OracleCache(ratio=s.ratio, head_dim=s.head_dim, n_rot=s.n_rot, cap_raw=s.cap_raw,
-                     base=s.rope_base, dtype=s.dtype, n_tokens=wl.context,
-                     index_dim=s.index_dim, index_rot=s.index_rot,
-                     **{k: np_(v) for k, v in hist.items()})
-    return oc, {k: np_(v) for k, v in inp.items()}
+    f = lambda t: t.float().numpy()
+    return OracleCache(ratio=s.ratio, head_dim=s.head_dim, n_rot=s.n_rot, cap_raw=s.cap_raw,
+                       base=s.rope_base, dtype=s.dtype, n_tokens=n_tokens,
+                       index_dim=s.index_dim, index_rot=s.index_rot,
+                       **{k: f(v) for k, v in hist.items()})
 
 
-def oracle_sample(wl: synth.Workload):
-    """Time one bounded oracle pass; return (seconds spent, seconds the oracle
-    would take for one whole step of the workload, description)."""
-    from oracle import layer as olayer
-    if wl.mode == "decode":
-        kinds = {}
-        for il, s in enumerate(wl.layers):
-            kinds.setdefault(s.ratio, []).append(il)
-        spent, per_seq = 0.0, 0.0
-        for ratio, ils in kinds.items():
-            oc, inp = _oracle_layer_case(wl, ils[0])
-            t0 = time.perf_counter()
-            olayer.decode_step(oc, wl.context, inp, wl.layers[ils[0]].top_k)
-            dt = time.perf_counter() - t0
-            spent += dt
-            per_seq += dt * len(ils)
-        desc = (f"sequence 0 only, one layer of each ratio {sorted(kinds)} "
-                f"(append + top-k + attention), scaled by layers per ratio and by {wl.batch} sequences")
-        return spent, per_seq * wl.batch, desc
+def _build_unit(wl: synth.Workload, unit):
+    """State for one unit of oracle work. Units: ("dec", ratio, il, b) one
+    decode step of layer il for sequence b; ("app",) the prefill chunk's
+    compressor append; ("qry", (t, ...)) the indexer top-k and attention of
+    those chunk queries."""
+    import numpy as np
+    f = lambda t: t.float().numpy()
+    if unit[0] == "dec":
+        _, _, il, b = unit
+        one = _one_seq(wl, b)
+        s = wl.layers[il]
+        cap = (wl.context + 1) // s.ratio + 1 if s.ratio else 0
+        oc = _oracle_cache(s, synth.cache_history(one, il, wl.context, comp_cap=cap), wl.context)
+        inp = {k: f(v) for k, v in synth.step_inputs(one, il, wl.context, 1).items()}
+        state = {k: getattr(oc, k).copy() for k in ("attn_state_kv", "attn_state_score",
+                                                     "index_state_kv", "index_state_score")
+                 if getattr(oc, k) is not None}
+        return {"oc": oc, "inp": inp, "state": state, "s": s}
     s = wl.layers[0]
-    oc, inp = _oracle_layer_case(wl, 0)
+    one = _one_seq(wl, 0)
+    p0, T = wl.context, wl.chunk
+    cap = (p0 + T) // 4 + 1
+    oc = _oracle_cache(s, synth.cache_history(one, 0, p0, comp_cap=cap), p0)
+    sd, key = one.seed, ("cpu-sample", p0, T)
+    inp = {n: f(synth.normal((1, T, w), sd, *key, n, dtype=s.dtype))
+           for n, w in (("raw_kv_in", s.head_dim), ("attn_cand", s.head_dim),
+                        ("attn_score", s.head_dim), ("idx_cand", s.index_dim),
+                        ("idx_score", s.index_dim))}
+    inp.update({k: f(v) for k, v in synth.layer_weights(one, 0).items()})
+    state = {k: getattr(oc, k).copy() for k in ("attn_state_kv", "attn_state_score",
+                                                 "index_state_kv", "index_state_score")}
+    if unit[0] == "app":
+        return {"oc": oc, "inp": inp, "state": state, "s": s, "p0": p0}
+    from oracle import layer as olayer
     ring = oc.raw_kv.copy()
-    t0 = time.perf_counter()
-    rows = olayer.compress_append(oc, wl.context, inp, chunk=True)
-    t_app = time.perf_counter() - t0
-    nq = 2
-    qs = [(0, 0), (0, wl.chunk - 1)]
-    t0 = time.perf_counter()
-    tk = olayer.index_topk(oc, wl.context, inp["q_idx"], inp["w"], s.top_k, queries=qs)
-    olayer.attention(oc, wl.context, inp["q"], tk, None, ring=ring, chunk_rows=rows, queries=qs)
-    t_q = (time.perf_counter() - t0) / nq
-    desc = (f"whole-chunk compressor append + {nq} of {wl.chunk} queries (indexer scan, top-k, "
-            "attention), queries scaled to the chunk")
-    return t_app + nq * t_q, (t_app + wl.chunk * t_q) * wl.batch, desc
+    rows = olayer.compress_append(oc, p0, inp, chunk=True)
+    ts = unit[1]
+    n = len(ts)
+    q = f(synth.normal((n, s.n_heads, s.head_dim), sd, *key, "q", dtype=s.dtype)).astype(np.float64)
+    q_idx = f(synth.normal((n, s.index_heads, s.index_dim), sd, *key, "qidx", dtype=s.dtype))
+    w = f(synth.normal((n, s.index_heads), sd, *key, "w", dtype=s.dtype))
+    return {"oc": oc, "s": s, "p0": p0, "ring": ring, "rows": rows, "ts": ts, "q": q,
+            "q_idx": q_idx, "w": w}
 
 
-def _threads():
-    return int(os.environ.get("OPENBLAS_NUM_THREADS", "1"))
+def _run_unit(unit, st):
+    """The timed oracle work of one unit (state restored first where the work
+    changes it: the same position is appended again on every repeat)."""
+    from oracle import layer as olayer
+    oc = st["oc"]
+    if unit[0] == "dec":
+        for k, v in st["state"].items():
+            getattr(oc, k)[...] = v
+        oc.n_tokens = st["p"]
+        olayer.decode_step(oc, st["p"], st["inp"], st["s"].top_k)
+        return
+    if unit[0] == "app":
+        for k, v in st["state"].items():
+            getattr(oc, k)[...] = v
+        oc.n_tokens = st["p0"]
+        olayer.compress_append(oc, st["p0"], st["inp"], chunk=True)
+        return
+    from oracle.attention import attention_query, comp_row_ids
+    from oracle.indexer import index_topk_query
+    s, p0 = st["s"], st["p0"]
+    for j, t in enumerate(st["ts"]):
+        p = p0 + t
+        tk = index_topk_query(st["q_idx"][j], st["w"][j], oc.index_comp_kv[0], p, oc.base,
+                              oc.index_rot, oc.dtype, s.top_k)
+        win = olayer._window_rows(oc, 0, p, p0, st["ring"], st["rows"])
+        ids = comp_row_ids(oc.ratio, p, oc.n_comp, tk)
+        attention_query(st["q"][j], p, win, oc.attn_comp_kv[0, ids], oc.base, oc.n_rot,
+                        1.0 / s.head_dim ** 0.5, oc.dtype)
 
 
-def cpu_baseline(wl: synth.Workload, budget_s: float = 10.0):
-    spent_all, est = 0.0, []
-    while spent_all < budget_s:
-        spent, step_s, desc = oracle_sample(wl)
-        spent_all += spent
-        est.append(step_s)
-    step_s = statistics.median(est)
-    tokens = wl.batch * (1 if wl.mode == "decode" else wl.chunk)
-    return {"value": tokens / step_s, "unit": "tok/s", "cores": _threads(), "kind": "oracle",
-            "sample": f"{desc}; {len(est)} repeats, {spent_all:.1f} s of CPU work"}
+def _oracle_worker(conn, wl_name, units):
+    """Child process: build every unit once, then on each command (a unit
+    kind) run its units of that kind and reply with the start and end of the
+    work on the host's monotonic clock."""
+    wl = WORKLOADS_BY_NAME[wl_name]
+    built = []
+    for u in units:
+        st = _build_unit(wl, u)
+        if u[0] == "dec":
+            st["p"] = wl.context
+        built.append((u, st))
+    conn.send("ready")
+    while True:
+        kind = conn.recv()
+        if kind is None:
+            break
+        t0 = time.perf_counter()
+        for u, st in built:
+            if _unit_kind(u) == kind:
+                _run_unit(u, st)
+        conn.send((t0, time.perf_counter()))
+    conn.close()
+
+
+def _unit_kind(u):
+    return ("dec", u[1]) if u[0] == "dec" else (u[0],)
+
+
+def oracle_plan(wl: synth.Workload, cores: int):
+    """Units of a bounded sample and how a step is built from them.
+
+    Returns (units, phases, desc): phases is a list of (kind, factor): a step
+    costs sum(factor * wall time of that kind's phase)."""
+    if wl.mode == "decode":
+        by = {}
+        for il, s in enumerate(wl.layers):
+            by.setdefault(s.ratio, []).append(il)
+        units, phases, parts = [], [], []
+        for ratio, ils in sorted(by.items()):
+            n_l = len(ils)
+            seqs = list(range(wl.batch)) if cores > 1 else [0]
+            per = max(1, min(n_l, -(-cores // len(seqs)))) if cores > 1 else 1
+            for il in ils[:per]:
+                units += [("dec", ratio, il, b) for b in seqs]
+            factor = n_l / per * (wl.batch / len(seqs))
+            phases.append((("dec", ratio), factor))
+            parts.append(f"ratio {ratio}: {per} of {n_l} layers x {len(seqs)} of {wl.batch} "
+                         f"sequences (x{factor:g})")
+        return units, phases, "decode step (append + top-k + attention) per (layer, sequence); "             + "; ".join(parts)
+    T = wl.chunk
+    n_q = max(4, 4 * cores)
+    ts = [round(i * (T - 1) / (n_q - 1)) for i in range(n_q)]
+    units = [("app",)] + [("qry", tuple(ts[i::cores])) for i in range(min(cores, n_q))]
+    phases = [(("app",), float(wl.batch)), (("qry",), T / n_q * wl.batch)]
+    return units, phases, (f"compressor append of the whole {T}-token chunk (x{wl.batch}), then "
+                           f"{n_q} of {T} queries (indexer scan, top-k, attention; "
+                           f"x{T / n_q * wl.batch:g})")
+
+
+class OraclePool:
+    """`cores` spawned worker processes, each holding its units' state."""
+
+    def __init__(self, wl: synth.Workload, cores: int):
+        import multiprocessing as mp
+        self.units, self.phases, self.desc = oracle_plan(wl, cores)
+        ctx = mp.get_context("spawn")
+        n = min(cores, len(self.units))
+        # deal the units of every kind round-robin over the workers
+        share = [[] for _ in range(n)]
+        for kind, _ in self.phases:
+            ku = [u for u in self.units if _unit_kind(u) == kind]
+            for i, u in enumerate(ku):
+                share[i % n].append(u)
+        self.conns, self.procs, self.share = [], [], share
+        # one BLAS / OpenMP thread per worker: the children read these at start
+        keep = {k: os.environ.get(k) for k in SINGLE_THREAD_ENV}
+        os.environ.update({k: "1" for k in SINGLE_THREAD_ENV})
+        try:
+            for sh in share:
+                a, b = ctx.Pipe()
+                pr = ctx.Process(target=_oracle_worker, args=(b, wl.name, sh), daemon=True)
+                pr.start()
+                self.conns.append(a)
+                self.procs.append(pr)
+        finally:
+            for k, v in keep.items():
+                if v is None:
+                    os.environ.pop(k, None)
+                else:
+                    os.environ[k] = v
+        for c in self.conns:
+            assert c.recv() == "ready"
+        self.cores = n
+
+    def step(self):
+        """(seconds of sampled work on the wall clock, estimated seconds of one
+        whole step)."""
+        spent, est = 0.0, 0.0
+        for kind, factor in self.phases:
+            for c in self.conns:
+                c.send(kind)
+            ts = [c.recv() for c in self.conns]
+            busy = [(t0, t1) for (t0, t1), sh in zip(ts, self.share)
+                    if any(_unit_kind(u) == kind for u in sh)]
+            wall = max(t1 for _, t1 in busy) - min(t0 for t0, _ in busy)
+            spent += wall
+            est += factor * wall
+        return spent, est
+
+    def close(self):
+        for c in self.conns:
+            try:
+                c.send(None)
+            except OSError:
+                pass
+        for pr in self.procs:
+            pr.join(timeout=30)
+
+
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def _tokens(wl):
+    return wl.batch * (1 if wl.mode == "decode" else wl.chunk)
+
+
+def time_oracle(wl: synth.Workload, cores: int, budget_s: float, min_steps: int = 1):
+    """Repeat the sampled step until budget_s of wall time; median estimate."""
+    pool = OraclePool(wl, cores)
+    try:
+        pool.step()                       # warm-up
+        spent, est = 0.0, []
+        while spent < budget_s or len(est) < min_steps:
+            sp, e = pool.step()
+            spent += sp
+            est.append(e)
+        step_s = statistics.median(est)
+        return {"value": _tokens(wl) / step_s, "unit": "tok/s", "cores": pool.cores,
+                "kind": "oracle", "step_s_estimated": step_s,
+                "sample": f"{pool.desc}; {len(est)} repeats, {spent:.1f} s of wall time"}
+    finally:
+        pool.close()
+
+
+def cpu_baseline(wl: synth.Workload, budget_s: float = 8.0):
+    """The oracle on every host core (headline) and on one core."""
+    allc = time_oracle(wl, host_cores(), budget_s)
+    one = time_oracle(wl, 1, budget_s / 2)
+    allc["one_core"] = {k: one[k] for k in ("value", "unit", "cores", "sample")}
+    return allc
 
 
 def reference_arm(wl: synth.Workload, steps: int, warmup: int, world: int):
-    tokens = wl.batch * (1 if wl.mode == "decode" else wl.chunk)
-    for _ in range(warmup):
-        oracle_sample(wl)
-    vals, spent_all, desc = [], 0.0, ""
-    for _ in range(steps):
-        spent, step_s, desc = oracle_sample(wl)
-        spent_all += spent
-        vals.append(step_s)
-    step_s = statistics.median(vals)
-    v = tokens / step_s
+    pool = OraclePool(wl, host_cores())
+    try:
+        for _ in range(warmup):
+            pool.step()
+        spent, est = [], []
+        for _ in range(steps):
+            sp, e = pool.step()
+            spent.append(sp)
+            est.append(e)
+    finally:
+        pool.close()
+    step_s = statistics.median(est)
+    v = _tokens(wl) / step_s
+    sampled = statistics.median(spent)
     return {"metric": METRIC, "value": v, "unit": "tok/s", "n_gpus": world, "steps": steps,
             "warmup": warmup, "ms_per_step": step_s * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic",
             "impl": "reference",
+            "ms_per_step_is": "extrapolated from the timed sample (see extrapolation)",
+            "extrapolation": {"timed_ms_per_step": sampled * 1e3,
+                              "factor": step_s / sampled if sampled > 0 else None,
+                              "sample": pool.desc},
             "config": {"workload": wl.name, "mode": wl.mode, "batch_per_gpu": wl.batch,
                        "context": wl.context},
-            "cpu_baseline": {"value": v, "unit": "tok/s", "cores": _threads(), "kind": "oracle",
-                             "sample": desc},
+            "cpu_baseline": {"value": v, "unit": "tok/s", "cores": pool.cores, "kind": "oracle",
+                             "sample": pool.desc},
             "e2e": {"value": v, "unit": "tok/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
+
+
+def boundary(wl: synth.Workload) -> synth.Workload:
+    """The same decode workload one token earlier: at p = 131,071 (3 mod 4,
+    127 mod 128) every compressed layer's append emits a row, so the pooling,
+    RMSNorm, rotation and insertion of both lanes run in the timed step."""
+    return synth.Workload(wl.name + "_boundary", wl.seed, wl.batch, wl.layers, wl.context - 1,
+                          wl.mode, wl.chunk, wl.hidden)
+
+
+def summary(r: dict) -> dict:
+    """The keys of another workload's line carried in the default line."""
+    keys = ("value", "unit", "ms_per_step", "median_ms_per_step", "p10_p90_ms_per_step",
+            "dtype", "roofline", "calls", "e2e", "clocks", "gpu_launches", "steps")
+    out = {k: r[k] for k in keys if k in r}
+    out["config"] = {k: r["config"][k] for k in ("workload", "mode", "batch_per_gpu", "context",
+                                                  "positions", "tokens_per_step_per_gpu", "l2",
+                                                  "algorithmic_GB_per_step", "step_GB/s")}
+    return out
 
 
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--workload", default="flash43", choices=sorted(WORKLOADS))
     ap.add_argument("--impl", default="gpu", choices=["gpu", "reference"])
     ap.add_argument("--no-graph", action="store_true")
@@ -671,6 +904,9 @@ def main():
                     help="compressor step 8 on: FP8 round trip of attention rows, FP4 QAT "
                          "round trip of indexer rows and queries")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="default workload only: skip the other workloads' keys "
+                         "(c4a / c128a decode, prefill chunk, boundary step)")
     ap.add_argument("--write-traffic", metavar="NCU_CSV",
                     help="record per-call DRAM bytes of --workload from an ncu CSV and exit")
     ap.add_argument("--captured-on", default=None,
@@ -697,7 +933,20 @@ def main():
         torch.distributed.init_process_group("nccl")
     device = torch.device("cuda", local)
     torch.cuda.set_device(device)
-    res, _ = run_gpu(args, wl, rank, world, device)
+    res, R = run_gpu(args, wl, rank, world, device)
+    del R
+    if world == 1 and args.workload == "flash43" and not args.no_extras:
+        torch.cuda.empty_cache()
+        res["workloads"] = {}
+        for name in ("c4a_decode", "c128a_decode", "prefill"):
+            r, R = run_gpu(args, WORKLOADS[name], rank, world, device)
+            del R
+            torch.cuda.empty_cache()
+            res["workloads"][name] = summary(r)
+        r, R = run_gpu(args, boundary(wl), rank, world, device)
+        del R
+        torch.cuda.empty_cache()
+        res["boundary_step"] = summary(r)
     if rank == 0:
         if not args.no_cpu_baseline:
             res["cpu_baseline"] = cpu_baseline(wl)

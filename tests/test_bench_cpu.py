@@ -92,3 +92,26 @@ def test_reference_arm_line_keeps_the_contract():
     assert line["e2e"] == {"value": line["value"], "unit": line["unit"],
                            "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
     assert line["config"]["workload"] == bench.WORKLOADS["tiny"].name
+    ex = line["extrapolation"]         # the step time is scaled from a timed sample
+    assert ex["factor"] == pytest.approx(line["ms_per_step"] / ex["timed_ms_per_step"])
+
+
+def test_oracle_sample_plan_scales_to_a_whole_step():
+    """The CPU oracle's sample and its scale factors: on many cores every
+    sequence of a layer of each kind runs in parallel and the layers of a
+    kind scale it; on one core one (layer, sequence) per kind scales by
+    layers x sequences; a prefill chunk samples queries evenly."""
+    wl = bench.WORKLOADS["flash43"]
+    units, phases, _ = bench.oracle_plan(wl, 16)
+    f = dict(phases)
+    assert f[("dec", 0)] == 1.0 and f[("dec", 4)] == 10.5 and f[("dec", 128)] == 10.0
+    assert sum(1 for u in units if u[:2] == ("dec", 4)) == 16      # 2 layers x 8 sequences
+    units, phases, _ = bench.oracle_plan(wl, 1)
+    f = dict(phases)
+    assert f[("dec", 0)] == 16 and f[("dec", 4)] == 168 and f[("dec", 128)] == 160
+    assert len(units) == 3
+    wl = bench.WORKLOADS["prefill"]
+    units, phases, _ = bench.oracle_plan(wl, 4)
+    qs = sorted(t for u in units if u[0] == "qry" for t in u[1])
+    assert len(qs) == 16 and qs[0] == 0 and qs[-1] == wl.chunk - 1
+    assert dict(phases)[("qry",)] == wl.chunk / 16
