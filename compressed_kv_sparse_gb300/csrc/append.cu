@@ -17,6 +17,7 @@
 // for tokens before pos0, from the state as it was before the chunk; a second
 // launch then writes the state as the token-by-token process would leave it.
 #include "quant.cuh"
+#include "tc.cuh"
 
 namespace ds4a {
 namespace {
@@ -221,20 +222,12 @@ __device__ void raw_row(const T *src, T *dst, uint32_t D, uint32_t n_rot, uint32
   }
 }
 
+// One lane's decode step in one block: store the token into its window slot
+// and, at a ratio boundary, pool, normalise, rotate and append the row, then
+// (ratio 4) move slots 4..7 to 0..3.
 template <typename T>
-__global__ void __launch_bounds__(kThreads) append_step_kernel(AppendArgs a) {
-  __shared__ float red[32];
-  pdl_wait();
-  pdl_trigger();
-  const uint32_t b = blockIdx.x, p = seq_base(a.seq_pos, a.pos0, b), role = blockIdx.y + a.y0;
-  if (role == 0) {
-    const T *src = static_cast<const T *>(a.raw_in) + (size_t)b * a.head_dim;
-    T *dst = static_cast<T *>(a.raw_dst) +
-             ((size_t)b * a.cap_raw + p % a.cap_raw) * a.head_dim;
-    raw_row(src, dst, a.head_dim, a.n_rot, p, a.cos, a.sin);
-    return;
-  }
-  const LaneArgs &L = a.lane[role - 1];
+__device__ void lane_step_block(const AppendArgs &a, const LaneArgs &L, uint32_t b, uint32_t p,
+                                float *red) {
   const uint32_t r = a.ratio, W = a.window, width = L.width;
   const uint32_t slot = r == 4 ? 4 + p % 4 : p % r;
   const T *cand = static_cast<const T *>(L.cand) + (size_t)b * width;
@@ -262,6 +255,218 @@ __global__ void __launch_bounds__(kThreads) append_step_kernel(AppendArgs a) {
         skv[(size_t)s * width + c] = skv[(size_t)(4 + s) * width + c];
         ssc[(size_t)s * width + c] = ssc[(size_t)(4 + s) * width + c];
       }
+    }
+  }
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kThreads) append_step_kernel(AppendArgs a) {
+  __shared__ float red[32];
+  pdl_wait();
+  pdl_trigger();
+  const uint32_t b = blockIdx.x, p = seq_base(a.seq_pos, a.pos0, b), role = blockIdx.y + a.y0;
+  if (role == 0) {
+    const T *src = static_cast<const T *>(a.raw_in) + (size_t)b * a.head_dim;
+    T *dst = static_cast<T *>(a.raw_dst) +
+             ((size_t)b * a.cap_raw + p % a.cap_raw) * a.head_dim;
+    raw_row(src, dst, a.head_dim, a.n_rot, p, a.cos, a.sin);
+    return;
+  }
+  lane_step_block<T>(a, a.lane[role - 1], b, p, red);
+}
+
+// Decode step on clusters of kSplit CTAs, for compressed layers whose
+// attention rows are 512 or 1024 wide: every (sequence, role) is one cluster.
+// The raw row and the attention lane are split by channel: CTA c owns channels
+// [c w / kSplit, (c + 1) w / kSplit) (64 of a 512-wide row: one FP8 block).
+// The attention lane stores the token's candidate and score and, at a window
+// boundary, pools its channels over the W slots (spread over the CTA's eight
+// warps, W / 8 slots per thread with every load in flight at once; then the
+// per-channel maxima, then the weighted sums combined in warp order), adds the
+// squares of its pooled channels, and takes the row's RMS from the cluster's
+// partial sums (read in rank order from each CTA's shared memory, so every
+// CTA gets the same value) before it normalises, rotates, rounds and stores
+// its channels; ratio 4 then moves its channels of slots 4..7 to 0..3. One CTA
+// per sequence would read the whole window state alone (512 KiB on ratio 128).
+// The indexer lane (ratio 4, a 128-wide row with its norm and the optional
+// FP4 round trip over the whole row) runs in the cluster's first CTA.
+constexpr uint32_t kSplit = 8;
+constexpr uint32_t kSlotGroups = kThreads / 32;   // 8 warps x 32 channel pairs
+
+template <typename T, uint32_t W>
+__global__ void __launch_bounds__(kThreads) append_step_split_kernel(AppendArgs a) {
+  constexpr uint32_t SPT = W / kSlotGroups;   // slots per thread
+  __shared__ float sm_max[kSlotGroups][64], sm_den[kSlotGroups][64], sm_num[kSlotGroups][64];
+  __shared__ float part;
+  __shared__ float red[32];
+  pdl_wait();
+  pdl_trigger();
+  const uint32_t rank = blockIdx.x % kSplit, cl = blockIdx.x / kSplit;
+  const uint32_t b = cl % a.batch, role = cl / a.batch + a.y0;
+  const uint32_t p = seq_base(a.seq_pos, a.pos0, b);
+  const uint32_t t = threadIdx.x, pr = t & 31, g = t >> 5;
+  if (role == 0) {   // the raw row: this CTA's channels
+    const uint32_t D = a.head_dim, n_nope = D - a.n_rot, c = rank * (D / kSplit) + 2 * t;
+    if (2 * t < D / kSplit) {
+      const T *src = static_cast<const T *>(a.raw_in) + (size_t)b * D;
+      T *dst = static_cast<T *>(a.raw_dst) + ((size_t)b * a.cap_raw + p % a.cap_raw) * D;
+      float x0 = ld_f32(src, c), x1 = ld_f32(src, c + 1);
+      if (c >= n_nope) {
+        const uint32_t fi = (c - n_nope) / 2;
+        const float co = a.cos[(size_t)p * (a.n_rot / 2) + fi];
+        const float si = a.sin[(size_t)p * (a.n_rot / 2) + fi];
+        const float r0 = x0 * co - x1 * si, r1 = x0 * si + x1 * co;
+        x0 = r0;
+        x1 = r1;
+      }
+      st_elem(dst, c, x0);
+      st_elem(dst, c + 1, x1);
+    }
+    return;
+  }
+  const LaneArgs &L = a.lane[role - 1];
+  if (L.norm) {   // the indexer lane: whole rows in the first CTA
+    if (rank == 0) lane_step_block<T>(a, L, b, p, red);
+    return;
+  }
+  const uint32_t r = a.ratio, width = L.width, cpc = width / kSplit;   // channels per CTA
+  const uint32_t slot = r == 4 ? 4 + p % 4 : p % r;
+  float *skv = L.state_kv + (size_t)b * W * width;
+  float *ssc = L.state_score + (size_t)b * W * width;
+  const T *cand = static_cast<const T *>(L.cand) + (size_t)b * width;
+  const T *score = static_cast<const T *>(L.score) + (size_t)b * width;
+  const uint32_t cbase = rank * cpc;
+  for (uint32_t c = cbase + t; c < cbase + cpc; c += kThreads) {
+    skv[(size_t)slot * width + c] = ld_f32(cand, c);
+    ssc[(size_t)slot * width + c] = ld_f32(score, c);
+  }
+  if ((p + 1) % r != 0) return;   // uniform over the cluster
+  const uint32_t i = (p + 1) / r - 1;
+  const T *ape = static_cast<const T *>(L.ape);
+  const T *gamma = static_cast<const T *>(L.gamma);
+  __syncthreads();   // the token's slot is written
+  // channels cbase + 64 q + 2 pr, + 1 (q < cpc / 64); slots g, g + 8, ...
+  const uint32_t nq = cpc / 64;
+  float y[2][2];
+  for (uint32_t q = 0; q < nq; ++q) {
+    const uint32_t c = cbase + 64 * q + 2 * pr;
+    float2 kv[SPT], sg[SPT];
+#pragma unroll
+    for (uint32_t j = 0; j < SPT; ++j) {
+      const uint32_t sl = g + kSlotGroups * j;
+      kv[j] = *reinterpret_cast<const float2 *>(skv + (size_t)sl * width + c);
+      const float2 sc = *reinterpret_cast<const float2 *>(ssc + (size_t)sl * width + c);
+      sg[j] = make_float2(sc.x + ld_f32(ape, (size_t)sl * width + c),
+                          sc.y + ld_f32(ape, (size_t)sl * width + c + 1));
+    }
+    float m0 = -INFINITY, m1 = -INFINITY;
+#pragma unroll
+    for (uint32_t j = 0; j < SPT; ++j) {
+      m0 = fmaxf(m0, sg[j].x);
+      m1 = fmaxf(m1, sg[j].y);
+    }
+    sm_max[g][2 * pr] = m0;
+    sm_max[g][2 * pr + 1] = m1;
+    __syncthreads();
+    float M0 = -INFINITY, M1 = -INFINITY;
+#pragma unroll
+    for (uint32_t gg = 0; gg < kSlotGroups; ++gg) {
+      M0 = fmaxf(M0, sm_max[gg][2 * pr]);
+      M1 = fmaxf(M1, sm_max[gg][2 * pr + 1]);
+    }
+    float d0 = 0.f, n0 = 0.f, d1 = 0.f, n1 = 0.f;
+    if (M0 != -INFINITY) {
+#pragma unroll
+      for (uint32_t j = 0; j < SPT; ++j) {
+        const float w = expf(sg[j].x - M0);
+        if (w > 0.f) {
+          d0 += w;
+          n0 += w * kv[j].x;
+        }
+      }
+    }
+    if (M1 != -INFINITY) {
+#pragma unroll
+      for (uint32_t j = 0; j < SPT; ++j) {
+        const float w = expf(sg[j].y - M1);
+        if (w > 0.f) {
+          d1 += w;
+          n1 += w * kv[j].y;
+        }
+      }
+    }
+    sm_den[g][2 * pr] = d0;
+    sm_den[g][2 * pr + 1] = d1;
+    sm_num[g][2 * pr] = n0;
+    sm_num[g][2 * pr + 1] = n1;
+    __syncthreads();
+    if (g == 0) {
+      float D0 = 0.f, N0 = 0.f, D1 = 0.f, N1 = 0.f;
+#pragma unroll
+      for (uint32_t gg = 0; gg < kSlotGroups; ++gg) {
+        D0 += sm_den[gg][2 * pr];
+        N0 += sm_num[gg][2 * pr];
+        D1 += sm_den[gg][2 * pr + 1];
+        N1 += sm_num[gg][2 * pr + 1];
+      }
+      y[q][0] = D0 > 0.f ? N0 / D0 : 0.f;
+      y[q][1] = D1 > 0.f ? N1 / D1 : 0.f;
+    }
+    __syncthreads();   // the shared partials are reused by the next 64 channels
+  }
+  if (r == 4) {   // every read of slots 0..3 is done: the frontier moves
+    for (uint32_t c = cbase + t; c < cbase + cpc; c += kThreads) {
+#pragma unroll
+      for (int sl = 0; sl < 4; ++sl) {
+        skv[(size_t)sl * width + c] = skv[(size_t)(4 + sl) * width + c];
+        ssc[(size_t)sl * width + c] = ssc[(size_t)(4 + sl) * width + c];
+      }
+    }
+  }
+  // RMS over the whole row: this CTA's squares, then every rank's in order
+  if (g == 0) {
+    float ss = 0.f;
+    for (uint32_t q = 0; q < nq; ++q) ss += y[q][0] * y[q][0] + y[q][1] * y[q][1];
+    ss = warp_sum(ss);
+    if (pr == 0) part = ss;
+  }
+  cluster_sync_all();
+  float tot = 0.f;
+  if (g == 0) {
+    const uint32_t addr = smem_u32(&part);
+    for (uint32_t rr = 0; rr < kSplit; ++rr) tot += ld_cluster_f32(mapa_shared(addr, rr));
+  }
+  cluster_sync_all();   // every rank's partial has been read
+  if (g != 0) return;
+  const float inv = 1.0f / sqrtf(tot / (float)width + kRmsEps);
+  const uint32_t n_nope = width - L.n_rot;
+  size_t prow;
+  const bool mapped = L.map.phys(b, i, prow);
+  T *row = static_cast<T *>(L.comp) + prow * width;
+  for (uint32_t q = 0; q < nq; ++q) {
+    const uint32_t c = cbase + 64 * q + 2 * pr;
+    float v0 = ld_f32(gamma, c) * (y[q][0] * inv);
+    float v1 = ld_f32(gamma, c + 1) * (y[q][1] * inv);
+    if (c >= n_nope) {
+      const uint32_t fi = (c - n_nope) / 2;
+      const float co = L.cos[(size_t)(i * r) * (L.n_rot / 2) + fi];
+      const float si = L.sin[(size_t)(i * r) * (L.n_rot / 2) + fi];
+      const float r0 = v0 * co - v1 * si, r1 = v0 * si + v1 * co;
+      v0 = r0;
+      v1 = r1;
+    }
+    if (L.quant == 1) {   // FP8 on the non-RoPE dims: this warp's 64 channels are one block
+      const bool in = c < n_nope;
+      const float am = warp_max(in ? fmaxf(fabsf(v0), fabsf(v1)) : 0.f);
+      const int ke = block_scale_exp(am, kE4M3);
+      if (in) {
+        v0 = quant_dequant(v0, ke, kE4M3);
+        v1 = quant_dequant(v1, ke, kE4M3);
+      }
+    }
+    if (mapped) {
+      st_elem(row, c, v0);
+      st_elem(row, c + 1, v1);
     }
   }
 }
@@ -387,6 +592,32 @@ __global__ void state_reset_kernel(float *kv, float *score, size_t n) {
 
 template <typename T>
 cudaError_t launch_append_t(const AppendArgs &a, cudaStream_t s) {
+  // compressed-layer decode with 512- or 1024-wide rows: one cluster per
+  // (sequence, role)
+  if (a.T == 1 && a.direct && a.ratio != 0 && a.head_dim % (64 * kSplit) == 0 &&
+      a.head_dim <= 128 * kSplit) {
+    const uint32_t roles = (a.y0 ? 0u : 1u) + (uint32_t)a.n_lanes;
+    if (!roles) return cudaSuccess;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute at[2];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = kSplit;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    at[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.gridDim = dim3(roles * a.batch * kSplit);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    cfg.attrs = at;
+    cfg.numAttrs = 2;
+    cudaError_t e = a.ratio == 4 ? cudaLaunchKernelEx(&cfg, append_step_split_kernel<T, 8>, a)
+                                 : cudaLaunchKernelEx(&cfg, append_step_split_kernel<T, 128>, a);
+    if (e != cudaSuccess) return e;
+    note_launches(1);
+    return cudaGetLastError();
+  }
   if (a.T == 1 && a.direct) {
     const uint32_t roles = (a.y0 ? 0u : 1u) + (uint32_t)a.n_lanes;
     if (!roles) return cudaSuccess;

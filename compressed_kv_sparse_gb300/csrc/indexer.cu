@@ -24,6 +24,7 @@
 #include <cmath>
 
 #include "quant.cuh"
+#include "select.cuh"
 
 namespace ds4a {
 namespace {
@@ -54,13 +55,12 @@ __host__ __device__ inline IndexWs index_ws_split(void *ws, uint32_t nq, uint32_
 // ticket, overflow) and candidates [nq][3][kCandGlobal] (row, S~, error bound).
 // The row norms of the error bound live in the cache (written when rows are
 // appended).
-constexpr uint32_t kHistBins = 4096;
-constexpr uint32_t kCandGlobal = 4096;
 struct TcWs {
   int *err;
-  float *scores;
+  float *scores;        // [nq][sstride]
   __nv_bfloat16 *qbf;
   uint32_t *hist, *ctrl, *cand;
+  uint32_t sstride;     // floats per query row of scores: comp_cap rounded up to 32
 };
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 inline TcWs tc_ws_split(void *ws, uint32_t nq, uint32_t B, uint32_t Hi, uint32_t Di,
@@ -72,8 +72,9 @@ inline TcWs tc_ws_split(void *ws, uint32_t nq, uint32_t B, uint32_t Hi, uint32_t
   off = align_up(off + 16, 1024);
   w.qbf = reinterpret_cast<__nv_bfloat16 *>(base + off);
   off = align_up(off + (size_t)nq * Hi * Di * 2, 256);
+  w.sstride = (comp_cap + 31u) & ~31u;   // 128-byte aligned rows (bulk copies)
   w.scores = reinterpret_cast<float *>(base + off);
-  off = align_up(off + (size_t)nq * comp_cap * 4, 256);
+  off = align_up(off + (size_t)nq * w.sstride * 4, 256);
   w.hist = reinterpret_cast<uint32_t *>(base + off);
   off = align_up(off + (size_t)nq * kHistBins * 4, 256);
   w.ctrl = reinterpret_cast<uint32_t *>(base + off);
@@ -283,131 +284,6 @@ __global__ void __launch_bounds__(kRowsPerBlock)
   scores[(size_t)qi * a.comp_cap + row0 + s] = tot;
 }
 
-// Order-preserving unsigned key of an fp32 score (+0 and -0 share a key).
-__device__ __forceinline__ uint32_t warp_sum_u32(uint32_t v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  return v;
-}
-
-__device__ __forceinline__ uint32_t score_key(float f) {
-  if (f == 0.f) f = 0.f;
-  const uint32_t u = __float_as_uint(f);
-  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-}
-
-// Block-wide exclusive prefix of a 0/1 flag; returns the prefix, adds the
-// block total to *total. Uses warp ballots; `wsum` holds 32 ints.
-__device__ __forceinline__ uint32_t block_flag_scan(bool flag, uint32_t *wsum,
-                                                    uint32_t *total) {
-  const uint32_t lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-  const uint32_t bal = __ballot_sync(0xffffffffu, flag);
-  const uint32_t in_warp = __popc(bal & ((1u << lane) - 1u));
-  if (lane == 0) wsum[wid] = __popc(bal);
-  __syncthreads();
-  if (wid == 0) {
-    const uint32_t nw = blockDim.x >> 5;
-    uint32_t v = lane < nw ? wsum[lane] : 0u;
-    uint32_t incl = v;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const uint32_t n = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= (uint32_t)o) incl += n;
-    }
-    if (lane < nw) wsum[lane] = incl - v;
-    if (lane == 31) wsum[32] = incl;
-  }
-  __syncthreads();
-  const uint32_t r = wsum[wid] + in_warp;
-  const uint32_t tot = wsum[32];
-  __syncthreads();
-  *total = tot;
-  return r;
-}
-
-// k-th largest of key(s), s < n, by an 8-bit radix select. Returns the key
-// and, in *need, how many rows with exactly that key belong to the top k.
-template <typename KeyF>
-__device__ uint32_t radix_kth(KeyF key, uint32_t n, uint32_t k, uint32_t *hist, uint32_t *sel,
-                              uint32_t *need_out) {
-  uint32_t prefix = 0, mask = 0, need = k;
-  for (int shift = 24; shift >= 0; shift -= 8) {
-    for (uint32_t i = threadIdx.x; i < 256; i += blockDim.x) hist[i] = 0;
-    __syncthreads();
-    // warp-aggregated: lanes with the same digit add once (keys of similar
-    // magnitude share their top digits, so per-lane atomics would serialise)
-    for (uint32_t base = 0; base < n; base += blockDim.x) {
-      const uint32_t s = base + threadIdx.x;
-      uint32_t bin = 256u;
-      if (s < n) {
-        const uint32_t kk = key(s);
-        if ((kk & mask) == prefix) bin = (kk >> shift) & 255u;
-      }
-      const uint32_t peers = __match_any_sync(0xffffffffu, bin);
-      if (bin < 256u && (threadIdx.x & 31) == (uint32_t)(__ffs(peers) - 1))
-        atomicAdd(&hist[bin], (uint32_t)__popc(peers));
-    }
-    __syncthreads();
-    if (threadIdx.x < 32) {
-      // digit holding the need-th largest key: lane l covers digits
-      // 255 - 8l .. 248 - 8l; a scan over lanes runs from the top digit down
-      const uint32_t lane = threadIdx.x;
-      uint32_t c[8], tot = 0;
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        c[j] = hist[255 - 8 * lane - j];
-        tot += c[j];
-      }
-      uint32_t incl = tot;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const uint32_t v = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= (uint32_t)o) incl += v;
-      }
-      uint32_t cum = incl - tot;
-      if (cum < need && incl >= need) {
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          if (cum + c[j] >= need) {
-            sel[0] = 255 - 8 * lane - j;
-            sel[1] = cum;
-            break;
-          }
-          cum += c[j];
-        }
-      }
-    }
-    __syncthreads();
-    prefix |= sel[0] << shift;
-    mask |= 255u << shift;
-    need -= sel[1];
-    __syncthreads();
-  }
-  *need_out = need;
-  return prefix;
-}
-
-// Write, in ascending order of s, every s with key > kth and the first
-// `need` with key == kth (ties to the lower index); out[pos] = map(s).
-template <typename KeyF, typename MapF>
-__device__ void ordered_emit(KeyF key, uint32_t n, uint32_t kth, uint32_t need, uint32_t k,
-                             int32_t *out, uint32_t *wsum, MapF map) {
-  uint32_t eq_seen = 0, out_pos = 0;
-  for (uint32_t base = 0; base < n; base += blockDim.x) {
-    const uint32_t s = base + threadIdx.x;
-    const uint32_t kk = s < n ? key(s) : 0u;
-    const bool gt = s < n && kk > kth;
-    const bool eq = s < n && kk == kth;
-    uint32_t eq_tot, sel_tot;
-    const uint32_t eq_rank = eq_seen + block_flag_scan(eq, wsum, &eq_tot);
-    const bool take = gt || (eq && eq_rank < need);
-    const uint32_t pos = out_pos + block_flag_scan(take, wsum, &sel_tot);
-    if (take && pos < k) out[pos] = (int32_t)map(s);
-    eq_seen += eq_tot;
-    out_pos += sel_tot;
-  }
-}
-
 __global__ void __launch_bounds__(kSelectThreads)
     topk_select_kernel(IndexArgs a, const float *scores) {
   __shared__ uint32_t hist[256];
@@ -425,45 +301,6 @@ __global__ void __launch_bounds__(kSelectThreads)
   uint32_t need;
   const uint32_t kth = radix_kth(key, vis, k, hist, sel, &need);
   ordered_emit(key, vis, kth, need, k, out, wsum, [](uint32_t x) { return x; });
-}
-
-__device__ __forceinline__ float key_to_float(uint32_t k) {
-  return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
-}
-
-constexpr float kRel = 2.4e-7f;        // slack for the rounding of the bound arithmetic
-constexpr uint32_t kQB = 132;          // row stride (bf16) of q' in shared memory: the 8-byte
-                                        // loads of 16 lanes at 16 rows hit 32 distinct banks
-
-// Block-wide exclusive prefix sum of v (every thread gets its prefix and the
-// total). `wsum` holds 33 words.
-__device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t *wsum, uint32_t *total) {
-  const uint32_t lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-  uint32_t incl = v;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const uint32_t n = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= (uint32_t)o) incl += n;
-  }
-  if (lane == 31) wsum[wid] = incl;
-  __syncthreads();
-  if (wid == 0) {
-    const uint32_t nw = blockDim.x >> 5;
-    const uint32_t x = lane < nw ? wsum[lane] : 0u;
-    uint32_t in2 = x;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const uint32_t n = __shfl_up_sync(0xffffffffu, in2, o);
-      if (lane >= (uint32_t)o) in2 += n;
-    }
-    if (lane < nw) wsum[lane] = in2 - x;
-    if (lane == 31) wsum[32] = in2;
-  }
-  __syncthreads();
-  const uint32_t r = wsum[wid] + incl - v;
-  *total = wsum[32];
-  __syncthreads();
-  return r;
 }
 
 // Select kernel configurations: 1024 threads when several blocks share a
@@ -491,221 +328,6 @@ struct SelCfg {
 inline uint32_t select_groups(uint32_t nq) {
   uint32_t g = (uint32_t)num_sms() / (nq ? nq : 1);
   return g < 1 ? 1 : (g > 16 ? 16 : g);
-}
-
-// Unbiased exponent of a nonzero fp32 value; subnormals report -140 (below
-// any of their magnitudes), inf / NaN 128.
-__device__ __forceinline__ int exp_of(float x) {
-  const int f = (int)((__float_as_uint(x) >> 23) & 0xFFu);
-  return f == 0 ? -140 : f - 127;
-}
-__device__ __forceinline__ int warp_min_i(int v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v = min(v, __shfl_xor_sync(0xffffffffu, v, o));
-  return v;
-}
-__device__ __forceinline__ int warp_max_i(int v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v = max(v, __shfl_xor_sync(0xffffffffu, v, o));
-  return v;
-}
-
-// The exact recipe adds fl(q * k) to the running dot product in ascending d.
-// For two bf16 factors the product has at most 16 significant bits, so
-// fl(q * k) = q * k unless it is subnormal or overflows, and then
-// fma(q, k, acc) rounds exactly like acc + fl(q * k). The exponent ranges of
-// q' (eq_min, eq_max, over nonzero entries) and of the key rows decide which
-// form is used.
-__device__ __forceinline__ bool fma_exact(int eq_min, int eq_max, int ek_min, int ek_max) {
-  return eq_min + ek_min >= -126 && eq_max + ek_max <= 125;
-}
-
-// Exponent range of the nonzero entries among four key values, over the warp.
-__device__ __forceinline__ void key_exp_range(const float (&kk)[4], int &emin, int &emax) {
-  emin = 1000;
-  emax = -1000;
-#pragma unroll
-  for (int e = 0; e < 4; ++e) {
-    if (kk[e] != 0.f) {
-      emin = min(emin, exp_of(kk[e]));
-      emax = max(emax, exp_of(kk[e]));
-    }
-  }
-  emin = warp_min_i(emin);
-  emax = warp_max_i(emax);
-}
-
-__device__ __forceinline__ void bf16x4(uint2 v, float &a, float &b, float &c, float &d) {
-  a = __uint_as_float(v.x << 16);
-  b = __uint_as_float(v.x & 0xFFFF0000u);
-  c = __uint_as_float(v.y << 16);
-  d = __uint_as_float(v.y & 0xFFFF0000u);
-}
-
-// Exact recipe for key row `kr` against the 64 x 128 query in shared memory
-// (one warp, two heads per lane); lane 0 returns the score.
-__device__ __forceinline__ float rescore_row(const __nv_bfloat16 *qsm, const float *wsh, float *kb,
-                                             float *rel, const __nv_bfloat16 *kr, uint32_t lane,
-                                             int eq_min, int eq_max) {
-  __syncwarp();
-  int emin, emax;
-  {
-    float kk[4];
-    bf16x4(*reinterpret_cast<const uint2 *>(kr + 4 * lane), kk[0], kk[1], kk[2], kk[3]);
-    *reinterpret_cast<float4 *>(kb + 4 * lane) = make_float4(kk[0], kk[1], kk[2], kk[3]);
-    key_exp_range(kk, emin, emax);
-  }
-  const bool exact = fma_exact(eq_min, eq_max, emin, emax);
-  __syncwarp();
-  const float4 *k4 = reinterpret_cast<const float4 *>(kb);
-#pragma unroll
-  for (uint32_t j = 0; j < 2; ++j) {
-    const uint32_t h = lane + 32 * j;
-    const uint2 *q2 = reinterpret_cast<const uint2 *>(qsm + (size_t)h * kQB);
-    float acc = 0.f;
-#pragma unroll 4
-    for (uint32_t c = 0; c < 32; ++c) {
-      float q0, q1, q2v, q3;
-      bf16x4(q2[c], q0, q1, q2v, q3);
-      const float4 k = k4[c];
-      if (exact) {
-        acc = fmaf(q0, k.x, acc);
-        acc = fmaf(q1, k.y, acc);
-        acc = fmaf(q2v, k.z, acc);
-        acc = fmaf(q3, k.w, acc);
-      } else {
-        acc = __fadd_rn(acc, __fmul_rn(q0, k.x));
-        acc = __fadd_rn(acc, __fmul_rn(q1, k.y));
-        acc = __fadd_rn(acc, __fmul_rn(q2v, k.z));
-        acc = __fadd_rn(acc, __fmul_rn(q3, k.w));
-      }
-    }
-    rel[h] = acc > 0.f ? acc : 0.f;
-  }
-  __syncwarp();
-  float tot = 0.f;
-  if (lane == 0) {
-#pragma unroll 16
-    for (uint32_t h = 0; h < 64; ++h) tot = __fadd_rn(tot, __fmul_rn(wsh[h], rel[h]));
-  }
-  return tot;
-}
-
-// Per-head ReLU dots of RPP band rows (fp32 keys at k4, RPP x 128) against
-// head h of q': one q' load serves RPP rows. `exact`: every product is exact,
-// so the fused form rounds like the separate one.
-template <int RPP>
-__device__ __forceinline__ void band_dots(const uint2 *q2, const float4 *k4, bool exact,
-                                          float (&acc)[RPP]) {
-#pragma unroll
-  for (int rr = 0; rr < RPP; ++rr) acc[rr] = 0.f;
-  if (exact) {
-#pragma unroll 4
-    for (uint32_t c = 0; c < 32; ++c) {
-      float q0, q1, q2v, q3;
-      bf16x4(q2[c], q0, q1, q2v, q3);
-#pragma unroll
-      for (int rr = 0; rr < RPP; ++rr) {
-        const float4 k = k4[rr * 32 + c];
-        acc[rr] = fmaf(q0, k.x, acc[rr]);
-        acc[rr] = fmaf(q1, k.y, acc[rr]);
-        acc[rr] = fmaf(q2v, k.z, acc[rr]);
-        acc[rr] = fmaf(q3, k.w, acc[rr]);
-      }
-    }
-  } else {
-#pragma unroll 2
-    for (uint32_t c = 0; c < 32; ++c) {
-      float q0, q1, q2v, q3;
-      bf16x4(q2[c], q0, q1, q2v, q3);
-#pragma unroll
-      for (int rr = 0; rr < RPP; ++rr) {
-        const float4 k = k4[rr * 32 + c];
-        acc[rr] = __fadd_rn(acc[rr], __fmul_rn(q0, k.x));
-        acc[rr] = __fadd_rn(acc[rr], __fmul_rn(q1, k.y));
-        acc[rr] = __fadd_rn(acc[rr], __fmul_rn(q2v, k.z));
-        acc[rr] = __fadd_rn(acc[rr], __fmul_rn(q3, k.w));
-      }
-    }
-  }
-}
-
-// Exact recipe for the band rows (whole block, NW warps): rounds of 2 NW rows;
-// their keys go to `kbuf` as fp32. The NW / 2 warp pairs split a round's rows
-// evenly, RPP = ceil(rows / (NW / 2)) <= 4 consecutive rows per pair; warp
-// 2g + t of pair g takes heads 32 t + lane, so one q' load serves RPP rows
-// and one key load all 32 heads of a warp. Per-head ReLU dots land in `relb`
-// [2 NW rows][64 heads]; one thread per row sums them in ascending h.
-// Results replace cS[band[i]].
-template <int NW>
-__device__ __forceinline__ void rescore_band(const __nv_bfloat16 *qsm, const float *wsh,
-                                             float *kbuf, float *relb, const uint32_t *band,
-                                             uint32_t nband, const uint32_t *cidx, float *cS,
-                                             const __nv_bfloat16 *keys, const RowMap &map,
-                                             uint32_t b, uint32_t *rexact,
-                                             int eq_min, int eq_max) {
-  const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  constexpr uint32_t RPR = 2 * NW, NP = NW / 2;
-  for (uint32_t base = 0; base < nband; base += RPR) {
-    const uint32_t nr = min(RPR, nband - base);
-#pragma unroll
-    for (uint32_t t = 0; t < 2; ++t) {
-      const uint32_t rr = 2 * warp + t;
-      if (rr < nr) {   // warp-uniform
-        float kk[4];
-        bf16x4(*reinterpret_cast<const uint2 *>(keys + map.row_of(b, cidx[band[base + rr]]) * 128 +
-                                                4 * lane),
-               kk[0], kk[1], kk[2], kk[3]);
-        *reinterpret_cast<float4 *>(kbuf + rr * 128 + 4 * lane) =
-            make_float4(kk[0], kk[1], kk[2], kk[3]);
-        int emin, emax;
-        key_exp_range(kk, emin, emax);
-        if (lane == 0) rexact[rr] = fma_exact(eq_min, eq_max, emin, emax) ? 1u : 0u;
-      }
-    }
-    __syncthreads();
-    const uint32_t rpp = (nr + NP - 1) / NP;   // 1 .. 4
-    const uint32_t g0 = (warp >> 1) * rpp, h = 32 * (warp & 1) + lane;
-    if (g0 < nr) {   // warp-uniform
-      const uint32_t cnt = min(rpp, nr - g0);
-      bool exact = true;
-      for (uint32_t rr = 0; rr < cnt; ++rr) exact = exact && rexact[g0 + rr] != 0u;
-      const uint2 *q2 = reinterpret_cast<const uint2 *>(qsm + (size_t)h * kQB);
-      const float4 *k4 = reinterpret_cast<const float4 *>(kbuf + g0 * 128);
-      // (rows past cnt read keys of the next pair or stale data: never stored)
-      float acc[4];
-      if (rpp == 1) {
-        float a1[1];
-        band_dots<1>(q2, k4, exact, a1);
-        acc[0] = a1[0];
-      } else if (rpp == 2) {
-        float a2[2];
-        band_dots<2>(q2, k4, exact, a2);
-        acc[0] = a2[0];
-        acc[1] = a2[1];
-      } else if (rpp == 3) {
-        float a3[3];
-        band_dots<3>(q2, k4, exact, a3);
-        acc[0] = a3[0];
-        acc[1] = a3[1];
-        acc[2] = a3[2];
-      } else {
-        band_dots<4>(q2, k4, exact, acc);
-      }
-#pragma unroll
-      for (uint32_t rr = 0; rr < 4; ++rr)
-        if (rr < cnt) relb[(g0 + rr) * 64 + h] = acc[rr] > 0.f ? acc[rr] : 0.f;
-    }
-    __syncthreads();
-    if (threadIdx.x < nr) {
-      const float *rl = relb + threadIdx.x * 64;
-      float tot = 0.f;
-#pragma unroll 16
-      for (uint32_t hh = 0; hh < 64; ++hh) tot = __fadd_rn(tot, __fmul_rn(wsh[hh], rl[hh]));
-      cS[band[base + threadIdx.x]] = tot;
-    }
-    __syncthreads();
-  }
 }
 
 // Certified selection for bf16 layers (64 heads x 128 dims).
@@ -763,7 +385,7 @@ __global__ void __launch_bounds__(NT, NT == 256 ? 4 : 1)
       for (uint32_t j = threadIdx.x; j < k; j += blockDim.x) out[j] = j < vis ? (int32_t)j : -1;
     return;
   }
-  float *sc = w.scores + (size_t)qi * a.comp_cap;
+  float *sc = w.scores + (size_t)qi * w.sstride;
   const float *nr = a.norms;   // row r of this sequence: nr[a.map.row_of(b, r)]
   const float *nr_c = a.map.table ? nullptr : a.norms + (size_t)b * a.comp_cap;   // contiguous
   const __nv_bfloat16 *qb = w.qbf + (size_t)qi * Hi * Di;
@@ -1247,6 +869,7 @@ cudaError_t launch_index_tc(const IndexArgs &a, cudaStream_t s) {
     t.qbf = w.qbf;
     t.w = a.w;
     t.scores = w.scores;
+    t.score_stride = w.sstride;
     t.hist = scorer_hist ? w.hist : nullptr;
     t.err = w.err;
     t.map = a.map;

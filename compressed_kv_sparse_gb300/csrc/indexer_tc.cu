@@ -58,7 +58,8 @@ struct ScoreParams {
   RowMap map;               // paged keys (map.table != NULL): 64-row blocks of the pool
   const uint32_t *seq_pos;  // [B] per-sequence positions (ragged decode) or NULL
   const __nv_bfloat16 *w;   // [B][T][Hi]
-  float *scores;            // [B][T][comp_cap]
+  float *scores;            // [B][T][score_stride]
+  uint32_t score_stride;
   uint32_t *hist;           // [B*T][4096] counts of the top 12 bits of the score keys
   int *err;
 };
@@ -349,7 +350,7 @@ __global__ void __launch_bounds__(Cfg<QG>::kThreads, 1)
                         ((acc8[4] + acc8[5]) + (acc8[6] + acc8[7]));
         const uint32_t t = g * QG + q;
         const bool valid = t < P.T && grow < vis_of(P, b, t);
-        if (valid) P.scores[((size_t)b * P.T + t) * P.comp_cap + grow] = s;
+        if (valid) P.scores[((size_t)b * P.T + t) * P.score_stride + grow] = s;
         // histogram of the keys' top 12 bits (lanes in one bin add once), per
         // CTA in shared memory, added to the query's when the query changes
         if (QG == 1) {   // (the selection samples its threshold otherwise)
@@ -404,6 +405,7 @@ cudaError_t launch_qg(const IndexTcArgs &a, cudaStream_t s) {
   P.total_items = a.batch * P.n_groups * P.tiles_per;
   P.w = static_cast<const __nv_bfloat16 *>(a.w);
   P.scores = a.scores;
+  P.score_stride = a.score_stride;
   P.hist = a.hist;
   P.err = a.err;
   P.map = a.map;

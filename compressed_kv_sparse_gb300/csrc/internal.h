@@ -137,7 +137,8 @@ struct IndexTcArgs {
   const void *keys;   // [B][comp_cap][128] bf16
   const void *qbf;    // [B][T][64][128] bf16, rotated queries
   const void *w;      // [B][T][64] bf16
-  float *scores;      // [B][T][comp_cap]
+  float *scores;      // [B][T][score_stride]
+  uint32_t score_stride;
   uint32_t *hist;     // [B*T][4096], zeroed before the call
   int *err;
   RowMap map;         // rows of keys
