@@ -179,7 +179,6 @@ ds4a_status append_parts(ds4a_layer_cache *c, uint32_t pos0, uint32_t T, uint32_
   ds4a_status st = check_cache(c);
   if (st) return st;
   if (T == 0) return DS4A_ERR_SHAPE;
-  if (c->seq_pos && T != 1) return DS4A_ERR_ARG;   // ragged batches decode one token
   if (!lanes || (lanes & ~(DS4A_LANE_RAW | DS4A_LANE_ATTN | DS4A_LANE_INDEX))) return DS4A_ERR_ARG;
   const bool raw = lanes & DS4A_LANE_RAW;
   const bool la = lanes & DS4A_LANE_ATTN, li = lanes & DS4A_LANE_INDEX;
@@ -291,7 +290,6 @@ ds4a_status index_topk_check(const ds4a_layer_cache *c, uint32_t pos0, uint32_t 
   if (T == 0 || n_heads == 0 || n_heads > 128 || top_k == 0 || top_k > 2048) return DS4A_ERR_SHAPE;
   if (!q_idx || !w || !topk) return DS4A_ERR_ARG;
   if ((uint64_t)pos0 + T > c->n_tokens) return DS4A_ERR_POSITION;
-  if (c->seq_pos && T != 1) return DS4A_ERR_ARG;
   const uint32_t Hp = (n_heads + 7u) & ~7u;
   if (((size_t)c->index_dim * Hp + Hp + 128 * (size_t)(c->index_dim + 1)) * 4 > 227 * 1024)
     return DS4A_ERR_SHAPE;
@@ -342,7 +340,6 @@ static ds4a_status attn_common(const ds4a_layer_cache *c, uint32_t pos0, uint32_
                                void *ws, size_t ws_bytes, cudaStream_t s) {
   if (T == 0 || n_heads == 0 || n_heads > 128) return DS4A_ERR_SHAPE;
   if (!q || !out) return DS4A_ERR_ARG;
-  if (c->seq_pos && T != 1) return DS4A_ERR_ARG;
   if (!std::isfinite(scale)) return DS4A_ERR_ARG;
   if (c->ratio == 4 && (!topk || top_k == 0 || top_k > 2048)) return DS4A_ERR_ARG;
   const size_t need = attn_ws_bytes(c->dtype, c->ratio, c->batch, T, n_heads, c->head_dim,
@@ -413,8 +410,8 @@ ds4a_status ds4a_sparse_attn_prefill_chunk(ds4a_layer_cache *c, uint32_t pos0, u
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   st = attn_common(c, pos0, T, q, n_heads, raw_chunk, topk, top_k, scale, out, ws, ws_bytes, s);
   if (st) return st;
-  return cuda_status(launch_ring_commit(c->dtype, c->batch, T, pos0, c->cap_raw, c->head_dim,
-                                        raw_chunk, c->raw_kv, s));
+  return cuda_status(launch_ring_commit(c->dtype, c->batch, T, pos0, c->seq_pos, c->cap_raw,
+                                        c->head_dim, raw_chunk, c->raw_kv, s));
 }
 
 }  // extern "C"

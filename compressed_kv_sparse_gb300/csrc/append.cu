@@ -497,15 +497,19 @@ struct ChunkSlot {
   }
 };
 
+// n_emit: compressed rows per lane the grid has room for (the most any
+// sequence completes in the chunk); sequence b, whose chunk starts at p0 (its
+// own position in a ragged batch), completes (p0 + T) / r - p0 / r of them.
 template <typename T>
 __global__ void __launch_bounds__(kThreads)
     append_rows_kernel(AppendArgs a, uint32_t n_raw, uint32_t n_emit) {
   __shared__ float red[32];
   const uint32_t b = blockIdx.y;
+  const uint32_t p0 = seq_base(a.seq_pos, a.pos0, b);
   uint32_t x = blockIdx.x;
   if (x < n_raw) {
     const uint32_t t = (a.direct ? a.T - n_raw : 0) + x;
-    const uint32_t p = a.pos0 + t;
+    const uint32_t p = p0 + t;
     const T *src = static_cast<const T *>(a.raw_in) + ((size_t)b * a.T + t) * a.head_dim;
     T *dst = static_cast<T *>(a.raw_dst) +
              (a.direct ? ((size_t)b * a.cap_raw + p % a.cap_raw) * a.head_dim
@@ -516,8 +520,9 @@ __global__ void __launch_bounds__(kThreads)
   x -= n_raw;
   const uint32_t l = x / n_emit, e = x % n_emit;
   const LaneArgs &L = a.lane[l];
-  const uint32_t r = a.ratio, i = a.pos0 / r + e;
-  ChunkSlot<T> get{&L, r, a.window, b, i, a.pos0, a.T};
+  const uint32_t r = a.ratio, i = p0 / r + e;
+  if (e >= (p0 + a.T) / r - p0 / r) return;   // (ragged: fewer rows in this sequence)
+  ChunkSlot<T> get{&L, r, a.window, b, i, p0, a.T};
   pool_norm_rope_store<T>(L, a.window, b, i, i * r, get, red);
 }
 
@@ -527,7 +532,7 @@ __global__ void __launch_bounds__(kThreads) append_state_kernel(AppendArgs a) {
   const uint32_t b = blockIdx.x;
   const LaneArgs &L = a.lane[blockIdx.y];
   const uint32_t r = a.ratio, W = a.window, width = L.width;
-  const uint32_t pos0 = a.pos0, n = a.pos0 + a.T;
+  const uint32_t pos0 = seq_base(a.seq_pos, a.pos0, b), n = pos0 + a.T;
   float *skv = L.state_kv + (size_t)b * W * width;
   float *ssc = L.state_score + (size_t)b * W * width;
   const T *cand = static_cast<const T *>(L.cand) + (size_t)b * a.T * width;
@@ -628,7 +633,11 @@ cudaError_t launch_append_t(const AppendArgs &a, cudaStream_t s) {
     return cudaGetLastError();
   }
   const uint32_t n_raw = a.y0 ? 0u : a.direct ? (a.T < a.cap_raw ? a.T : a.cap_raw) : a.T;
-  const uint32_t n_emit = a.ratio ? (a.pos0 + a.T) / a.ratio - a.pos0 / a.ratio : 0;
+  // rows completed in the chunk; with per-sequence positions, the most any
+  // sequence can complete
+  const uint32_t n_emit = !a.ratio ? 0u
+                          : a.seq_pos ? a.T / a.ratio + 1u
+                                      : (a.pos0 + a.T) / a.ratio - a.pos0 / a.ratio;
   const uint32_t nblk = n_raw + n_emit * a.n_lanes;
   if (nblk) {
     append_rows_kernel<T><<<dim3(nblk, a.batch), kThreads, 0, s>>>(a, n_raw, n_emit ? n_emit : 1);

@@ -140,8 +140,8 @@ __global__ void __launch_bounds__(kThreads)
       if (r < nr) {
         if (g < n_w) {
           const uint32_t pos = p - n_w + 1 + g;
-          if (chunk && pos >= a.pos0)
-            off = (1ll << 62) | (long long)(pos - a.pos0) * D;
+          if (chunk && pos >= p - t)   // (p - t: this sequence's first chunk position)
+            off = (1ll << 62) | (long long)(pos - (p - t)) * D;
           else
             off = (long long)(pos % a.cap_raw) * D;
         } else {
@@ -305,10 +305,11 @@ __global__ void attn_merge_kernel(AttnArgs a, Plan pl, const float *part) {
 
 template <typename T>
 __global__ void ring_commit_kernel(const T *chunk, T *ring, uint32_t T_len, uint32_t pos0,
-                                   uint32_t cap, uint32_t D, uint32_t n) {
+                                   const uint32_t *seq_pos, uint32_t cap, uint32_t D, uint32_t n) {
   const uint32_t t = T_len - n + blockIdx.x, b = blockIdx.y;
+  const uint32_t p = seq_base(seq_pos, pos0, b) + t;
   const T *src = chunk + ((size_t)b * T_len + t) * D;
-  T *dst = ring + ((size_t)b * cap + (pos0 + t) % cap) * D;
+  T *dst = ring + ((size_t)b * cap + p % cap) * D;
   for (uint32_t d = threadIdx.x; d < D; d += blockDim.x) dst[d] = src[d];
 }
 
@@ -368,19 +369,19 @@ cudaError_t launch_attention(const AttnArgs &a, cudaStream_t s) {
 }
 
 cudaError_t launch_ring_commit(int dtype, uint32_t batch, uint32_t T, uint32_t pos0,
-                               uint32_t cap_raw, uint32_t head_dim, const void *chunk, void *ring,
-                               cudaStream_t s) {
+                               const uint32_t *seq_pos, uint32_t cap_raw, uint32_t head_dim,
+                               const void *chunk, void *ring, cudaStream_t s) {
   const uint32_t n = T < cap_raw ? T : cap_raw;
   if (!n) return cudaSuccess;
   note_launches(1);
   if (dtype == DS4A_BF16)
     ring_commit_kernel<__nv_bfloat16><<<dim3(n, batch), 128, 0, s>>>(
         static_cast<const __nv_bfloat16 *>(chunk), static_cast<__nv_bfloat16 *>(ring), T, pos0,
-        cap_raw, head_dim, n);
+        seq_pos, cap_raw, head_dim, n);
   else
     ring_commit_kernel<float><<<dim3(n, batch), 128, 0, s>>>(
-        static_cast<const float *>(chunk), static_cast<float *>(ring), T, pos0, cap_raw,
-        head_dim, n);
+        static_cast<const float *>(chunk), static_cast<float *>(ring), T, pos0, seq_pos,
+        cap_raw, head_dim, n);
   return cudaGetLastError();
 }
 

@@ -99,7 +99,7 @@ __device__ __forceinline__ uint32_t rows_bound(const TcAttnParams &P, uint32_t q
 
 // Query-level geometry shared by every role: tiles t0, t0 + ts, ... < t1.
 struct QueryGeo {
-  uint32_t qi, b, p, n_w, n_list, N, t0, t1, ts;
+  uint32_t qi, b, p0, p, n_w, n_list, N, t0, t1, ts;   // p0: the sequence's first chunk position
   const int32_t *tk;
 };
 
@@ -108,7 +108,8 @@ __device__ __forceinline__ QueryGeo query_geo(const TcAttnParams &P, uint32_t qi
   QueryGeo g;
   g.qi = qi;
   g.b = qi / P.T;
-  g.p = seq_base(P.seq_pos, P.pos0, g.b) + qi % P.T;
+  g.p0 = seq_base(P.seq_pos, P.pos0, g.b);
+  g.p = g.p0 + qi % P.T;
   g.n_w = min(g.p + 1, P.cap_raw);
   g.tk = P.topk ? P.topk + (size_t)qi * P.top_k : nullptr;
   g.n_list = 0;
@@ -150,8 +151,8 @@ __device__ __forceinline__ const __nv_bfloat16 *row_src(const TcAttnParams &P, c
                                                         uint32_t r) {
   if (r < g.n_w) {
     const uint32_t pos = g.p - g.n_w + 1 + r;
-    if (P.chunk && pos >= P.pos0)
-      return P.chunk + ((size_t)g.b * P.T + (pos - P.pos0)) * kD;
+    if (P.chunk && pos >= g.p0)
+      return P.chunk + ((size_t)g.b * P.T + (pos - g.p0)) * kD;
     return P.ring + ((size_t)g.b * P.cap_raw + pos % P.cap_raw) * kD;
   }
   if (r < g.N) {

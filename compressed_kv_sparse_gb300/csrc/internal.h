@@ -109,7 +109,7 @@ struct AppendArgs {
   int n_lanes;             // lanes to append (lane[0 .. n_lanes-1])
   LaneArgs lane[2];
   uint32_t y0;             // 1: the raw rows are not part of this append
-  const uint32_t *seq_pos; // [B] per-sequence positions (ragged decode) or NULL
+  const uint32_t *seq_pos; // [B] per-sequence first positions (ragged batches) or NULL
 };
 cudaError_t launch_append(const AppendArgs &a, cudaStream_t s);
 
@@ -183,8 +183,8 @@ uint32_t attn_decode_cluster(int dtype, uint32_t ratio, uint32_t batch, uint32_t
                              uint32_t head_dim, uint32_t n_rot, uint32_t cap_raw,
                              uint32_t comp_cap, uint32_t top_k);
 cudaError_t launch_ring_commit(int dtype, uint32_t batch, uint32_t T, uint32_t pos0,
-                               uint32_t cap_raw, uint32_t head_dim, const void *chunk,
-                               void *ring, cudaStream_t s);
+                               const uint32_t *seq_pos, uint32_t cap_raw, uint32_t head_dim,
+                               const void *chunk, void *ring, cudaStream_t s);
 cudaError_t launch_state_reset(float *kv, float *score, size_t n, cudaStream_t s);
 cudaError_t launch_index_norms(int dtype, const void *rows, const RowMap &map, uint32_t dim,
                                uint32_t batch, uint32_t n_rows, float *norm, uint32_t *norm_max,

@@ -115,13 +115,18 @@ typedef enum { DS4A_F32 = 0, DS4A_BF16 = 1 } ds4a_dtype;
  *                    written to, and reads of its rows return rows of block 0.
  *  max_blocks, n_blocks  see block_table (ignored when it is NULL).
  *  seq_pos           NULL: every sequence is at the call's position. Non-NULL
- *                    (ragged decode batches): [B] uint32 DEVICE array, the
- *                    position of sequence b's token in this decode step. The
- *                    append, top-k and attention calls of the step (T = 1
- *                    only; T > 1 with seq_pos is DS4A_ERR_ARG) place and read
- *                    sequence b's token at seq_pos[b] instead of pos. The
- *                    host checks use pos and n_tokens: the caller keeps every
- *                    seq_pos[b] <= pos, and updates the array between steps.
+ *                    (ragged batches): [B] uint32 DEVICE array, the position
+ *                    of sequence b's first token in this call: a decode step
+ *                    (T = 1) places and reads sequence b's token at seq_pos[b]
+ *                    instead of pos, and a prefill chunk (T > 1) covers
+ *                    positions seq_pos[b] .. seq_pos[b] + T - 1 of sequence b
+ *                    instead of pos0 .. pos0 + T - 1 (each sequence's raw
+ *                    window, compressor boundaries, visible rows and window
+ *                    commit follow its own positions). The host checks use the
+ *                    call's pos0 and n_tokens: the caller keeps every
+ *                    seq_pos[b] <= pos0 (the capacity and rope-table checks
+ *                    then cover every sequence) and updates the array between
+ *                    calls.
  *
  * State layout: ratio 4 keeps the last complete group of 4 tokens in slots
  * 0..3 and token p of the current group in slot 4 + p % 4 (page §5's 8-row

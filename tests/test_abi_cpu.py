@@ -179,15 +179,16 @@ def test_argument_checks_reject_before_launch(L):
     assert L.ds4a_compress_append(ctypes.byref(bad), 10, 1, *P, None, None) == -2
     bad.max_blocks, bad.n_blocks = 1, 0
     assert L.ds4a_compress_append(ctypes.byref(bad), 10, 1, *P, None, None) == -1
-    # ragged positions are for decode steps: chunks (T > 1) are refused by every call
+    # per-sequence positions (ragged batches) take chunks as well as single
+    # tokens: the calls check the call's pos0 against n_tokens as before
     rg = _fake_cache()
     rg.seq_pos = fake
-    assert L.ds4a_compress_append(ctypes.byref(rg), 10, 2, *P, None, None) == -1
-    assert L.ds4a_index_topk(ctypes.byref(rg), 8, 2, fake, fake, 64, 512, fake, fake, 1 << 30,
-                             None) == -1
-    assert L.ds4a_sparse_attn_prefill_chunk(ctypes.byref(rg), 8, 2, fake, 64, fake, fake, 512,
-                                            0.1, fake, fake, 1 << 30, None) == -1
-    assert L.ds4a_compress_append(ctypes.byref(rg), 9, 1, *P, None, None) == -4   # T = 1 passes on
+    assert L.ds4a_compress_append(ctypes.byref(rg), 9, 2, *P, None, None) == -4
+    assert L.ds4a_index_topk(ctypes.byref(rg), 9, 2, fake, fake, 64, 512, fake, fake, 1 << 30,
+                             None) == -4
+    assert L.ds4a_sparse_attn_prefill_chunk(ctypes.byref(rg), 7, 2, fake, 64, fake, fake, 512,
+                                            0.1, fake, fake, 1 << 30, None) == -4
+    assert L.ds4a_compress_append(ctypes.byref(rg), 9, 1, *P, None, None) == -4
     # step-8 flags: unknown bit, FP4 off ratio 4, FP4 with Di not a power of two,
     # FP8 on a window-only layer
     for ratio, q, dim, want in ((4, 4, 128, -1), (128, 2, 128, -1), (4, 2, 96, -2),

@@ -1,5 +1,7 @@
 """Paged compressed rows (block_table): every call must give bit-identical
-results to the contiguous cache holding the same logical rows.
+results to the contiguous cache holding the same logical rows, and match the
+oracle run on those logical rows (vLLM page, "DeepSeek V4 アテンション
+アーキテクチャ": 256-position logical blocks).
 
 Blocks are 256 token positions, so 64 rows on c4a and 2 on c128a. The tables
 here are random permutations of a pool larger than the batch needs, and
@@ -10,7 +12,8 @@ import pytest
 import torch
 
 import synth
-from helpers import gpu_cache, to_dev
+from helpers import TOL, gpu_cache, np_, oracle_cache, rel_l2, to_dev, to_np
+from oracle import layer as olayer
 from test_gpu_parity import lib_
 
 pytestmark = pytest.mark.gpu
@@ -114,3 +117,24 @@ def test_paged_equals_contiguous(ratio, dtype, B, p0, T, share):
                  "index_state_score", "index_norm_max"):
         if getattr(ref, name) is not None:
             assert torch.equal(getattr(ref, name), getattr(pg, name)), name
+    # the paged results against the oracle on the same logical rows (shared
+    # prefix blocks included)
+    oc = oracle_cache(shape, hist, p0)
+    k = shape.top_k
+    if T == 1:
+        o_ref, tk_ref = olayer.decode_step(oc, p0, to_np(inp), k)
+        got_o = np_(b["out"])
+        got_tk = None if tk_ref is None else b["topk"][:, 0].cpu().numpy()
+    else:
+        o_ref, tk_ref = olayer.prefill_chunk(oc, p0, to_np(inp), k)
+        got_o = np_(b["out"])
+        got_tk = None if tk_ref is None else b["topk"].cpu().numpy()
+    if tk_ref is not None:
+        assert np.array_equal(got_tk, tk_ref)
+    assert rel_l2(got_o, o_ref) <= TOL[dtype]
+    for name in ("attn_comp_kv", "index_comp_kv"):
+        if getattr(pg, name) is not None:
+            assert rel_l2(np_(pg.logical(name))[:, :n], getattr(oc, name)[:, :n]) <= TOL[dtype], name
+    for name in ("attn_state_kv", "attn_state_score", "index_state_kv", "index_state_score"):
+        if getattr(pg, name) is not None:
+            assert np.array_equal(np_(getattr(pg, name)), getattr(oc, name)), name

@@ -118,7 +118,8 @@ def test_append_chunked_equals_one_call_on_gpu_and_oracle():
 def test_append_lanes_on_two_streams_equal_one_call(T):
     """The indexer lane on one stream and the raw rows plus attention lane on
     another (ds4a_compress_append_lanes, then n_tokens set by the caller) leave
-    exactly the cache of one ds4a_compress_append."""
+    exactly the cache of one ds4a_compress_append, and that cache matches the
+    oracle's append (vLLM page, "GPU 計算飽和": multi-stream partitioning)."""
     lib = lib_()
     shape = synth.LayerShape(ratio=4)
     p0 = 1023 if T == 1 else 1021
@@ -146,6 +147,12 @@ def test_append_lanes_on_two_streams_equal_one_call(T):
         assert torch.equal(getattr(ref, name), getattr(got, name)), name
     if T > 1:
         assert torch.equal(chunk_ref, chunk_got)
+    # and the two-stream cache against the oracle directly
+    oc = oracle_cache(shape, hist, p0)
+    rows = olayer.compress_append(oc, p0, to_np(inp), chunk=T > 1)
+    compare_cache(got, oc, "bf16", f"two streams T{T}")
+    if T > 1:
+        assert rel_l2(np_(chunk_got), rows) <= TOL["bf16"]
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
