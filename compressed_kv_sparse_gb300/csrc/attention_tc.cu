@@ -305,8 +305,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  pdl_wait();
-  pdl_trigger();
+  // the loaders wait for the previous launch themselves, after they have
+  // started the first query's Q load
+  const bool loader = warp >= 4 && warp < 8;
+  if (!loader) {
+    pdl_wait();
+    pdl_trigger();
+  }
   // this launch's view of the error word (see ErrWord), read before the wait
   // so that its latency overlaps the previous launch
   const ErrWord ew{P.err, err_base};
@@ -337,18 +342,42 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       return true;
     };
-    for (uint32_t qi = q_first; qi < P.n_q; qi += q_step) {
-      if (rank * kRows >= rows_bound(P, qi)) continue;   // no rows for this rank
-      if (!mbar_wait_warp(&S.q_empty, (qn & 1) ^ 1, ew)) goto done_loader;
-      // Q first (it needs no list): eight TMA boxes of 64 heads x 64 dims, in
-      // the 128-byte swizzled K-major layout the S MMAs read
+    // Q (it needs no list): eight TMA boxes of 64 heads x 64 dims, in the
+    // 128-byte swizzled K-major layout the S MMAs read. The first query's
+    // is issued before the wait for the previous launch: the queries are the
+    // caller's input, written before that launch began (as are the rotation
+    // tables), while the top-k lists and the new raw row are not.
+    auto issue_q = [&](uint32_t qi) {
       if (lt == 0) {
         mbar_arrive_expect_tx(&S.q_tma, 8 * kQBlk);
 #pragma unroll
         for (uint32_t kb = 0; kb < 8; ++kb)
           tma_load_2d(S.q + kb * kQBlk, &tmap_q, &S.q_tma, (int)(64 * kb), (int)(qi * kH));
       }
+    };
+    const bool q_early = q_first < P.n_q && rank * kRows < rows_bound(P, q_first);
+    if (q_early) issue_q(q_first);
+    pdl_wait();
+    pdl_trigger();
+    for (uint32_t qi = q_first; qi < P.n_q; qi += q_step) {
+      if (rank * kRows >= rows_bound(P, qi)) continue;   // no rows for this rank
+      if (!mbar_wait_warp(&S.q_empty, (qn & 1) ^ 1, ew)) goto done_loader;
+      if (!(q_early && qi == q_first)) issue_q(qi);
       {
+        // this thread's 16-byte chunks of the tail: chunk lt (+ 128 i) of
+        // block 7 hold pairs 4 lc .. 4 lc + 3 of head id / 8; their
+        // coefficients load while the list is read
+        const uint32_t pq = seq_base(P.seq_pos, P.pos0, qi / P.T) + qi % P.T;
+        float co[16], si[16];
+#pragma unroll
+        for (uint32_t i = 0; i < 4; ++i) {
+          const uint32_t id = lt + 128 * i, h = id >> 3, lc = (id & 7) ^ (h & 7);
+#pragma unroll
+          for (uint32_t e = 0; e < 4; ++e) {
+            co[4 * i + e] = P.cos[(size_t)pq * 32 + 4 * lc + e];
+            si[4 * i + e] = P.sin[(size_t)pq * 32 + 4 * lc + e];
+          }
+        }
         const QueryGeo g = query_geo(P, qi, rank, C, lane);
         if (g.t0 >= g.t1) {          // the list is shorter than the bound: nothing to do
           // (Q still lands: wait for it so the buffer is never written twice at once)
@@ -358,18 +387,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         // the first tile's rows start loading before Q is rotated
         if (!issue_tile(g, g.t0, n)) goto done_loader;
-        // this thread's 16-byte chunks of the tail: chunk lt (+ 128 i) of block 7
-        // holds pairs 4 lc .. 4 lc + 3 of head id / 8; coefficients load meanwhile
-        float co[16], si[16];
-#pragma unroll
-        for (uint32_t i = 0; i < 4; ++i) {
-          const uint32_t id = lt + 128 * i, h = id >> 3, lc = (id & 7) ^ (h & 7);
-#pragma unroll
-          for (uint32_t e = 0; e < 4; ++e) {
-            co[4 * i + e] = P.cos[(size_t)g.p * 32 + 4 * lc + e];
-            si[4 * i + e] = P.sin[(size_t)g.p * 32 + 4 * lc + e];
-          }
-        }
         if (!mbar_wait_warp(&S.q_tma, qt & 1, ew)) goto done_loader;   // Q landed
         ++qt;
         // rotate the tail (dims 448..511 = block 7) at position p, in place
