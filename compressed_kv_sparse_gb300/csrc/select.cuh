@@ -315,13 +315,13 @@ __device__ __forceinline__ void band_dots(const uint2 *q2, const float4 *k4, boo
   }
 }
 
-// Exact recipe for the band rows (whole block, NW warps): rounds of 2 NW rows;
-// their keys go to `kbuf` as fp32. The NW / 2 warp pairs split a round's rows
-// evenly, RPP = ceil(rows / (NW / 2)) <= 4 consecutive rows per pair; warp
-// 2g + t of pair g takes heads 32 t + lane, so one q' load serves RPP rows
-// and one key load all 32 heads of a warp. Per-head ReLU dots land in `relb`
-// [2 NW rows][64 heads]; one thread per row sums them in ascending h.
-// Results replace cS[band[i]].
+// Exact recipe for the band rows (whole block, NW warps), in rounds of 2 NW
+// rows: every key row of the round is loaded first (two per warp, both loads
+// in flight before either converts) as fp32 into `kbuf` [2 NW][128], with the
+// row's exponent range; then thread t takes head t % 64 of the row pair
+// t / 64 (one q' load serves both rows, and every lane of a warp reads the
+// same keys) and writes both ReLU dots to `relb` [2 NW][64]; then one thread
+// per row sums w_h ReLU(dot_h) in ascending h. Results replace cS[band[i]].
 template <int NW>
 __device__ __forceinline__ void rescore_band(const __nv_bfloat16 *qsm, const float *wsh,
                                              float *kbuf, float *relb, const uint32_t *band,
@@ -330,17 +330,23 @@ __device__ __forceinline__ void rescore_band(const __nv_bfloat16 *qsm, const flo
                                              uint32_t b, uint32_t *rexact,
                                              int eq_min, int eq_max) {
   const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  constexpr uint32_t RPR = 2 * NW, NP = NW / 2;
+  constexpr uint32_t RPR = 2 * NW, NT = 32 * NW;
   for (uint32_t base = 0; base < nband; base += RPR) {
     const uint32_t nr = min(RPR, nband - base);
+    uint2 kv[2];
 #pragma unroll
     for (uint32_t t = 0; t < 2; ++t) {
-      const uint32_t rr = 2 * warp + t;
+      const uint32_t rr = warp + NW * t;
+      if (rr < nr)   // warp-uniform
+        kv[t] = *reinterpret_cast<const uint2 *>(keys + map.row_of(b, cidx[band[base + rr]]) * 128 +
+                                                 4 * lane);
+    }
+#pragma unroll
+    for (uint32_t t = 0; t < 2; ++t) {
+      const uint32_t rr = warp + NW * t;
       if (rr < nr) {   // warp-uniform
         float kk[4];
-        bf16x4(*reinterpret_cast<const uint2 *>(keys + map.row_of(b, cidx[band[base + rr]]) * 128 +
-                                                4 * lane),
-               kk[0], kk[1], kk[2], kk[3]);
+        bf16x4(kv[t], kk[0], kk[1], kk[2], kk[3]);
         *reinterpret_cast<float4 *>(kbuf + rr * 128 + 4 * lane) =
             make_float4(kk[0], kk[1], kk[2], kk[3]);
         int emin, emax;
@@ -349,37 +355,19 @@ __device__ __forceinline__ void rescore_band(const __nv_bfloat16 *qsm, const flo
       }
     }
     __syncthreads();
-    const uint32_t rpp = (nr + NP - 1) / NP;   // 1 .. 4
-    const uint32_t g0 = (warp >> 1) * rpp, h = 32 * (warp & 1) + lane;
-    if (g0 < nr) {   // warp-uniform
-      const uint32_t cnt = min(rpp, nr - g0);
-      bool exact = true;
-      for (uint32_t rr = 0; rr < cnt; ++rr) exact = exact && rexact[g0 + rr] != 0u;
+    // (row pair, head): rows 2 rp and 2 rp + 1 of the round against head h
+    const uint32_t n_pairs = (nr + 1) / 2;
+    for (uint32_t it = threadIdx.x; it < n_pairs * 64; it += NT) {
+      const uint32_t rp = it >> 6, h = it & 63, r0 = 2 * rp;
       const uint2 *q2 = reinterpret_cast<const uint2 *>(qsm + (size_t)h * kQB);
-      const float4 *k4 = reinterpret_cast<const float4 *>(kbuf + g0 * 128);
-      // (rows past cnt read keys of the next pair or stale data: never stored)
-      float acc[4];
-      if (rpp == 1) {
-        float a1[1];
-        band_dots<1>(q2, k4, exact, a1);
-        acc[0] = a1[0];
-      } else if (rpp == 2) {
-        float a2[2];
-        band_dots<2>(q2, k4, exact, a2);
-        acc[0] = a2[0];
-        acc[1] = a2[1];
-      } else if (rpp == 3) {
-        float a3[3];
-        band_dots<3>(q2, k4, exact, a3);
-        acc[0] = a3[0];
-        acc[1] = a3[1];
-        acc[2] = a3[2];
-      } else {
-        band_dots<4>(q2, k4, exact, acc);
-      }
-#pragma unroll
-      for (uint32_t rr = 0; rr < 4; ++rr)
-        if (rr < cnt) relb[(g0 + rr) * 64 + h] = acc[rr] > 0.f ? acc[rr] : 0.f;
+      const float4 *k4 = reinterpret_cast<const float4 *>(kbuf + r0 * 128);
+      // (a lone last row reads the next row's stale keys: never stored)
+      const bool two = r0 + 1 < nr;
+      const bool exact = rexact[r0] != 0u && (!two || rexact[r0 + 1] != 0u);
+      float acc[2];
+      band_dots<2>(q2, k4, exact, acc);
+      relb[r0 * 64 + h] = acc[0] > 0.f ? acc[0] : 0.f;
+      if (two) relb[(r0 + 1) * 64 + h] = acc[1] > 0.f ? acc[1] : 0.f;
     }
     __syncthreads();
     if (threadIdx.x < nr) {
