@@ -13,13 +13,6 @@ namespace ds4a {
 // pdl_wait() (the previous grid has completed and its writes are visible)
 // before its first global memory access, then pdl_trigger() so that the next
 // kernel can be scheduled as soon as SMs free up.
-// Atomic add with acquire-release semantics at GPU scope; returns the old value.
-__device__ __forceinline__ uint32_t atom_add_acq_rel_gpu(uint32_t *p, uint32_t v) {
-  uint32_t old;
-  asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
-  return old;
-}
-
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");

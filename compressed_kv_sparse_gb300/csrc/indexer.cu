@@ -25,6 +25,7 @@
 
 #include "quant.cuh"
 #include "select.cuh"
+#include "tc.cuh"
 
 namespace ds4a {
 namespace {
@@ -50,16 +51,14 @@ __host__ __device__ inline IndexWs index_ws_split(void *ws, uint32_t nq, uint32_
 }
 
 // Workspace of bf16 layers: err word, qbf [nq][Hi][Di] bf16, scores
-// [nq][comp_cap] (fp32), per-query histograms of the scores' top 12 key bits
-// [nq][4096], per-query control words [nq][4] (candidate count, finished-block
-// ticket, overflow) and candidates [nq][3][kCandGlobal] (row, S~, error bound).
-// The row norms of the error bound live in the cache (written when rows are
-// appended).
+// [nq][comp_cap rounded up to 32] (fp32) and per-query histograms of the
+// scores' top 12 key bits [nq][4096]. The row norms of the error bound live
+// in the cache (written when rows are appended).
 struct TcWs {
   int *err;
   float *scores;        // [nq][sstride]
   __nv_bfloat16 *qbf;
-  uint32_t *hist, *ctrl, *cand;
+  uint32_t *hist;
   uint32_t sstride;     // floats per query row of scores: comp_cap rounded up to 32
 };
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -76,19 +75,15 @@ inline TcWs tc_ws_split(void *ws, uint32_t nq, uint32_t B, uint32_t Hi, uint32_t
   w.scores = reinterpret_cast<float *>(base + off);
   off = align_up(off + (size_t)nq * w.sstride * 4, 256);
   w.hist = reinterpret_cast<uint32_t *>(base + off);
-  off = align_up(off + (size_t)nq * kHistBins * 4, 256);
-  w.ctrl = reinterpret_cast<uint32_t *>(base + off);
-  off = align_up(off + (size_t)nq * 16, 256);
-  w.cand = reinterpret_cast<uint32_t *>(base + off);
-  off += (size_t)nq * 3 * kCandGlobal * 4;
+  off += (size_t)nq * kHistBins * 4;
   if (total) *total = off;
   return w;
 }
 
 // bf16 layers: q' = rotated query rounded to bf16 (fp32 recipe), one thread
 // per `per` dims (a 16-byte unit of 8, or a pair when the query is not 16-byte
-// aligned); the same grid clears the call's counters (error word, control
-// words and, when the scorer builds them, histograms). With the FP4 QAT round
+// aligned); the same grid clears the call's error word and, when the scorer
+// builds them, the key histograms. With the FP4 QAT round
 // trip, units are always 8 dims (loaded one by one when `vec` is false) and
 // the Di / 8 lanes of a head row run the transform together.
 __global__ void index_qbf_kernel(IndexArgs a, TcWs w, bool clear_hist, uint32_t per, bool vec) {
@@ -100,7 +95,6 @@ __global__ void index_qbf_kernel(IndexArgs a, TcWs w, bool clear_hist, uint32_t 
   const uint32_t n_units = nq * Hi * upr;
   const uint32_t i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i == 0) *w.err = 0;
-  if (i < nq * 4) w.ctrl[i] = 0u;
   if (clear_hist && i < nq * (kHistBins / 4))
     reinterpret_cast<uint4 *>(w.hist)[i] = make_uint4(0u, 0u, 0u, 0u);
   if (i >= n_units) return;
@@ -327,7 +321,7 @@ struct SelCfg {
 // Blocks per query: one wave of 1024-thread blocks (one per SM), at most 16.
 inline uint32_t select_groups(uint32_t nq) {
   uint32_t g = (uint32_t)num_sms() / (nq ? nq : 1);
-  return g < 1 ? 1 : (g > 16 ? 16 : g);
+  return g < 1 ? 1 : (g > 8 ? 8 : g);
 }
 
 // Certified selection for bf16 layers (64 heads x 128 dims).
@@ -338,9 +332,10 @@ inline uint32_t select_groups(uint32_t nq) {
 // largest gives theta_S with at least k rows S~ >= theta_S, so with
 // E = A max ||k|| and theta = theta_S - E (- slack) at least k rows have
 // L_s >= theta, and every row with U_s < theta is beaten by k rows. The G
-// blocks of a query filter their share of the rows (U_s >= theta) into a
-// candidate list; the last block to finish (atomic ticket, no waiting) runs
-// the certified selection on the candidates: tau~ = k-th largest S~, rows with
+// blocks of a query form a thread-block cluster: each filters its share of
+// the rows (U_s >= theta) into the candidate lists of the cluster's first
+// block (distributed shared memory), and after one cluster barrier that
+// block runs the certified selection on the candidates: tau~ = k-th largest S~, rows with
 // L_s > tau~ + E are in, rows with U_s < tau~ - E are out, the rest are
 // rescored with the exact recipe and the final selection is exact (ties to
 // the lower index). If the candidates overflow, the same selection runs over
@@ -390,11 +385,6 @@ __global__ void __launch_bounds__(NT, NT == 256 ? 4 : 1)
   const float *nr_c = a.map.table ? nullptr : a.norms + (size_t)b * a.comp_cap;   // contiguous
   const __nv_bfloat16 *qb = w.qbf + (size_t)qi * Hi * Di;
   const __nv_bfloat16 *wq = static_cast<const __nv_bfloat16 *>(a.w) + (size_t)qi * Hi;
-  uint32_t *ctrl = w.ctrl + (size_t)qi * 4;
-  // candidates of a query (several blocks per query): rows, S~, error bounds
-  uint32_t *cand = w.cand + (size_t)qi * 3 * kCandGlobal;
-  float *cand_s = reinterpret_cast<float *>(cand + kCandGlobal);
-  float *cand_e = cand_s + kCandGlobal;
 
   // A = c * sum_h |w_h| ||q'_h|| (HPW heads per warp); q' rows to shared
   // memory as fp32, with the exponent range of their nonzero entries
@@ -455,9 +445,12 @@ __global__ void __launch_bounds__(NT, NT == 256 ? 4 : 1)
   // a rank that leaves ~1.6 k rows above it; the filter below counts the rows
   // at or above it exactly, and too few sends the block to the full pass.
   if (threadIdx.x == 0) {
-    s_misc[2] = 0;   // this block's candidate count
+    s_misc[2] = 0;   // candidates (several blocks: the cluster's count, in its first block)
     s_misc[3] = 0;   // rows with S~ >= theta_S (one block per query)
   }
+  // several blocks per query form a cluster: every block appends its
+  // candidates to the first block's lists, whose count is zeroed above
+  if (G > 1) cluster_arrive();
   float theta_s;
   if (G > 1) {
     const uint32_t *hq = w.hist + (size_t)qi * kHistBins;
@@ -519,9 +512,14 @@ __global__ void __launch_bounds__(NT, NT == 256 ? 4 : 1)
   auto err_of = [&](float S, float nm) { return A * nm + fabsf(S) * kRel + eta; };
 
   // ---- this block's share of the rows: candidates with U >= theta, gathered
-  // in shared memory (four rows per thread loaded before any is classified);
-  // with several blocks per query each block then reserves one range of the
-  // query's list in global memory for the last block to finish
+  // in shared memory (four rows per thread loaded before any is classified):
+  // the block's own lists, or, with several blocks per query, the lists of
+  // the cluster's first block (slots from its count, stores through
+  // distributed shared memory), which then finishes alone
+  if (G > 1) cluster_wait();
+  const uint32_t c_cnt = mapa_shared(smem_u32(&s_misc[2]), 0);
+  const uint32_t c_idx = mapa_shared(smem_u32(cidx), 0), c_S = mapa_shared(smem_u32(cS), 0);
+  const uint32_t c_e = mapa_shared(smem_u32(ce), 0);
   {
     const uint32_t per = ((vis + G * 32 - 1) / (G * 32)) * 32;
     const uint32_t r0 = g * per, r1 = min(vis, r0 + per);
@@ -548,65 +546,43 @@ __global__ void __launch_bounds__(NT, NT == 256 ? 4 : 1)
         const uint32_t bal = __ballot_sync(0xffffffffu, c);
         if (bal) {
           uint32_t slot = 0;
-          if (lane == 0) slot = atomicAdd(&s_misc[2], (uint32_t)__popc(bal));
+          if (lane == 0)
+            slot = G > 1 ? atom_add_cluster(c_cnt, (uint32_t)__popc(bal))
+                         : atomicAdd(&s_misc[2], (uint32_t)__popc(bal));
           slot = __shfl_sync(0xffffffffu, slot, 0) + __popc(bal & ((1u << lane) - 1u));
           if (c && slot < CAP) {
-            cidx[slot] = r;
-            cS[slot] = S;
-            ce[slot] = e;
+            if (G > 1) {
+              st_cluster_u32(c_idx + 4 * slot, r);
+              st_cluster_u32(c_S + 4 * slot, __float_as_uint(S));
+              st_cluster_u32(c_e + 4 * slot, __float_as_uint(e));
+            } else {
+              cidx[slot] = r;
+              cS[slot] = S;
+              ce[slot] = e;
+            }
           }
         }
       }
     }
   }
   if (G > 1) {
-    __syncthreads();
-    const uint32_t nb = s_misc[2];
-    if (threadIdx.x == 0) {
-      const uint32_t at = atomicAdd(&ctrl[0], nb);
-      s_misc[5] = at;
-      if (nb > CAP || at + nb > kCandGlobal) ctrl[2] = 1u;   // overflow: full pass
-    }
-    __syncthreads();
-    const uint32_t at = s_misc[5], nbc = min(nb, CAP);
-    for (uint32_t i = threadIdx.x; i < nbc && at + i < kCandGlobal; i += NT) {
-      cand[at + i] = cidx[i];
-      cand_s[at + i] = cS[i];
-      cand_e[at + i] = ce[i];
-    }
-    // the ticket: an acquire-release add at GPU scope publishes this block's
-    // candidates (ordered before it by the barrier) and, in the last block,
-    // makes every other block's visible to the threads after the next barrier
-    __syncthreads();
-    if (threadIdx.x == 0) s_misc[1] = atom_add_acq_rel_gpu(&ctrl[1], 1u) == G - 1 ? 1u : 0u;
-    __syncthreads();
-    if (!s_misc[1]) return;
+    // every block's candidates are in the first block's lists: it finishes
+    cluster_arrive();
+    cluster_wait();
+    if (g != 0) return;
   } else {
     __syncthreads();
   }
 
   const __nv_bfloat16 *keys = static_cast<const __nv_bfloat16 *>(a.keys);   // rows via a.map
   float *kb = kbuf + warp * 128, *rel = relb + warp * 64;
-  const uint32_t nc = G == 1 ? s_misc[2] : *(volatile uint32_t *)&ctrl[0];
-  const bool fast = nc <= CAP && (G == 1 ? s_misc[3] >= k : *(volatile uint32_t *)&ctrl[2] == 0u);
+  const uint32_t nc = s_misc[2];
+  const bool fast = nc <= CAP && (G == 1 ? s_misc[3] >= k : true);
   uint32_t need;
   if (fast) {
     // ---- certified selection on the candidates
     if (threadIdx.x == 0) s_misc[5] = 0u;
     __syncthreads();
-    if (G > 1) {
-      for (uint32_t j = threadIdx.x; j < nc; j += blockDim.x) {
-        uint32_t r = __ldcg(&cand[j]);
-        const float S = __ldcg(&cand_s[j]), e = __ldcg(&cand_e[j]);
-        if (r >= vis) {   // never expected: the selection below recomputes from the scores
-          s_misc[5] = 1u;
-          r = 0;
-        }
-        cidx[j] = r;
-        cS[j] = S;
-        ce[j] = e;
-      }
-    }
     const uint32_t words = (vis + 31) / 32;
     for (uint32_t i = threadIdx.x; i < words; i += blockDim.x) bitmap[i] = 0u;
     if (G == 1) {
@@ -852,7 +828,7 @@ cudaError_t launch_index_tc(const IndexArgs &a, cudaStream_t s) {
   const bool scorer_hist = select_groups(nq) > 1;
   size_t nthreads = (size_t)nq * a.n_heads * a.dim / per;
   if (scorer_hist && (size_t)nq * (kHistBins / 4) > nthreads) nthreads = (size_t)nq * (kHistBins / 4);
-  if ((size_t)nq * 4 > nthreads) nthreads = (size_t)nq * 4;
+  if (nthreads == 0) nthreads = 1;
   cudaError_t eq = launch_pdl(index_qbf_kernel, dim3((unsigned)((nthreads + 255) / 256)),
                               dim3(256), 0, s, a, w, scorer_hist, per, vec);
   if (eq != cudaSuccess) return eq;
@@ -904,8 +880,23 @@ cudaError_t launch_index_tc(const IndexArgs &a, cudaStream_t s) {
     static int smem_set = 0;
     cudaError_t e = ensure_smem(topk_select_tc_kernel<1024>, smem, &smem_set);
     if (e != cudaSuccess) return e;
-    e = launch_pdl(topk_select_tc_kernel<1024>, dim3(nq * G), dim3(1024), smem, s, a, w, (float)cb,
-                   G);
+    // the G blocks of a query form a cluster (their candidates go to the
+    // first block's shared memory)
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute at[2];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = G;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    at[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.gridDim = dim3(nq * G);
+    cfg.blockDim = dim3(1024);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cfg.attrs = at;
+    cfg.numAttrs = 2;
+    e = cudaLaunchKernelEx(&cfg, topk_select_tc_kernel<1024>, a, w, (float)cb, G);
     if (e != cudaSuccess) return e;
   }
   note_launches(1);

@@ -12,7 +12,6 @@ namespace ds4a {
 namespace {
 
 constexpr uint32_t kHistBins = 4096;    // bins of the top 12 bits of a score key
-constexpr uint32_t kCandGlobal = 4096;  // candidates per query in the workspace
 
 // Order-preserving unsigned key of an fp32 score (+0 and -0 share a key).
 __device__ __forceinline__ uint32_t warp_sum_u32(uint32_t v) {
