@@ -393,8 +393,10 @@ ds4a_status ds4a_set_decode_cluster(uint32_t C) {
 
 uint32_t ds4a_decode_cluster_size(const ds4a_layer_cache *c, uint32_t n_heads, uint32_t top_k) {
   if (check_cache(c) != DS4A_OK) return 0;
+  // (a decode call's token is at n_tokens - 1)
   return attn_decode_cluster(c->dtype, c->ratio, c->batch, n_heads, c->head_dim, c->n_rot,
-                             c->cap_raw, c->comp_cap, c->ratio == 4 ? top_k : 0);
+                             c->cap_raw, c->comp_cap, c->ratio == 4 ? top_k : 0,
+                             comp_rows(c, c->n_tokens), c->n_tokens);
 }
 
 ds4a_status ds4a_sparse_attn_prefill_chunk(ds4a_layer_cache *c, uint32_t pos0, uint32_t T,

@@ -34,6 +34,21 @@ __host__ __device__ inline uint32_t rows_max(uint32_t ratio, uint32_t cap_raw,
   return cap_raw + (ratio == 4 ? top_k : ratio == 128 ? comp_cap : 0);
 }
 
+// Rows of any query of a call whose last position is at most pos_end - 1
+// (the window, then the listed or visible compressed rows): at most
+// rows_max, and tighter once the position is known.
+inline uint32_t rows_at(uint32_t ratio, uint32_t cap_raw, uint32_t comp_cap, uint32_t top_k,
+                        uint32_t n_comp, uint64_t pos_end) {
+  const uint32_t w = (uint32_t)(pos_end < cap_raw ? pos_end : cap_raw);
+  uint64_t c = 0;
+  if (ratio == 4) c = pos_end / 4 < top_k ? pos_end / 4 : top_k;
+  else if (ratio == 128) c = pos_end / 128;
+  if (ratio && c > n_comp) c = n_comp;
+  const uint64_t r = (uint64_t)w + c;
+  const uint32_t bound = rows_max(ratio, cap_raw, comp_cap, top_k);
+  return r < bound ? (uint32_t)r : bound;
+}
+
 inline Plan make_plan(uint32_t ratio, uint32_t batch, uint32_t T, uint32_t H, uint32_t D,
                       uint32_t cap_raw, uint32_t comp_cap, uint32_t top_k) {
   Plan pl;
@@ -338,7 +353,11 @@ cudaError_t launch_attention_t(const AttnArgs &a, cudaStream_t s) {
 // thread-block cluster); word 0 of the workspace is its error word (never
 // reset: a launch compares it with its value at the start).
 cudaError_t launch_attention_tc_path(const AttnArgs &a, cudaStream_t s) {
-  const uint32_t rmax = rows_max(a.ratio, a.cap_raw, a.comp_cap, a.top_k);
+  // decode: the row bound at the call's position (the workspace is sized
+  // for the shape's bound, which is never smaller)
+  const uint32_t rmax = a.T == 1 ? rows_at(a.ratio, a.cap_raw, a.comp_cap, a.top_k, a.n_comp,
+                                           (uint64_t)a.pos0 + 1)
+                                 : rows_max(a.ratio, a.cap_raw, a.comp_cap, a.top_k);
   return launch_attention_tc(a, rmax, static_cast<int *>(a.ws), s);
 }
 
@@ -356,9 +375,10 @@ size_t attn_ws_bytes(int dtype, uint32_t ratio, uint32_t batch, uint32_t T, uint
 
 uint32_t attn_decode_cluster(int dtype, uint32_t ratio, uint32_t batch, uint32_t n_heads,
                              uint32_t head_dim, uint32_t n_rot, uint32_t cap_raw,
-                             uint32_t comp_cap, uint32_t top_k) {
+                             uint32_t comp_cap, uint32_t top_k, uint32_t n_comp,
+                             uint64_t pos_end) {
   if (!attn_tc_supported(dtype, n_heads, head_dim, n_rot)) return 0;
-  return attn_tc_decode_cluster(rows_max(ratio, cap_raw, comp_cap, top_k), batch);
+  return attn_tc_decode_cluster(rows_at(ratio, cap_raw, comp_cap, top_k, n_comp, pos_end), batch);
 }
 
 cudaError_t launch_attention(const AttnArgs &a, cudaStream_t s) {

@@ -177,11 +177,12 @@ cudaError_t launch_attention_tc(const AttnArgs &a, uint32_t rows_max, int *err, 
 // decode launch of `n_q` queries with at most `rows_max` rows each uses.
 void attn_tc_force_cluster(uint32_t C);
 uint32_t attn_tc_decode_cluster(uint32_t rows_max, uint32_t n_q);
-// The same for the arguments of a decode call: 0 when it does not run on the
-// tensor-core kernel.
+// The same for the arguments of a decode call whose token is at position
+// pos_end - 1: 0 when it does not run on the tensor-core kernel.
 uint32_t attn_decode_cluster(int dtype, uint32_t ratio, uint32_t batch, uint32_t n_heads,
                              uint32_t head_dim, uint32_t n_rot, uint32_t cap_raw,
-                             uint32_t comp_cap, uint32_t top_k);
+                             uint32_t comp_cap, uint32_t top_k, uint32_t n_comp,
+                             uint64_t pos_end);
 cudaError_t launch_ring_commit(int dtype, uint32_t batch, uint32_t T, uint32_t pos0,
                                const uint32_t *seq_pos, uint32_t cap_raw, uint32_t head_dim,
                                const void *chunk, void *ring, cudaStream_t s);

@@ -403,19 +403,20 @@ ds4a_status ds4a_wait_selftest(void *ws, size_t ws_bytes, uint32_t limit_us,
  * Cluster size of the tensor-core decode attention (bf16 layers, 64 heads x
  * 512 dims, 64 rotated dims). That kernel spreads each query's 128-row tiles
  * over a thread-block cluster of C CTAs and merges their partial outputs. C
- * is chosen from the tile count (a bound from the cache's shape: cap_raw +
- * top_k rows on ratio 4, cap_raw + comp_cap on ratio 128, cap_raw on ratio 0)
- * and the device's cluster occupancy, so that the batch runs in one wave;
- * sizes above 8 are used only where the device allows them.
+ * is chosen from the tile count (a bound on a query's rows at the call's
+ * position: min(pos + 1, cap_raw) window rows plus min(top_k, (pos + 1) / 4)
+ * on ratio 4, (pos + 1) / 128 on ratio 128, each at most the compressed rows
+ * held) and the device's cluster occupancy, so that the batch runs in one
+ * wave; sizes above 8 are used only where the device allows them.
  *
  * ds4a_set_decode_cluster(C): 0 (the default) keeps the automatic choice;
  * 1 .. 16 forces C for every later decode launch of this process (a tuning
  * and test hook), reduced to the call's tile count, and ignored where the
  * device cannot launch that size. DS4A_ERR_ARG for C > 16.
  * ds4a_decode_cluster_size: the C that ds4a_sparse_attn_decode uses for this
- * cache and these arguments, with the current device current; 0 when the call
- * does not run on that kernel (fp32 layers, other head shapes) or the cache
- * fails its checks.
+ * cache and these arguments at pos = n_tokens - 1 (the token appended last),
+ * with the current device current; 0 when the call does not run on that
+ * kernel (fp32 layers, other head shapes) or the cache fails its checks.
  */
 ds4a_status ds4a_set_decode_cluster(uint32_t C);
 uint32_t ds4a_decode_cluster_size(const ds4a_layer_cache *cache, uint32_t n_heads,
