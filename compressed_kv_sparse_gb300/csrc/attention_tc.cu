@@ -16,15 +16,21 @@
 // when a score exceeds it by 2^8, so the common path needs no reduction across
 // rows; the per-head sums come from the tensor core (ones x P^T).
 //
-// Decode: the tiles of a query are spread over a thread-block cluster (rank c
-// takes tiles c, c + C, ...). Each CTA writes its unnormalised O and per-head
-// (max, sum) to the workspace straight from TMEM; after one cluster barrier,
-// rank c pulls heads [64c/C, 64(c+1)/C) of every rank into its freed tile
-// buffer (cp.async from L2), combines them in rank order, normalises, rotates
-// the tail back and writes bf16 rows. (On this part the L2 round trip moves
-// these 128 KiB per CTA faster than distributed shared memory does.) A query
-// that fits one CTA (C = 1) and prefill write the output directly: it is
-// staged in the P buffer 128 dims at a time and stored as 16-byte segments.
+// Decode: a query's 64 heads are split into two groups of 32, each its own
+// set of CTAs over the same rows (S^T then has N = 32; P keeps the 64-column
+// layout with the other group's columns zero, so PV and the sums are the
+// 64-head MMAs). The tiles of a (query, head group) are spread over a
+// thread-block cluster (rank c takes tiles c, c + C, ...). Each CTA writes its
+// normalised O and per-head (max, sum) to the workspace straight from TMEM;
+// after one cluster barrier, rank c pulls heads [32c/C, 32(c+1)/C) of the
+// group from every rank into its freed tile buffer (bulk copies from L2),
+// combines them in rank order, rotates the tail back and writes bf16 rows.
+// (On this part the L2 round trip moves these bytes faster than distributed
+// shared memory does.) Splitting the heads halves each CTA's softmax and
+// exchange and doubles the CTAs a small batch puts to work. A (query, head
+// group) that fits one CTA (C = 1) and prefill write the output directly: it
+// is staged in the P buffer 128 dims at a time and stored as 16-byte
+// segments.
 //
 // Warps 0-3: softmax and output epilogue (TMEM lanes = rows, then dims);
 // warps 4-7: gather loaders (cp.async, zero fill for masked rows) and the query
@@ -42,6 +48,15 @@ namespace {
 
 constexpr int kH = 64, kD = 512, kNope = 448, kRows = 128;
 constexpr int kQBlk = kH * 128;        // one 64-dim block of Q: 64 heads x 128 B
+// Heads per CTA: decode splits a query's 64 heads over two clusters (every
+// rank reads the same rows for half the heads); prefill keeps all 64.
+template <bool DEC>
+struct Heads {
+  static constexpr int NH = DEC ? 32 : 64;   // heads of this CTA
+  static constexpr int HG = kH / NH;         // head groups per query
+  static constexpr int NHF = NH / 32;        // 32-column halves of the S accumulator
+  static constexpr int QBLK = NH * 128;      // one 64-dim block of this CTA's Q
+};
 constexpr int kKBlk = kRows * 128;     // one 64-dim block of the row tile
 constexpr int kThreads = 288;
 constexpr uint32_t kMaxCluster = 16;   // cluster size; beyond 8 (the portable limit) when the
@@ -179,20 +194,20 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 // weights 2^(m_j - M) / sum_j 2^(m_j - M) l_j. A rank without rows left
 // m = -inf and zeros; one with only masked rows left m = -inf and O = 0.
 // CM: compile-time bound on the cluster size C (the loops over ranks unroll)
-template <uint32_t CM>
-__device__ __forceinline__ bool merge_heads(const TcAttnParams &P, Smem &S, uint32_t qi,
+template <uint32_t CM, int NH>
+__device__ __forceinline__ bool merge_heads(const TcAttnParams &P, Smem &S, uint32_t vq,
                                             uint32_t rank, uint32_t C, ErrWord ew) {
-  const uint32_t t = threadIdx.x;
-  const uint32_t h0 = rank * kH / C, h1 = (rank + 1) * kH / C, nh = h1 - h0;
-  const __nv_bfloat16 *part = P.part + (size_t)qi * C * kH * kD;
-  const float *ml = P.ml + (size_t)qi * C * kH * 2;
+  const uint32_t t = threadIdx.x, qi = vq / (kH / NH), hq0 = (vq % (kH / NH)) * NH;
+  const uint32_t h0 = rank * NH / C, h1 = (rank + 1) * NH / C, nh = h1 - h0;
+  const __nv_bfloat16 *part = P.part + (size_t)vq * C * NH * kD;
+  const float *ml = P.ml + (size_t)vq * C * NH * 2;
   __nv_bfloat16 *recv = reinterpret_cast<__nv_bfloat16 *>(S.kv);
   // rank j's rows h0 .. h1 - 1 are contiguous: one bulk copy per rank
   if (t == 0) {
     fence_proxy_async_global();
     mbar_arrive_expect_tx(&S.mg_bar, C * nh * kD * 2);
     for (uint32_t j = 0; j < C; ++j)
-      bulk_load(recv + (size_t)j * nh * kD, part + ((size_t)j * kH + h0) * kD, nh * kD * 2,
+      bulk_load(recv + (size_t)j * nh * kD, part + ((size_t)j * NH + h0) * kD, nh * kD * 2,
                 &S.mg_bar);
   }
   if (t < nh) {
@@ -200,8 +215,8 @@ __device__ __forceinline__ bool merge_heads(const TcAttnParams &P, Smem &S, uint
     float m[CM], l[CM], M = -INFINITY;
 #pragma unroll
     for (uint32_t j = 0; j < CM; ++j) {
-      m[j] = j < C ? __ldcg(ml + ((size_t)j * kH + h) * 2) : -INFINITY;   // written by peers
-      l[j] = j < C ? __ldcg(ml + ((size_t)j * kH + h) * 2 + 1) : 0.f;
+      m[j] = j < C ? __ldcg(ml + ((size_t)j * NH + h) * 2) : -INFINITY;   // written by peers
+      l[j] = j < C ? __ldcg(ml + ((size_t)j * NH + h) * 2 + 1) : 0.f;
     }
 #pragma unroll
     for (uint32_t j = 0; j < CM; ++j) M = fmaxf(M, m[j]);
@@ -246,7 +261,7 @@ __device__ __forceinline__ bool merge_heads(const TcAttnParams &P, Smem &S, uint
     // rotate back by -p: (x0, x1) -> (x0 c + x1 s, -x0 s + x1 c)
     const float r0 = a0 * co0 + a1 * si0, r1 = -a0 * si0 + a1 * co0;
     const float r2 = a2 * co1 + a3 * si1, r3 = -a2 * si1 + a3 * co1;
-    *reinterpret_cast<uint2 *>(P.out + ((size_t)qi * kH + h0 + i) * kD + d) =
+    *reinterpret_cast<uint2 *>(P.out + ((size_t)qi * kH + hq0 + h0 + i) * kD + d) =
         make_uint2(pack_bf16(r0, r1), pack_bf16(r2, r3));
   }
   return true;
@@ -261,14 +276,26 @@ __global__ void __launch_bounds__(kThreads, 1)
   Smem &S = *reinterpret_cast<Smem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                       ~(uintptr_t)1023);
   const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // decode: cluster of C CTAs per query, rank c takes tiles c, c + C, ...;
-  // prefill: one whole query at a time per CTA
+  // decode: cluster of C CTAs per (query, head group), rank c takes tiles
+  // c, c + C, ...; prefill: one whole query at a time per CTA
   constexpr bool dec = DEC;
+  using HS = Heads<DEC>;
+  constexpr int NH = HS::NH, NHF = HS::NHF, QBLK = HS::QBLK;
   const uint32_t C = dec ? P.cluster : 1u;
   const uint32_t rank = dec ? cluster_ctarank() : 0u;
-  const uint32_t q_first = dec ? blockIdx.x / C : blockIdx.x;
+  const uint32_t vq = dec ? blockIdx.x / C : 0u;          // decode: (query, head group)
+  const uint32_t hq0 = dec ? (vq % HS::HG) * NH : 0u;     // first head of this CTA
+  const uint32_t q_first = dec ? vq / HS::HG : blockIdx.x;
   const uint32_t q_step = dec ? P.n_q : gridDim.x;
   const int err_base = *(volatile int *)P.err;
+  if (NH < kH) {
+    // heads NH .. 63 of every P row stay zero: the PV and sum MMAs read all
+    // 64 columns, and those of the other group contribute nothing
+    uint4 *pz = reinterpret_cast<uint4 *>(S.p);
+    for (uint32_t i = threadIdx.x; i < kRows * 128 / 16; i += blockDim.x)
+      pz[i] = make_uint4(0u, 0u, 0u, 0u);
+    fence_proxy_async();
+  }
 
   if (threadIdx.x == 0) {
     mbar_init(&S.kv_full, 128);
@@ -349,10 +376,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // tables), while the top-k lists and the new raw row are not.
     auto issue_q = [&](uint32_t qi) {
       if (lt == 0) {
-        mbar_arrive_expect_tx(&S.q_tma, 8 * kQBlk);
+        mbar_arrive_expect_tx(&S.q_tma, 8 * QBLK);
 #pragma unroll
         for (uint32_t kb = 0; kb < 8; ++kb)
-          tma_load_2d(S.q + kb * kQBlk, &tmap_q, &S.q_tma, (int)(64 * kb), (int)(qi * kH));
+          tma_load_2d(S.q + kb * QBLK, &tmap_q, &S.q_tma, (int)(64 * kb), (int)(qi * kH + hq0));
       }
     };
     const bool q_early = q_first < P.n_q && rank * kRows < rows_bound(P, q_first);
@@ -368,9 +395,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         // block 7 hold pairs 4 lc .. 4 lc + 3 of head id / 8; their
         // coefficients load while the list is read
         const uint32_t pq = seq_base(P.seq_pos, P.pos0, qi / P.T) + qi % P.T;
-        float co[16], si[16];
+        constexpr uint32_t kQC = NH / 16;   // tail chunks per loader thread
+        float co[4 * kQC], si[4 * kQC];
 #pragma unroll
-        for (uint32_t i = 0; i < 4; ++i) {
+        for (uint32_t i = 0; i < kQC; ++i) {
           const uint32_t id = lt + 128 * i, h = id >> 3, lc = (id & 7) ^ (h & 7);
 #pragma unroll
           for (uint32_t e = 0; e < 4; ++e) {
@@ -391,9 +419,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++qt;
         // rotate the tail (dims 448..511 = block 7) at position p, in place
 #pragma unroll
-        for (uint32_t i = 0; i < 4; ++i) {
+        for (uint32_t i = 0; i < kQC; ++i) {
           const uint32_t id = lt + 128 * i, h = id >> 3, pc = id & 7;
-          uint4 *ptr = reinterpret_cast<uint4 *>(S.q + 7 * kQBlk + h * 128 + pc * 16);
+          uint4 *ptr = reinterpret_cast<uint4 *>(S.q + 7 * QBLK + h * 128 + pc * 16);
           uint4 v = *ptr;
           uint32_t w4[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
@@ -423,7 +451,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     cp_async_wait_all();
   } else if (warp == 8) {
     // ------------------------------------------------------------ MMA issue
-    constexpr uint32_t idS = idesc_bf16_f32(kRows, kH);
+    constexpr uint32_t idS = idesc_bf16_f32(kRows, NH);
     constexpr uint32_t idPV = idesc_bf16_f32(kRows, kH) | kIdescMajorA_MN | kIdescMajorB_MN;
     const uint32_t q_base = smem_u32(S.q), kv_base = smem_u32(S.kv), p_base = smem_u32(S.p);
     uint32_t n = 0, qn = 0;
@@ -443,7 +471,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (uint32_t kk = 0; kk < 4; ++kk)
               mma_bf16(tmS, sdesc_sw128(kv_base + kb * kKBlk + kk * 32),
-                       sdesc_sw128(q_base + kb * kQBlk + kk * 32), idS, (kb | kk) ? 1u : 0u);
+                       sdesc_sw128(q_base + kb * QBLK + kk * 32), idS, (kb | kk) ? 1u : 0u);
           mma_commit(&S.s_full);
           if (last) mma_commit(&S.q_empty);
           ok = mbar_wait(&S.p_full, n & 1, ew);
@@ -503,7 +531,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto write_p = [&](bool valid) {
       bool flag = false;
 #pragma unroll
-      for (uint32_t hf = 0; hf < 2; ++hf) {
+      for (uint32_t hf = 0; hf < (uint32_t)NHF; ++hf) {
         uint32_t a[32];
         tmem_ld32(tmS + lane_base + 32 * hf, a);
         tmem_ld_wait();
@@ -542,7 +570,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           // its code is fetched cold, and an unrolled form measured ~2 us of
           // instruction fetch
 #pragma unroll 1
-          for (uint32_t c = 0; c < (uint32_t)kH; c += 8) {
+          for (uint32_t c = 0; c < (uint32_t)NH; c += 8) {
             uint32_t a8[8];
             tmem_ld8(tmS + lane_base + c, a8);
             tmem_ld_wait();
@@ -558,7 +586,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!group_sync(&S.sm_bar, sm_phase, ew)) goto done_softmax;
           const uint32_t k0 = max(max(tkey[0 * kH], tkey[1 * kH]), max(tkey[2 * kH], tkey[3 * kH]));
           any_valid = k0 != 0u;   // a valid row has a key above 0 for every head
-          if (r < kH) {
+          if (r < (uint32_t)NH) {
             const uint32_t mk = max(max(tkey[0 * kH + r], tkey[1 * kH + r]),
                                     max(tkey[2 * kH + r], tkey[3 * kH + r]));
             const float mx = __uint_as_float((mk & 0x80000000u) ? (mk & 0x7fffffffu) : ~mk);
@@ -567,13 +595,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!group_sync(&S.sm_bar, sm_phase, ew)) goto done_softmax;
           if (!mbar_wait_warp(&S.p_empty, (n & 1) ^ 1, ew)) goto done_softmax;
           // the scores (S stays until this tile's P is done)
-          uint32_t a0[32], a1[32];
-          tmem_ld32(tmS + lane_base, a0);
-          tmem_ld32(tmS + lane_base + 32, a1);
-          tmem_ld_wait();
           bool unused = false;
-          p_half(valid, a0, 0, unused);
-          p_half(valid, a1, 1, unused);
+          if (NHF == 2) {
+            uint32_t a0[32], a1[32];
+            tmem_ld32(tmS + lane_base, a0);
+            tmem_ld32(tmS + lane_base + 32, a1);
+            tmem_ld_wait();
+            p_half(valid, a0, 0, unused);
+            p_half(valid, a1, 1, unused);
+          } else {
+            uint32_t a0[32];
+            tmem_ld32(tmS + lane_base, a0);
+            tmem_ld_wait();
+            p_half(valid, a0, 0, unused);
+          }
           fence_proxy_async();
           tc_fence_before();
           mbar_arrive(&S.p_full);
@@ -590,7 +625,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           // rare path: exact tile max per head, raise the running max, rescale
           // O and L, rewrite P
 #pragma unroll 1
-          for (uint32_t hf = 0; hf < 2; ++hf) {
+          for (uint32_t hf = 0; hf < (uint32_t)NHF; ++hf) {
             uint32_t a[32];
             tmem_ld32(tmS + lane_base + 32 * hf, a);
             tmem_ld_wait();
@@ -601,7 +636,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
           if (!group_sync(&S.sm_bar, sm_phase, ew)) goto done_softmax;
-          if (r < kH) {
+          if (r < (uint32_t)NH) {
             const float M = fmaxf(fmaxf(S.tmax[0][r], S.tmax[1][r]), fmaxf(S.tmax[2][r], S.tmax[3][r]));
             const float mo = S.mref[r], mn = fmaxf(mo, M);
             S.alpha[r] = exp2f(mo - mn);
@@ -610,14 +645,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!group_sync(&S.sm_bar, sm_phase, ew)) goto done_softmax;
           if (!first) {
 #pragma unroll 1
-            for (uint32_t m = 0; m < 10; ++m) {   // O^T (8 x 32 columns) then L (2 x 32)
+            for (uint32_t m = 0; m < 5 * (uint32_t)NHF; ++m) {   // O^T (4 dim blocks) then L
               uint32_t a[32];
-              const uint32_t ta = (m < 8 ? tmO + m * 32 : tmL + (m - 8) * 32) + lane_base;
+              const uint32_t blk = m / NHF, hf = m % NHF;
+              const uint32_t ta = (blk < 4 ? tmO + blk * kH : tmL) + 32 * hf + lane_base;
               tmem_ld32(ta, a);
               tmem_ld_wait();
 #pragma unroll
               for (int h = 0; h < 32; ++h)
-                a[h] = __float_as_uint(__uint_as_float(a[h]) * S.alpha[32 * (m & 1) + h]);
+                a[h] = __float_as_uint(__uint_as_float(a[h]) * S.alpha[32 * hf + h]);
               tmem_st32(ta, a);
             }
             tmem_st_wait();
@@ -632,7 +668,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (has_tiles) {
         if (!mbar_wait_warp(&S.o_full, qn & 1, ew)) goto done_softmax;
         tc_fence_after();
-        if (warp < 2) {   // every row of L holds the sums: warp w keeps heads 32w + lane
+        if (warp < (uint32_t)NHF) {   // every row of L holds the sums: warp w keeps heads 32w + lane
           uint32_t a[32];
           tmem_ld32(tmL + lane_base + 32 * warp, a);
           tmem_ld_wait();
@@ -647,14 +683,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!group_sync(&S.sm_bar, sm_phase, ew)) goto done_softmax;
       if (dec && C > 1) {
         // (max, sum) of this rank for the cluster merge; O follows from TMEM
-        if (r < kH) {
-          float *ml = P.ml + ((size_t)(qi * C + rank) * kH + r) * 2;
+        if (r < (uint32_t)NH) {
+          float *ml = P.ml + ((size_t)(vq * C + rank) * NH + r) * 2;
           ml[0] = (has_tiles && any_valid) ? S.mref[r] : -INFINITY;
           ml[1] = has_tiles ? S.lsh[r] : 0.f;
         }
         if (r == 0) S.has_tiles = has_tiles ? 1u : 0u;
       } else {
-        // normalise, rotate the tail back by -p, stage [64 heads][128 dims]
+        // normalise, rotate the tail back by -p, stage [NH heads][128 dims]
         // bf16 in the P buffer, then write 16-byte row segments
         uint8_t *stage = S.p;
 #pragma unroll 1
@@ -662,7 +698,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t d = m * 128 + r;
           const float co = ep_co, si = ep_si;   // used by the tail dims only (m = 3)
 #pragma unroll 1
-          for (uint32_t hf = 0; hf < 2; ++hf) {
+          for (uint32_t hf = 0; hf < (uint32_t)NHF; ++hf) {
             uint32_t a[32];
             tmem_ld32(tmO + lane_base + m * kH + 32 * hf, a);
             tmem_ld_wait();
@@ -683,9 +719,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
           if (!group_sync(&S.sm_bar, sm_phase, ew)) goto done_softmax;
-          __nv_bfloat16 *o = P.out + (size_t)qi * kH * kD + m * 128;
+          __nv_bfloat16 *o = P.out + ((size_t)qi * kH + hq0) * kD + m * 128;
 #pragma unroll
-          for (uint32_t i = 0; i < 8; ++i) {
+          for (uint32_t i = 0; i < (uint32_t)NH / 8; ++i) {
             const uint32_t c = r + 128 * i, h = c >> 4, seg = c & 15;
             *reinterpret_cast<uint4 *>(o + (size_t)h * kD + seg * 8) =
                 *reinterpret_cast<const uint4 *>(stage + h * 256 + seg * 16);
@@ -708,19 +744,22 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   if (dec && C > 1) {
-    // this rank's O / L as [64 heads][512] bf16 straight to the workspace.
-    // Warp w reads TMEM lanes 32 (w % 4) .. + 31 (dims) for heads 32 (w / 4)
-    // .. + 31; lanes 2i, 2i + 1 hold dims d, d + 1: the even lane stores the
-    // bf16 pair of head h, the odd lane that of head h + 1 (one swap each)
+    // this rank's O / L as [NH heads][512] bf16 straight to the workspace.
+    // Warp w reads TMEM lanes 32 (w % 4) .. + 31 (dims) for heads 32 hf ..
+    // + 31 of dim blocks m0 .. m1 - 1 (64 heads: hf = w / 4, every block; 32
+    // heads: hf = 0, two blocks per warp); lanes 2i, 2i + 1 hold dims d, d + 1:
+    // the even lane stores the bf16 pair of head h, the odd lane that of head
+    // h + 1 (one swap each)
     if (warp < 8) {
-      __nv_bfloat16 *dst = P.part + ((size_t)q_first * C + rank) * kH * kD;
-      const uint32_t qw = warp & 3, hf = warp >> 2, dl = 32 * qw + lane;
+      __nv_bfloat16 *dst = P.part + ((size_t)vq * C + rank) * NH * kD;
+      const uint32_t qw = warp & 3, hf = NHF == 2 ? warp >> 2 : 0u, dl = 32 * qw + lane;
+      const uint32_t m0 = NHF == 2 ? 0u : 2 * (warp >> 2), m1 = NHF == 2 ? 4u : m0 + 2;
       const bool had = S.has_tiles != 0, odd = lane & 1;
       float li[32];
 #pragma unroll
       for (int h = 0; h < 32; ++h) li[h] = had ? S.linv[32 * hf + h] : 0.f;
 #pragma unroll 1
-      for (uint32_t m = 0; m < 4; ++m) {
+      for (uint32_t m = m0; m < m1; ++m) {
         uint32_t a[32];
         if (had) {
           tmem_ld32(tmO + ((32 * qw) << 16) + m * kH + 32 * hf, a);
@@ -747,9 +786,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     cluster_sync_all();   // every rank's O and (max, sum) are in the workspace
     if (warp < 8) {
       if (C <= 8)
-        merge_heads<8>(P, S, q_first, rank, C, ew);
+        merge_heads<8, NH>(P, S, vq, rank, C, ew);
       else
-        merge_heads<kMaxCluster>(P, S, q_first, rank, C, ew);
+        merge_heads<kMaxCluster, NH>(P, S, vq, rank, C, ew);
     }
   }
 }
@@ -846,7 +885,7 @@ void attn_tc_force_cluster(uint32_t C) {
 }
 
 uint32_t attn_tc_decode_cluster(uint32_t rows_max, uint32_t n_q) {
-  return decode_cluster(rows_max, n_q, sizeof(Smem) + 1024);
+  return decode_cluster(rows_max, n_q * Heads<true>::HG, sizeof(Smem) + 1024);
 }
 
 bool attn_tc_supported(int dtype, uint32_t H, uint32_t D, uint32_t n_rot) {
@@ -897,15 +936,17 @@ cudaError_t launch_attention_tc(const AttnArgs &a, uint32_t rows_max, int *err, 
   cudaError_t e = a.T == 1 ? ensure_smem(k_dec, smem, &smem_set[1][paged])
                            : ensure_smem(k_pf, smem, &smem_set[0][paged]);
   if (e != cudaSuccess) return e;
-  // Q as [n_q * 64 heads][512] bf16 rows; boxes of 64 heads x 64 dims
+  // Q as [n_q * 64 heads][512] bf16 rows; boxes of one CTA's heads x 64 dims
   CUtensorMap tq;
   const uint64_t qd[2] = {(uint64_t)kD, (uint64_t)P.n_q * kH};
   const uint64_t qs[1] = {(uint64_t)kD * 2};
-  const uint32_t qb[2] = {64, (uint32_t)kH};
+  const uint32_t qb[2] = {64, (uint32_t)(a.T == 1 ? Heads<true>::NH : Heads<false>::NH)};
   e = make_tmap_bf16(&tq, a.q, 2, qd, qs, qb);
   if (e != cudaSuccess) return e;
   if (a.T == 1) {
-    P.cluster = decode_cluster(rows_max, P.n_q, smem);
+    // one cluster of P.cluster CTAs per (query, head group)
+    const uint32_t n_vq = P.n_q * Heads<true>::HG;
+    P.cluster = decode_cluster(rows_max, n_vq, smem);
     P.ml = reinterpret_cast<float *>(P.part + (size_t)P.n_q * P.cluster * kH * kD);
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute at[2];
@@ -913,7 +954,7 @@ cudaError_t launch_attention_tc(const AttnArgs &a, uint32_t rows_max, int *err, 
     at[0].val.clusterDim.x = P.cluster;
     at[0].val.clusterDim.y = 1;
     at[0].val.clusterDim.z = 1;
-    cfg.gridDim = dim3(P.n_q * P.cluster);
+    cfg.gridDim = dim3(n_vq * P.cluster);
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
