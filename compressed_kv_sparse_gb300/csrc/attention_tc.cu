@@ -33,6 +33,11 @@
 // segments.
 //
 // Warps 0-3: softmax and output epilogue (TMEM lanes = rows, then dims);
+// In decode on ratios 0 and 128 the rows of a tile are contiguous (the
+// window is the whole 128-slot ring once p >= 127, a compressed tile is 128
+// consecutive rows): such a tile is eight TMA boxes issued by one thread
+// instead of 8192 16-byte gathers.
+//
 // warps 4-7: gather loaders (cp.async, zero fill for masked rows) and the query
 // rotation; warp 8: MMA issue (one thread) and TMEM allocation. Every wait is
 // bounded (tc.cuh); a timeout sets the error word and the CTA winds down.
@@ -68,6 +73,11 @@ struct TcAttnParams {
   RowMap map;         // rows of comp
   const uint32_t *seq_pos;   // [B] per-sequence positions (ragged decode) or NULL
   uint32_t cluster;   // decode: CTAs per query (one cluster); 0: prefill, persistent CTAs
+  // decode tiles of contiguous rows by TMA instead of row gathers (ratios 0
+  // and 128): bit 0 the window tile as the whole 128-slot ring, bit 1 (ratio
+  // 128) the compressed tiles (the visible rows, the same count for every
+  // sequence)
+  uint32_t tma_rows;
   uint32_t n_q;       // queries = batch * T
   float c2;           // softmax scale * log2(e)
   const __nv_bfloat16 *q, *ring, *chunk, *comp;
@@ -88,6 +98,7 @@ struct Smem {
   uint64_t kv_full, kv_empty[4];   // kv_full: the whole tile landed; kv_empty[m]: blocks 2m, 2m+1 free
   uint64_t q_full, q_empty, s_full, p_full, p_empty, o_full, o_empty, sm_bar;
   uint64_t q_tma;   // the query's eight Q blocks landed (TMA transaction count)
+  uint64_t kv_tma;  // a tile loaded by TMA landed
   uint64_t mg_bar;  // decode merge: the peers' partial O slices landed
   float mref[kH], alpha[kH], lsh[kH], linv[kH];
   float tmax[4][kH];
@@ -158,6 +169,17 @@ __device__ __forceinline__ QueryGeo query_geo(const TcAttnParams &P, uint32_t qi
   g.t1 = (g.N + kRows - 1) / kRows;
   g.ts = ts;
   return g;
+}
+
+// How tile `tile` of a decode query loads: 0 row gathers, 1 the whole ring
+// by TMA (the window of 128 rows, in slot order: the softmax does not depend
+// on the order of the rows), 2 compressed rows 128 (tile - 1) .. by TMA.
+template <bool DEC, bool PAGED>
+__device__ __forceinline__ uint32_t tile_kind(const TcAttnParams &P, const QueryGeo &g,
+                                              uint32_t tile) {
+  if (!DEC || g.n_w != (uint32_t)kRows) return 0;
+  if (tile == 0) return (P.tma_rows & 1u) ? 1u : 0u;
+  return (!PAGED && (P.tma_rows & 2u) && P.ratio == 128) ? 2u : 0u;
 }
 
 // Source row of list entry r (nullptr: masked).
@@ -271,7 +293,9 @@ __device__ __forceinline__ bool merge_heads(const TcAttnParams &P, Smem &S, uint
 // CTAs); two instantiations keep each path's code to itself
 template <bool DEC, bool PAGED>
 __global__ void __launch_bounds__(kThreads, 1)
-    attn_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, TcAttnParams P) {
+    attn_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
+                   const __grid_constant__ CUtensorMap tmap_ring,
+                   const __grid_constant__ CUtensorMap tmap_comp, TcAttnParams P) {
   extern __shared__ uint8_t smem_raw[];
   Smem &S = *reinterpret_cast<Smem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                       ~(uintptr_t)1023);
@@ -309,10 +333,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&S.o_empty, 4);
     mbar_init(&S.sm_bar, 128);
     mbar_init(&S.q_tma, 1);
+    mbar_init(&S.kv_tma, 1);
     mbar_init(&S.mg_bar, 1);
     S.flagcnt[0] = S.flagcnt[1] = S.flagcnt[2] = 0;
     fence_mbar_init();
     prefetch_tmap(&tmap_q);
+    if (P.tma_rows) {
+      prefetch_tmap(&tmap_ring);
+      prefetch_tmap(&tmap_comp);
+    }
   }
   if (warp == 8) tmem_alloc(&S.tmem, 512);
   tc_fence_before();
@@ -346,10 +375,26 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp >= 4 && warp < 8) {
     // ------------------------------------------------------------ loaders
     const uint32_t lt = threadIdx.x - 128, lw = warp - 4;
-    uint32_t n = 0, qn = 0, qt = 0;   // qt: Q loads issued (q_tma phases)
+    uint32_t n = 0, qn = 0, qt = 0, nk = 0;   // qt: Q loads issued, nk: TMA tiles issued
     // issue all eight 64-dim blocks of a tile (one cp.async group each) as
-    // their slots free up; rows of this lane: lw*32 + lane/8 + 4i, chunk lane%8
+    // their slots free up; rows of this lane: lw*32 + lane/8 + 4i, chunk lane%8.
+    // A tile of contiguous rows is eight TMA boxes of 128 rows x 64 dims
+    // (one thread), in the same swizzled layout.
     auto issue_tile = [&](const QueryGeo &g, uint32_t tile, uint32_t n) -> bool {
+      if (const uint32_t kind = tile_kind<DEC, PAGED>(P, g, tile)) {
+        for (uint32_t kb = 0; kb < 8; ++kb) {
+          if ((kb & 1) == 0 && !mbar_wait_warp(&S.kv_empty[kb >> 1], (n & 1) ^ 1, ew)) return false;
+          if (lt == 0) {
+            if (kb == 0) mbar_arrive_expect_tx(&S.kv_tma, 8 * kKBlk);
+            if (kind == 1)
+              tma_load_3d(S.kv + kb * kKBlk, &tmap_ring, &S.kv_tma, (int)(64 * kb), 0, (int)g.b);
+            else
+              tma_load_3d(S.kv + kb * kKBlk, &tmap_comp, &S.kv_tma, (int)(64 * kb),
+                          (int)(kRows * (tile - 1)), (int)g.b);
+          }
+        }
+        return true;
+      }
       const __nv_bfloat16 *src[8];
 #pragma unroll
       for (uint32_t i = 0; i < 8; ++i)
@@ -442,6 +487,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           // blocks land measured slower)
           cp_async_wait_all();
           fence_proxy_async();
+          if (tile_kind<DEC, PAGED>(P, g, tile)) {   // (one thread watches the TMA tile)
+            if (lt == 0 && !mbar_wait(&S.kv_tma, nk & 1, ew)) goto done_loader;
+            ++nk;
+          }
           mbar_arrive(&S.kv_full);
         }
       }
@@ -454,7 +503,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr uint32_t idS = idesc_bf16_f32(kRows, NH);
     constexpr uint32_t idPV = idesc_bf16_f32(kRows, kH) | kIdescMajorA_MN | kIdescMajorB_MN;
     const uint32_t q_base = smem_u32(S.q), kv_base = smem_u32(S.kv), p_base = smem_u32(S.p);
-    uint32_t n = 0, qn = 0;
+    uint32_t n = 0, qn = 0, nk = 0;
     bool ok = true;
     for (uint32_t qi = q_first; qi < P.n_q && ok; qi += q_step) {
       if (rank * kRows >= rows_bound(P, qi)) continue;
@@ -465,6 +514,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (uint32_t tile = g.t0; ok && tile < g.t1; tile += g.ts, ++n) {
           const bool first = tile == g.t0, last = tile + g.ts >= g.t1;
           ok = mbar_wait(&S.kv_full, n & 1, ew);
+          if (ok && tile_kind<DEC, PAGED>(P, g, tile)) ok = mbar_wait(&S.kv_tma, nk++ & 1, ew);
           if (!ok) break;
           tc_fence_after();
           for (uint32_t kb = 0; kb < 8; ++kb)
@@ -943,6 +993,26 @@ cudaError_t launch_attention_tc(const AttnArgs &a, uint32_t rows_max, int *err, 
   const uint32_t qb[2] = {64, (uint32_t)(a.T == 1 ? Heads<true>::NH : Heads<false>::NH)};
   e = make_tmap_bf16(&tq, a.q, 2, qd, qs, qb);
   if (e != cudaSuccess) return e;
+  // decode tiles of contiguous rows: the ring [B][128][512] (one box of its
+  // 128 slots per 64 dims) and, on ratio 128 with one position for every
+  // sequence, the visible compressed rows [B][n_list][512] (rows past n_list
+  // read as zeros); a map that cannot be built leaves the gathers
+  CUtensorMap tr = tq, tcmp = tq;
+  P.tma_rows = 0;
+  // (ratio 4 keeps its window on the gathers: its first rank runs the window
+  // tile beside the list tiles, and by TMA it measured slower)
+  if (a.T == 1 && a.cap_raw == (uint32_t)kRows && a.ratio != 4) {
+    const uint64_t rd[3] = {(uint64_t)kD, (uint64_t)a.cap_raw, (uint64_t)a.batch};
+    const uint64_t rs[2] = {(uint64_t)kD * 2, (uint64_t)a.cap_raw * kD * 2};
+    const uint32_t rb[3] = {64, (uint32_t)kRows, 1};
+    if (make_tmap_bf16(&tr, a.ring, 3, rd, rs, rb) == cudaSuccess) P.tma_rows |= 1u;
+    const uint32_t n_list = a.ratio == 128 ? min((a.pos0 + 1) / 128, a.n_comp) : 0u;
+    if (a.ratio == 128 && !paged && !a.seq_pos && n_list >= (uint32_t)kRows) {
+      const uint64_t cd[3] = {(uint64_t)kD, (uint64_t)n_list, (uint64_t)a.batch};
+      const uint64_t cs[2] = {(uint64_t)kD * 2, (uint64_t)a.comp_cap * kD * 2};
+      if (make_tmap_bf16(&tcmp, a.comp, 3, cd, cs, rb) == cudaSuccess) P.tma_rows |= 2u;
+    }
+  }
   if (a.T == 1) {
     // one cluster of P.cluster CTAs per (query, head group)
     const uint32_t n_vq = P.n_q * Heads<true>::HG;
@@ -962,13 +1032,13 @@ cudaError_t launch_attention_tc(const AttnArgs &a, uint32_t rows_max, int *err, 
     at[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = at;
     cfg.numAttrs = 2;
-    e = cudaLaunchKernelEx(&cfg, k_dec, tq, P);
+    e = cudaLaunchKernelEx(&cfg, k_dec, tq, tr, tcmp, P);
     note_launches(1);
     return e != cudaSuccess ? e : cudaGetLastError();
   }
   P.cluster = 0;
   const uint32_t grid = min(P.n_q, (uint32_t)num_sms());
-  e = launch_pdl(k_pf, dim3(grid), dim3(kThreads), smem, s, tq, P);
+  e = launch_pdl(k_pf, dim3(grid), dim3(kThreads), smem, s, tq, tr, tcmp, P);
   note_launches(1);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
