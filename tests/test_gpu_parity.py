@@ -331,7 +331,10 @@ def test_attn_decode_tiny_fp32(ratio):
     run_attn(lib_(), shape, 2, 300, 1, 300)
 
 
-@pytest.mark.parametrize("ratio,p", [(4, 1000), (128, 65536), (0, 77), (4, 5)])
+# (0, 500) and (128, 20000) take the TMA tiles: the whole ring, and 156
+# compressed rows as one full and one part-filled tile (rows past 156 zero)
+@pytest.mark.parametrize("ratio,p", [(4, 1000), (128, 65536), (0, 77), (4, 5), (0, 500),
+                                     (128, 20000)])
 def test_attn_decode_bf16(ratio, p):
     shape = synth.LayerShape(ratio=ratio)
     run_attn(lib_(), shape, 3, p, 1, p, topk_mode="pad")
