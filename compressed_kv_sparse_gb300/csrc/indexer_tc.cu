@@ -158,18 +158,23 @@ __global__ void __launch_bounds__(Cfg<QG>::kThreads, 1)
       // one 128-row key tile: two 64-dim K blocks, each one box of 128 rows
       // (contiguous keys) or two boxes of 64 rows from the tile's two
       // physical blocks (paged)
+      // the keys stream through once: evict-first, so they do not push the
+      // step's code and small reused arrays out of L2
+      const uint64_t pol = l2_evict_first_policy();
       auto issue_a = [&](uint32_t st, uint32_t b, uint32_t tile) {
         uint8_t *dst = sA + (size_t)st * kABytes;
         mbar_arrive_expect_tx(&a_full[st], kABytes);
         if (!P.map.table) {
-          tma_load_3d(dst, &tmap_k, &a_full[st], 0, (int)(tile * kRows), (int)b);
-          tma_load_3d(dst + kKBlockBytes, &tmap_k, &a_full[st], 64, (int)(tile * kRows), (int)b);
+          tma_load_3d_hint(dst, &tmap_k, &a_full[st], 0, (int)(tile * kRows), (int)b, pol);
+          tma_load_3d_hint(dst + kKBlockBytes, &tmap_k, &a_full[st], 64, (int)(tile * kRows),
+                           (int)b, pol);
         } else {
 #pragma unroll
           for (uint32_t hb = 0; hb < 2; ++hb) {
             const int y = (int)P.map.row_of(b, tile * kRows + 64 * hb);
-            tma_load_2d(dst + hb * (kKBlockBytes / 2), &tmap_k, &a_full[st], 0, y);
-            tma_load_2d(dst + kKBlockBytes + hb * (kKBlockBytes / 2), &tmap_k, &a_full[st], 64, y);
+            tma_load_2d_hint(dst + hb * (kKBlockBytes / 2), &tmap_k, &a_full[st], 0, y, pol);
+            tma_load_2d_hint(dst + kKBlockBytes + hb * (kKBlockBytes / 2), &tmap_k, &a_full[st],
+                             64, y, pol);
           }
         }
       };
