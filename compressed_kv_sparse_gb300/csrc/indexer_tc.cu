@@ -75,15 +75,76 @@ __device__ __forceinline__ uint32_t vis_of(const ScoreParams &P, uint32_t b, uin
   return min((seq_base(P.seq_pos, P.pos0, b) + t + 1) / 4, P.n_comp);
 }
 
+// Walk over the work items it .. end - 1, item = (b * n_groups + g) *
+// tiles_per + tile, without a division per item. A tile is visited when some
+// row of it is visible to the group's last query (n_vis: the group's visible
+// tiles); the rest of a group is skipped in one step. Every role walks the
+// same items in the same order.
+struct Walk {
+  uint32_t it, end, b, g, tile, n_vis;
+};
+
 template <int QG>
-__device__ __forceinline__ bool decode_item(const ScoreParams &P, uint32_t item, uint32_t &b,
-                                            uint32_t &g, uint32_t &tile) {
-  tile = item % P.tiles_per;
-  const uint32_t rest = item / P.tiles_per;
-  g = rest % P.n_groups;
-  b = rest / P.n_groups;
+__device__ __forceinline__ uint32_t visible_tiles(const ScoreParams &P, uint32_t b, uint32_t g) {
   const uint32_t last = min(P.T, (g + 1) * QG) - 1;
-  return tile * kRows < vis_of(P, b, last);   // false: every row of the tile is invisible
+  return min(P.tiles_per, (vis_of(P, b, last) + kRows - 1) / kRows);
+}
+
+template <int QG>
+__device__ __forceinline__ Walk walk_start(const ScoreParams &P, uint32_t i0, uint32_t i1) {
+  Walk w;
+  w.it = i0;
+  w.end = i1;
+  w.tile = i0 % P.tiles_per;
+  const uint32_t rest = i0 / P.tiles_per;
+  w.g = rest % P.n_groups;
+  w.b = rest / P.n_groups;
+  w.n_vis = i0 < i1 ? visible_tiles<QG>(P, w.b, w.g) : 0u;
+  return w;
+}
+
+// Moves to the first visible item at or after the current one; false when
+// the range is done.
+template <int QG>
+__device__ __forceinline__ bool walk_valid(const ScoreParams &P, Walk &w) {
+  while (w.it < w.end) {
+    if (w.tile < w.n_vis) return true;
+    w.it += P.tiles_per - w.tile;   // the group's first tile past its visible ones
+    w.tile = 0;
+    if (++w.g == P.n_groups) {
+      w.g = 0;
+      ++w.b;
+    }
+    if (w.it < w.end) w.n_vis = visible_tiles<QG>(P, w.b, w.g);
+  }
+  return false;
+}
+
+template <int QG>
+__device__ __forceinline__ void walk_next(const ScoreParams &P, Walk &w) {
+  ++w.it;
+  if (++w.tile == P.tiles_per) {
+    w.tile = 0;
+    if (++w.g == P.n_groups) {
+      w.g = 0;
+      ++w.b;
+    }
+    if (w.it < w.end) w.n_vis = visible_tiles<QG>(P, w.b, w.g);
+  }
+}
+
+// d0 += a0 * b0, d1 += a1 * b1 as one packed fp32 pair FMA (round to nearest
+// each, as two fmaf)
+__device__ __forceinline__ void ffma2(float &d0, float &d1, float a0, float a1, float b0,
+                                      float b1) {
+  asm("{\n\t.reg .b64 ra, rb, rc;\n\t"
+      "mov.b64 ra, {%2, %3};\n\t"
+      "mov.b64 rb, {%4, %5};\n\t"
+      "mov.b64 rc, {%0, %1};\n\t"
+      "fma.rn.f32x2 rc, ra, rb, rc;\n\t"
+      "mov.b64 {%0, %1}, rc;\n\t}"
+      : "+f"(d0), "+f"(d1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
 }
 
 template <int QG>
@@ -181,19 +242,17 @@ __global__ void __launch_bounds__(Cfg<QG>::kThreads, 1)
       // the key tiles of the first stages load before the wait for the
       // previous launch: the rows were written two or more launches back
       uint32_t pre = 0;
-      for (uint32_t it = it0; it < it1 && pre < (uint32_t)C::kStages; ++it) {
-        uint32_t b, g, tile;
-        if (!decode_item<QG>(P, it, b, g, tile)) continue;
-        issue_a(pre, b, tile);
+      for (Walk w = walk_start<QG>(P, it0, it1); pre < (uint32_t)C::kStages && walk_valid<QG>(P, w);
+           walk_next<QG>(P, w)) {
+        issue_a(pre, w.b, w.tile);
         issued[pre] = 0;
         ++pre;
       }
       pdl_wait();
       pdl_trigger();
       uint32_t n_vis = 0;
-      for (uint32_t it = it0; it < it1; ++it) {
-        uint32_t b, g, tile;
-        if (!decode_item<QG>(P, it, b, g, tile)) continue;
+      for (Walk w = walk_start<QG>(P, it0, it1); walk_valid<QG>(P, w); walk_next<QG>(P, w)) {
+        const uint32_t b = w.b, g = w.g, tile = w.tile;
         const int32_t bg = (int32_t)(b * P.n_groups + g);
         if (bg != cur) {
           if (cur >= 0) {
@@ -232,10 +291,8 @@ __global__ void __launch_bounds__(Cfg<QG>::kThreads, 1)
       uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0, bf_phase = 0;
       int32_t cur = -1;
       const uint32_t a_base = smem_u32(sA), b_base = smem_u32(sB);
-      for (uint32_t it = it0; it < it1; ++it) {
-        uint32_t b, g, tile;
-        if (!decode_item<QG>(P, it, b, g, tile)) continue;
-        const int32_t bg = (int32_t)(b * P.n_groups + g);
+      for (Walk w = walk_start<QG>(P, it0, it1); walk_valid<QG>(P, w); walk_next<QG>(P, w)) {
+        const int32_t bg = (int32_t)(w.b * P.n_groups + w.g);
         if (bg != cur) {
           if (cur >= 0) mma_commit(b_empty);
           if (!mbar_wait(b_full, bf_phase, P.err)) break;
@@ -298,9 +355,9 @@ __global__ void __launch_bounds__(Cfg<QG>::kThreads, 1)
     if (QG == 1) {
       for (uint32_t i = et; i < 4096; i += 128) shist[i] = 0;
     }
-    for (uint32_t it = it0; it < it1 && ok; ++it) {
-      uint32_t b, g, tile;
-      if (!decode_item<QG>(P, it, b, g, tile)) continue;
+    uint32_t vis_q = 0;   // rows visible to this warp's query of the current group
+    for (Walk w = walk_start<QG>(P, it0, it1); ok && walk_valid<QG>(P, w); walk_next<QG>(P, w)) {
+      const uint32_t b = w.b, g = w.g, tile = w.tile;
       const int32_t bg = (int32_t)(b * P.n_groups + g);
       if (bg != cur) {
         if (QG == 1 && !flush_hist(cur)) {
@@ -314,6 +371,8 @@ __global__ void __launch_bounds__(Cfg<QG>::kThreads, 1)
                           : 0.f;
         }
         __syncwarp();
+        const uint32_t tq = g * QG + q0;
+        vis_q = tq < P.T ? vis_of(P, b, tq) : 0u;
         cur = bg;
       }
       if (!mbar_wait_warp(&acc_full[acc], acc_phase, P.err)) {
@@ -336,7 +395,8 @@ __global__ void __launch_bounds__(Cfg<QG>::kThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(&acc_empty[acc]);
         // approximate score: any summation order is covered by the error
-        // bound, so eight independent chains and vector loads of the weights
+        // bound, so eight independent chains (as four packed pairs) and
+        // vector loads of the weights
         const float4 *wq4 = reinterpret_cast<const float4 *>(sw + q * kHeads);
         float acc8[8];
 #pragma unroll
@@ -345,16 +405,16 @@ __global__ void __launch_bounds__(Cfg<QG>::kThreads, 1)
         for (int h4 = 0; h4 < 16; ++h4) {
           const float4 w4 = wq4[h4];
           const uint32_t *rr = h4 < 8 ? r0 : r1;
-          const int hb = (h4 & 7) * 4;
-          acc8[(2 * h4) & 7] = fmaf(w4.x, fmaxf(__uint_as_float(rr[hb + 0]), 0.f), acc8[(2 * h4) & 7]);
-          acc8[(2 * h4 + 1) & 7] = fmaf(w4.y, fmaxf(__uint_as_float(rr[hb + 1]), 0.f), acc8[(2 * h4 + 1) & 7]);
-          acc8[(2 * h4) & 7] = fmaf(w4.z, fmaxf(__uint_as_float(rr[hb + 2]), 0.f), acc8[(2 * h4) & 7]);
-          acc8[(2 * h4 + 1) & 7] = fmaf(w4.w, fmaxf(__uint_as_float(rr[hb + 3]), 0.f), acc8[(2 * h4 + 1) & 7]);
+          const int hb = (h4 & 7) * 4, c = (2 * h4) & 7;
+          ffma2(acc8[c], acc8[c + 1], w4.x, w4.y, fmaxf(__uint_as_float(rr[hb + 0]), 0.f),
+                fmaxf(__uint_as_float(rr[hb + 1]), 0.f));
+          ffma2(acc8[c], acc8[c + 1], w4.z, w4.w, fmaxf(__uint_as_float(rr[hb + 2]), 0.f),
+                fmaxf(__uint_as_float(rr[hb + 3]), 0.f));
         }
         const float s = ((acc8[0] + acc8[1]) + (acc8[2] + acc8[3])) +
                         ((acc8[4] + acc8[5]) + (acc8[6] + acc8[7]));
         const uint32_t t = g * QG + q;
-        const bool valid = t < P.T && grow < vis_of(P, b, t);
+        const bool valid = grow < vis_q;
         if (valid) P.scores[((size_t)b * P.T + t) * P.score_stride + grow] = s;
         // histogram of the keys' top 12 bits (lanes in one bin add once), per
         // CTA in shared memory, added to the query's when the query changes
