@@ -59,6 +59,9 @@ struct TcWs {
   float *scores;        // [nq][sstride]
   __nv_bfloat16 *qbf;
   uint32_t *hist;
+  float *qnorm;         // [nq][Hi] upper bound of ||q'_h||
+  uint32_t *qexp;       // [nq][Hi] exponent range of the nonzero entries of q'_h:
+                        // int16 minimum | int16 maximum << 16 (1000 | -1000: all zero)
   uint32_t sstride;     // floats per query row of scores: comp_cap rounded up to 32
 };
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -75,7 +78,11 @@ inline TcWs tc_ws_split(void *ws, uint32_t nq, uint32_t B, uint32_t Hi, uint32_t
   w.scores = reinterpret_cast<float *>(base + off);
   off = align_up(off + (size_t)nq * w.sstride * 4, 256);
   w.hist = reinterpret_cast<uint32_t *>(base + off);
-  off += (size_t)nq * kHistBins * 4;
+  off = align_up(off + (size_t)nq * kHistBins * 4, 256);
+  w.qnorm = reinterpret_cast<float *>(base + off);
+  off = align_up(off + (size_t)nq * Hi * 4, 256);
+  w.qexp = reinterpret_cast<uint32_t *>(base + off);
+  off += (size_t)nq * Hi * 4;
   if (total) *total = off;
   return w;
 }
@@ -86,13 +93,16 @@ inline TcWs tc_ws_split(void *ws, uint32_t nq, uint32_t B, uint32_t Hi, uint32_t
 // builds them, the key histograms. With the FP4 QAT round
 // trip, units are always 8 dims (loaded one by one when `vec` is false) and
 // the Di / 8 lanes of a head row run the transform together.
-__global__ void index_qbf_kernel(IndexArgs a, TcWs w, bool clear_hist, uint32_t per, bool vec) {
+__global__ void index_qbf_kernel(IndexArgs a, TcWs w, bool clear_hist, bool vec) {
   pdl_wait();
   pdl_trigger();
+  // one thread per 8 dims: a head row of Di = 128 dims is an aligned group of
+  // 16 lanes
+  constexpr uint32_t per = 8;
   const uint32_t Hi = a.n_heads, Di = a.dim, n_nope = Di - a.rot;
   const uint32_t nq = a.batch * a.T;
-  const uint32_t upr = Di / per;                  // units (per dims each) per head row
-  const uint32_t n_units = nq * Hi * upr;
+  const uint32_t upr = Di / per;                  // lanes per head row
+  const uint32_t n_units = nq * Hi * upr;         // a multiple of 32
   const uint32_t i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i == 0) *w.err = 0;
   if (clear_hist && i < nq * (kHistBins / 4))
@@ -100,35 +110,26 @@ __global__ void index_qbf_kernel(IndexArgs a, TcWs w, bool clear_hist, uint32_t 
   if (i >= n_units) return;
   const uint32_t row = i / upr, c0 = (i - row * upr) * per;   // row = query * Hi + head
   const uint32_t p = seq_base(a.seq_pos, a.pos0, (row / Hi) / a.T) + (row / Hi) % a.T;
-  // rotate the pairs of w4 (dims c0, c0 + 1, ...) that lie in the tail
-  auto rot = [&](uint32_t *w4, uint32_t n) {
-    for (uint32_t e = 0; e < n; ++e) {
-      const uint32_t c = c0 + 2 * e;
-      if (c < n_nope) continue;
-      const float x0 = __uint_as_float(w4[e] << 16), x1 = __uint_as_float(w4[e] & 0xFFFF0000u);
-      const uint32_t fi = (c - n_nope) / 2;
-      const float co = a.cos[(size_t)p * (a.rot / 2) + fi];
-      const float si = a.sin[(size_t)p * (a.rot / 2) + fi];
-      const float r0 = __fsub_rn(__fmul_rn(x0, co), __fmul_rn(x1, si));
-      const float r1 = __fadd_rn(__fmul_rn(x0, si), __fmul_rn(x1, co));
-      const __nv_bfloat162 r = __floats2bfloat162_rn(r0, r1);
-      w4[e] = *reinterpret_cast<const uint32_t *>(&r);
-    }
-  };
-  if (a.qat) {   // uniform; per == 8, a head row is an aligned group of upr lanes
+  const uint32_t lane = threadIdx.x & 31;
+  // the 8 bf16 inputs as pairs (16-byte loads when aligned)
+  uint32_t w4[4];
+  if (vec) {
+    const uint4 q4 = reinterpret_cast<const uint4 *>(a.q_idx)[i];
+    w4[0] = q4.x;
+    w4[1] = q4.y;
+    w4[2] = q4.z;
+    w4[3] = q4.w;
+  } else {
+    const uint16_t *q = static_cast<const uint16_t *>(a.q_idx) + (size_t)i * per;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) w4[e] = (uint32_t)q[2 * e] | ((uint32_t)q[2 * e + 1] << 16);
+  }
+  if (a.qat) {   // uniform
     float v[8];
-    if (vec) {
-      const uint4 q4 = reinterpret_cast<const uint4 *>(a.q_idx)[i];
-      const uint32_t w4[4] = {q4.x, q4.y, q4.z, q4.w};
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        v[2 * e] = __uint_as_float(w4[e] << 16);
-        v[2 * e + 1] = __uint_as_float(w4[e] & 0xFFFF0000u);
-      }
-    } else {
-      const __nv_bfloat16 *q = static_cast<const __nv_bfloat16 *>(a.q_idx) + (size_t)i * 8;
-#pragma unroll
-      for (int e = 0; e < 8; ++e) v[e] = __bfloat162float(q[e]);
+    for (int e = 0; e < 4; ++e) {
+      v[2 * e] = __uint_as_float(w4[e] << 16);
+      v[2 * e + 1] = __uint_as_float(w4[e] & 0xFFFF0000u);
     }
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
@@ -141,25 +142,68 @@ __global__ void index_qbf_kernel(IndexArgs a, TcWs w, bool clear_hist, uint32_t 
       v[2 * e] = __fsub_rn(__fmul_rn(x0, co), __fmul_rn(x1, si));
       v[2 * e + 1] = __fadd_rn(__fmul_rn(x0, si), __fmul_rn(x1, co));
     }
-    const uint32_t lane = threadIdx.x & 31;
-    const uint32_t mask = upr == 32 ? 0xffffffffu : ((1u << upr) - 1u) << (lane & ~(upr - 1u));
+    const uint32_t mask = ((1u << upr) - 1u) << (lane & ~(upr - 1u));
     fp4_qat_lanes8(v, lane & (upr - 1u), upr, mask, a.had_c);
-    uint32_t o4[4];
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
       const __nv_bfloat162 r = __floats2bfloat162_rn(v[2 * e], v[2 * e + 1]);
-      o4[e] = *reinterpret_cast<const uint32_t *>(&r);
+      w4[e] = *reinterpret_cast<const uint32_t *>(&r);
     }
-    reinterpret_cast<uint4 *>(w.qbf)[i] = make_uint4(o4[0], o4[1], o4[2], o4[3]);
-  } else if (per == 8) {
-    const uint4 v = reinterpret_cast<const uint4 *>(a.q_idx)[i];
-    uint32_t w4[4] = {v.x, v.y, v.z, v.w};
-    if (c0 + 8 > n_nope) rot(w4, 4);
-    reinterpret_cast<uint4 *>(w.qbf)[i] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
-  } else {
-    uint32_t w1[1] = {reinterpret_cast<const uint32_t *>(a.q_idx)[i]};
-    rot(w1, 1);
-    reinterpret_cast<uint32_t *>(w.qbf)[i] = w1[0];
+  } else if (c0 + per > n_nope) {
+    // rotate the pairs that lie in the tail
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const uint32_t c = c0 + 2 * e;
+      if (c < n_nope) continue;
+      const float x0 = __uint_as_float(w4[e] << 16), x1 = __uint_as_float(w4[e] & 0xFFFF0000u);
+      const uint32_t fi = (c - n_nope) / 2;
+      const float co = a.cos[(size_t)p * (a.rot / 2) + fi];
+      const float si = a.sin[(size_t)p * (a.rot / 2) + fi];
+      const float r0 = __fsub_rn(__fmul_rn(x0, co), __fmul_rn(x1, si));
+      const float r1 = __fadd_rn(__fmul_rn(x0, si), __fmul_rn(x1, co));
+      const __nv_bfloat162 r = __floats2bfloat162_rn(r0, r1);
+      w4[e] = *reinterpret_cast<const uint32_t *>(&r);
+    }
+  }
+  reinterpret_cast<uint4 *>(w.qbf)[i] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+  // per head row of the stored q': an upper bound of its Euclidean norm (from
+  // squares scaled by 2^-e, e the exponent of its largest |value|, so tiny
+  // magnitudes do not underflow) and the exponent range of its nonzero
+  // entries, for the selection's error bound and exactness test
+  float x[8], mx = 0.f;
+  int emin = 1000, emax = -1000;
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    x[2 * e] = __uint_as_float(w4[e] << 16);
+    x[2 * e + 1] = __uint_as_float(w4[e] & 0xFFFF0000u);
+  }
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    mx = fmaxf(mx, fabsf(x[e]));
+    if (x[e] != 0.f) {
+      emin = min(emin, exp_of(x[e]));
+      emax = max(emax, exp_of(x[e]));
+    }
+  }
+#pragma unroll
+  for (uint32_t o = upr / 2; o > 0; o >>= 1) {   // within the 16-lane group
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    emin = min(emin, __shfl_xor_sync(0xffffffffu, emin, o));
+    emax = max(emax, __shfl_xor_sync(0xffffffffu, emax, o));
+  }
+  int eh = 0;
+  if (mx > 0.f) frexpf(mx, &eh);
+  float ss = 0.f;
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    const float y = ldexpf(x[e], -eh);
+    ss = fmaf(y, y, ss);
+  }
+#pragma unroll
+  for (uint32_t o = upr / 2; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+  if ((lane & (upr - 1u)) == 0) {
+    w.qnorm[row] = mx > 0.f ? norm_from_scaled(ss, eh) : 0.f;
+    w.qexp[row] = ((uint32_t)emin & 0xFFFFu) | ((uint32_t)emax << 16);
   }
 }
 
@@ -303,7 +347,6 @@ __global__ void __launch_bounds__(kSelectThreads)
 template <int NT>
 struct SelCfg {
   static constexpr int NW = NT / 32;                  // warps
-  static constexpr int HPW = 64 / NW;                 // q' heads per warp (A term)
   static constexpr int BPT = 4096 / NT;               // histogram bins per thread
   static constexpr int RPR = 2 * NW;                  // band rows per rescoring round
   static constexpr uint32_t CAP = NT == 1024 ? 4096u : 1536u;   // candidates in smem
@@ -386,52 +429,34 @@ __global__ void __launch_bounds__(NT, NT == 256 ? 4 : 1)
   const __nv_bfloat16 *qb = w.qbf + (size_t)qi * Hi * Di;
   const __nv_bfloat16 *wq = static_cast<const __nv_bfloat16 *>(a.w) + (size_t)qi * Hi;
 
-  // A = c * sum_h |w_h| ||q'_h|| (HPW heads per warp); q' rows to shared
-  // memory as fp32, with the exponent range of their nonzero entries
+  // A = c * sum_h |w_h| ||q'_h|| and the exponent range of the nonzero
+  // entries of q', from the per-head norms and ranges the query rotation
+  // wrote (warps 0 and 1, one head per lane); q' rows to shared memory
   if (threadIdx.x == 0) {
     s_qexp[0] = 1000;
     s_qexp[1] = -1000;
   }
   __syncthreads();
-  {
-    float part = 0.f, wabs = 0.f;
-    int emin = 1000, emax = -1000;
-#pragma unroll
-    for (uint32_t j = 0; j < (uint32_t)SC::HPW; ++j) {
-      const uint32_t h = warp + SC::NW * j;
-      const uint2 v = *reinterpret_cast<const uint2 *>(qb + (size_t)h * Di + 4 * lane);
-      const float x0 = __uint_as_float(v.x << 16), x1 = __uint_as_float(v.x & 0xFFFF0000u);
-      const float x2 = __uint_as_float(v.y << 16), x3 = __uint_as_float(v.y & 0xFFFF0000u);
-      *reinterpret_cast<uint2 *>(qsm + (size_t)h * kQB + 4 * lane) = v;
-      const float xx[4] = {x0, x1, x2, x3};
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        if (xx[e] != 0.f) {
-          emin = min(emin, exp_of(xx[e]));
-          emax = max(emax, exp_of(xx[e]));
-        }
-      }
-      // ||q'_h|| from power-of-two scaled squares (tiny magnitudes would
-      // underflow), an upper bound
-      const float mx = warp_max(fmaxf(fmaxf(fabsf(x0), fabsf(x1)), fmaxf(fabsf(x2), fabsf(x3))));
-      int eh = 0;
-      if (mx > 0.f) frexpf(mx, &eh);
-      const float y0 = ldexpf(x0, -eh), y1 = ldexpf(x1, -eh);
-      const float y2 = ldexpf(x2, -eh), y3 = ldexpf(x3, -eh);
-      const float ss = warp_sum(fmaf(y0, y0, fmaf(y1, y1, fmaf(y2, y2, y3 * y3))));
-      const float wa = fabsf(__bfloat162float(wq[h]));
-      part += wa * (mx > 0.f ? norm_from_scaled(ss, eh) : 0.f);
-      wabs += wa;
-    }
-    emin = warp_min_i(emin);
-    emax = warp_max_i(emax);
+  if (warp < 2) {
+    const uint32_t h = threadIdx.x;
+    const float wv = __bfloat162float(wq[h]), wa = fabsf(wv);
+    const uint32_t ex = w.qexp[(size_t)qi * Hi + h];
+    const float part = warp_sum(wa * w.qnorm[(size_t)qi * Hi + h]);
+    const float wabs = warp_sum(wa);
+    const int emin = warp_min_i((int)(int16_t)(ex & 0xFFFFu));
+    const int emax = warp_max_i((int)(int16_t)(ex >> 16));
     if (lane == 0) {
       s_red[warp] = part;
       s_wabs[warp] = wabs;
       atomicMin(&s_qexp[0], emin);
       atomicMax(&s_qexp[1], emax);
     }
-    if (threadIdx.x < Hi) wsh[threadIdx.x] = __bfloat162float(wq[threadIdx.x]);
+    wsh[h] = wv;
+  }
+  for (uint32_t i = threadIdx.x; i < Hi * (Di / 4); i += NT) {
+    const uint32_t h = i / (Di / 4), c = 4 * (i % (Di / 4));
+    *reinterpret_cast<uint2 *>(qsm + (size_t)h * kQB + c) =
+        *reinterpret_cast<const uint2 *>(qb + (size_t)h * Di + c);
   }
   // everything above read only what was written two or more launches back
   // (q', head weights, row norms); the scores and histograms need the scorer
@@ -497,7 +522,7 @@ __global__ void __launch_bounds__(NT, NT == 256 ? 4 : 1)
   }
   __syncthreads();
   float At = 0.f, Wt = 0.f;
-  for (uint32_t i = 0; i < (uint32_t)SC::NW; ++i) {
+  for (uint32_t i = 0; i < 2; ++i) {
     At += s_red[i];
     Wt += s_wabs[i];
   }
@@ -523,46 +548,72 @@ __global__ void __launch_bounds__(NT, NT == 256 ? 4 : 1)
   {
     const uint32_t per = ((vis + G * 32 - 1) / (G * 32)) * 32;
     const uint32_t r0 = g * per, r1 = min(vis, r0 + per);
-    constexpr uint32_t J = 4;
-    for (uint32_t pass = r0; pass < r1; pass += J * NT) {
-      float Sv[J], Nv[J];
+    // four consecutive rows per thread and step, two steps in flight; 16-byte
+    // loads where the four rows are whole and the norms 16-byte aligned (the
+    // score rows always are)
+    const bool v4 = nr_c != nullptr && (reinterpret_cast<uintptr_t>(nr_c) & 15u) == 0;
+    constexpr uint32_t J = 2;
+    uint32_t n_ge = 0;   // rows with S~ >= theta_S (one block per query)
+    for (uint32_t pass = r0; pass < r1; pass += J * 4 * NT) {
+      float Sv[J][4], Nv[J][4];
 #pragma unroll
       for (uint32_t j = 0; j < J; ++j) {
-        const uint32_t r = pass + j * NT + threadIdx.x;
-        Sv[j] = r < r1 ? sc[r] : 0.f;
-        Nv[j] = r < r1 ? (nr_c ? nr_c[r] : nr[a.map.row_of(b, r)]) : 0.f;
+        const uint32_t rb = pass + 4 * (j * NT + threadIdx.x);
+        if (v4 && rb + 4 <= r1) {
+          const float4 s4 = *reinterpret_cast<const float4 *>(sc + rb);
+          const float4 n4 = *reinterpret_cast<const float4 *>(nr_c + rb);
+          Sv[j][0] = s4.x;
+          Sv[j][1] = s4.y;
+          Sv[j][2] = s4.z;
+          Sv[j][3] = s4.w;
+          Nv[j][0] = n4.x;
+          Nv[j][1] = n4.y;
+          Nv[j][2] = n4.z;
+          Nv[j][3] = n4.w;
+        } else {
+#pragma unroll
+          for (uint32_t u = 0; u < 4; ++u) {
+            const uint32_t r = rb + u;
+            Sv[j][u] = r < r1 ? sc[r] : 0.f;
+            Nv[j][u] = r < r1 ? (nr_c ? nr_c[r] : nr[a.map.row_of(b, r)]) : 0.f;
+          }
+        }
       }
 #pragma unroll
       for (uint32_t j = 0; j < J; ++j) {
-        const uint32_t r = pass + j * NT + threadIdx.x;
-        const bool ok = r < r1;
-        const float S = Sv[j];
-        const float e = ok ? err_of(S, Nv[j]) : 0.f;
-        const bool c = ok && S + e >= theta;
-        if (G == 1) {
-          const uint32_t ge = __ballot_sync(0xffffffffu, ok && S >= theta_s);
-          if (lane == 0 && ge) atomicAdd(&s_misc[3], (uint32_t)__popc(ge));
-        }
-        const uint32_t bal = __ballot_sync(0xffffffffu, c);
-        if (bal) {
-          uint32_t slot = 0;
-          if (lane == 0)
-            slot = G > 1 ? atom_add_cluster(c_cnt, (uint32_t)__popc(bal))
-                         : atomicAdd(&s_misc[2], (uint32_t)__popc(bal));
-          slot = __shfl_sync(0xffffffffu, slot, 0) + __popc(bal & ((1u << lane) - 1u));
-          if (c && slot < CAP) {
-            if (G > 1) {
-              st_cluster_u32(c_idx + 4 * slot, r);
-              st_cluster_u32(c_S + 4 * slot, __float_as_uint(S));
-              st_cluster_u32(c_e + 4 * slot, __float_as_uint(e));
-            } else {
-              cidx[slot] = r;
-              cS[slot] = S;
-              ce[slot] = e;
+#pragma unroll
+        for (uint32_t u = 0; u < 4; ++u) {
+          const uint32_t r = pass + 4 * (j * NT + threadIdx.x) + u;
+          const bool ok = r < r1;
+          const float S = Sv[j][u];
+          const float e = ok ? err_of(S, Nv[j][u]) : 0.f;
+          const bool c = ok && S + e >= theta;
+          n_ge += (ok && S >= theta_s) ? 1u : 0u;
+          const uint32_t bal = __ballot_sync(0xffffffffu, c);
+          if (bal) {
+            uint32_t slot = 0;
+            if (lane == 0)
+              slot = G > 1 ? atom_add_cluster(c_cnt, (uint32_t)__popc(bal))
+                           : atomicAdd(&s_misc[2], (uint32_t)__popc(bal));
+            slot = __shfl_sync(0xffffffffu, slot, 0) + __popc(bal & ((1u << lane) - 1u));
+            if (c && slot < CAP) {
+              if (G > 1) {
+                st_cluster_u32(c_idx + 4 * slot, r);
+                st_cluster_u32(c_S + 4 * slot, __float_as_uint(S));
+                st_cluster_u32(c_e + 4 * slot, __float_as_uint(e));
+              } else {
+                cidx[slot] = r;
+                cS[slot] = S;
+                ce[slot] = e;
+              }
             }
           }
         }
       }
+    }
+    if (G == 1) {
+      n_ge = warp_sum_u32(n_ge);
+      if (lane == 0 && n_ge) atomicAdd(&s_misc[3], n_ge);
     }
   }
   if (G > 1) {
@@ -818,10 +869,10 @@ inline double gamma_n(double n) {
 cudaError_t launch_index_tc(const IndexArgs &a, cudaStream_t s) {
   const uint32_t nq = a.batch * a.T;
   TcWs w = tc_ws_split(a.ws, nq, a.batch, a.n_heads, a.dim, a.comp_cap, nullptr);
-  // q' in 16-byte units of 8 dims (4-byte pairs when the query is not
-  // 16-byte aligned)
-  const bool vec = reinterpret_cast<uintptr_t>(a.q_idx) % 16 == 0 && a.dim % 8 == 0;
-  const uint32_t per = vec || a.qat ? 8u : 2u;
+  // q' in units of 8 dims (one 16-byte load each when the query is 16-byte
+  // aligned, else eight 2-byte loads)
+  const bool vec = reinterpret_cast<uintptr_t>(a.q_idx) % 16 == 0;
+  const uint32_t per = 8;
   if ((size_t)nq * a.n_heads * a.dim >= (1ull << 31)) return cudaErrorInvalidValue;
   // the scorer builds key histograms when several select blocks share a
   // query; with one block per query the selection samples its threshold
@@ -830,7 +881,7 @@ cudaError_t launch_index_tc(const IndexArgs &a, cudaStream_t s) {
   if (scorer_hist && (size_t)nq * (kHistBins / 4) > nthreads) nthreads = (size_t)nq * (kHistBins / 4);
   if (nthreads == 0) nthreads = 1;
   cudaError_t eq = launch_pdl(index_qbf_kernel, dim3((unsigned)((nthreads + 255) / 256)),
-                              dim3(256), 0, s, a, w, scorer_hist, per, vec);
+                              dim3(256), 0, s, a, w, scorer_hist, vec);
   if (eq != cudaSuccess) return eq;
   note_launches(1);
   const uint32_t vis_max = min((a.pos0 + a.T) / 4, a.n_comp);

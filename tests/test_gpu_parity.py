@@ -220,6 +220,32 @@ def run_index(lib, shape, B, p0, T, seed=11, grid=False, queries=None):
     return got
 
 
+def test_index_tc_query_unaligned():
+    """bf16 indexer with q_idx at a 2-byte offset (not 16-byte aligned): the
+    query rotation loads element by element; the lists must equal the
+    oracle's, at one decode token and across a chunk whose tail queries see
+    rows past the first 4 k."""
+    lib = lib_()
+    shape = synth.LayerShape(ratio=4)
+    for B, p0, T in ((3, 6000, 1), (1, 4000, 9)):
+        wl = synth.Workload("qun16", 26, B, (shape,), p0 + T, "prefill")
+        cap = (p0 + T) // 4 + 1
+        hist = synth.cache_history(wl, 0, p0 + T, comp_cap=cap)
+        q_idx = synth.normal((B, T, 64, 128), 26, "q", dtype="bf16")
+        w = synth.normal((B, T, 64), 26, "w", dtype="bf16")
+        buf = torch.empty(q_idx.numel() + 1, dtype=torch.bfloat16, device=DEV)
+        qd = buf[1:].view(q_idx.shape)
+        qd.copy_(q_idx.to(DEV))
+        assert qd.data_ptr() % 16 != 0
+        gc = gpu_cache(shape, B, cap, p0 + T + 1, hist, p0 + T)
+        topk = torch.empty((B, T, 512), dtype=torch.int32, device=DEV)
+        ws = lib.workspace(gc.workspace_bytes(lib.CALL_INDEX_TOPK, T, 64, 512))
+        lib.ds4a_index_topk(gc, p0, T, qd, w.to(DEV), 64, 512, topk, ws)
+        torch.cuda.synchronize()
+        ref = olayer.index_topk(oracle_cache(shape, hist, p0 + T), p0, np_(q_idx), np_(w), 512)
+        assert np.array_equal(topk.cpu().numpy(), ref), (B, p0, T)
+
+
 @pytest.mark.parametrize("q_exp,k_exp", [(-70, -60), (-100, -40)])
 def test_index_tc_tiny_magnitudes(q_exp, k_exp):
     """bf16 indexer with query and key entries near the bottom of the fp32
