@@ -23,6 +23,9 @@
 // down, still freeing its TMEM.
 #include <cuda_bf16.h>
 
+#include <algorithm>
+#include <vector>
+
 #include "common.cuh"
 #include "tc.cuh"
 
@@ -52,9 +55,16 @@ struct Cfg {
                                   kEpiWarps * QG * kHeads * 4 + kHistBytes;
 };
 
+constexpr uint32_t kMaxSplit = 256;   // CTAs of a range table (more: the even item split)
+
 struct ScoreParams {
   uint32_t batch, T, pos0, comp_cap, n_comp, n_groups, tiles_per, total_items;
   uint32_t cta_per_group;   // > 0: that many CTAs per (sequence, group), none crossing one
+  // split > 0: CTA j takes the items it_start[j] .. it_start[j + 1] - 1, an even
+  // share of the visible tiles (computed on the host when every sequence
+  // starts at pos0)
+  uint32_t split;
+  uint32_t it_start[kMaxSplit + 1];
   RowMap map;               // paged keys (map.table != NULL): 64-row blocks of the pool
   const uint32_t *seq_pos;  // [B] per-sequence positions (ragged decode) or NULL
   const __nv_bfloat16 *w;   // [B][T][Hi]
@@ -177,6 +187,9 @@ __global__ void __launch_bounds__(Cfg<QG>::kThreads, 1)
         min(P.tiles_per, (vis_of(P, bg / P.n_groups, last) + kRows - 1) / kRows);
     it0 = bg * P.tiles_per + j * nt / P.cta_per_group;
     it1 = bg * P.tiles_per + (j + 1) * nt / P.cta_per_group;
+  } else if (P.split) {
+    it0 = P.it_start[blockIdx.x];
+    it1 = P.it_start[blockIdx.x + 1];
   } else {
     const uint32_t per = (P.total_items + gridDim.x - 1) / gridDim.x;
     it0 = min(P.total_items, blockIdx.x * per);
@@ -485,6 +498,7 @@ cudaError_t launch_qg(const IndexTcArgs &a, cudaStream_t s) {
   const uint32_t sms = (uint32_t)num_sms(), n_bg = a.batch * P.n_groups;
   uint32_t grid = min(P.total_items, sms);
   P.cta_per_group = 0;
+  P.split = 0;
   if (n_bg <= sms) {
     const uint32_t cpg = sms / n_bg;
     const uint32_t max_contig = (P.total_items + grid - 1) / grid;
@@ -492,6 +506,33 @@ cudaError_t launch_qg(const IndexTcArgs &a, cudaStream_t s) {
       P.cta_per_group = cpg;
       grid = n_bg * cpg;
     }
+  }
+  if (!P.cta_per_group && !a.seq_pos && grid <= kMaxSplit) {
+    // a chunk's later queries see more rows: split the visible tiles, not
+    // the items, evenly (every sequence has the same visible tiles per group)
+    std::vector<uint32_t> tg(P.n_groups);
+    uint64_t vb = 0;
+    for (uint32_t g = 0; g < P.n_groups; ++g) {
+      const uint32_t last = std::min(a.T, (g + 1) * QG) - 1;
+      const uint32_t vis = std::min((a.pos0 + last + 1) / 4, a.n_comp);
+      tg[g] = std::min(P.tiles_per, (vis + kRows - 1) / kRows);
+      vb += tg[g];
+    }
+    const uint64_t V = vb * a.batch;
+    uint32_t j = 1;
+    uint64_t cum = 0;
+    P.it_start[0] = 0;
+    for (uint32_t b = 0; b < a.batch && j < grid; ++b)
+      for (uint32_t g = 0; g < P.n_groups && j < grid; ++g) {
+        const uint32_t n = tg[g];
+        while (j < grid && (uint64_t)j * V / grid < cum + n) {
+          P.it_start[j] = (b * P.n_groups + g) * P.tiles_per + (uint32_t)((uint64_t)j * V / grid - cum);
+          ++j;
+        }
+        cum += n;
+      }
+    for (; j <= grid; ++j) P.it_start[j] = P.total_items;
+    P.split = 1;
   }
   e = launch_pdl(index_score_tc_kernel<QG>, dim3(grid), dim3(C::kThreads), C::kSmem, s, tk, tq, P);
   if (e != cudaSuccess) return e;
