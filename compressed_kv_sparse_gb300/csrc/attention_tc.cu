@@ -753,29 +753,37 @@ __global__ void __launch_bounds__(kThreads, 1)
         // normalise, rotate the tail back by -p, stage [NH heads][128 dims]
         // bf16 in the P buffer, then write 16-byte row segments
         uint8_t *stage = S.p;
+        float li[NH];   // 1 / L per head, for the four chunks
+#pragma unroll
+        for (int h = 0; h < NH; ++h) li[h] = S.linv[h];
+        const bool odd = lane & 1;
 #pragma unroll 1
         for (uint32_t m = 0; m < 4; ++m) {
-          const uint32_t d = m * 128 + r;
-          const float co = ep_co, si = ep_si;   // used by the tail dims only (m = 3)
-#pragma unroll 1
+          const bool rot = m == 3 && r >= 64;   // warp-uniform: the rotated tail dims
+          const float co = ep_co, si = ep_si;   // (the pair's coefficients: both lanes)
+          uint32_t ab[NHF][32];
+#pragma unroll
+          for (uint32_t hf = 0; hf < (uint32_t)NHF; ++hf)
+            tmem_ld32(tmO + lane_base + m * kH + 32 * hf, ab[hf]);
+          tmem_ld_wait();
+#pragma unroll
           for (uint32_t hf = 0; hf < (uint32_t)NHF; ++hf) {
-            uint32_t a[32];
-            tmem_ld32(tmO + lane_base + m * kH + 32 * hf, a);
-            tmem_ld_wait();
-            __nv_bfloat16 *srow = reinterpret_cast<__nv_bfloat16 *>(stage) + (32 * hf) * 128 + r;
-            if (m == 3 && r >= 64) {   // warp-uniform: the rotated tail dims
 #pragma unroll
-              for (int h = 0; h < 32; ++h) {
-                float v = __uint_as_float(a[h]) * S.linv[32 * hf + h];
-                const float other = __shfl_xor_sync(0xffffffffu, v, 1);
-                // (x0, x1) -> (x0 c + x1 s, -x0 s + x1 c)
-                v = (d & 1) ? (v * co - other * si) : (v * co + other * si);
-                srow[h * 128] = __float2bfloat16_rn(v);
+            for (int h = 0; h < 32; h += 2) {
+              const float v0 = __uint_as_float(ab[hf][h]) * li[32 * hf + h];
+              const float v1 = __uint_as_float(ab[hf][h + 1]) * li[32 * hf + h + 1];
+              // lanes 2i, 2i + 1 hold dims d, d + 1 of heads h, h + 1: one
+              // swap gives the even lane head h's pair and the odd lane head
+              // h + 1's, rotated in place and stored as one bf16 pair
+              const float recv = __shfl_xor_sync(0xffffffffu, odd ? v0 : v1, 1);
+              float x0 = odd ? recv : v0, x1 = odd ? v1 : recv;
+              if (rot) {   // (x0, x1) -> (x0 c + x1 s, -x0 s + x1 c)
+                const float y0 = x0 * co + x1 * si, y1 = -x0 * si + x1 * co;
+                x0 = y0;
+                x1 = y1;
               }
-            } else {
-#pragma unroll
-              for (int h = 0; h < 32; ++h)
-                srow[h * 128] = __float2bfloat16_rn(__uint_as_float(a[h]) * S.linv[32 * hf + h]);
+              const uint32_t row = 32 * hf + h + (odd ? 1u : 0u);
+              *reinterpret_cast<uint32_t *>(stage + row * 256 + (r & ~1u) * 2) = pack_bf16(x0, x1);
             }
           }
           if (!group_sync(&S.sm_bar, sm_phase, ew)) goto done_softmax;
