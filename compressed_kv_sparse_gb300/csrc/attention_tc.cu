@@ -750,9 +750,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (r == 0) S.has_tiles = has_tiles ? 1u : 0u;
       } else {
-        // normalise, rotate the tail back by -p, stage [NH heads][128 dims]
-        // bf16 in the P buffer, then write 16-byte row segments
-        uint8_t *stage = S.p;
+        // normalise, rotate the tail back by -p and store bf16 pairs straight
+        // from registers, four 128-dim chunks (no staging, no barrier)
         float li[NH];   // 1 / L per head, for the four chunks
 #pragma unroll
         for (int h = 0; h < NH; ++h) li[h] = S.linv[h];
@@ -761,6 +760,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (uint32_t m = 0; m < 4; ++m) {
           const bool rot = m == 3 && r >= 64;   // warp-uniform: the rotated tail dims
           const float co = ep_co, si = ep_si;   // (the pair's coefficients: both lanes)
+          __nv_bfloat16 *o = P.out + ((size_t)qi * kH + hq0) * kD + m * 128;
           uint32_t ab[NHF][32];
 #pragma unroll
           for (uint32_t hf = 0; hf < (uint32_t)NHF; ++hf)
@@ -783,18 +783,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 x1 = y1;
               }
               const uint32_t row = 32 * hf + h + (odd ? 1u : 0u);
-              *reinterpret_cast<uint32_t *>(stage + row * 256 + (r & ~1u) * 2) = pack_bf16(x0, x1);
+              *reinterpret_cast<uint32_t *>(o + (size_t)row * kD + (r & ~1u)) = pack_bf16(x0, x1);
             }
           }
-          if (!group_sync(&S.sm_bar, sm_phase, ew)) goto done_softmax;
-          __nv_bfloat16 *o = P.out + ((size_t)qi * kH + hq0) * kD + m * 128;
-#pragma unroll
-          for (uint32_t i = 0; i < (uint32_t)NH / 8; ++i) {
-            const uint32_t c = r + 128 * i, h = c >> 4, seg = c & 15;
-            *reinterpret_cast<uint4 *>(o + (size_t)h * kD + seg * 8) =
-                *reinterpret_cast<const uint4 *>(stage + h * 256 + seg * 16);
-          }
-          if (!group_sync(&S.sm_bar, sm_phase, ew)) goto done_softmax;
         }
       }
       if (has_tiles) {
