@@ -419,13 +419,16 @@ __global__ void __launch_bounds__(Cfg<QG>::kThreads, 1)
         // approximate score: any summation order is covered by the error
         // bound, so eight independent chains (as four packed pairs) and
         // vector loads of the weights
-        const float4 *wq4 = reinterpret_cast<const float4 *>(sw + q * kHeads);
+        const uint32_t wq_s = smem_u32(sw + q * kHeads);   // (explicit shared loads)
         float acc8[8];
 #pragma unroll
         for (int j = 0; j < 8; ++j) acc8[j] = 0.f;
 #pragma unroll
         for (int h4 = 0; h4 < 16; ++h4) {
-          const float4 w4 = wq4[h4];
+          float4 w4;
+          asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                       : "=f"(w4.x), "=f"(w4.y), "=f"(w4.z), "=f"(w4.w)
+                       : "r"(wq_s + 16u * h4));
           const uint32_t *rr = h4 < 8 ? r0 : r1;
           const int hb = (h4 & 7) * 4, c = (2 * h4) & 7;
           ffma2(acc8[c], acc8[c + 1], w4.x, w4.y, fmaxf(__uint_as_float(rr[hb + 0]), 0.f),
