@@ -453,11 +453,15 @@ __global__ void __launch_bounds__(NT, NT == 256 ? 4 : 1)
     }
     wsh[h] = wv;
   }
+  // (asynchronous: the rows are first read by the rescoring, after the
+  // waits at the start of the selection)
   for (uint32_t i = threadIdx.x; i < Hi * (Di / 4); i += NT) {
     const uint32_t h = i / (Di / 4), c = 4 * (i % (Di / 4));
-    *reinterpret_cast<uint2 *>(qsm + (size_t)h * kQB + c) =
-        *reinterpret_cast<const uint2 *>(qb + (size_t)h * Di + c);
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(smem_u32(qsm + (size_t)h * kQB + c)),
+                 "l"(qb + (size_t)h * Di + c)
+                 : "memory");
   }
+  asm volatile("cp.async.commit_group;" ::: "memory");
   // everything above read only what was written two or more launches back
   // (q', head weights, row norms); the scores and histograms need the scorer
   pdl_wait();
@@ -544,39 +548,30 @@ __global__ void __launch_bounds__(NT, NT == 256 ? 4 : 1)
   if (G > 1) cluster_wait();
   const uint32_t c_cnt = mapa_shared(smem_u32(&s_misc[2]), 0);
   const uint32_t c_idx = mapa_shared(smem_u32(cidx), 0), c_S = mapa_shared(smem_u32(cS), 0);
-  const uint32_t c_e = mapa_shared(smem_u32(ce), 0);
   {
     const uint32_t per = ((vis + G * 32 - 1) / (G * 32)) * 32;
     const uint32_t r0 = g * per, r1 = min(vis, r0 + per);
-    // four consecutive rows per thread and step, two steps in flight; 16-byte
-    // loads where the four rows are whole and the norms 16-byte aligned (the
-    // score rows always are)
-    const bool v4 = nr_c != nullptr && (reinterpret_cast<uintptr_t>(nr_c) & 15u) == 0;
-    constexpr uint32_t J = 2;
+    // four consecutive rows per thread and step (one 16-byte load where the
+    // four are whole: the score rows are 16-byte aligned), three steps in
+    // flight. The test bounds each row's error with the largest row norm (a
+    // superset of the rows with U >= theta, no norm loads); the candidates'
+    // own bounds follow from their norms below.
+    constexpr uint32_t J = 3;
     uint32_t n_ge = 0;   // rows with S~ >= theta_S (one block per query)
     for (uint32_t pass = r0; pass < r1; pass += J * 4 * NT) {
-      float Sv[J][4], Nv[J][4];
+      float Sv[J][4];
 #pragma unroll
       for (uint32_t j = 0; j < J; ++j) {
         const uint32_t rb = pass + 4 * (j * NT + threadIdx.x);
-        if (v4 && rb + 4 <= r1) {
+        if (rb + 4 <= r1) {
           const float4 s4 = *reinterpret_cast<const float4 *>(sc + rb);
-          const float4 n4 = *reinterpret_cast<const float4 *>(nr_c + rb);
           Sv[j][0] = s4.x;
           Sv[j][1] = s4.y;
           Sv[j][2] = s4.z;
           Sv[j][3] = s4.w;
-          Nv[j][0] = n4.x;
-          Nv[j][1] = n4.y;
-          Nv[j][2] = n4.z;
-          Nv[j][3] = n4.w;
         } else {
 #pragma unroll
-          for (uint32_t u = 0; u < 4; ++u) {
-            const uint32_t r = rb + u;
-            Sv[j][u] = r < r1 ? sc[r] : 0.f;
-            Nv[j][u] = r < r1 ? (nr_c ? nr_c[r] : nr[a.map.row_of(b, r)]) : 0.f;
-          }
+          for (uint32_t u = 0; u < 4; ++u) Sv[j][u] = rb + u < r1 ? sc[rb + u] : 0.f;
         }
       }
 #pragma unroll
@@ -586,8 +581,7 @@ __global__ void __launch_bounds__(NT, NT == 256 ? 4 : 1)
           const uint32_t r = pass + 4 * (j * NT + threadIdx.x) + u;
           const bool ok = r < r1;
           const float S = Sv[j][u];
-          const float e = ok ? err_of(S, Nv[j][u]) : 0.f;
-          const bool c = ok && S + e >= theta;
+          const bool c = ok && S + (E + fabsf(S) * kRel) >= theta;
           n_ge += (ok && S >= theta_s) ? 1u : 0u;
           const uint32_t bal = __ballot_sync(0xffffffffu, c);
           if (bal) {
@@ -600,11 +594,9 @@ __global__ void __launch_bounds__(NT, NT == 256 ? 4 : 1)
               if (G > 1) {
                 st_cluster_u32(c_idx + 4 * slot, r);
                 st_cluster_u32(c_S + 4 * slot, __float_as_uint(S));
-                st_cluster_u32(c_e + 4 * slot, __float_as_uint(e));
               } else {
                 cidx[slot] = r;
                 cS[slot] = S;
-                ce[slot] = e;
               }
             }
           }
@@ -630,7 +622,14 @@ __global__ void __launch_bounds__(NT, NT == 256 ? 4 : 1)
   const uint32_t nc = s_misc[2];
   const bool fast = nc <= CAP && (G == 1 ? s_misc[3] >= k : true);
   uint32_t need;
+  asm volatile("cp.async.wait_all;" ::: "memory");   // (this thread's q' rows)
   if (fast) {
+    // each candidate's own error bound, from its row norm (read by the
+    // classification, several barriers on)
+    for (uint32_t j = threadIdx.x; j < nc; j += blockDim.x) {
+      const uint32_t r = cidx[j];
+      ce[j] = err_of(cS[j], nr_c ? nr_c[r] : nr[a.map.row_of(b, r)]);
+    }
     // ---- certified selection on the candidates
     if (threadIdx.x == 0) s_misc[5] = 0u;
     __syncthreads();
