@@ -516,8 +516,10 @@ __global__ void __launch_bounds__(NT, NT == 256 ? 4 : 1)
     // exact count rarely sends the block to the full pass)
     const uint32_t rs = min(ns, ((k + stride - 1) / stride) * 8 / 5 + 8);
     uint32_t need_s;
+    // (three digits: the lower edge of the 24-bit key bin of that value,
+    // a relative 2^-15 below it at most)
     theta_s = key_to_float(radix_kth([&](uint32_t j) { return score_key(smp[j]); }, ns, rs,
-                                     hist, sel, &need_s));
+                                     hist, sel, &need_s, 8));
   }
   if (scorer_err) {   // no scores: no list
     if (g == 0)

@@ -57,11 +57,14 @@ __device__ __forceinline__ uint32_t block_flag_scan(bool flag, uint32_t *wsum,
 
 // k-th largest of key(s), s < n, by an 8-bit radix select. Returns the key
 // and, in *need, how many rows with exactly that key belong to the top k.
+// With last_shift = 8 or 16 it stops after three or two digits and returns
+// the lowest key with the k-th largest key's top 24 or 16 bits (at least k
+// keys are >= it).
 template <typename KeyF>
 __device__ uint32_t radix_kth(KeyF key, uint32_t n, uint32_t k, uint32_t *hist, uint32_t *sel,
-                              uint32_t *need_out) {
+                              uint32_t *need_out, int last_shift = 0) {
   uint32_t prefix = 0, mask = 0, need = k;
-  for (int shift = 24; shift >= 0; shift -= 8) {
+  for (int shift = 24; shift >= last_shift; shift -= 8) {
     for (uint32_t i = threadIdx.x; i < 256; i += blockDim.x) hist[i] = 0;
     __syncthreads();
     // warp-aggregated: lanes with the same digit add once (keys of similar
@@ -283,8 +286,9 @@ __device__ __forceinline__ void band_dots(const uint2 *q2, const float4 *k4, boo
                                           float (&acc)[RPP]) {
 #pragma unroll
   for (int rr = 0; rr < RPP; ++rr) acc[rr] = 0.f;
+  constexpr int kUnroll = RPP >= 4 ? 2 : 4;
   if (exact) {
-#pragma unroll 4
+#pragma unroll kUnroll
     for (uint32_t c = 0; c < 32; ++c) {
       float q0, q1, q2v, q3;
       bf16x4(q2[c], q0, q1, q2v, q3);
@@ -317,10 +321,11 @@ __device__ __forceinline__ void band_dots(const uint2 *q2, const float4 *k4, boo
 // Exact recipe for the band rows (whole block, NW warps), in rounds of 2 NW
 // rows: every key row of the round is loaded first (two per warp, both loads
 // in flight before either converts) as fp32 into `kbuf` [2 NW][128], with the
-// row's exponent range; then thread t takes head t % 64 of the row pair
-// t / 64 (one q' load serves both rows, and every lane of a warp reads the
-// same keys) and writes both ReLU dots to `relb` [2 NW][64]; then one thread
-// per row sums w_h ReLU(dot_h) in ascending h. Results replace cS[band[i]].
+// row's exponent range; then thread t takes head t % 64 of the row group
+// t / 64 (two rows with 1024 threads, four with 256: one q' load serves the
+// group, and every lane of a warp reads the same keys) and writes their ReLU
+// dots to `relb` [2 NW][64]; then one thread per row sums w_h ReLU(dot_h) in
+// ascending h. Results replace cS[band[i]].
 template <int NW>
 __device__ __forceinline__ void rescore_band(const __nv_bfloat16 *qsm, const float *wsh,
                                              float *kbuf, float *relb, const uint32_t *band,
@@ -354,19 +359,25 @@ __device__ __forceinline__ void rescore_band(const __nv_bfloat16 *qsm, const flo
       }
     }
     __syncthreads();
-    // (row pair, head): rows 2 rp and 2 rp + 1 of the round against head h
-    const uint32_t n_pairs = (nr + 1) / 2;
-    for (uint32_t it = threadIdx.x; it < n_pairs * 64; it += NT) {
-      const uint32_t rp = it >> 6, h = it & 63, r0 = 2 * rp;
+    // (row group, head): rows RPP g .. RPP g + RPP - 1 of the round against
+    // head h (RPP = 4 where that leaves one item per thread: four
+    // independent chains instead of two items in turn)
+    constexpr uint32_t RPP = NT >= 1024 ? 2 : 4;
+    const uint32_t n_grp = (nr + RPP - 1) / RPP;
+    for (uint32_t it = threadIdx.x; it < n_grp * 64; it += NT) {
+      const uint32_t rp = it >> 6, h = it & 63, r0 = RPP * rp;
       const uint2 *q2 = reinterpret_cast<const uint2 *>(qsm + (size_t)h * kQB);
       const float4 *k4 = reinterpret_cast<const float4 *>(kbuf + r0 * 128);
-      // (a lone last row reads the next row's stale keys: never stored)
-      const bool two = r0 + 1 < nr;
-      const bool exact = rexact[r0] != 0u && (!two || rexact[r0 + 1] != 0u);
-      float acc[2];
-      band_dots<2>(q2, k4, exact, acc);
-      relb[r0 * 64 + h] = acc[0] > 0.f ? acc[0] : 0.f;
-      if (two) relb[(r0 + 1) * 64 + h] = acc[1] > 0.f ? acc[1] : 0.f;
+      // (rows past the round's last read stale keys: never stored)
+      const uint32_t nv = min(RPP, nr - r0);
+      bool exact = true;
+#pragma unroll
+      for (uint32_t rr = 0; rr < RPP; ++rr) exact = exact && (rr >= nv || rexact[r0 + rr] != 0u);
+      float acc[RPP];
+      band_dots<RPP>(q2, k4, exact, acc);
+#pragma unroll
+      for (uint32_t rr = 0; rr < RPP; ++rr)
+        if (rr < nv) relb[(r0 + rr) * 64 + h] = acc[rr] > 0.f ? acc[rr] : 0.f;
     }
     __syncthreads();
     if (threadIdx.x < nr) {
