@@ -129,6 +129,11 @@ struct QueryGeo {
   const int32_t *tk;
 };
 
+// SCAN: read the list for its end (prefill: a chunk query's list may hold
+// rows past its visible ones). A decode list holds visible rows, then -1, so
+// decode takes the bound min(top_k, visible) and masks the -1 entries row by
+// row, with no dependent list read before the first gather.
+template <bool SCAN>
 __device__ __forceinline__ QueryGeo query_geo(const TcAttnParams &P, uint32_t qi, uint32_t t0,
                                               uint32_t ts, uint32_t lane) {
   QueryGeo g;
@@ -139,7 +144,9 @@ __device__ __forceinline__ QueryGeo query_geo(const TcAttnParams &P, uint32_t qi
   g.n_w = min(g.p + 1, P.cap_raw);
   g.tk = P.topk ? P.topk + (size_t)qi * P.top_k : nullptr;
   g.n_list = 0;
-  if (P.ratio == 4) {
+  if (P.ratio == 4 && !SCAN) {
+    g.n_list = min(P.top_k, min((g.p + 1) / 4, P.n_comp));
+  } else if (P.ratio == 4) {
     const uint32_t vis = min((g.p + 1) / 4, P.n_comp);
     // the list ends at its first entry >= vis; 16 independent loads per round
     g.n_list = P.top_k;
@@ -461,7 +468,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             si[4 * i + e] = P.sin[(size_t)pq * 32 + 4 * lc + e];
           }
         }
-        const QueryGeo g = query_geo(P, qi, rank, C, lane);
+        const QueryGeo g = query_geo<!DEC>(P, qi, rank, C, lane);
         if (g.t0 >= g.t1) {          // the list is shorter than the bound: nothing to do
           // (Q still lands: wait for it so the buffer is never written twice at once)
           if (!mbar_wait_warp(&S.q_tma, qt & 1, ew)) goto done_loader;
@@ -517,7 +524,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     for (uint32_t qi = q_first; qi < P.n_q && ok; qi += q_step) {
       if (rank * kRows >= rows_bound(P, qi)) continue;
-      const QueryGeo g = query_geo(P, qi, rank, C, lane);
+      const QueryGeo g = query_geo<!DEC>(P, qi, rank, C, lane);
       if (g.t0 >= g.t1) continue;
       if (lane == 0) {
         ok = mbar_wait(&S.q_full, qn & 1, ew);
@@ -602,7 +609,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (uint32_t qi = q_first; qi < P.n_q; qi += q_step) {
       const bool maybe = rank * kRows < rows_bound(P, qi);
       QueryGeo g = {};
-      if (maybe) g = query_geo(P, qi, rank, C, lane);
+      if (maybe) g = query_geo<!DEC>(P, qi, rank, C, lane);
       const bool has_tiles = maybe && g.t0 < g.t1;
       bool any_valid = false;
       // the rotation coefficients of this thread's tail dim in the direct
