@@ -191,13 +191,27 @@ __global__ void index_qbf_kernel(IndexArgs a, TcWs w, bool clear_hist, bool vec)
     emin = min(emin, __shfl_xor_sync(0xffffffffu, emin, o));
     emax = max(emax, __shfl_xor_sync(0xffffffffu, emax, o));
   }
+  // mx = f 2^eh with f in [0.5, 1); scaling by 2^-eh is one multiply,
+  // rounded like ldexpf, while 2^-eh is a normal fp32 value (biased exponent
+  // of mx in 1 .. 252), else ldexpf
   int eh = 0;
-  if (mx > 0.f) frexpf(mx, &eh);
   float ss = 0.f;
+  const uint32_t mb = __float_as_uint(mx) >> 23;   // biased exponent (mx >= 0)
+  if (mb >= 1u && mb <= 252u) {
+    eh = (int)mb - 126;
+    const float sc = __uint_as_float((uint32_t)(127 - eh) << 23);
 #pragma unroll
-  for (int e = 0; e < 8; ++e) {
-    const float y = ldexpf(x[e], -eh);
-    ss = fmaf(y, y, ss);
+    for (int e = 0; e < 8; ++e) {
+      const float y = x[e] * sc;
+      ss = fmaf(y, y, ss);
+    }
+  } else if (mx > 0.f) {
+    frexpf(mx, &eh);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const float y = ldexpf(x[e], -eh);
+      ss = fmaf(y, y, ss);
+    }
   }
 #pragma unroll
   for (uint32_t o = upr / 2; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
