@@ -607,7 +607,7 @@ __global__ void __launch_bounds__(NT, NT == 256 ? 4 : 1)
                            : atomicAdd(&s_misc[2], (uint32_t)__popc(bal));
             slot = __shfl_sync(0xffffffffu, slot, 0) + __popc(bal & ((1u << lane) - 1u));
             if (c && slot < CAP) {
-              if (G > 1) {
+              if (NT == 1024) {   // (only this width runs several blocks per query)
                 st_cluster_u32(c_idx + 4 * slot, r);
                 st_cluster_u32(c_S + 4 * slot, __float_as_uint(S));
               } else {
