@@ -170,8 +170,9 @@ __global__ void index_qbf_kernel(IndexArgs a, TcWs w, bool clear_hist, bool vec)
   // squares scaled by 2^-e, e the exponent of its largest |value|, so tiny
   // magnitudes do not underflow) and the exponent range of its nonzero
   // entries, for the selection's error bound and exactness test
-  float x[8], mx = 0.f;
-  int emin = 1000, emax = -1000;
+  // (the exponent range is that of the smallest nonzero and the largest
+  // magnitude: the exponent grows with the magnitude)
+  float x[8], mx = 0.f, mn = INFINITY;
 #pragma unroll
   for (int e = 0; e < 4; ++e) {
     x[2 * e] = __uint_as_float(w4[e] << 16);
@@ -179,17 +180,14 @@ __global__ void index_qbf_kernel(IndexArgs a, TcWs w, bool clear_hist, bool vec)
   }
 #pragma unroll
   for (int e = 0; e < 8; ++e) {
-    mx = fmaxf(mx, fabsf(x[e]));
-    if (x[e] != 0.f) {
-      emin = min(emin, exp_of(x[e]));
-      emax = max(emax, exp_of(x[e]));
-    }
+    const float ax = fabsf(x[e]);
+    mx = fmaxf(mx, ax);
+    mn = fminf(mn, ax > 0.f ? ax : INFINITY);
   }
 #pragma unroll
   for (uint32_t o = upr / 2; o > 0; o >>= 1) {   // within the 16-lane group
     mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-    emin = min(emin, __shfl_xor_sync(0xffffffffu, emin, o));
-    emax = max(emax, __shfl_xor_sync(0xffffffffu, emax, o));
+    mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
   }
   // mx = f 2^eh with f in [0.5, 1); scaling by 2^-eh is one multiply,
   // rounded like ldexpf, while 2^-eh is a normal fp32 value (biased exponent
@@ -216,6 +214,7 @@ __global__ void index_qbf_kernel(IndexArgs a, TcWs w, bool clear_hist, bool vec)
 #pragma unroll
   for (uint32_t o = upr / 2; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
   if ((lane & (upr - 1u)) == 0) {
+    const int emin = mx > 0.f ? exp_of(mn) : 1000, emax = mx > 0.f ? exp_of(mx) : -1000;
     w.qnorm[row] = mx > 0.f ? norm_from_scaled(ss, eh) : 0.f;
     w.qexp[row] = ((uint32_t)emin & 0xFFFFu) | ((uint32_t)emax << 16);
   }

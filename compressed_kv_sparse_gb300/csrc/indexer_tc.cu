@@ -241,9 +241,11 @@ __global__ void __launch_bounds__(Cfg<QG>::kThreads, 1)
       // one 128-row key tile: two 64-dim K blocks, each one box of 128 rows
       // (contiguous keys) or two boxes of 64 rows from the tile's two
       // physical blocks (paged)
-      // the keys stream through once: evict-first, so they do not push the
-      // step's code and small reused arrays out of L2
-      const uint64_t pol = l2_evict_first_policy();
+      // one query per group (decode): the keys stream through once, so
+      // evict-first keeps them from pushing the step's code and small reused
+      // arrays out of L2; every group of a chunk rereads the same keys, which
+      // stay at the default priority
+      const uint64_t pol = QG == 1 ? l2_evict_first_policy() : l2_evict_normal_policy();
       auto issue_a = [&](uint32_t st, uint32_t b, uint32_t tile) {
         uint8_t *dst = sA + (size_t)st * kABytes;
         mbar_arrive_expect_tx(&a_full[st], kABytes);
