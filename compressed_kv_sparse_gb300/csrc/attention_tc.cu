@@ -446,8 +446,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     const bool q_early = q_first < P.n_q && rank * kRows < rows_bound(P, q_first);
     if (q_early) issue_q(q_first);
-    pdl_wait();
-    pdl_trigger();
+    // The loaders' own wait for the previous launch. Decode reads nothing of
+    // it before the first rows (the rotation coefficients are inputs and a
+    // decode list is not scanned), so its first query's coefficients and
+    // geometry are prepared before the wait; prefill scans its lists, so it
+    // waits here.
+    bool waited = false;
+    auto wait_prev = [&]() {
+      if (!waited) {
+        pdl_wait();
+        pdl_trigger();
+        waited = true;
+      }
+    };
+    if (!DEC) wait_prev();
     for (uint32_t qi = q_first; qi < P.n_q; qi += q_step) {
       if (rank * kRows >= rows_bound(P, qi)) continue;   // no rows for this rank
       if (!mbar_wait_warp(&S.q_empty, (qn & 1) ^ 1, ew)) goto done_loader;
@@ -476,6 +488,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           continue;
         }
         // the first tile's rows start loading before Q is rotated
+        wait_prev();
         if (!issue_tile(g, g.t0, n)) goto done_loader;
         if (!mbar_wait_warp(&S.q_tma, qt & 1, ew)) goto done_loader;   // Q landed
         ++qt;
