@@ -12,9 +12,10 @@
 // S^T (64 columns) and O^T (256 columns) live in TMEM. The softmax thread of a
 // row reads its 64 head scores from its TMEM lane and writes its probabilities
 // as one 128-byte row of P. The running maximum of each head starts at the
-// scores of the first valid row and is only raised (rescaling O and the sums)
-// when a score exceeds it by 2^8, so the common path needs no reduction across
-// rows; the per-head sums come from the tensor core (ones x P^T).
+// exact per-head maximum of the query's first tile and is only raised
+// (rescaling O and the sums) when a later score exceeds it by 2^8, so later
+// tiles need no reduction across rows; the per-head sums come from the tensor
+// core (ones x P^T).
 //
 // Decode: a query's 64 heads are split into two groups of 32, each its own
 // set of CTAs over the same rows (S^T then has N = 32; P keeps the 64-column
@@ -28,16 +29,16 @@
 // (On this part the L2 round trip moves these bytes faster than distributed
 // shared memory does.) Splitting the heads halves each CTA's softmax and
 // exchange and doubles the CTAs a small batch puts to work. A (query, head
-// group) that fits one CTA (C = 1) and prefill write the output directly: it
-// is staged in the P buffer 128 dims at a time and stored as 16-byte
-// segments.
+// group) that fits one CTA (C = 1) and prefill write the output directly from
+// registers: lane pairs (dims d, d + 1) swap one value per pair of heads, so
+// each thread rotates and stores one head's bf16 pair.
 //
-// Warps 0-3: softmax and output epilogue (TMEM lanes = rows, then dims);
 // In decode on ratios 0 and 128 the rows of a tile are contiguous (the
 // window is the whole 128-slot ring once p >= 127, a compressed tile is 128
 // consecutive rows): such a tile is eight TMA boxes issued by one thread
 // instead of 8192 16-byte gathers.
 //
+// Warps 0-3: softmax and output epilogue (TMEM lanes = rows, then dims);
 // warps 4-7: gather loaders (cp.async, zero fill for masked rows) and the query
 // rotation; warp 8: MMA issue (one thread) and TMEM allocation. Every wait is
 // bounded (tc.cuh); a timeout sets the error word and the CTA winds down.

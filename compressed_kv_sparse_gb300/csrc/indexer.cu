@@ -389,13 +389,16 @@ inline uint32_t select_groups(uint32_t nq) {
 // E = A max ||k|| and theta = theta_S - E (- slack) at least k rows have
 // L_s >= theta, and every row with U_s < theta is beaten by k rows. The G
 // blocks of a query form a thread-block cluster: each filters its share of
-// the rows (U_s >= theta) into the candidate lists of the cluster's first
-// block (distributed shared memory), and after one cluster barrier that
-// block runs the certified selection on the candidates: tau~ = k-th largest S~, rows with
-// L_s > tau~ + E are in, rows with U_s < tau~ - E are out, the rest are
-// rescored with the exact recipe and the final selection is exact (ties to
-// the lower index). If the candidates overflow, the same selection runs over
-// every visible row in place.
+// the rows into the candidate lists of the cluster's first block
+// (distributed shared memory), bounding every row's error with the largest
+// row norm (a superset of the rows with U_s >= theta; one block per query
+// takes theta_S from a sample of the scores instead). After one cluster
+// barrier that block gives each candidate its own bound from its norm and
+// runs the certified selection on the candidates: tau~ = k-th largest S~,
+// rows with L_s > tau~ + E are in, rows with U_s < tau~ - E are out, the rest
+// are rescored with the exact recipe and the final selection is exact (ties
+// to the lower index). If the candidates overflow, the same selection runs
+// over every visible row in place.
 template <int NT>
 __global__ void __launch_bounds__(NT, NT == 256 ? 4 : 1)
     topk_select_tc_kernel(IndexArgs a, TcWs w, float cb, uint32_t G) {

@@ -10,15 +10,17 @@
 // buffers so the epilogue of one tile overlaps the MMA of the next). Each
 // epilogue thread owns one TMEM lane = one key row of its warp's queries: it
 // reads their 64 head dots each and applies ReLU and the head weights; with
-// QG = 1 (decode) it also
-// counts the top 12 bits of each score key into a per-CTA histogram that the
-// selection uses to place its threshold.
+// QG = 1 (decode) it also counts the top 12 bits of each score key into a
+// per-CTA histogram that the selection uses to place its threshold.
 //
 // Persistent kernel, one CTA per SM: warp 0 issues TMA, warp 1 issues MMAs
 // (one thread each), warps 2.. run the epilogue (4 for one query per group,
 // 16 for four: one query each, four per TMEM lane quarter). Work items are
 // (sequence, query group, 128-row tile), split into contiguous ranges so the
-// B operand (the query group's heads) is reloaded only when the group changes.
+// B operand (the query group's heads) is reloaded only when the group
+// changes: an even share of one group's visible tiles per CTA (decode), or
+// an even share of all visible tiles from a host-computed range table
+// (chunks, whose later queries see more rows).
 // Every wait is bounded (tc.cuh); on a timeout the kernel sets *err and winds
 // down, still freeing its TMEM.
 #include <cuda_bf16.h>
