@@ -25,10 +25,8 @@
 // down, still freeing its TMEM.
 #include <cuda_bf16.h>
 
-#include <algorithm>
-#include <vector>
-
 #include "common.cuh"
+#include "split.h"
 #include "tc.cuh"
 
 namespace ds4a {
@@ -526,28 +524,8 @@ cudaError_t launch_qg(const IndexTcArgs &a, cudaStream_t s) {
   if (!P.cta_per_group && !a.seq_pos && grid <= kMaxSplit) {
     // a chunk's later queries see more rows: split the visible tiles, not
     // the items, evenly (every sequence has the same visible tiles per group)
-    std::vector<uint32_t> tg(P.n_groups);
-    uint64_t vb = 0;
-    for (uint32_t g = 0; g < P.n_groups; ++g) {
-      const uint32_t last = std::min(a.T, (g + 1) * QG) - 1;
-      const uint32_t vis = std::min((a.pos0 + last + 1) / 4, a.n_comp);
-      tg[g] = std::min(P.tiles_per, (vis + kRows - 1) / kRows);
-      vb += tg[g];
-    }
-    const uint64_t V = vb * a.batch;
-    uint32_t j = 1;
-    uint64_t cum = 0;
-    P.it_start[0] = 0;
-    for (uint32_t b = 0; b < a.batch && j < grid; ++b)
-      for (uint32_t g = 0; g < P.n_groups && j < grid; ++g) {
-        const uint32_t n = tg[g];
-        while (j < grid && (uint64_t)j * V / grid < cum + n) {
-          P.it_start[j] = (b * P.n_groups + g) * P.tiles_per + (uint32_t)((uint64_t)j * V / grid - cum);
-          ++j;
-        }
-        cum += n;
-      }
-    for (; j <= grid; ++j) P.it_start[j] = P.total_items;
+    split_visible_tiles(a.batch, a.T, QG, a.pos0, a.n_comp, kRows, P.n_groups, P.tiles_per, grid,
+                        P.it_start);
     P.split = 1;
   }
   e = launch_pdl(index_score_tc_kernel<QG>, dim3(grid), dim3(C::kThreads), C::kSmem, s, tk, tq, P);
